@@ -1,0 +1,431 @@
+"""Benchmark: verified tree nodes/s for one GDN layer's verify + commit round.
+
+One step = one pass of the whole hot path over one batch: forest packing
+(bole_pack_forest), closed-form verification (bole_tree_verify) and the
+factorised commit of the accepted paths (bole_commit), all through the C ABI
+on one CUDA stream.  Inputs are seeded synthetic workloads (see
+gated_deltanet_verification_gb300/inputs.py); the default workload is the
+batched packed forest (16 requests x 32 heads, 32-node trees of depth <= 8,
+dk = dv = 128, bf16 q/k/v, fp32 state).
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
+torch.cuda.synchronize(), CUDA events on the launching stream.  Inputs rotate
+over enough independent copies that the bytes touched between two uses of
+the same copy exceed 3x the L2 cache, so every step streams from HBM.  The
+committed state of a copy becomes that copy's next S_pre, as in a serving
+loop.  Per-kernel durations come from events around each launch.
+
+--impl reference runs the CPU oracle (fp64, all host cores) on the same
+workload: the slow reference arm, not a target.
+Multi-GPU (torchrun): requests are independent, so every rank runs its own
+batch (seeded by rank) with no collective on the data path ("weak" scaling);
+rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("verified tree nodes/sec (GDN verify+commit, 1×GB300); "
+          "achieved HBM GB/s vs peak")
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="bole", choices=["bole", "reference"])
+    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--shape", default="chain", help="tree shape for config 4")
+    p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic traffic and work (per launch)
+# ---------------------------------------------------------------------------
+
+def path_lengths(batch):
+    L = np.zeros(batch.B, dtype=np.int64)
+    for b in range(batch.B):
+        a = int(batch.accepted[b])
+        o = batch.offsets[b]
+        n = 0
+        while a >= 0:
+            n += 1
+            a = int(batch.parent[o + a])
+        L[b] = n
+    return L
+
+
+def algorithmic(batch):
+    """Bytes each kernel must move at least once, and tensor flops of verify."""
+    B, H, dk, dv, N = batch.B, batch.H, batch.dk, batch.dv, batch.N
+    s_in = 2 if batch.dtype == "bf16" else 4
+    topo_pack = 4 * (B + 1) + 4 * N + 4 * N + 16 * N + 4 * B
+    verify = (B * H * dk * dv * 4 + N * H * (2 * dk + dv) * s_in + 8 * N * H
+              + N * H * dv * (s_in + 4) + 4 * N * H + 4 * (B + 1) + 4 * N + 20 * N + 4 * B)
+    L = path_lengths(batch)
+    committed = int(np.sum(L > 0))
+    commit = (2 * committed * H * dk * dv * 4 + int(np.sum(L)) * H * (dk * s_in + 4 * dv + 4)
+              + 4 * (B + 1) + 4 * B + 4 * int(np.sum(L)))
+    sizes = np.diff(batch.offsets)
+    depths = batch.node_depths()
+    flops = 0
+    for b in range(B):
+        T = int(sizes[b])
+        if T == 0:
+            continue
+        d = int(depths[batch.offsets[b]:batch.offsets[b + 1]].max())
+        flops += H * (4 * T * dk * dv + 4 * T * T * dk + 2 * d * T * T * dv + 2 * T * T * dv)
+    flops += int(np.sum(L)) * H * 2 * dk * dv
+    return {"pack": topo_pack, "verify": verify, "commit": commit, "verify_flops": flops}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def run_oracle_sample(batch, target_s: float):
+    """Time the oracle's verify + commit over whole repetitions of the batch
+    until about target_s seconds have passed; returns nodes/s and details."""
+    import oracle
+    oracle.load()
+    threads = oracle.default_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(batch, nthreads=threads)
+        oracle.commit(batch, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or reps >= 1000:
+            break
+    return reps * batch.N / el, el, reps, threads
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from gated_deltanet_verification_gb300 import inputs
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from gated_deltanet_verification_gb300 import bole, build, device
+
+    build.build()
+    flags = bole.FLAG_FORCE_SIMT if args.force_simt else 0
+    seed = 1000 + args.config + 7919 * rank
+    batch = inputs.config_batch(args.config, seed=seed, shape=args.shape)
+    alg = algorithmic(batch)
+    step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
+    n_sets = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
+
+    sets = []
+    for _ in range(n_sets):
+        db = device.to_device(batch, device=dev)
+        rb = device.alloc_round(db, flags)
+        sets.append((db, rb))
+    stream = torch.cuda.current_stream()
+    tc_used = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
+               and batch.dv == 128 and batch.max_T <= 64
+               and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
+                                       torch.bfloat16, flags) == 0)
+    launches_per_step = 1 + (1 if tc_used else 2) + 1
+
+    def step(i, ev=None):
+        db, rb = sets[i % n_sets]
+        if ev is not None:
+            ev[0].record(stream)
+        device.pack(db, rb, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        device.verify(db, rb, flags, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        device.commit(db, rb, flags, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    for _, rb in sets:
+        bole.check_status(rb.status, "warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    for _, rb in sets:
+        bole.check_status(rb.status, "timed steps")
+    elapsed_ms = start.elapsed_time(end)
+    per_kernel = {"pack": [], "verify": [], "commit": []}
+    for e in evs:
+        per_kernel["pack"].append(e[0].elapsed_time(e[1]))
+        per_kernel["verify"].append(e[1].elapsed_time(e[2]))
+        per_kernel["commit"].append(e[2].elapsed_time(e[3]))
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    hbm, tflops, peak_kind = measured_peaks()
+    ms_step = elapsed_ms / args.steps
+    nodes_total = batch.N * args.steps * world
+    value = nodes_total / (elapsed_ms / 1e3)
+    avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
+    kern_rf = {}
+    for k in ("pack", "verify", "commit"):
+        gbs = alg[k] / (avg[k] * 1e-3) / 1e9 if avg[k] > 0 else 0.0
+        kern_rf[k] = {"ms": round(avg[k], 5), "alg_bytes": int(alg[k]),
+                      "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    dominant = max(("verify", "commit"), key=lambda k: avg[k])
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant,
+                "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": kern_rf[dominant]["frac"], "traffic": None, "peak_source": peak_kind,
+                "step_achieved_gbs": round(step_gbs, 1), "step_frac": round(step_gbs / hbm, 4),
+                "verify_plus_commit_frac": round(
+                    (alg["verify"] + alg["commit"]) / ((avg["verify"] + avg["commit"]) * 1e-3)
+                    / 1e9 / hbm, 4)}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, el, reps, thr = run_oracle_sample(batch, args.cpu_seconds)
+        cpu = {"value": round(v, 1), "unit": "nodes/s", "cores": thr, "kind": "oracle",
+               "sample": f"{reps} full repetition(s) of the workload's verify + commit "
+                         f"({batch.N} nodes x {batch.H} heads each), {el:.1f} s"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if tc_used else "f32", "io_dtype": batch.dtype, "data": "synthetic",
+        "config": {"workload": inputs.CONFIG_NAMES[args.config]
+                   + (f" [{args.shape}]" if args.config == 4 else ""),
+                   "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
+                   "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
+                   "seed": seed, "kernels": "tcgen05" if tc_used else "cuda-core",
+                   "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)"},
+        "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
+    }
+    print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, batch, sets, flags, stream, world):
+    """Same metric through the public API with host buffers: per step the
+    per-round inputs (tree, q/k/v, gates, accepted) are copied from pinned
+    host memory, the round runs, and the outputs O and the status word are
+    copied back.  The state slots stay resident in HBM (they are the
+    persistent per-request state the commit updates in place)."""
+    import torch
+    from gated_deltanet_verification_gb300 import device
+
+    db0 = sets[0][0]
+    names = ["offsets", "parent", "q", "k", "v", "gamma", "beta", "accepted"]
+    host = {n: torch.empty_like(getattr(db0, n), device="cpu").pin_memory() for n in names}
+    for n in names:
+        host[n].copy_(getattr(db0, n).cpu())
+    rb0 = sets[0][1]
+    O_host = torch.empty_like(rb0.O, device="cpu").pin_memory()
+    st_host = torch.empty_like(rb0.status, device="cpu").pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = O_host.numel() * O_host.element_size() + st_host.numel() * st_host.element_size()
+
+    def step(i):
+        db, rb = sets[i % len(sets)]
+        for n in names:
+            getattr(db, n).copy_(host[n], non_blocking=True)
+        device.run_round(db, rb, flags, stream)
+        O_host.copy_(rb.O, non_blocking=True)
+        st_host.copy_(rb.status, non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(batch.N * args.steps * world / (ms / 1e3), 1), "unit": "nodes/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / args.steps, 5)}
+
+
+def reference_arm(args, world, rank):
+    """The CPU oracle timed on the host cores, same workload and metric."""
+    if rank != 0:
+        return 0
+    from gated_deltanet_verification_gb300 import inputs
+    batch = inputs.config_batch(args.config, shape=args.shape)
+    import oracle
+    oracle.load()
+    thr = oracle.default_threads()
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.verify(batch, nthreads=thr)
+        oracle.commit(batch, nthreads=thr)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(batch, nthreads=thr)
+        oracle.commit(batch, nthreads=thr)
+    el = time.perf_counter() - t0
+    value = batch.N * args.steps / el
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "nodes/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": inputs.CONFIG_NAMES[args.config]
+                   + (f" [{args.shape}]" if args.config == 4 else ""),
+                   "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
+                   "dv": batch.dv, "nodes": batch.N},
+        "cpu_baseline": {"value": round(value, 1), "unit": "nodes/s", "cores": thr,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} full repetitions of the workload"},
+        "e2e": {"value": round(value, 1), "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,194 @@
+"""Python binding of libbole.so: argument marshalling only.
+
+Every step of the verification runs in the library's CUDA kernels; this
+module turns torch tensors into device pointers, picks the current CUDA
+stream and allocates outputs with torch (device memory plumbing).  It never
+falls back to a CPU or PyTorch implementation: if the library is missing the
+import of any entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_BAD_TOPOLOGY = 3
+ERR_DEPTH = 4
+ERR_WORKSPACE = 5
+ERR_CUDA = 6
+ERR_TIMEOUT = 7
+
+F32 = 0
+BF16 = 1
+FLAG_FORCE_SIMT = 0x1
+MAX_TREE_NODES = 128
+STATUS_WORDS = 4
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class BoleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = int(code)
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libbole.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with "
+                    "`python -m gated_deltanet_verification_gb300.build`")
+            L = ctypes.CDLL(path)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            U = ctypes.c_uint
+            L.bole_status_string.argtypes = [I]
+            L.bole_status_string.restype = ctypes.c_char_p
+            L.bole_version.argtypes = []
+            L.bole_version.restype = I
+            L.bole_workspace_size.argtypes = [I, I, I, I, I, I, U]
+            L.bole_workspace_size.restype = S
+            L.bole_pack_forest.argtypes = [P, P, I, I, I, P, P, P, P, P]
+            L.bole_pack_forest.restype = I
+            L.bole_tree_verify.argtypes = [P, P, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                           I, P, P, P, P, S, P, U, P]
+            L.bole_tree_verify.restype = I
+            L.bole_commit.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I, P, U, P]
+            L.bole_commit.restype = I
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().bole_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return lib().bole_version()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libbole must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(code: int, what: str) -> None:
+    if code != OK:
+        raise BoleError(code, what)
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(STATUS_WORDS, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor, what: str = "device status") -> None:
+    """Synchronising read of a device status block; raises on a recorded fault."""
+    st = status.cpu().tolist()
+    if st[0] != OK:
+        raise BoleError(st[0], f"{what} (request {st[1]}, node {st[2]}, detail {st[3]})")
+
+
+def workspace_size(B: int, H: int, dk: int, dv: int, max_T: int, dtype=torch.bfloat16,
+                   flags: int = 0) -> int:
+    code = BF16 if dtype == torch.bfloat16 else F32
+    return int(lib().bole_workspace_size(B, H, dk, dv, max_T, code, flags))
+
+
+def pack_forest(offsets: torch.Tensor, parent: torch.Tensor, max_depth: int, *,
+                depth: Optional[torch.Tensor] = None, anc: Optional[torch.Tensor] = None,
+                req_depth: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
+    """bole_pack_forest: returns (depth [N], anc [N,4], req_depth [B], status [4])."""
+    B = offsets.numel() - 1
+    N = parent.numel()
+    dev = offsets.device
+    depth = torch.empty(N, dtype=torch.int32, device=dev) if depth is None else depth
+    anc = torch.empty((N, 4), dtype=torch.int32, device=dev) if anc is None else anc
+    req_depth = torch.empty(max(B, 0), dtype=torch.int32, device=dev) if req_depth is None \
+        else req_depth
+    status = new_status(dev) if status is None else status
+    _check(lib().bole_pack_forest(_ptr(offsets), _ptr(parent), B, N, int(max_depth), _ptr(depth),
+                                  _ptr(anc), _ptr(req_depth), _ptr(status), _stream(stream)),
+           "bole_pack_forest")
+    return depth, anc, req_depth, status
+
+
+def tree_verify(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_depth, max_T: int,
+                max_depth: int, *, O=None, U=None, logP=None, workspace=None, status=None,
+                flags: int = 0, stream=None):
+    """bole_tree_verify: returns (O, U, logP)."""
+    B = offsets.numel() - 1
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    code = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    O = torch.empty((N, H, dv), dtype=q.dtype, device=dev) if O is None else O
+    U = torch.empty((N, H, dv), dtype=torch.float32, device=dev) if U is None else U
+    logP = torch.empty((N, H), dtype=torch.float32, device=dev) if logP is None else logP
+    if workspace is None:
+        nbytes = lib().bole_workspace_size(B, H, dk, dv, int(max_T), code, flags)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(lib().bole_tree_verify(
+        _ptr(S_pre), _ptr(q), _ptr(k), _ptr(v), code, _ptr(gamma), _ptr(beta), _ptr(offsets),
+        _ptr(parent), _ptr(depth), _ptr(anc), _ptr(req_depth), B, H, dk, dv, N, int(max_T),
+        int(max_depth), _ptr(O), _ptr(U), _ptr(logP), _ptr(workspace), workspace.numel(),
+        _ptr(status), int(flags), _stream(stream)), "bole_tree_verify")
+    return O, U, logP
+
+
+def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int = 0,
+           stream=None) -> torch.Tensor:
+    """bole_commit: overwrites S in place with the accepted paths' states; returns S."""
+    B = offsets.numel() - 1
+    N, H, dk = k.shape
+    dv = U.shape[-1]
+    if status is None:
+        status = new_status(k.device)
+    _check(lib().bole_commit(_ptr(S), _ptr(k), _dtype_code(k), _ptr(U), _ptr(logP),
+                             _ptr(offsets), _ptr(parent), _ptr(accepted), B, H, dk, dv, N,
+                             _ptr(status), int(flags), _stream(stream)), "bole_commit")
+    return S
+
+
+__all__ = ["lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
+           "tree_verify", "commit", "new_status", "check_status", "BoleError", "OK",
+           "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
+           "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT"]

@@ -1,0 +1,142 @@
+// C ABI: host-side validation, kernel choice and launches.  No entry point
+// allocates memory or keeps state between calls.
+#include <stdint.h>
+
+#include "common.cuh"
+
+using namespace bole;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_dim(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+
+bool valid_dtype(bole_dtype t) { return t == BOLE_F32 || t == BOLE_BF16; }
+
+bole_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BOLE_OK : BOLE_ERR_CUDA; }
+
+bool use_tc_verify(const VerifyArgs &a, unsigned flags)
+{
+    return !(flags & BOLE_FLAG_FORCE_SIMT) && tc_verify_supported(a);
+}
+
+} // namespace
+
+extern "C" {
+
+const char *bole_status_string(int status)
+{
+    switch (status) {
+    case BOLE_OK: return "ok";
+    case BOLE_ERR_INVALID_ARG: return "invalid argument";
+    case BOLE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BOLE_ERR_BAD_TOPOLOGY: return "bad tree topology";
+    case BOLE_ERR_DEPTH: return "tree deeper than max_depth";
+    case BOLE_ERR_WORKSPACE: return "workspace missing or too small";
+    case BOLE_ERR_CUDA: return "CUDA runtime error";
+    case BOLE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int bole_version(void) { return 100; }
+
+size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, bole_dtype qkv_dtype,
+                           unsigned flags)
+{
+    if (B < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || max_T < 1 ||
+        max_T > BOLE_MAX_TREE_NODES || !valid_dtype(qkv_dtype))
+        return 0;
+    VerifyArgs a = {};
+    a.dtype = qkv_dtype;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T;
+    if (use_tc_verify(a, flags)) return 0;
+    return simt_workspace_bytes(B, H, max_T);
+}
+
+bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int B, int N,
+                             int max_depth, int32_t *depth, uint32_t *anc, int32_t *req_depth,
+                             int32_t *dev_status, bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || max_depth < 0 || max_depth > BOLE_MAX_TREE_NODES - 1)
+        return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && !req_depth)) return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!parent || !depth || !anc)) return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
+    if (!aligned(anc, 16) || !aligned(offsets, 4) || !aligned(parent, 4) || !aligned(depth, 4) ||
+        !aligned(req_depth, 4) || !aligned(dev_status, 16))
+        return BOLE_ERR_INVALID_ARG;
+    return from_cuda(launch_pack(offsets, parent, B, N, max_depth, depth, anc, req_depth,
+                                 dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, const void *v,
+                             bole_dtype qkv_dtype, const float *gamma, const float *beta,
+                             const int32_t *offsets, const int32_t *parent, const int32_t *depth,
+                             const uint32_t *anc, const int32_t *req_depth, int B, int H, int dk,
+                             int dv, int N, int max_T, int max_depth, void *O, float *U,
+                             float *logP, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, unsigned flags, bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(qkv_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if (max_T < 1 || max_T > BOLE_MAX_TREE_NODES || max_depth < 0 ||
+        max_depth > BOLE_MAX_TREE_NODES - 1)
+        return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * max_T) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && (!S_pre || !req_depth))) return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !gamma || !beta || !parent || !depth || !anc || !O || !U ||
+                  !logP))
+        return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {S_pre, q, k, v, O, U, anc, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {gamma, beta, offsets, parent, depth, req_depth, logP};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+
+    VerifyArgs a;
+    a.S_pre = S_pre; a.q = q; a.k = k; a.v = v; a.dtype = qkv_dtype;
+    a.gamma = gamma; a.beta = beta;
+    a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
+    a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.st = dev_status;
+
+    const bool tc = use_tc_verify(a, flags);
+    const size_t need = tc ? 0 : simt_workspace_bytes(B, H, max_T);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return BOLE_ERR_WORKSPACE;
+    if (B == 0 || N == 0) return BOLE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(tc ? launch_tc_verify(a, s) : launch_simt_verify(a, s));
+}
+
+bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
+                        const float *logP, const int32_t *offsets, const int32_t *parent,
+                        const int32_t *accepted, int B, int H, int dk, int dv, int N,
+                        int32_t *dev_status, unsigned flags, bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(k_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && (!S || !accepted))) return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!k || !U || !logP || !parent)) return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {S, k, U, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {logP, offsets, parent, accepted};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+    if (B == 0 || N == 0) return BOLE_OK;
+
+    CommitArgs a;
+    a.S = S; a.k = k; a.dtype = k_dtype; a.U = U; a.logP = logP;
+    a.offsets = offsets; a.parent = parent; a.accepted = accepted;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.st = dev_status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = !(flags & BOLE_FLAG_FORCE_SIMT) && tc_commit_supported(a);
+    return from_cuda(tc ? launch_tc_commit(a, s) : launch_simt_commit(a, s));
+}
+
+} // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bole.h"
+
+namespace bole {
+
+constexpr int kMaxTree = BOLE_MAX_TREE_NODES;
+
+// First fault wins: {code, request, node, detail}.
+__device__ __forceinline__ void report(int32_t *st, int code, int b, int i, int aux)
+{
+    if (atomicCAS(st, 0, code) == 0) {
+        st[1] = b;
+        st[2] = i;
+        st[3] = aux;
+    }
+}
+
+__device__ __forceinline__ bool faulted(const int32_t *st)
+{
+    return *(const volatile int32_t *)st != 0;
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x)
+{
+    return __bfloat162float(x);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x)
+{
+    return __float2bfloat16_rn(x);
+}
+
+// ---- launchers (one per kernel family; each returns the launch error) ----
+
+cudaError_t launch_pack(const int32_t *offsets, const int32_t *parent, int B, int N, int max_depth,
+                        int32_t *depth, uint32_t *anc, int32_t *req_depth, int32_t *st,
+                        cudaStream_t s);
+
+struct VerifyArgs {
+    const float *S_pre;
+    const void *q, *k, *v;
+    bole_dtype dtype;
+    const float *gamma, *beta;
+    const int32_t *offsets, *parent, *depth;
+    const uint32_t *anc;
+    const int32_t *req_depth;
+    int B, H, dk, dv, N, max_T, max_depth;
+    void *O;
+    float *U, *logP;
+    void *ws;
+    int32_t *st;
+};
+
+struct CommitArgs {
+    float *S;
+    const void *k;
+    bole_dtype dtype;
+    const float *U, *logP;
+    const int32_t *offsets, *parent, *accepted;
+    int B, H, dk, dv, N;
+    int32_t *st;
+};
+
+size_t simt_workspace_bytes(int B, int H, int max_T);
+cudaError_t launch_simt_verify(const VerifyArgs &a, cudaStream_t s);
+cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
+
+bool tc_verify_supported(const VerifyArgs &a);
+cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s);
+bool tc_commit_supported(const CommitArgs &a);
+cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s);
+
+} // namespace bole

@@ -1,0 +1,98 @@
+"""Device-resident copies of a packed forest and one verify + commit round
+through the C ABI (the call sequence a serving loop makes each round)."""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import bole
+
+
+@dataclasses.dataclass
+class DeviceBatch:
+    B: int
+    H: int
+    dk: int
+    dv: int
+    N: int
+    max_T: int
+    max_depth: int
+    offsets: torch.Tensor
+    parent: torch.Tensor
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    gamma: torch.Tensor
+    beta: torch.Tensor
+    S: torch.Tensor          # state slots: S_pre before commit, S_new after
+    accepted: torch.Tensor
+
+
+def to_device(batch, device="cuda", dtype: Optional[torch.dtype] = None) -> DeviceBatch:
+    """Copy a TreeBatch (numpy) to the device; q/k/v in the batch's dtype."""
+    if dtype is None:
+        dtype = torch.bfloat16 if batch.dtype == "bf16" else torch.float32
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dt)
+
+    return DeviceBatch(
+        batch.B, batch.H, batch.dk, batch.dv, batch.N, max(batch.max_T, 1), batch.max_depth,
+        t(batch.offsets, torch.int32), t(batch.parent, torch.int32), t(batch.q, dtype),
+        t(batch.k, dtype), t(batch.v, dtype), t(batch.gamma, torch.float32),
+        t(batch.beta, torch.float32), t(batch.S_pre, torch.float32),
+        t(batch.accepted, torch.int32))
+
+
+@dataclasses.dataclass
+class RoundBuffers:
+    depth: torch.Tensor
+    anc: torch.Tensor
+    req_depth: torch.Tensor
+    status: torch.Tensor
+    O: torch.Tensor
+    U: torch.Tensor
+    logP: torch.Tensor
+    workspace: torch.Tensor
+
+
+def alloc_round(db: DeviceBatch, flags: int = 0) -> RoundBuffers:
+    dev = db.q.device
+    ws = bole.workspace_size(db.B, db.H, db.dk, db.dv, db.max_T, db.q.dtype, flags)
+    return RoundBuffers(
+        depth=torch.empty(db.N, dtype=torch.int32, device=dev),
+        anc=torch.empty((db.N, 4), dtype=torch.int32, device=dev),
+        req_depth=torch.empty(max(db.B, 1), dtype=torch.int32, device=dev),
+        status=bole.new_status(dev),
+        O=torch.empty((db.N, db.H, db.dv), dtype=db.q.dtype, device=dev),
+        U=torch.empty((db.N, db.H, db.dv), dtype=torch.float32, device=dev),
+        logP=torch.empty((db.N, db.H), dtype=torch.float32, device=dev),
+        workspace=torch.empty(max(ws, 16), dtype=torch.uint8, device=dev),
+    )
+
+
+def pack(db: DeviceBatch, rb: RoundBuffers, stream=None) -> None:
+    bole.pack_forest(db.offsets, db.parent, db.max_depth, depth=rb.depth, anc=rb.anc,
+                     req_depth=rb.req_depth[:db.B], status=rb.status, stream=stream)
+
+
+def verify(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:
+    bole.tree_verify(db.S, db.q, db.k, db.v, db.gamma, db.beta, db.offsets, db.parent, rb.depth,
+                     rb.anc, rb.req_depth[:db.B], db.max_T, db.max_depth, O=rb.O, U=rb.U,
+                     logP=rb.logP, workspace=rb.workspace, status=rb.status, flags=flags,
+                     stream=stream)
+
+
+def commit(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:
+    bole.commit(db.S, db.k, rb.U, rb.logP, db.offsets, db.parent, db.accepted,
+                status=rb.status, flags=flags, stream=stream)
+
+
+def run_round(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:
+    """pack -> verify -> commit, all asynchronous on one stream."""
+    pack(db, rb, stream)
+    verify(db, rb, flags, stream)
+    commit(db, rb, flags, stream)

@@ -1,0 +1,156 @@
+/*
+ * bole.h -- C ABI of the GB300 (sm_103a) library for closed-form tree
+ * verification of Gated DeltaNet layers.
+ *
+ * The method is the one of "Bole: Efficient Tree Speculation for
+ * Hybrid-Attention Language Models":
+ *   - every proposal node i of a tree sees the committed prefix and its own
+ *     proposal ancestors A(i), never a sibling branch (Section II-B);
+ *   - its output is given in closed form from one immutable pre-tree state
+ *     S_pre (Theorem 1, Eq. (2)):
+ *         O = D_P Q S_pre + C (I+G)^{-1} D_beta (V - D_P K S_pre)
+ *     with the cumulative decay P_i = prod of gamma over A(i) and i (Lemma 1,
+ *     Eq. (4)), G_ij = beta_i (P_i/P_j) k_i.k_j for j in A(i) (Lemma 2,
+ *     Eq. (5)), C_ij = (P_i/P_j) q_i.k_j for j in A(i) or j = i, and the
+ *     inverse equal to the finite Neumann sum of (-G)^m, m <= d (Lemma 3,
+ *     Eq. (6)), evaluated by the recurrence Z <- -G Z, U += Z (Eq. (8));
+ *   - the per-node factors (P, K, U) replace per-node state snapshots
+ *     (Eq. (9)); after sampling, commit rebuilds the accepted node a's exact
+ *     state S_new = P_a S_pre + (D_a K_a)^T U_a (Eq. (10)), in place.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory and keeps no global mutable state.
+ *     All calls are asynchronous on `stream` (a cudaStream_t; NULL selects
+ *     the legacy default stream) and may be captured in CUDA graphs.
+ *   - Packed forest: B requests' trees are concatenated node-major.
+ *     offsets[B+1] (int32, offsets[0] = 0, non-decreasing, offsets[B] = N)
+ *     delimits request b's nodes [offsets[b], offsets[b+1]).  parent[N]
+ *     (int32) holds request-LOCAL parent indices, -1 = the committed root,
+ *     and parent[i] < i (parent before child).  At most 128 nodes per tree.
+ *   - Depth of a node = number of strict proposal ancestors (a child of the
+ *     committed root has depth 0).  `max_depth` is an upper bound; the
+ *     kernels run exactly the per-request depth (extra Neumann steps would
+ *     add exact zeros since G^(d+1) = 0).
+ *   - Layouts (row-major, last index contiguous):
+ *       S_pre / S     [B, H, dk, dv] float32 (one dk x dv state per head)
+ *       q, k          [N, H, dk]  bf16 or float32 (bole_dtype)
+ *       v             [N, H, dv]  same dtype as q, k
+ *       gamma, beta   [N, H] float32; gamma in (0, 1] (decay), beta = write gate
+ *       O             [N, H, dv]  same dtype as q/k/v
+ *       U             [N, H, dv]  float32 (the propagated deltas u_i)
+ *       logP          [N, H]      float32, log of the cumulative decay P_i
+ *   - Supported sizes: dk, dv multiples of 16 in [16, 128]; H >= 1;
+ *     B >= 0 (B = 0 or N = 0 launches nothing); 16-byte aligned pointers.
+ *   - Errors: arguments that the host can check (null pointers, sizes,
+ *     alignment, workspace) make the call return an error code synchronously
+ *     and launch nothing.  Faults in device data (topology, depth, sizes
+ *     larger than declared) are written to `dev_status` (int32[4]:
+ *     {code, request, node, detail}); the first fault wins, later kernels of
+ *     the round see it and write no outputs.  No kernel traps or spins
+ *     without bound; a bounded wait that expires records BOLE_ERR_TIMEOUT.
+ *     BOLE_ERR_CUDA means a CUDA runtime call (launch, attribute) failed.
+ */
+#ifndef BOLE_H_
+#define BOLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bole_stream_t; /* same type as cudaStream_t */
+
+typedef enum bole_status {
+    BOLE_OK = 0,
+    BOLE_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, misalignment */
+    BOLE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+    BOLE_ERR_BAD_TOPOLOGY = 3, /* parent[i] >= i or < -1, tree > 128 nodes, bad offsets */
+    BOLE_ERR_DEPTH = 4,        /* a tree is deeper than max_depth */
+    BOLE_ERR_WORKSPACE = 5,    /* workspace missing or smaller than bole_workspace_size */
+    BOLE_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+    BOLE_ERR_TIMEOUT = 7       /* a bounded device-side wait expired */
+} bole_status;
+
+typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
+
+#define BOLE_MAX_TREE_NODES 128
+#define BOLE_STATUS_WORDS 4
+
+/* Flags for bole_tree_verify / bole_commit / bole_workspace_size. */
+#define BOLE_FLAG_FORCE_SIMT 0x1u /* use the FP32 CUDA-core kernels even where the
+                                     tcgen05 tensor-core kernels apply */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *bole_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bole_version(void);
+
+/* Bytes of device workspace bole_tree_verify needs for these sizes (0 when
+ * the chosen kernels keep every intermediate on chip).  max_T bounds every
+ * tree's node count (1..128).  The workspace holds the short-lived tree
+ * factors (G, C) of one call -- the "verification scratch" of the pages'
+ * state lifecycle (Section IV-D) -- and may be reused by the next call. */
+size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, bole_dtype qkv_dtype,
+                           unsigned flags);
+
+/* Round-level topology step (Section IV-C; forest packing, review Section 3).
+ * Validates the packed forest and derives, per node, its depth and its
+ * ancestor-or-self bit mask, and per request its depth.
+ *   offsets [B+1], parent [N]   in: the packed forest (device)
+ *   depth   [N]   int32         out: strict-ancestor count
+ *   anc     [N,4] uint32        out: bit j of word j/32 set iff local node j is
+ *                                    an ancestor of the node or the node itself
+ *   req_depth [B] int32         out: max depth over the request (0 if empty)
+ *   dev_status [4] int32        out: zeroed by this call, then the first fault:
+ *                                    BOLE_ERR_BAD_TOPOLOGY or BOLE_ERR_DEPTH
+ * Integer only; results are exact. */
+bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int B, int N,
+                             int max_depth, int32_t *depth, uint32_t *anc, int32_t *req_depth,
+                             int32_t *dev_status, bole_stream_t stream);
+
+/* Closed-form verification of every node of every tree (Theorem 1, Eq. (2),
+ * value-tiled as in Eq. (7), propagation by the finite Neumann recurrence of
+ * Eq. (8)).  S_pre is read only (immutable during verification, Section
+ * IV-D).  Inputs: S_pre, q, k, v, gamma, beta as laid out above; offsets and
+ * parent of the packed forest; depth, anc, req_depth from bole_pack_forest.
+ * max_T bounds the tree sizes (1..128), max_depth the depths (0..127).
+ * Outputs: O (dtype of q/k/v), U (float32) and logP (float32) -- U, logP and
+ * the caller's k buffer are the factors commit needs; keep them alive until
+ * bole_commit.  workspace: device buffer of at least
+ * bole_workspace_size(...) bytes (NULL allowed when that size is 0).
+ * Kernel choice: bf16 inputs with dk = dv = 128 and max_T <= 64 run the
+ * TMA + tcgen05 tensor-core kernel (tf32 state products, fp32 accumulation);
+ * everything else, or flags & BOLE_FLAG_FORCE_SIMT, runs the FP32 CUDA-core
+ * kernels (producer of G, C into the workspace + value-tiled solve). */
+bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, const void *v,
+                             bole_dtype qkv_dtype, const float *gamma, const float *beta,
+                             const int32_t *offsets, const int32_t *parent, const int32_t *depth,
+                             const uint32_t *anc, const int32_t *req_depth, int B, int H, int dk,
+                             int dv, int N, int max_T, int max_depth, void *O, float *U,
+                             float *logP, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, unsigned flags, bole_stream_t stream);
+
+/* Factorised commit (Eq. (10)): for every request b with accepted[b] = a >= 0
+ * (request-local node index) and every head,
+ *     S <- P_a S + sum over j on the path root..a of (P_a / P_j) k_j u_j^T
+ * written in place over S ([B,H,dk,dv] float32, which held S_pre during the
+ * verification that produced U and logP).  accepted[b] = -1 leaves request b's
+ * state untouched.  k is the same buffer verification read; U and logP are its
+ * outputs.  bf16 k with dk = dv = 128 uses the TMA + tcgen05 kernel (one
+ * tensor-core product per head over the accepted path); otherwise, or with
+ * BOLE_FLAG_FORCE_SIMT, the FP32 CUDA-core kernel.  Must be stream-ordered after
+ * the verification.  Device faults (accepted[b] >= tree size) go to dev_status. */
+bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
+                        const float *logP, const int32_t *offsets, const int32_t *parent,
+                        const int32_t *accepted, int B, int H, int dk, int dv, int N,
+                        int32_t *dev_status, unsigned flags, bole_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BOLE_H_ */

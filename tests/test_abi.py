@@ -1,0 +1,88 @@
+"""The C ABI library: it builds, loads without a GPU, exports every entry
+point include/*.h declares, and rejects host-checkable argument errors
+before touching CUDA.  CPU only (no compute calls)."""
+import ctypes
+import glob
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(bole_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from gated_deltanet_verification_gb300 import build
+    path = build.build()
+    from gated_deltanet_verification_gb300 import bole
+    return bole.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert {"bole_pack_forest", "bole_tree_verify", "bole_commit", "bole_workspace_size",
+            "bole_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from gated_deltanet_verification_gb300 import bole
+    assert bole.status_string(0) == "ok"
+    for code in range(1, 8):
+        assert bole.status_string(code) not in ("ok", "unknown status")
+    assert bole.status_string(99) == "unknown status"
+
+
+def test_workspace_size_rules(lib):
+    f = lib.bole_workspace_size
+    f.restype = ctypes.c_size_t
+    # fp32 inputs use the CUDA-core path: two dense T x T factors per unit
+    assert f(2, 3, 16, 16, 8, 0, 0) == 2 * 4 * 2 * 3 * 8 * 8
+    # invalid sizes report 0
+    assert f(2, 3, 12, 16, 8, 0, 0) == 0
+    assert f(2, 3, 16, 16, 129, 0, 0) == 0
+    assert f(2, 0, 16, 16, 8, 0, 0) == 0
+
+
+def test_host_validation_without_gpu(lib):
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake = c(1 << 20)  # never dereferenced: validation fails first
+    # pack: null offsets
+    assert lib.bole_pack_forest(None, fake, 1, 4, 3, fake, fake, fake, fake, None) == \
+        bole.ERR_INVALID_ARG
+    # pack: max_depth out of range
+    assert lib.bole_pack_forest(fake, fake, 1, 4, 200, fake, fake, fake, fake, None) == \
+        bole.ERR_INVALID_ARG
+    args = [fake, fake, fake, fake, 1, fake, fake, fake, fake, fake, fake, fake]
+    # dk not a multiple of 16
+    assert lib.bole_tree_verify(*args, 1, 1, 24, 128, 4, 8, 3, fake, fake, fake, fake, 0, fake,
+                                0, None) == bole.ERR_INVALID_ARG
+    # N larger than B * max_T
+    assert lib.bole_tree_verify(*args, 1, 1, 128, 128, 65, 64, 3, fake, fake, fake, fake, 0, fake,
+                                0, None) == bole.ERR_INVALID_ARG
+    # misaligned state pointer
+    args_mis = [c((1 << 20) + 4)] + args[1:]
+    assert lib.bole_tree_verify(*args_mis, 1, 1, 128, 128, 4, 8, 3, fake, fake, fake, fake, 0,
+                                fake, 0, None) == bole.ERR_INVALID_ARG
+    # CUDA-core path needs a workspace
+    assert lib.bole_tree_verify(*args, 1, 1, 128, 128, 4, 8, 3, fake, fake, fake, None, 0, fake,
+                                bole.FLAG_FORCE_SIMT, None) == bole.ERR_WORKSPACE
+    # commit: null accepted
+    assert lib.bole_commit(fake, fake, 1, fake, fake, fake, fake, None, 1, 1, 128, 128, 4, fake,
+                           0, None) == bole.ERR_INVALID_ARG

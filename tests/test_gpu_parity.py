@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle,
+on the same seeded inputs.  Integer outputs must match bit for bit; O, U and
+the committed state within relative Frobenius 1e-5 (float32 q/k/v) or 1e-2
+(bf16 q/k/v, float32 state).  logP is compared with an absolute bound
+derived from float32 summation of at most 128 logs (|L| < 200 here)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import rel_fro
+from gated_deltanet_verification_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_verification_gb300 import build
+    build.build()
+
+
+def _run(batch, flags=0, dtype=None):
+    from gated_deltanet_verification_gb300 import bole, device
+    db = device.to_device(batch, dtype=dtype)
+    rb = device.alloc_round(db, flags)
+    device.pack(db, rb)
+    device.verify(db, rb, flags)
+    O = rb.O.float().cpu().numpy().astype(np.float64)
+    U = rb.U.cpu().numpy().astype(np.float64)
+    logP = rb.logP.cpu().numpy().astype(np.float64)
+    device.commit(db, rb, flags)
+    S_new = db.S.cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    bole.check_status(rb.status)
+    return dict(depth=rb.depth.cpu().numpy(), anc=rb.anc.cpu().numpy().view(np.uint32),
+                req=rb.req_depth[:batch.B].cpu().numpy(), O=O, U=U, logP=logP, S_new=S_new)
+
+
+def _check(batch, got, tol):
+    depth, anc, req, st = oracle.pack(batch.offsets, batch.parent, batch.max_depth)
+    assert st == oracle.OK
+    assert np.array_equal(got["depth"], depth)
+    assert np.array_equal(got["anc"], anc)
+    assert np.array_equal(got["req"], req)
+    O, U, logP = oracle.verify(batch)
+    S_new = oracle.commit(batch)
+    errs = {"O": rel_fro(got["O"], O), "U": rel_fro(got["U"], U),
+            "S_new": rel_fro(got["S_new"], S_new)}
+    assert np.max(np.abs(got["logP"] - logP)) < 2e-4 * max(1.0, np.max(np.abs(logP)))
+    for name, e in errs.items():
+        assert e <= tol, f"{batch.name}: {name} rel err {e:.3e} > {tol}"
+    return errs
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_config_parity(cfg):
+    b = I.config_batch(cfg)
+    errs = _check(b, _run(b), TOL[b.dtype])
+    print(b.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("shape", I.SHAPES_CFG4)
+def test_shape_extremes_parity(shape):
+    b = I.config_batch(4, shape=shape)
+    errs = _check(b, _run(b), TOL[b.dtype])
+    print(b.name, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_cuda_core_path_parity(cfg):
+    """The FP32 CUDA-core kernels on the bf16 workloads (forced)."""
+    from gated_deltanet_verification_gb300 import bole
+    b = I.config_batch(cfg)
+    _check(b, _run(b, flags=bole.FLAG_FORCE_SIMT), TOL["bf16"])
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_fp32_inputs_parity(cfg):
+    """Same workloads with float32 q/k/v: float32 tolerance."""
+    b = I.config_batch(cfg)
+    b.dtype = "f32"
+    _check(b, _run(b, dtype=torch.float32), TOL["f32"])
+
+
+@pytest.mark.parametrize("sizes,shape,dtype,dk,dv", [
+    ([1, 2, 63, 64, 65, 128], "random", "f32", 32, 48),
+    ([1, 2, 63, 64], "random", "bf16", 128, 128),
+    ([64, 0, 17, 0, 64], "chain", "bf16", 128, 128),
+    ([5, 0, 3], "star", "f32", 16, 16),
+    ([128, 100], "4ary", "bf16", 64, 128),
+    ([40, 33, 64], "random", "bf16", 128, 128),
+])
+def test_ragged_and_edge_shapes(sizes, shape, dtype, dk, dv):
+    b = I.random_batch(seed=sum(sizes) + dk, B=len(sizes), H=3, dk=dk, dv=dv, sizes=sizes,
+                       max_depth=127 if shape != "random" else 9, dtype=dtype, sigma=0.05,
+                       accept="uniform", shape=shape)
+    _check(b, _run(b), TOL[dtype])
+
+
+@pytest.mark.parametrize("which", ["none", "root_child"])
+def test_commit_edge_paths(which):
+    b = I.random_batch(seed=3, B=3, H=2, dk=128, dv=128, sizes=[20, 31, 9], max_depth=6,
+                       dtype="bf16", sigma=0.05, accept="uniform")
+    b.accepted[:] = -1 if which == "none" else 0
+    got = _run(b)
+    S_new = oracle.commit(b)
+    assert rel_fro(got["S_new"], S_new) <= TOL["bf16"]
+    if which == "none":
+        assert np.array_equal(got["S_new"], b.S_pre.astype(np.float64))
+
+
+def test_device_topology_faults():
+    """Bad parents and over-deep trees are reported in the status block; the
+    verification and commit kernels then leave their outputs untouched."""
+    from gated_deltanet_verification_gb300 import bole, device
+    b = I.random_batch(seed=5, B=2, H=2, dk=128, dv=128, sizes=[12, 9], max_depth=4,
+                       dtype="bf16", sigma=0.05, accept="uniform")
+    bad = b.parent.copy()
+    bad[12 + 4] = 7  # node 4 of request 1 points forward
+    db = device.to_device(b)
+    db.parent.copy_(torch.from_numpy(bad))
+    rb = device.alloc_round(db)
+    rb.O.fill_(3.0)
+    S_before = db.S.clone()
+    device.run_round(db, rb)
+    torch.cuda.synchronize()
+    st = rb.status.cpu().tolist()
+    assert st[0] == bole.ERR_BAD_TOPOLOGY and st[1] == 1 and st[2] == 4
+    assert torch.all(rb.O.float() == 3.0)
+    assert torch.equal(db.S, S_before)
+    # depth bound violated
+    db2 = device.to_device(b)
+    db2.max_depth = 1
+    rb2 = device.alloc_round(db2)
+    device.pack(db2, rb2)
+    torch.cuda.synchronize()
+    st2 = rb2.status.cpu().tolist()
+    assert st2[0] == bole.ERR_DEPTH
+    with pytest.raises(bole.BoleError):
+        bole.check_status(rb2.status)
+
+
+def test_empty_batch():
+    from gated_deltanet_verification_gb300 import bole
+    offsets = torch.zeros(1, dtype=torch.int32, device="cuda")
+    parent = torch.zeros(0, dtype=torch.int32, device="cuda")
+    depth, anc, req, st = bole.pack_forest(offsets, parent, 3)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist()[0] == 0
