@@ -87,18 +87,22 @@ def test_fp32_inputs_parity(cfg):
     _check(b, _run(b, dtype=torch.float32), TOL["f32"])
 
 
-@pytest.mark.parametrize("sizes,shape,dtype,dk,dv", [
-    ([1, 2, 63, 64, 65, 128], "random", "f32", 32, 48),
-    ([1, 2, 63, 64], "random", "bf16", 128, 128),
-    ([64, 0, 17, 0, 64], "chain", "bf16", 128, 128),
-    ([5, 0, 3], "star", "f32", 16, 16),
-    ([128, 100], "4ary", "bf16", 64, 128),
-    ([40, 33, 64], "random", "bf16", 128, 128),
+@pytest.mark.parametrize("sizes,shape,dtype,dk,dv,max_depth", [
+    ([1, 2, 63, 64, 65, 128], "random", "f32", 32, 48, 9),
+    ([1, 2, 63, 64], "random", "bf16", 128, 128, 9),
+    ([64, 0, 17, 0, 64], "chain", "bf16", 128, 128, 127),
+    ([32, 20, 5, 1], "chain", "bf16", 128, 128, 31),
+    ([64, 7], "star", "bf16", 128, 128, 1),
+    ([64, 50, 21], "4ary", "bf16", 128, 128, 3),
+    ([5, 0, 3], "star", "f32", 16, 16, 1),
+    ([128, 100], "4ary", "bf16", 64, 128, 3),
+    ([40, 33, 64], "random", "bf16", 128, 128, 12),
+    ([64] * 20, "random", "bf16", 128, 128, 30),
 ])
-def test_ragged_and_edge_shapes(sizes, shape, dtype, dk, dv):
+def test_ragged_and_edge_shapes(sizes, shape, dtype, dk, dv, max_depth):
     b = I.random_batch(seed=sum(sizes) + dk, B=len(sizes), H=3, dk=dk, dv=dv, sizes=sizes,
-                       max_depth=127 if shape != "random" else 9, dtype=dtype, sigma=0.05,
-                       accept="uniform", shape=shape)
+                       max_depth=max_depth, dtype=dtype, sigma=0.05, accept="uniform",
+                       shape=shape)
     _check(b, _run(b), TOL[dtype])
 
 
