@@ -236,7 +236,7 @@ def main(argv=None):
     tc_used = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
                and batch.dv == 128 and batch.max_T <= 64
                and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
-                                       torch.bfloat16, flags) == 0)
+                                       batch.max_depth, torch.bfloat16, flags) == 0)
     launches_per_step = 1 + (1 if tc_used else 2) + 1
 
     def step(i, ev=None):

@@ -63,7 +63,7 @@ def lib() -> ctypes.CDLL:
             L.bole_status_string.restype = ctypes.c_char_p
             L.bole_version.argtypes = []
             L.bole_version.restype = I
-            L.bole_workspace_size.argtypes = [I, I, I, I, I, I, U]
+            L.bole_workspace_size.argtypes = [I, I, I, I, I, I, I, U]
             L.bole_workspace_size.restype = S
             L.bole_pack_forest.argtypes = [P, P, I, I, I, P, P, P, P, P]
             L.bole_pack_forest.restype = I
@@ -122,10 +122,10 @@ def check_status(status: torch.Tensor, what: str = "device status") -> None:
         raise BoleError(st[0], f"{what} (request {st[1]}, node {st[2]}, detail {st[3]})")
 
 
-def workspace_size(B: int, H: int, dk: int, dv: int, max_T: int, dtype=torch.bfloat16,
-                   flags: int = 0) -> int:
+def workspace_size(B: int, H: int, dk: int, dv: int, max_T: int, max_depth: int,
+                   dtype=torch.bfloat16, flags: int = 0) -> int:
     code = BF16 if dtype == torch.bfloat16 else F32
-    return int(lib().bole_workspace_size(B, H, dk, dv, max_T, code, flags))
+    return int(lib().bole_workspace_size(B, H, dk, dv, max_T, max_depth, code, flags))
 
 
 def pack_forest(offsets: torch.Tensor, parent: torch.Tensor, max_depth: int, *,
@@ -162,7 +162,7 @@ def tree_verify(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_de
     U = torch.empty((N, H, dv), dtype=torch.float32, device=dev) if U is None else U
     logP = torch.empty((N, H), dtype=torch.float32, device=dev) if logP is None else logP
     if workspace is None:
-        nbytes = lib().bole_workspace_size(B, H, dk, dv, int(max_T), code, flags)
+        nbytes = lib().bole_workspace_size(B, H, dk, dv, int(max_T), int(max_depth), code, flags)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)

@@ -42,15 +42,16 @@ const char *bole_status_string(int status)
 
 int bole_version(void) { return 100; }
 
-size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, bole_dtype qkv_dtype,
-                           unsigned flags)
+size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_depth,
+                           bole_dtype qkv_dtype, unsigned flags)
 {
     if (B < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || max_T < 1 ||
-        max_T > BOLE_MAX_TREE_NODES || !valid_dtype(qkv_dtype))
+        max_T > BOLE_MAX_TREE_NODES || max_depth < 0 || max_depth > BOLE_MAX_TREE_NODES - 1 ||
+        !valid_dtype(qkv_dtype))
         return 0;
     VerifyArgs a = {};
     a.dtype = qkv_dtype;
-    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T; a.max_depth = max_depth;
     if (use_tc_verify(a, flags)) return 0;
     return simt_workspace_bytes(B, H, max_T);
 }

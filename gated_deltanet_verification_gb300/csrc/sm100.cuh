@@ -139,6 +139,17 @@ __device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, ui
                  : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 operands here), one CTA.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -147,12 +158,23 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// Instruction descriptors (fp32 accumulator).  Measured on sm_103a: kind::tf32
+// reads both operands K-major only (an MN-major tf32 operand yields zeros);
+// kind::f16 accepts an MN-major B.
 // Instruction descriptor, kind::tf32, fp32 accumulator.
 //   [4,6) D format (1 = f32)   [7,10) A format (2 = tf32)   [10,13) B format
 //   [15] A MN-major   [16] B MN-major   [17,23) N >> 3   [24,29) M >> 4
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn_major, bool b_mn_major)
 {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
@@ -175,6 +197,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col_f32)
 {
     return (uint32_t)row * 128u + ((((uint32_t)col_f32 >> 2) ^ ((uint32_t)row & 7u)) << 4) +
            (((uint32_t)col_f32 & 3u) << 2);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a
+// 128B-swizzled tile (any element type).
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk)
+{
+    return (uint32_t)row * 128u + ((((uint32_t)chunk) ^ ((uint32_t)row & 7u)) << 4);
 }
 
 // TMEM loads / stores, 32 lanes x 32 bits, 32 consecutive columns per thread.

@@ -4,19 +4,20 @@
 // Verification, one CTA per (request, head), trees of up to 64 nodes:
 //   1. TMA streams the head's S_pre (128 x 128 fp32, 128B-swizzled, four
 //      32-column boxes) into shared memory while the CTA stages [Q;K] of the
-//      tree as one 128 x 128 tf32 operand (rows 0..63 = q, 64..127 = k).
-//   2. tcgen05 products into tensor memory: the Gram [Q;K] K^T (exact: bf16
-//      products in tf32, fp32 accumulation) and the state products
-//      [Q;K] S_pre (tf32, fp32 accumulation).
+//      tree as one 128 x 128 bf16 operand (rows 0..63 = q, 64..127 = k).
+//   2. S_pre is split exactly into bf16 S_hi + S_lo (S - S_hi rounds to bf16
+//      with ~2^-18 relative residue), and tcgen05 computes in tensor memory the
+//      Gram [Q;K] K^T and the state products [Q;K] (S_hi + S_lo), all with bf16
+//      products (exact) and fp32 accumulation.
 //   3. From the Gram the CTA forms the ancestor-masked factors
 //      G_ij = beta_i (P_i/P_j) k_i.k_j and C_ij = (P_i/P_j) q_i.k_j (Lemma 2,
 //      Lemma 1), stored compactly by ancestor depth, and runs the d-step
 //      Neumann recurrence Z <- -G Z, W += Z (Eq. (8)) on the identity, which
 //      yields W = (I+G)^{-1} (Lemma 3); M = C W follows.  All on chip.
 //   4. Epilogue of the state products: B0 = D_P Q S_pre stays in tensor
-//      memory, R = D_beta (V - D_P K S_pre) goes to shared memory.
-//   5. One more tcgen05 product [M; W] R accumulates M R onto B0 (giving O)
-//      and writes W R (= U) in the other 64 rows.
+//      memory, R = D_beta (V - D_P K S_pre) goes to shared memory (as R^T).
+//   5. One more tcgen05 product (tf32) [M; W] R accumulates M R onto B0
+//      (giving O) and writes W R (= U) in the other 64 rows.
 // Deviation from the pages' kernel: the Neumann recurrence runs on the
 // T x T identity instead of on each value tile's R.  The tree factor W does
 // not depend on the value columns, so the d dependent steps stay small and
@@ -45,11 +46,13 @@ constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 200 ms bound on any device wait
 
 // ---- verification shared-memory plan (bytes from a 1024-aligned base) ----
-constexpr int OFF_S = 0;                      // S_pre tile: 4 x [128 rows x 128 B]
-constexpr int OFF_A1 = OFF_S + 65536;         // [Q;K] tf32, K-major, 4 K-atoms x 16 KB
-constexpr int OFF_A2 = OFF_A1;                // [M;W] tf32, K-major, 2 K-atoms (after MMA1)
-constexpr int OFF_B2 = OFF_A1 + 32768;        // R tf32, MN-major, 4 N-atoms x 8 KB
-constexpr int OFF_G = OFF_A1 + 65536;         // compact G  [64][33] f32
+constexpr int OFF_ST = 0;                     // S_pre fp32 staging: 4 x [128 rows x 128 B]
+constexpr int OFF_A2 = OFF_ST;                // [M;W] tf32, K-major, 2 K-atoms (after the split)
+constexpr int OFF_B2 = OFF_ST + 32768;        // R^T tf32, K-major, 2 K-atoms
+constexpr int OFF_SHI = OFF_ST + 65536;       // S_hi bf16, MN-major, 2 N-atoms x 16 KB
+constexpr int OFF_SLO = OFF_SHI + 32768;      // S_lo bf16
+constexpr int OFF_A1 = OFF_SLO + 32768;       // [Q;K] bf16, K-major, 2 K-atoms x 16 KB
+constexpr int OFF_G = OFF_A1 + 32768;         // compact G  [64][33] f32
 constexpr int OFF_C = OFF_G + kT * kLd * 4;   // compact C
 constexpr int OFF_ZA = OFF_C + kT * kLd * 4;  // Neumann iterates
 constexpr int OFF_ZB = OFF_ZA + kT * kLd * 4;
@@ -65,9 +68,11 @@ constexpr int OFF_BAR = OFF_MASK + kT * 8;    // 4 mbarriers
 constexpr int OFF_TSLOT = OFF_BAR + 4 * 8;
 constexpr int OFF_FLAG = OFF_TSLOT + 4;
 constexpr int VERIFY_SMEM = OFF_FLAG + 16 + 1024; // + alignment slack
+static_assert(VERIFY_SMEM <= 227 * 1024, "verification shared memory");
 
-constexpr uint32_t IDESC_GRAM = idesc_tf32(128, 64, false, false);
-constexpr uint32_t IDESC_NN = idesc_tf32(128, 128, false, true); // B MN-major (N contiguous)
+constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
+constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
+constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
@@ -97,7 +102,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    float *sS = reinterpret_cast<float *>(sm + OFF_S);
+    float *sSt = reinterpret_cast<float *>(sm + OFF_ST);
+    uint8_t *sHi = sm + OFF_SHI;
+    uint8_t *sLo = sm + OFF_SLO;
     uint8_t *sA1 = sm + OFF_A1;
     uint8_t *sA2 = sm + OFF_A2;
     uint8_t *sB2 = sm + OFF_B2;
@@ -151,12 +158,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const uint32_t tmem = *tslot;
     if (tid == 0) {
         prefetch_tensormap(&tmS);
-        mbar_arrive_expect_tx(&bar[0], 4 * 128 * 128);
+        mbar_arrive_expect_tx(&bar[0], 4 * 32 * 128 * 4);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tma_load_2d(sS + c * 4096, &tmS, &bar[0], 32 * c, unit * kD);
+        for (int c = 0; c < 4; ++c) tma_load_2d(sSt + c * 4096, &tmS, &bar[0], 32 * c, unit * kD);
     }
 
-    // ---- topology and cumulative decay (Lemma 1) ----
+    // ---- topology and gates ----
     if (tid < kT) {
         const int i = tid;
         if (i < T) {
@@ -175,47 +182,33 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
             up[i] = -1;
         }
     }
-    // [Q;K] -> tf32 K-major operand (zeros beyond the tree)
+    // [Q;K] -> bf16 K-major operand (two 64-element K-atoms; zeros beyond the tree)
     for (int item = tid; item < 128 * 16; item += kThreads) {
         const int m = item >> 4, g = item & 15;
         const int node = m & 63;
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (node < T) {
-            const __nv_bfloat16 *src = ((m < 64) ? q : k) + ((size_t)(o + node) * H + h) * kD + g * 8;
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(src), f);
-        }
-        uint8_t *dst = sA1 + (g >> 2) * 16384;
-        const int col = (g & 3) * 8;
-        *reinterpret_cast<float4 *>(dst + sw128_offset(m, col)) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4 *>(dst + sw128_offset(m, col + 4)) = make_float4(f[4], f[5], f[6], f[7]);
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (node < T)
+            val = *reinterpret_cast<const uint4 *>(((m < 64) ? q : k) +
+                                                   ((size_t)(o + node) * H + h) * kD + g * 8);
+        *reinterpret_cast<uint4 *>(sA1 + (g >> 3) * 16384 + sw128_chunk(m, g & 7)) = val;
     }
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- MMA 1: Gram and state products (one elected thread) ----
+    // ---- MMA 1a: Gram [Q;K] K^T (one elected thread) ----
+    const uint32_t a1 = smem_addr(sA1);
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t a1 = smem_addr(sA1);
-        for (int kk = 0; kk < 16; ++kk) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_tf32_ss(tmem + 128, sdesc_sw128(a1 + off, 16, 1024),
+            mma_bf16_ss(tmem + 128, sdesc_sw128(a1 + off, 16, 1024),
                         sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
         }
         mma_commit(&bar[1]);
-        if (!mbar_wait(&bar[0], 0, kWaitNs)) {
-            report(st, BOLE_ERR_TIMEOUT, b, -1, 1);
-            *flag = 1;
-        }
-        const uint32_t s0 = smem_addr(sS);
-        for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_tf32_ss(tmem, sdesc_sw128(a1 + off, 16, 1024),
-                        sdesc_sw128(s0 + kk * 1024, 16384, 1024), IDESC_NN, kk > 0);
-        }
-        mma_commit(&bar[2]);
     }
 
-    // pointer jumping along parent links while the tensor core works
+    // cumulative decay by pointer jumping along parent links (Lemma 1)
     for (int round = 0; round < 6; ++round) {
         float nl = 0.f;
         int nu = -1;
@@ -254,7 +247,46 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         Za[i * kLd + t] = val;
         Wc[i * kLd + t] = val;
     }
+
+    // ---- S_pre = S_hi + S_lo, both bf16, MN-major (64-column atoms) ----
+    if (!mbar_wait(&bar[0], 0, kWaitNs)) {
+        report(st, BOLE_ERR_TIMEOUT, b, -1, 1);
+        *flag = 1;
+    }
+    for (int item = tid; item < 128 * 16; item += kThreads) {
+        const int r = item >> 4, c8 = item & 15; // row r, columns 8*c8 .. 8*c8+7
+        const uint8_t *box = reinterpret_cast<const uint8_t *>(sSt) + (c8 >> 2) * 16384;
+        const float4 x0 = *reinterpret_cast<const float4 *>(box + sw128_chunk(r, (c8 & 3) * 2));
+        const float4 x1 = *reinterpret_cast<const float4 *>(box + sw128_chunk(r, (c8 & 3) * 2 + 1));
+        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        __nv_bfloat162 hi2[4], lo2[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * t]);
+            const __nv_bfloat16 h1 = __float2bfloat16_rn(xs[2 * t + 1]);
+            hi2[t] = __halves2bfloat162(h0, h1);
+            lo2[t] = __floats2bfloat162_rn(xs[2 * t] - __bfloat162float(h0),
+                                           xs[2 * t + 1] - __bfloat162float(h1));
+        }
+        const uint32_t off = (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7);
+        *reinterpret_cast<uint4 *>(sHi + off) = *reinterpret_cast<const uint4 *>(hi2);
+        *reinterpret_cast<uint4 *>(sLo + off) = *reinterpret_cast<const uint4 *>(lo2);
+    }
+    fence_proxy_async_smem();
     __syncthreads();
+
+    // ---- MMA 1b: state products [Q;K] (S_hi + S_lo) ----
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t shi = smem_addr(sHi), slo = smem_addr(sLo);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sdesc_sw128(a1 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tmem, ad, sdesc_sw128(shi + kk * 2048, 16384, 1024), IDESC_STATE, kk > 0);
+            mma_bf16_ss(tmem, ad, sdesc_sw128(slo + kk * 2048, 16384, 1024), IDESC_STATE, 1);
+        }
+        mma_commit(&bar[2]);
+    }
 
     // ---- Gram epilogue: compact G and C (Lemma 2 / Lemma 1 read-out) ----
     const int rowgrp = warp & 3, half = warp >> 2;
@@ -305,7 +337,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         }
     }
 
-    // ---- state epilogue: B0 = P Q S_pre in place; R = beta (v - P K S_pre) ----
+    // ---- state epilogue: B0 = P Q S_pre in place; R^T = (beta (v - P K S_pre))^T ----
     if (!mbar_wait(&bar[2], 0, kWaitNs)) {
         report(st, BOLE_ERR_TIMEOUT, b, -1, 3);
         *flag = 1;
@@ -336,22 +368,15 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
 #pragma unroll
                         for (int t = 0; t < 8; ++t) vv[u * 8 + t] = f[t];
                     }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) vv[t] = 0.f;
                 }
-                uint8_t *dst = sB2 + (col0 >> 5) * 8192;
+                // R^T: row = value column c, K index = node i (tf32, K-major)
+                uint8_t *dst = sB2 + (i >> 5) * 16384;
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    float4 r4;
-                    r4.x = (i < T) ? bt * (vv[4 * c4 + 0] - p * x[4 * c4 + 0]) : 0.f;
-                    r4.y = (i < T) ? bt * (vv[4 * c4 + 1] - p * x[4 * c4 + 1]) : 0.f;
-                    r4.z = (i < T) ? bt * (vv[4 * c4 + 2] - p * x[4 * c4 + 2]) : 0.f;
-                    r4.w = (i < T) ? bt * (vv[4 * c4 + 3] - p * x[4 * c4 + 3]) : 0.f;
-                    *reinterpret_cast<float4 *>(dst + sw128_offset(i, 4 * c4)) = r4;
+                for (int t = 0; t < 32; ++t) {
+                    const float r = (i < T) ? bt * (vv[t] - p * x[t]) : 0.f;
+                    *reinterpret_cast<float *>(dst + sw128_offset(col0 + t, i & 31)) = r;
+                    x[t] = 0.f;
                 }
-#pragma unroll
-                for (int t = 0; t < 32; ++t) x[t] = 0.f;
                 tmem_st32(tmem + lane_base + col0, x);
             }
         }
@@ -385,13 +410,15 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA 2: [M; W] R accumulated onto [B0; 0] ----
+    // ---- MMA 2 (tf32): [M; W] R accumulated onto [B0; 0] ----
     if (tid == 0) {
         tc_fence_after();
         const uint32_t a2 = smem_addr(sA2), b2 = smem_addr(sB2);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            mma_tf32_ss(tmem, sdesc_sw128(a2 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                        sdesc_sw128(b2 + kk * 1024, 8192, 1024), IDESC_NN, 1);
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_tf32_ss(tmem, sdesc_sw128(a2 + off, 16, 1024), sdesc_sw128(b2 + off, 16, 1024),
+                        IDESC_TF32, 1);
         }
         mma_commit(&bar[3]);
     }
@@ -432,8 +459,6 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     }
     tc_fence_before();
     __syncthreads();
-    if (*(volatile int *)flag != 0 && tid == 0) mbar_wait(&bar[0], 0, kWaitNs); // drain the TMA
-    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
@@ -442,7 +467,7 @@ constexpr int kCommitThreads = 128;
 constexpr int kChunk = 32; // path nodes per MMA K chunk
 constexpr int CO_S = 0;                       // S tile, 64 KB
 constexpr int CO_A = 65536;                   // (D_a K_a)^T chunk: 128 rows x 32 tf32, 16 KB
-constexpr int CO_B = CO_A + 16384;            // U_a chunk: 32 K-rows x 128 tf32 (4 N-atoms)
+constexpr int CO_B = CO_A + 16384;            // U_a^T chunk: 128 rows x 32 tf32, 16 KB
 constexpr int CO_PATH = CO_B + 16384;         // int[128]
 constexpr int CO_COEF = CO_PATH + 512;        // float[128]
 constexpr int CO_BAR = CO_COEF + 512;         // 2 mbarriers
@@ -538,14 +563,20 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                 *reinterpret_cast<float4 *>(sA + sw128_offset(r, 4 * c4)) =
                     make_float4(av[4 * c4], av[4 * c4 + 1], av[4 * c4 + 2], av[4 * c4 + 3]);
         }
-        // B[t][c] = u_{j_t}[c], MN-major: 4 N-atoms of 32 columns, 4 KB each
-        for (int item = tid; item < kChunk * 32; item += kCommitThreads) {
-            const int tt = item >> 5, c4 = item & 31;
-            const int t = ch * kChunk + tt;
-            float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < L)
-                u4 = *reinterpret_cast<const float4 *>(U + ((size_t)(o + path[t]) * H + h) * kD + 4 * c4);
-            *reinterpret_cast<float4 *>(sB + (c4 >> 3) * 4096 + sw128_offset(tt, (4 * c4) & 31)) = u4;
+        // B^T[c][t] = u_{j_t}[c] (row c = tid), K-major, one 128-byte atom
+        {
+            const int c = tid;
+#pragma unroll
+            for (int t4 = 0; t4 < kChunk / 4; ++t4) {
+                float uv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = ch * kChunk + 4 * t4 + e;
+                    uv[e] = (t < L) ? U[((size_t)(o + path[t]) * H + h) * kD + c] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(sB + sw128_offset(c, 4 * t4)) =
+                    make_float4(uv[0], uv[1], uv[2], uv[3]);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -555,7 +586,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
 #pragma unroll
             for (int kk = 0; kk < kChunk / 8; ++kk)
                 mma_tf32_ss(tmem, sdesc_sw128(sa + kk * 32, 16, 1024),
-                            sdesc_sw128(sb + kk * 1024, 4096, 1024), IDESC_NN, (ch > 0 || kk > 0));
+                            sdesc_sw128(sb + kk * 32, 16, 1024), IDESC_TF32, (ch > 0 || kk > 0));
             mma_commit(&bar[1]);
         }
         if (!mbar_wait(&bar[1], ch & 1, kWaitNs)) {
@@ -643,7 +674,7 @@ cudaError_t make_state_map(CUtensorMap *map, const float *S, int units)
 bool tc_verify_supported(const VerifyArgs &a)
 {
     return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && a.max_T <= kT &&
-           a.max_depth < kSlots && encode_fn() != nullptr;
+           a.max_depth < kSlots;
 }
 
 cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
@@ -665,7 +696,7 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
 
 bool tc_commit_supported(const CommitArgs &a)
 {
-    return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && encode_fn() != nullptr;
+    return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD;
 }
 
 cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s)

@@ -61,7 +61,7 @@ class RoundBuffers:
 
 def alloc_round(db: DeviceBatch, flags: int = 0) -> RoundBuffers:
     dev = db.q.device
-    ws = bole.workspace_size(db.B, db.H, db.dk, db.dv, db.max_T, db.q.dtype, flags)
+    ws = bole.workspace_size(db.B, db.H, db.dk, db.dv, db.max_T, db.max_depth, db.q.dtype, flags)
     return RoundBuffers(
         depth=torch.empty(db.N, dtype=torch.int32, device=dev),
         anc=torch.empty((db.N, 4), dtype=torch.int32, device=dev),

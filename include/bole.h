@@ -91,11 +91,12 @@ int bole_version(void);
 
 /* Bytes of device workspace bole_tree_verify needs for these sizes (0 when
  * the chosen kernels keep every intermediate on chip).  max_T bounds every
- * tree's node count (1..128).  The workspace holds the short-lived tree
+ * tree's node count (1..128) and max_depth every tree's depth (0..127); pass
+ * the same values, dtype and flags as to bole_tree_verify.  The workspace holds the short-lived tree
  * factors (G, C) of one call -- the "verification scratch" of the pages'
  * state lifecycle (Section IV-D) -- and may be reused by the next call. */
-size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, bole_dtype qkv_dtype,
-                           unsigned flags);
+size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_depth,
+                           bole_dtype qkv_dtype, unsigned flags);
 
 /* Round-level topology step (Section IV-C; forest packing, review Section 3).
  * Validates the packed forest and derives, per node, its depth and its
@@ -122,8 +123,9 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * the caller's k buffer are the factors commit needs; keep them alive until
  * bole_commit.  workspace: device buffer of at least
  * bole_workspace_size(...) bytes (NULL allowed when that size is 0).
- * Kernel choice: bf16 inputs with dk = dv = 128 and max_T <= 64 run the
- * TMA + tcgen05 tensor-core kernel (tf32 state products, fp32 accumulation);
+ * Kernel choice: bf16 inputs with dk = dv = 128, max_T <= 64 and
+ * max_depth <= 31 run the TMA + tcgen05 tensor-core kernel (state products on
+ * an exact bf16 hi/lo split of S_pre, fp32 accumulation);
  * everything else, or flags & BOLE_FLAG_FORCE_SIMT, runs the FP32 CUDA-core
  * kernels (producer of G, C into the workspace + value-tiled solve). */
 bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, const void *v,
