@@ -124,7 +124,7 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * bole_commit.  workspace: device buffer of at least
  * bole_workspace_size(...) bytes (NULL allowed when that size is 0).
  * Kernel choice: bf16 inputs with dk = dv = 128, max_T <= 64 and
- * max_depth <= 31 run the TMA + tcgen05 tensor-core kernel (state products on
+ * max_depth <= 15 run the TMA + tcgen05 tensor-core kernel (state products on
  * an exact bf16 hi/lo split of S_pre, fp32 accumulation);
  * everything else, or flags & BOLE_FLAG_FORCE_SIMT, runs the FP32 CUDA-core
  * kernels (producer of G, C into the workspace + value-tiled solve). */

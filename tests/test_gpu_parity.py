@@ -92,12 +92,14 @@ def test_fp32_inputs_parity(cfg):
     ([1, 2, 63, 64], "random", "bf16", 128, 128, 9),
     ([64, 0, 17, 0, 64], "chain", "bf16", 128, 128, 127),
     ([32, 20, 5, 1], "chain", "bf16", 128, 128, 31),
+    ([16, 9, 12], "chain", "bf16", 128, 128, 15),
     ([64, 7], "star", "bf16", 128, 128, 1),
     ([64, 50, 21], "4ary", "bf16", 128, 128, 3),
     ([5, 0, 3], "star", "f32", 16, 16, 1),
     ([128, 100], "4ary", "bf16", 64, 128, 3),
     ([40, 33, 64], "random", "bf16", 128, 128, 12),
     ([64] * 20, "random", "bf16", 128, 128, 30),
+    ([64] * 20, "random", "bf16", 128, 128, 15),
 ])
 def test_ragged_and_edge_shapes(sizes, shape, dtype, dk, dv, max_depth):
     b = I.random_batch(seed=sum(sizes) + dk, B=len(sizes), H=3, dk=dk, dv=dv, sizes=sizes,
