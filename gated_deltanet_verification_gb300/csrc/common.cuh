@@ -11,8 +11,8 @@ namespace bole {
 
 constexpr int kMaxTree = BOLE_MAX_TREE_NODES;
 
-// First fault wins: {code, request, node, detail}.
-__device__ __forceinline__ void report(int32_t *st, int code, int b, int i, int aux)
+// First fault wins: {code, request, node, detail}.  Out of line (cold path).
+static __device__ __noinline__ void report(int32_t *st, int code, int b, int i, int aux)
 {
     if (atomicCAS(st, 0, code) == 0) {
         st[1] = b;

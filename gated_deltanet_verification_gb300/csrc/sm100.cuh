@@ -54,7 +54,8 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Bounded wait on an mbarrier phase: false once `limit_ns` has passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+// Kept out of line: it is called from many places and is never hot.
+static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();

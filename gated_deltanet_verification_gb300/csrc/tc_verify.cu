@@ -358,22 +358,33 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
         tc_fence_after();
         {
+            // stage the Gram rows in the S buffer (free once the state products are
+            // done): [128 rows][64 + 1] f32, rows 0..63 q_i.k_j, rows 64..127 k_i.k_j
+            float *gram = reinterpret_cast<float *>(sbuf);
             float g[32];
             tmem_ld32(tmem + lane_base + 128 + half * 32, g);
-            const int i = m & 63;
-            if (i < T) {
-                uint32_t bits = (uint32_t)(msk[i] >> (half * 32));
-                const bool isG = m >= 64;
-                if (isG && (i >> 5) == half) bits &= ~(1u << (i & 31)); // strict ancestors
-                const float Li = Ls[i];
-                const float scale = isG ? Bs[i] : 1.f;
-                float *dst = (isG ? Gc : Cc) + i * kLd;
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if ((bits >> t) & 1u) {
-                        const int j = half * 32 + t;
-                        dst[Ds[j]] = scale * expf(Li - Ls[j]) * g[t];
-                    }
+            for (int t = 0; t < 32; ++t) gram[m * 65 + half * 32 + t] = g[t];
+        }
+        compute_sync();
+        // one thread per (row, ancestor): C for rows 0..63, G (strict ancestors) for 64..127
+        {
+            const int r = tid >> 1, part = tid & 1; // two threads per operand row
+            const int i = r & 63;
+            if (i < T) {
+                const bool isG = r >= 64;
+                uint64_t bits = msk[i];
+                if (isG) bits &= ~(1ull << i);
+                const float *grow = reinterpret_cast<const float *>(sbuf) + r * 65;
+                float *dst = (isG ? Gc : Cc) + i * kLd;
+                const float Li = Ls[i], scale = isG ? Bs[i] : 1.f;
+                int n = 0;
+#pragma unroll 1
+                while (bits) {
+                    const int j = __ffsll((long long)bits) - 1;
+                    bits &= bits - 1;
+                    if ((n++ & 1) == part) dst[Ds[j]] = scale * __expf(Li - Ls[j]) * grow[j];
+                }
             }
         }
         // Neumann start Z^(0) = W = identity (the self entry sits at slot depth(i))
