@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
             L.bole_tree_verify.argtypes = [P, P, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I,
                                            I, P, P, P, P, S, P, U, P]
             L.bole_tree_verify.restype = I
+            L.bole_tree_verify_noalloc.argtypes = [P, P, P, P, I, P, P, P, P, P, P, P, I, I, I,
+                                                   I, I, I, I, P, P, P, P, P]
+            L.bole_tree_verify_noalloc.restype = I
             L.bole_commit.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I, P, U, P]
             L.bole_commit.restype = I
             _lib = L
@@ -174,6 +177,35 @@ def tree_verify(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_de
     return O, U, logP
 
 
+NOALLOC_MAX_FACTOR_ELEMS = 1 << 20
+
+
+def tree_verify_noalloc(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_depth,
+                        max_T: int, max_depth: int, *, O=None, U=None, logP=None, status=None,
+                        stream=None):
+    """bole_tree_verify_noalloc: the CUDA-core verification with library-owned
+    scratch, for callers that cannot allocate device memory when they verify.
+    Returns (O, U, logP); the caller may pass preallocated outputs."""
+    B = offsets.numel() - 1
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    code = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    O = torch.empty((N, H, dv), dtype=q.dtype, device=dev) if O is None else O
+    U = torch.empty((N, H, dv), dtype=torch.float32, device=dev) if U is None else U
+    logP = torch.empty((N, H), dtype=torch.float32, device=dev) if logP is None else logP
+    if status is None:
+        status = new_status(dev)
+    _check(lib().bole_tree_verify_noalloc(
+        _ptr(S_pre), _ptr(q), _ptr(k), _ptr(v), code, _ptr(gamma), _ptr(beta), _ptr(offsets),
+        _ptr(parent), _ptr(depth), _ptr(anc), _ptr(req_depth), B, H, dk, dv, N, int(max_T),
+        int(max_depth), _ptr(O), _ptr(U), _ptr(logP), _ptr(status), _stream(stream)),
+        "bole_tree_verify_noalloc")
+    return O, U, logP
+
+
 def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int = 0,
            stream=None) -> torch.Tensor:
     """bole_commit: overwrites S in place with the accepted paths' states; returns S."""
@@ -189,6 +221,6 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
 
 
 __all__ = ["lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
-           "tree_verify", "commit", "new_status", "check_status", "BoleError", "OK",
+           "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
            "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT"]

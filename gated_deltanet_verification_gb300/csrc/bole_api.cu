@@ -113,6 +113,43 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     return from_cuda(tc ? launch_tc_verify(a, s) : launch_simt_verify(a, s));
 }
 
+bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const void *k,
+                                     const void *v, bole_dtype qkv_dtype, const float *gamma,
+                                     const float *beta, const int32_t *offsets,
+                                     const int32_t *parent, const int32_t *depth,
+                                     const uint32_t *anc, const int32_t *req_depth, int B, int H,
+                                     int dk, int dv, int N, int max_T, int max_depth, void *O,
+                                     float *U, float *logP, int32_t *dev_status,
+                                     bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(qkv_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if (max_T < 1 || max_T > BOLE_MAX_TREE_NODES || max_depth < 0 ||
+        max_depth > BOLE_MAX_TREE_NODES - 1)
+        return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * max_T) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && (!S_pre || !req_depth))) return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !gamma || !beta || !parent || !depth || !anc || !O || !U ||
+                  !logP))
+        return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {S_pre, q, k, v, O, U, anc, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {gamma, beta, offsets, parent, depth, req_depth, logP};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+    if (!simt_noalloc_fits(B, H, max_T)) return BOLE_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0) return BOLE_OK;
+
+    VerifyArgs a;
+    a.S_pre = S_pre; a.q = q; a.k = k; a.v = v; a.dtype = qkv_dtype;
+    a.gamma = gamma; a.beta = beta;
+    a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
+    a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.st = dev_status;
+    return from_cuda(launch_simt_verify_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
                         const float *logP, const int32_t *offsets, const int32_t *parent,
                         const int32_t *accepted, int B, int H, int dk, int dv, int N,

@@ -73,6 +73,8 @@ struct CommitArgs {
 
 size_t simt_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_simt_verify(const VerifyArgs &a, cudaStream_t s);
+bool simt_noalloc_fits(int B, int H, int max_T);
+cudaError_t launch_simt_verify_noalloc(const VerifyArgs &a, cudaStream_t s);
 cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
 
 bool tc_verify_supported(const VerifyArgs &a);

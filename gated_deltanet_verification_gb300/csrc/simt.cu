@@ -7,6 +7,8 @@
 // and read out O = B0 + C U (Eq. (7)).  Every product is an FP32 FMA, so the
 // path meets float32 accuracy; it serves float32 inputs and any shape the
 // tensor-core kernels do not cover.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace bole {
@@ -355,6 +357,59 @@ cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s)
 {
     if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
     return a.dtype == BOLE_BF16 ? commit_typed<__nv_bfloat16>(a, s) : commit_typed<float>(a, s);
+}
+
+// ---- verification without any allocation ----
+// Some callers cannot allocate device memory when they verify: hosts that hand
+// the library only tensors they already own and no allocator, and serving
+// loops that forbid allocation on the hot path because an allocation can
+// synchronise the device.  For them the G, C scratch of the CUDA-core path
+// lives in this fixed, library-owned array (8 MiB, held by every GPU that
+// loads the library until the process exits).  Every call shares it and it
+// keeps the previous call's contents; the producer kernel rewrites every
+// entry the solve kernel reads, so nothing has to start at zero.  Calls whose
+// kernels overlap on the GPU race on the array.
+static __device__ __align__(256) float g_noalloc_scratch[2 * (size_t)BOLE_NOALLOC_MAX_FACTOR_ELEMS];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+} // namespace
+
+// The array's device address on the current device, resolved once per device
+// (host code cannot use the symbol itself: it names a host-side stand-in).
+static cudaError_t noalloc_scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+bool simt_noalloc_fits(int B, int H, int max_T)
+{
+    return (size_t)B * H * max_T * max_T <= (size_t)BOLE_NOALLOC_MAX_FACTOR_ELEMS;
+}
+
+cudaError_t launch_simt_verify_noalloc(const VerifyArgs &a, cudaStream_t s)
+{
+    if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    VerifyArgs b = a;
+    b.ws = scratch;
+    return launch_simt_verify(b, s);
 }
 
 } // namespace bole

@@ -136,6 +136,35 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
                              float *logP, void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, unsigned flags, bole_stream_t stream);
 
+/* Verification that allocates nothing -- the paper has no counterpart; this
+ * entry point exists for callers that cannot allocate device memory when they
+ * verify: hosts that give the library only tensors they already own and no
+ * allocator, and serving loops that forbid allocation on the hot path because
+ * an allocation can synchronise the device.  Same arguments, layouts, results
+ * and device-status behaviour as bole_tree_verify with BOLE_FLAG_FORCE_SIMT
+ * (the FP32 CUDA-core kernels), but the G, C scratch those kernels need lives
+ * in a fixed 8 MiB array owned by the library (every GPU that loads the
+ * library holds it until the process exits); no workspace is passed and
+ * nothing is allocated.
+ *   - Limit: B * H * max_T * max_T <= BOLE_NOALLOC_MAX_FACTOR_ELEMS; larger
+ *     problems return BOLE_ERR_UNSUPPORTED with nothing launched (use
+ *     bole_tree_verify with a caller-allocated workspace instead).
+ *   - The first call on each device resolves the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.  A failure there returns BOLE_ERR_CUDA.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents; calls whose kernels overlap on the GPU (different streams, or
+ *     several host threads) race on it -- order them on one stream. */
+#define BOLE_NOALLOC_MAX_FACTOR_ELEMS (1u << 20)
+bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const void *k,
+                                     const void *v, bole_dtype qkv_dtype, const float *gamma,
+                                     const float *beta, const int32_t *offsets,
+                                     const int32_t *parent, const int32_t *depth,
+                                     const uint32_t *anc, const int32_t *req_depth, int B, int H,
+                                     int dk, int dv, int N, int max_T, int max_depth, void *O,
+                                     float *U, float *logP, int32_t *dev_status,
+                                     bole_stream_t stream);
+
 /* Factorised commit (Eq. (10)): for every request b with accepted[b] = a >= 0
  * (request-local node index) and every head,
  *     S <- P_a S + sum over j on the path root..a of (P_a / P_j) k_j u_j^T
