@@ -48,7 +48,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="bole", choices=["bole", "reference"])
     p.add_argument("--config", type=int, default=2)
@@ -58,6 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--kernel-steps", type=int, default=200,
+                   help="steps of the separate per-kernel timing pass")
     return p.parse_args(argv)
 
 
@@ -100,6 +102,46 @@ def algorithmic(batch):
         flops += H * (4 * T * dk * dv + 4 * T * T * dk + 2 * d * T * T * dv + 2 * T * T * dv)
     flops += int(np.sum(L)) * H * 2 * dk * dv
     return {"pack": topo_pack, "verify": verify, "commit": commit, "verify_flops": flops}
+
+
+def recorded_traffic(kernel: str, config: int):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the capture (or no capture exists)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "gated_deltanet_verification_gb300", "csrc", "tc_verify.cu")
+    try:
+        lines = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+        want = dict((ln[0], ln[1]) for ln in lines if len(ln) == 2)
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != want.get("source_sha256"):
+            return None
+        for ln in lines:
+            if len(ln) == 3 and ln[0] == kernel and int(ln[1]) == config:
+                return int(ln[2])
+    except Exception:
+        return None
+    return None
+
+
+def rank_seed(config: int, rank: int) -> int:
+    """Each rank verifies its own batch of the same shape (weak scaling)."""
+    return 1000 + config + 7919 * rank
+
+
+def max_over_ranks(value: float, device) -> float:
+    """Slowest rank's value (the job's wall time); identity on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(nodes_per_rank: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job nodes/s: every rank's nodes over the slowest rank's time."""
+    return nodes_per_rank * steps * world / (elapsed_ms / 1e3)
 
 
 def measured_peaks():
@@ -221,7 +263,7 @@ def main(argv=None):
 
     build.build()
     flags = bole.FLAG_FORCE_SIMT if args.force_simt else 0
-    seed = 1000 + args.config + 7919 * rank
+    seed = rank_seed(args.config, rank)
     batch = inputs.config_batch(args.config, seed=seed, shape=args.shape)
     alg = algorithmic(batch)
     step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
@@ -237,7 +279,7 @@ def main(argv=None):
                and batch.dv == 128 and batch.max_T <= 64
                and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
                                        batch.max_depth, torch.bfloat16, flags) == 0)
-    launches_per_step = 1 + (1 if tc_used else 2) + 1
+    launches_per_step = 1 + (1 if tc_used else 2) + 1  # pack, verify (1 or 2 kernels), commit
 
     def step(i, ev=None):
         db, rb = sets[i % n_sets]
@@ -259,32 +301,38 @@ def main(argv=None):
     for _, rb in sets:
         bole.check_status(rb.status, "warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # ---- timed region: K steps, events only at its ends ----
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     start.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i, evs[i])
+        step(args.warmup + i)
     end.record(stream)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     clock_info = clocks.stop()
     for _, rb in sets:
         bole.check_status(rb.status, "timed steps")
     elapsed_ms = start.elapsed_time(end)
+
+    # ---- separate pass: per-kernel durations from events around each launch ----
+    ks = max(1, min(args.kernel_steps, args.steps))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ks)]
+    for i in range(ks):
+        step(args.warmup + args.steps + i, evs[i])
+    torch.cuda.synchronize()
     per_kernel = {"pack": [], "verify": [], "commit": []}
     for e in evs:
         per_kernel["pack"].append(e[0].elapsed_time(e[1]))
         per_kernel["verify"].append(e[1].elapsed_time(e[2]))
         per_kernel["commit"].append(e[2].elapsed_time(e[3]))
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
 
@@ -296,8 +344,7 @@ def main(argv=None):
 
     hbm, tflops, peak_kind = measured_peaks()
     ms_step = elapsed_ms / args.steps
-    nodes_total = batch.N * args.steps * world
-    value = nodes_total / (elapsed_ms / 1e3)
+    value = job_throughput(batch.N, args.steps, world, elapsed_ms)
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     kern_rf = {}
     for k in ("pack", "verify", "commit"):
@@ -306,9 +353,10 @@ def main(argv=None):
                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
     dominant = max(("verify", "commit"), key=lambda k: avg[k])
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+    traffic = recorded_traffic("tc_" + dominant + "_kernel", args.config) if tc_used else None
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
-                "frac": kern_rf[dominant]["frac"], "traffic": None, "peak_source": peak_kind,
+                "frac": kern_rf[dominant]["frac"], "traffic": traffic, "peak_source": peak_kind,
                 "step_achieved_gbs": round(step_gbs, 1), "step_frac": round(step_gbs / hbm, 4),
                 "verify_plus_commit_frac": round(
                     (alg["verify"] + alg["commit"]) / ((avg["verify"] + avg["commit"]) * 1e-3)
@@ -325,13 +373,15 @@ def main(argv=None):
         "metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "tf32" if tc_used else "f32", "io_dtype": batch.dtype, "data": "synthetic",
+        "dtype": "bf16x2+tf32 (f32 acc)" if tc_used else "f32", "io_dtype": batch.dtype,
+        "data": "synthetic",
         "config": {"workload": inputs.CONFIG_NAMES[args.config]
                    + (f" [{args.shape}]" if args.config == 4 else ""),
                    "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
                    "seed": seed, "kernels": "tcgen05" if tc_used else "cuda-core",
-                   "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)"},
+                   "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
+                   "kernel_timing": f"separate pass of {ks} steps with events per launch"},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
     }
@@ -380,18 +430,17 @@ def run_e2e(args, batch, sets, flags, stream, world):
     end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(batch.N * args.steps * world / (ms / 1e3), 1), "unit": "nodes/s",
+    ms = max_over_ranks(ms, "cuda")
+    return {"value": round(job_throughput(batch.N, args.steps, world, ms), 1), "unit": "nodes/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / args.steps, 5)}
 
 
 def reference_arm(args, world, rank):
-    """The CPU oracle timed on the host cores, same workload and metric."""
+    """The CPU oracle timed on the host cores, same workload and metric.  Each
+    step runs the oracle's verify + commit over a rotating slice of the
+    (request, head) units, sized so the whole run stays within about a minute;
+    nodes/s counts node-heads processed divided by the head count."""
     if rank != 0:
         return 0
     from gated_deltanet_verification_gb300 import inputs
@@ -399,15 +448,32 @@ def reference_arm(args, world, rank):
     import oracle
     oracle.load()
     thr = oracle.default_threads()
-    for _ in range(max(0, min(args.warmup, 1))):
-        oracle.verify(batch, nthreads=thr)
-        oracle.commit(batch, nthreads=thr)
+    units = batch.B * batch.H
+    sizes = np.diff(batch.offsets)
+
+    def run(u0, u1):
+        oracle.verify(batch, nthreads=thr, unit_begin=u0, unit_end=u1)
+        oracle.commit(batch, nthreads=thr, unit_begin=u0, unit_end=u1)
+        return int(sum(sizes[u // batch.H] for u in range(u0, u1)))
+
+    probe_units = min(units, max(1, 2 * thr))
+    t0 = time.perf_counter()
+    run(0, probe_units)
+    t_unit = (time.perf_counter() - t0) / probe_units
+    budget_s = 60.0
+    per_step = int(max(1, min(units, budget_s / max(1, args.steps) / max(t_unit, 1e-9))))
+    for w in range(max(0, min(args.warmup, 2))):
+        run(0, per_step)
+    node_heads, u0 = 0, 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.verify(batch, nthreads=thr)
-        oracle.commit(batch, nthreads=thr)
+        u1 = min(units, u0 + per_step)
+        node_heads += run(u0, u1)
+        u0 = 0 if u1 >= units else u1
     el = time.perf_counter() - t0
-    value = batch.N * args.steps / el
+    value = node_heads / batch.H / el
+    sample = (f"{per_step} of {units} (request, head) units per step, rotating; "
+              f"{node_heads} node-heads in {el:.1f} s")
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "nodes/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -418,8 +484,7 @@ def reference_arm(args, world, rank):
                    "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N},
         "cpu_baseline": {"value": round(value, 1), "unit": "nodes/s", "cores": thr,
-                         "kind": "oracle",
-                         "sample": f"{args.steps} full repetitions of the workload"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "nodes/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -75,7 +75,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_pack.restype = I
     lib.oracle_verify.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, I, I]
     lib.oracle_verify.restype = I
-    lib.oracle_commit.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I]
+    lib.oracle_commit.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, I, I, I]
     lib.oracle_commit.restype = I
     return lib
 
@@ -131,8 +131,10 @@ def verify(batch, nthreads: Optional[int] = None, unit_begin: int = 0, unit_end:
     return O, U, logP
 
 
-def commit(batch, accepted=None, nthreads: Optional[int] = None, lib=None):
-    """Committed state [B,H,dk,dv] float64 after replaying each accepted path."""
+def commit(batch, accepted=None, nthreads: Optional[int] = None, unit_begin: int = 0,
+           unit_end: int = -1, lib=None):
+    """Committed state [B,H,dk,dv] float64 after replaying each accepted path
+    (units outside [unit_begin, unit_end) are left zero)."""
     lib = lib or load()
     b = batch
     acc = _i32(b.accepted if accepted is None else accepted)
@@ -141,8 +143,8 @@ def commit(batch, accepted=None, nthreads: Optional[int] = None, lib=None):
     g, bt = _f64(b.gamma), _f64(b.beta)
     S_new = np.zeros((b.B, b.H, b.dk, b.dv))
     st = lib.oracle_commit(b.B, b.H, b.dk, b.dv, _ptr(offsets), _ptr(parent), _ptr(acc), _ptr(S),
-                           _ptr(k), _ptr(v), _ptr(g), _ptr(bt), _ptr(S_new),
-                           int(nthreads or default_threads()))
+                           _ptr(k), _ptr(v), _ptr(g), _ptr(bt), _ptr(S_new), int(unit_begin),
+                           int(unit_end), int(nthreads or default_threads()))
     if st != OK:
         raise ValueError(f"oracle_commit status {st}")
     return S_new

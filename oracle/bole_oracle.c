@@ -245,7 +245,8 @@ int oracle_verify(int B, int H, int dk, int dv, const int32_t *offsets, const in
 
 int oracle_commit(int B, int H, int dk, int dv, const int32_t *offsets, const int32_t *parent,
                   const int32_t *accepted, const double *S_pre, const double *k, const double *v,
-                  const double *gamma, const double *beta, double *S_new, int nthreads)
+                  const double *gamma, const double *beta, double *S_new, int unit_begin,
+                  int unit_end, int nthreads)
 {
     int s = check_topology(B, offsets, parent);
     if (s != ORACLE_OK) return s;
@@ -259,7 +260,7 @@ int oracle_commit(int B, int H, int dk, int dv, const int32_t *offsets, const in
     J.offsets = offsets; J.parent = parent; J.accepted = accepted;
     J.S_pre = S_pre; J.k = k; J.v = v; J.gamma = gamma; J.beta = beta;
     J.S_new = S_new;
-    J.unit_begin = 0;
-    J.unit_end = B * H;
+    J.unit_begin = unit_begin < 0 ? 0 : unit_begin;
+    J.unit_end = (unit_end < 0 || unit_end > B * H) ? B * H : unit_end;
     return run_threads(&J, commit_worker, nthreads);
 }
