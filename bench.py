@@ -104,9 +104,13 @@ def algorithmic(batch):
     return {"pack": topo_pack, "verify": verify, "commit": commit, "verify_flops": flops}
 
 
-def recorded_traffic(kernel: str, config: int):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the capture (or no capture exists)."""
+VERIFY_KERNELS = ["tc_factor_kernel", "tc_solve_kernel"]
+
+
+def recorded_traffic(kernels, config: int):
+    """DRAM bytes of one call (the sum over its kernels' launches) from the
+    committed ncu summary, or None when the kernel source changed since the
+    capture (or a kernel has no capture)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "gated_deltanet_verification_gb300", "csrc", "tc_verify.cu")
@@ -115,9 +119,9 @@ def recorded_traffic(kernel: str, config: int):
         want = dict((ln[0], ln[1]) for ln in lines if len(ln) == 2)
         if hashlib.sha256(open(src, "rb").read()).hexdigest() != want.get("source_sha256"):
             return None
-        for ln in lines:
-            if len(ln) == 3 and ln[0] == kernel and int(ln[1]) == config:
-                return int(ln[2])
+        got = {ln[0]: int(ln[2]) for ln in lines if len(ln) == 3 and int(ln[1]) == config}
+        if all(k in got for k in kernels):
+            return sum(got[k] for k in kernels)
     except Exception:
         return None
     return None
@@ -279,7 +283,7 @@ def main(argv=None):
                and batch.dv == 128 and batch.max_T <= 64
                and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
                                        batch.max_depth, torch.bfloat16, flags) == 0)
-    launches_per_step = 1 + (1 if tc_used else 2) + 1  # pack, verify (1 or 2 kernels), commit
+    launches_per_step = 1 + 2 + 1  # pack, verify (factor + solve kernels), commit
 
     def step(i, ev=None):
         db, rb = sets[i % n_sets]
@@ -353,7 +357,8 @@ def main(argv=None):
                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
     dominant = max(("verify", "commit"), key=lambda k: avg[k])
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
-    traffic = recorded_traffic("tc_" + dominant + "_kernel", args.config) if tc_used else None
+    traffic = recorded_traffic(VERIFY_KERNELS if dominant == "verify" else ["tc_commit_kernel"],
+                               args.config) if tc_used else None
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": kern_rf[dominant]["frac"], "traffic": traffic, "peak_source": peak_kind,

@@ -52,7 +52,7 @@ size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_dept
     VerifyArgs a = {};
     a.dtype = qkv_dtype;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T; a.max_depth = max_depth;
-    if (use_tc_verify(a, flags)) return 0;
+    if (use_tc_verify(a, flags)) return tc_workspace_bytes(B, H, max_T);
     return simt_workspace_bytes(B, H, max_T);
 }
 
@@ -105,7 +105,7 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.st = dev_status;
 
     const bool tc = use_tc_verify(a, flags);
-    const size_t need = tc ? 0 : simt_workspace_bytes(B, H, max_T);
+    const size_t need = tc ? tc_workspace_bytes(B, H, max_T) : simt_workspace_bytes(B, H, max_T);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return BOLE_ERR_WORKSPACE;
     if (B == 0 || N == 0) return BOLE_OK;

@@ -78,6 +78,7 @@ cudaError_t launch_simt_verify_noalloc(const VerifyArgs &a, cudaStream_t s);
 cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
 
 bool tc_verify_supported(const VerifyArgs &a);
+size_t tc_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s);
 bool tc_commit_supported(const CommitArgs &a);
 cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s);

@@ -6,16 +6,20 @@
 namespace bole {
 namespace {
 
-// One warp per request.  Lanes stride over the request's nodes; each lane
-// walks its node's parent links to the committed root (at most 128 steps,
-// guaranteed to end because every parent index was checked to be smaller).
-__global__ void __launch_bounds__(128) pack_kernel(const int32_t *__restrict__ offsets,
-                                                   const int32_t *__restrict__ parent, int B, int N,
-                                                   int max_depth, int32_t *__restrict__ depth,
-                                                   uint32_t *__restrict__ anc,
-                                                   int32_t *__restrict__ req_depth, int32_t *st)
+// One warp per request.  The request's parent array (at most 128 entries) is
+// staged in shared memory with coalesced loads, validated, and then every lane
+// walks its nodes' parent links there (at most 128 steps, guaranteed to end
+// because every parent index was checked to be smaller); depth = bits - 1.
+constexpr int kPackWarps = 4;
+
+__global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent, int B, int N,
+    int max_depth, int32_t *__restrict__ depth, uint32_t *__restrict__ anc,
+    int32_t *__restrict__ req_depth, int32_t *st)
 {
-    const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    __shared__ int sp[kPackWarps][kMaxTree];
+    const int wib = threadIdx.x >> 5;
+    const int b = (int)blockIdx.x * kPackWarps + wib;
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
     const int o = offsets[b], e = offsets[b + 1];
@@ -29,9 +33,11 @@ __global__ void __launch_bounds__(128) pack_kernel(const int32_t *__restrict__ o
         }
         return;
     }
+    int *par = sp[wib];
     int bad_i = -1;
     for (int i = lane; i < T; i += 32) {
         const int p = parent[o + i];
+        par[i] = p;
         if ((p < -1 || p >= i) && bad_i < 0) bad_i = i;
     }
     const unsigned badm = __ballot_sync(0xffffffffu, bad_i >= 0);
@@ -40,25 +46,24 @@ __global__ void __launch_bounds__(128) pack_kernel(const int32_t *__restrict__ o
         const int bi = __shfl_sync(0xffffffffu, bad_i, src);
         if (lane == 0) {
             req_depth[b] = 0;
-            report(st, BOLE_ERR_BAD_TOPOLOGY, b, bi, parent[o + bi]);
+            report(st, BOLE_ERR_BAD_TOPOLOGY, b, bi, par[bi]);
         }
         return;
     }
+    __syncwarp();
     int dmax = 0;
     for (int i = lane; i < T; i += 32) {
         uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        int d = -1;
-        for (int j = i; j >= 0; j = parent[o + j]) {
+        for (int j = i; j >= 0; j = par[j]) {
             const uint32_t bit = 1u << (j & 31);
             if (j < 32) w0 |= bit;
             else if (j < 64) w1 |= bit;
             else if (j < 96) w2 |= bit;
             else w3 |= bit;
-            ++d;
         }
+        const int d = __popc(w0) + __popc(w1) + __popc(w2) + __popc(w3) - 1;
         depth[o + i] = d;
-        uint4 m = make_uint4(w0, w1, w2, w3);
-        *reinterpret_cast<uint4 *>(anc + (size_t)(o + i) * 4) = m;
+        *reinterpret_cast<uint4 *>(anc + (size_t)(o + i) * 4) = make_uint4(w0, w1, w2, w3);
         dmax = max(dmax, d);
     }
 #pragma unroll
@@ -78,10 +83,9 @@ cudaError_t launch_pack(const int32_t *offsets, const int32_t *parent, int B, in
     cudaError_t e = cudaMemsetAsync(st, 0, sizeof(int32_t) * BOLE_STATUS_WORDS, s);
     if (e != cudaSuccess) return e;
     if (B <= 0) return cudaSuccess;
-    const int warps_per_block = 4;
-    const int blocks = (B + warps_per_block - 1) / warps_per_block;
-    pack_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(offsets, parent, B, N, max_depth, depth,
-                                                         anc, req_depth, st);
+    const int blocks = (B + kPackWarps - 1) / kPackWarps;
+    pack_kernel<<<blocks, 32 * kPackWarps, 0, s>>>(offsets, parent, B, N, max_depth, depth, anc,
+                                                   req_depth, st);
     return cudaGetLastError();
 }
 

@@ -45,55 +45,325 @@ constexpr int kSlots = 16;    // depth slots in the compact factors: depth <= 15
 constexpr int kLd = 17;       // padded row stride of the compact factors (bank spread)
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 200 ms bound on any device wait
 
-// ---- verification shared-memory plan (bytes from a 1024-aligned base) ----
-// One head per CTA, two CTAs per SM: while one CTA waits on memory or on the
-// tensor core, the other computes.
-//   S buffer (64 KB): four 16 KB boxes [128 rows x 128 B] of fp32 S_pre; the
-//     in-place split turns boxes (0,1) into (S_hi, S_lo) of columns 0..63 and
-//     boxes (2,3) into those of columns 64..127 (bf16, 128B-swizzled,
-//     N-contiguous); after the state products it holds [M;W] (first 32 KB,
-//     tf32 K-major) and R^T (second 32 KB, tf32 K-major).
-//   A1 (32 KB): [Q;K] bf16 K-major; once the state products are done it
-//     holds the compact factors G, C, the Neumann iterates and W.
-constexpr int OFF_SBUF = 0;
-constexpr int SBUF_BYTES = 65536;
-constexpr int OFF_A1 = SBUF_BYTES;
-constexpr int FAC_BYTES = kT * kLd * 4;       // one compact factor [64][17] f32
-constexpr int OFF_G = OFF_A1;                 // compact G (slot = ancestor depth)
-constexpr int OFF_C = OFF_G + FAC_BYTES;      // compact C
-constexpr int OFF_ZA = OFF_C + FAC_BYTES;     // Neumann iterates
-constexpr int OFF_ZB = OFF_ZA + FAC_BYTES;
-constexpr int OFF_W = OFF_ZB + FAC_BYTES;     // W = sum of iterates
-static_assert(OFF_W + FAC_BYTES <= OFF_A1 + 32768, "factors fit in the [Q;K] buffer");
-constexpr int OFF_ANCAT = OFF_A1 + 32768;     // [64][16] u8: ancestor at depth s
-constexpr int OFF_PAIRS = OFF_ANCAT + kT * kSlots; // u16 (i << 8 | t), t <= depth(i)
-constexpr int OFF_LG = OFF_PAIRS + kT * kSlots * 2; // log gamma
-constexpr int OFF_L = OFF_LG + kT * 4;        // log P
-constexpr int OFF_P = OFF_L + kT * 4;
-constexpr int OFF_BETA = OFF_P + kT * 4;
-constexpr int OFF_DEPTH = OFF_BETA + kT * 4;
-constexpr int OFF_SCAN = OFF_DEPTH + kT * 4;  // per-row inclusive pair counts
-constexpr int OFF_MASK = OFF_SCAN + kT * 4;   // u64 ancestor-or-self masks
-constexpr int OFF_BAR = OFF_MASK + kT * 8;    // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 16 * 8;    // TMEM slot, flag, pair count
-constexpr int VERIFY_SMEM = OFF_MISC + 32 + 1024; // + alignment slack
-static_assert(VERIFY_SMEM <= 113 * 1024, "two verification CTAs per SM");
+// ---- per-head pair records: the factor kernel's output, the solve kernel's input ----
+// For head (b, h) the records start at ((offsets[b] * H) + h * T_b) * kSlots and hold,
+// for every pair (node i, ancestor slot t <= depth(i)) with j the ancestor of i at
+// depth t: M_ij = (C W)_ij and W_ij.  At most T_b * kSlots records per head, so the
+// workspace is bounded by N * H * kSlots records (plus one count per head).
+struct PairRec {
+    float m, w;
+    int i, j;
+};
+static_assert(sizeof(PairRec) == 16, "16-byte records");
 
-constexpr int kComputeThreads = 256;          // warps 0..7: factors, splits, epilogues
-constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
+// =====================================================================
+// factor kernel: the per-(request, head) producer of the tree factors
+// =====================================================================
+// One CTA per (request, head), three CTAs per SM (58 KB shared memory, 64
+// tensor-memory columns).  It forms the cumulative decay, the Gram [Q;K] K^T
+// on tcgen05 (bf16 products, exact, fp32 accumulation), the ancestor-masked
+//   C_ij = exp(L_i - L_j) q_i.k_j        (j an ancestor of i or i itself)
+//   G_ij = beta_i exp(L_i - L_j) k_i.k_j (j a strict ancestor of i)
+// compactly by ancestor depth, runs the d-step Neumann recurrence
+// Z <- -G Z, W += Z on the identity (Eq. (8)), which gives W = (I+G)^{-1}
+// (Lemma 3), and writes M = C W and W as pair records.
+constexpr int kFThreads = 256;
+constexpr int kMaxPairs = kT * kSlots;
+constexpr int F_A1 = 0;                         // [Q;K] bf16 K-major, then the staged Gram
+constexpr int F_FAC = 32768;                    // G, C, Za, Zb, W: [64][17] f32 each
+constexpr int F_FAC_BYTES = kT * kLd * 4;
+constexpr int F_ANCAT = F_FAC + 5 * F_FAC_BYTES; // [64][16] u8
+constexpr int F_PAIRS = F_ANCAT + kT * kSlots;   // u16 (i << 8 | t)
+constexpr int F_L = F_PAIRS + kMaxPairs * 2;
+constexpr int F_BETA = F_L + kT * 4;
+constexpr int F_DEPTH = F_BETA + kT * 4;
+constexpr int F_BAR = F_DEPTH + kT * 4;         // mbarriers: A1, Gram
+constexpr int F_MISC = F_BAR + 16;              // TMEM slot, pair count
+constexpr int FACTOR_SMEM = F_MISC + 16 + 1024;
+static_assert(FACTOR_SMEM <= 75 * 1024, "three factor CTAs per SM");
 
 constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
-constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
-constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
-
-// mbarrier slots
-constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_STATE = 3, BAR_MMA2 = 4, BAR_CONV = 5,
-              BAR_OPS = 6;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kFThreads, 3)
+tc_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const float *__restrict__ gamma, const float *__restrict__ beta,
+                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
+                 const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth, int H,
+                 int N, float *__restrict__ logP, PairRec *__restrict__ recs,
+                 int32_t *__restrict__ counts, int32_t *st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *sA1 = sm + F_A1;
+    float *gram = reinterpret_cast<float *>(sm + F_A1); // [128][64], column XOR row % 32
+    float *Gc = reinterpret_cast<float *>(sm + F_FAC);
+    float *Cc = Gc + kT * kLd;
+    float *Za = Cc + kT * kLd;
+    float *Zb = Za + kT * kLd;
+    float *Wc = Zb + kT * kLd;
+    uint8_t *ancat = sm + F_ANCAT;
+    uint16_t *pairs = reinterpret_cast<uint16_t *>(sm + F_PAIRS);
+    float *Ls = reinterpret_cast<float *>(sm + F_L);
+    float *Bs = reinterpret_cast<float *>(sm + F_BETA);
+    int *Ds = reinterpret_cast<int *>(sm + F_DEPTH);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + F_BAR); // A1, Gram
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + F_MISC);
+    int *npair = reinterpret_cast<int *>(sm + F_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x;
+    const int b = unit / H, h = unit % H;
+    if (faulted(st)) return;
+    const int o = offsets[b], T = offsets[b + 1] - o;
+    if (T <= 0) return;
+    const int d = req_depth[b];
+    if (T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T) {
+        if (tid == 0)
+            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
+                   -1, T > kT ? T : d);
+        return;
+    }
+
+    if (tid == 32) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 64);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool ok = true;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], 32768);
+#pragma unroll
+        for (int ka = 0; ka < 2; ++ka) {
+            tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[0], 64 * ka, h, o);
+            tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[0], 64 * ka, h, o);
+        }
+    }
+
+    // ---- topology, cumulative decay and the (node, ancestor slot) pair list ----
+    // Warps 0 and 1 own rows 0..63 (row = tid) and also read the partner row
+    // tid ^ 32, so each warp sees every row's gate and depth through shuffles:
+    // L_i = sum of log gamma over the ancestors-or-self of i (the prefix along
+    // parent links, Lemma 1), the ancestor-by-depth table, and the offsets of
+    // each row's pairs by a 64-row scan, without a barrier.
+    if (tid < kT) {
+        const int i = tid, ip = i ^ 32;
+        int di = -1, dp = -1;
+        uint64_t mi = 0;
+        float bi = 0.f, lgi = 0.f, lgp = 0.f;
+        if (i < T) {
+            const size_t nh = (size_t)(o + i) * H + h;
+            di = depth_g[o + i];
+            const uint2 m2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
+            mi = ((uint64_t)m2.y << 32) | m2.x;
+            bi = beta[nh];
+            lgi = logf(gamma[nh]);
+        }
+        if (ip < T) {
+            dp = depth_g[o + ip];
+            lgp = logf(gamma[(size_t)(o + ip) * H + h]);
+        }
+        const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
+        const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
+        const int cnt = di + 1;
+        int maxcnt = cnt;
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1)
+            maxcnt = max(maxcnt, __shfl_xor_sync(0xffffffffu, maxcnt, sft));
+        float L = 0.f;
+        uint64_t mm = mi;
+        for (int t = 0; t < maxcnt; ++t) {
+            const int j = mm ? __ffsll((long long)mm) - 1 : 0;
+            const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
+            const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
+            if (mm) {
+                L += (j < 32) ? vlo : vhi;
+                ancat[i * kSlots + t] = (uint8_t)j;
+                mm &= mm - 1;
+            }
+        }
+        int c_lo = (i < 32) ? cnt : dp + 1, c_hi = (i < 32) ? dp + 1 : cnt;
+#pragma unroll
+        for (int sft = 1; sft < 32; sft <<= 1) {
+            const int ylo = __shfl_up_sync(0xffffffffu, c_lo, sft);
+            const int yhi = __shfl_up_sync(0xffffffffu, c_hi, sft);
+            if (lane >= sft) {
+                c_lo += ylo;
+                c_hi += yhi;
+            }
+        }
+        const int tot_lo = __shfl_sync(0xffffffffu, c_lo, 31);
+        const int tot_hi = __shfl_sync(0xffffffffu, c_hi, 31);
+        const int start = ((i < 32) ? c_lo : tot_lo + c_hi) - cnt;
+        for (int t = 0; t < cnt; ++t) {
+            pairs[start + t] = (uint16_t)((i << 8) | t);
+            const float id = (t == di) ? 1.f : 0.f; // Z^(0) = W = identity
+            Za[i * kLd + t] = id;
+            Wc[i * kLd + t] = id;
+        }
+        Ds[i] = di;
+        Bs[i] = bi;
+        Ls[i] = L;
+        if (i < T) logP[(size_t)(o + i) * H + h] = L;
+        if (i == 0) *npair = tot_lo + tot_hi;
+    }
+
+    // ---- Gram [Q;K] K^T on the tensor core, staged back into the [Q;K] buffer ----
+    if (tid == 0) {
+        ok &= mbar_wait(&bar[0], 0, kWaitNs);
+        tc_fence_after();
+        const uint32_t a1 = smem_addr(sA1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem, sdesc_sw128(a1 + off, 16, 1024),
+                        sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
+        }
+        mma_commit(&bar[1]);
+    }
+    ok &= mbar_wait(&bar[1], 0, kWaitNs);
+    tc_fence_after();
+    {
+        const int rowgrp = warp & 3, half = warp >> 2;
+        const int m = rowgrp * 32 + lane; // row 0..63 q_i.k_j, 64..127 k_i.k_j
+        float g[32];
+        tmem_ld32(tmem + ((uint32_t)(rowgrp * 32) << 16) + half * 32, g);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) gram[m * 64 + ((half * 32 + t) ^ (m & 31))] = g[t];
+    }
+    tc_fence_before();
+    __syncthreads();
+    const int P = *npair;
+
+    // ---- compact C and G, one thread per (node, ancestor slot) pair ----
+    for (int p = tid; p < P; p += kFThreads) {
+        const int pr = pairs[p];
+        const int i = pr >> 8, t = pr & 255;
+        const int j = ancat[i * kSlots + t];
+        const float ratio = __expf(Ls[i] - Ls[j]);
+        Cc[i * kLd + t] = ratio * gram[i * 64 + (j ^ (i & 31))];
+        if (t < Ds[i]) Gc[i * kLd + t] = Bs[i] * ratio * gram[(64 + i) * 64 + (j ^ (i & 31))];
+    }
+    __syncthreads();
+
+    // ---- W = sum_{m<=d} (-G)^m by Z <- -G Z, W += Z (Eq. (8) on the identity) ----
+    // Pair (i, t): row i's coefficient on its ancestor at depth t.  Z^(m) can be
+    // nonzero only where depth(i) - t >= m; one thread per pair.
+    {
+        float *Zc = Za, *Zn = Zb;
+        for (int step = 0; step < d; ++step) {
+            for (int p = tid; p < P; p += kFThreads) {
+                const int pr = pairs[p];
+                const int i = pr >> 8, t = pr & 255;
+                const int di = Ds[i];
+                if (t + step >= di) continue;
+                const float *gi = Gc + i * kLd;
+                const uint8_t *ai = ancat + i * kSlots;
+                float v0 = 0.f, v1 = 0.f;
+                int s2 = t + step;
+                for (; s2 + 1 < di; s2 += 2) {
+                    v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
+                    v1 = fmaf(gi[s2 + 1], Zc[ai[s2 + 1] * kLd + t], v1);
+                }
+                if (s2 < di) v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
+                const float val = -(v0 + v1);
+                Zn[i * kLd + t] = val;
+                Wc[i * kLd + t] += val;
+            }
+            __syncthreads();
+            float *tmp = Zc; Zc = Zn; Zn = tmp;
+        }
+    }
+
+    // ---- M = C W and W as pair records ----
+    PairRec *out = recs + ((size_t)o * H + (size_t)h * T) * kSlots;
+    for (int p = tid; p < P; p += kFThreads) {
+        const int pr = pairs[p];
+        const int i = pr >> 8, t = pr & 255;
+        const int di = Ds[i];
+        const float *ci = Cc + i * kLd;
+        const uint8_t *ai = ancat + i * kSlots;
+        float mval = 0.f;
+        for (int s2 = t; s2 <= di; ++s2) mval = fmaf(ci[s2], Wc[ai[s2] * kLd + t], mval);
+        PairRec r;
+        r.m = mval;
+        r.w = Wc[i * kLd + t];
+        r.i = i;
+        r.j = ai[t];
+        out[p] = r;
+    }
+    if (tid == 0) {
+        counts[unit] = P;
+        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// =====================================================================
+// solve kernel: value tile = the whole head (b_v = d_v = 128)
+// =====================================================================
+// Shared-memory plan (bytes from a 1024-aligned base), two CTAs per SM:
+//   S buffer (64 KB): four 16 KB boxes [128 rows x 128 B] of fp32 S_pre; the
+//     in-place split turns boxes (0,1) into (S_hi, S_lo) of columns 0..63 and
+//     boxes (2,3) into those of columns 64..127 (bf16, 128B-swizzled,
+//     N-contiguous); after the state products it holds [M;W] (first 32 KB,
+//     tf32 K-major) and R^T (second 32 KB, tf32 K-major).
+//   A1 (32 KB): [Q;K] bf16 K-major (rows 0..63 q, 64..127 k).
+//   V (16 KB): the head's value rows, two 128B-swizzled boxes [64 rows x 64
+//     bf16], loaded by TMA beside the state so the epilogue reads them from
+//     shared memory (row-per-thread global loads cost several microseconds).
+// Tensor memory (256 columns, 128 lanes = operand rows): columns 0..127 hold
+// [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R].  The
+// epilogues only read it, so no tensor-memory store sits between the state
+// products and the second MMA.
+constexpr int OFF_SBUF = 0;
+constexpr int SBUF_BYTES = 65536;
+constexpr int OFF_A1 = SBUF_BYTES;
+constexpr int OFF_V = OFF_A1 + 32768;
+constexpr int OFF_BAR = OFF_V + 16384;        // mbarriers
+constexpr int OFF_MISC = OFF_BAR + 8 * 8;     // TMEM slot
+constexpr int SOLVE_END = OFF_MISC + 16;
+// Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
+// plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
+// dynamic base, which is aligned when the kernel has no static shared memory
+// (checked in the kernel).  A request at the 113 KB edge would drop to one CTA
+// per SM as soon as anything else claimed shared memory.
+constexpr int SOLVE_SMEM = SOLVE_END + 256;
+static_assert(2 * (SOLVE_SMEM + 1024) <= 228 * 1024, "two solve CTAs per SM");
+static_assert(3 * SOLVE_SMEM > 228 * 1024, "at most two solve CTAs (2 x 256 TMEM columns) per SM");
+
+constexpr int kComputeThreads = 256;          // warps 0..7: split, epilogues, scatter
+constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
+
+constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
+constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
+
+// mbarrier slots
+constexpr int BAR_S = 0, BAR_A1 = 1, BAR_STATE = 2, BAR_MMA2 = 3, BAR_CONV = 4, BAR_OPS = 5,
+              BAR_V = 6;
+
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
 {
@@ -106,13 +376,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
     }
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y, int z)
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
 {
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -126,66 +393,52 @@ __device__ __forceinline__ void compute_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
 }
 
-// Verification kernel: one CTA per (request, head), trees of up to 64 nodes
-// and depth <= 15.  Warp 8 streams operands and issues the tensor-core
-// products; warps 0..7 do everything else.  All waits are bounded.
+// One CTA per (request, head): state products on tcgen05, R, and the
+// propagation + read-out product [M; W] R.  Warp 8 streams operands and
+// issues the tensor-core products; warps 0..7 do everything else.  All waits
+// are bounded.
 __global__ void __launch_bounds__(kThreads, 2)
-tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
-                 const __grid_constant__ CUtensorMap tmK, const __nv_bfloat16 *__restrict__ v,
-                 const float *__restrict__ gamma, const float *__restrict__ beta,
-                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
-                 const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth, int H,
-                 int N, __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
-                 float *__restrict__ logP, int32_t *st)
+tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const float *__restrict__ beta, const int32_t *__restrict__ offsets,
+                const int32_t *__restrict__ req_depth, const float *__restrict__ logP,
+                const PairRec *__restrict__ recs, const int32_t *__restrict__ counts, int H, int N,
+                __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout, int32_t *st)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sbuf = sm + OFF_SBUF;
     uint8_t *sA1 = sm + OFF_A1;
-    float *Gc = reinterpret_cast<float *>(sm + OFF_G);
-    float *Cc = reinterpret_cast<float *>(sm + OFF_C);
-    float *Za = reinterpret_cast<float *>(sm + OFF_ZA);
-    float *Zb = reinterpret_cast<float *>(sm + OFF_ZB);
-    float *Wc = reinterpret_cast<float *>(sm + OFF_W);
-    uint8_t *ancat = sm + OFF_ANCAT;
-    uint16_t *pairs = reinterpret_cast<uint16_t *>(sm + OFF_PAIRS);
-    float *Lg = reinterpret_cast<float *>(sm + OFF_LG);
-    float *Ls = reinterpret_cast<float *>(sm + OFF_L);
-    float *Ps = reinterpret_cast<float *>(sm + OFF_P);
-    float *Bs = reinterpret_cast<float *>(sm + OFF_BETA);
-    int *Ds = reinterpret_cast<int *>(sm + OFF_DEPTH);
-    int *scan = reinterpret_cast<int *>(sm + OFF_SCAN);
-    uint64_t *msk = reinterpret_cast<uint64_t *>(sm + OFF_MASK);
+    uint8_t *sV = sm + OFF_V;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
-    int *flag = reinterpret_cast<int *>(sm + OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
 
-    // Uniform early exits, before any barrier or tensor-memory allocation.
+    // Uniform early exits, before any barrier or tensor-memory allocation
+    // (the factor kernel reported any fault of this head).
     if (faulted(st)) return;
     const int o = offsets[b], T = offsets[b + 1] - o;
     if (T <= 0) return;
     const int d = req_depth[b];
-    if (T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T) {
-        if (tid == 0)
-            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
-                   -1, T > kT ? T : d);
+    if (T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T) return;
+    if (sm + SOLVE_END > smem_raw + SOLVE_SMEM) { // dynamic base too far from 1024 B
+        if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
 
+    if (tid == 32) {
+        for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
+        mbar_init(&bar[BAR_V], 1);
+        mbar_init(&bar[BAR_CONV], kComputeThreads);
+        mbar_init(&bar[BAR_OPS], kComputeThreads);
+        fence_mbar_init();
+    }
     if (warp == 0) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
-    }
-    if (tid == 32) {
-        for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
-        mbar_init(&bar[BAR_CONV], kComputeThreads);
-        mbar_init(&bar[BAR_OPS], kComputeThreads);
-        *flag = 0;
-        fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
@@ -197,31 +450,22 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         const uint32_t a1 = smem_addr(sA1), s0 = smem_addr(sbuf);
         bool ok = true;
         if (lane == 0) {
+            mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
             mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
 #pragma unroll
             for (int ka = 0; ka < 2; ++ka) {
                 tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
                 tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[BAR_A1], 64 * ka, h, o);
             }
-            mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+            mbar_arrive_expect_tx(&bar[BAR_V], 16384);
+            tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
+            tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
         }
-        // Gram [Q;K] K^T
-        ok &= mbar_wait(&bar[BAR_A1], 0, kWaitNs);
-        tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16_ss(tmem + 128, sdesc_sw128(a1 + off, 16, 1024),
-                            sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
-            }
-            mma_commit(&bar[BAR_GRAM]);
-        }
-        __syncwarp();
         // state products [Q;K] (S_hi + S_lo) once the split is in place
+        ok &= mbar_wait(&bar[BAR_A1], 0, kWaitNs);
         ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
         tc_fence_after();
         if (lane == 0) {
@@ -243,79 +487,32 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_tf32_ss(tmem, sdesc_sw128(s0 + off, 16, 1024), sdesc_sw128(b2 + off, 16, 1024),
-                            IDESC_TF32, 1);
+                mma_tf32_ss(tmem + 128, sdesc_sw128(s0 + off, 16, 1024),
+                            sdesc_sw128(b2 + off, 16, 1024), IDESC_TF32, kk > 0);
             }
             mma_commit(&bar[BAR_MMA2]);
         }
         __syncwarp();
-        if (!ok && lane == 0) {
-            report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
-            *flag = 1;
-        }
+        if (!ok && lane == 0) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
     } else {
         // ========================== compute warps =========================
         const int rowgrp = warp & 3, half = warp >> 2;
         const int m = rowgrp * 32 + lane;    // TMEM lane = operand row
         const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
         bool ok = true;
-
-        // ---- topology and gates ----
-        if (tid < kT) {
-            const int i = tid;
-            if (i < T) {
-                const size_t nh = (size_t)(o + i) * H + h;
-                Ds[i] = depth_g[o + i];
-                const uint2 m2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
-                msk[i] = ((uint64_t)m2.y << 32) | m2.x;
-                Bs[i] = beta[nh];
-                Lg[i] = logf(gamma[nh]);
-            } else {
-                Ds[i] = -1;
-                msk[i] = 0;
-                Bs[i] = 0.f;
-                Lg[i] = 0.f;
-            }
-        }
-        compute_sync();
-        // ---- cumulative decay L_i = sum of log gamma over the ancestors-or-self
-        //      (the prefix along parent links, Lemma 1) and the ancestor-by-depth
-        //      table; per-row pair counts scanned within each warp ----
-        if (tid < kT) {
-            const int i = tid;
-            float L = 0.f;
-            if (i < T) {
-                uint64_t mm = msk[i];
-                int t = 0;
-                while (mm) {
-                    const int j = __ffsll((long long)mm) - 1;
-                    ancat[i * kSlots + t++] = (uint8_t)j;
-                    L += Lg[j];
-                    mm &= mm - 1;
-                }
-                logP[(size_t)(o + i) * H + h] = L;
-            }
-            Ls[i] = L;
-            Ps[i] = (i < T) ? expf(L) : 0.f;
-            int incl = Ds[i] + 1;
+        // this thread's operand row: P_i for both halves, beta_i for the K half
+        const int i = m & 63;
+        const float p = (i < T) ? expf(logP[(size_t)(o + i) * H + h]) : 0.f;
+        const float bt = (m >= 64 && i < T) ? beta[(size_t)(o + i) * H + h] : 0.f;
+        // this thread's pair records (at most kMaxPairs / 256 = 4), fetched early
+        const int P = counts[unit];
+        const PairRec *rin = recs + ((size_t)o * H + (size_t)h * T) * kSlots;
+        PairRec rec[kMaxPairs / kComputeThreads];
 #pragma unroll
-            for (int sft = 1; sft < 32; sft <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, sft);
-                if (lane >= sft) incl += y;
-            }
-            scan[i] = incl;
+        for (int u = 0; u < kMaxPairs / kComputeThreads; ++u) {
+            const int p = tid + u * kComputeThreads;
+            if (p < P) rec[u] = rin[p];
         }
-        compute_sync();
-        // pair list (node i, ancestor slot t), t <= depth(i)
-        if (tid < kT) {
-            const int i = tid;
-            const int incl = scan[i] + ((i >= 32) ? scan[31] : 0);
-            const int di = Ds[i];
-            const int start = incl - (di + 1);
-            for (int t = 0; t <= di; ++t) pairs[start + t] = (uint16_t)((i << 8) | t);
-        }
-        const int P = scan[31] + scan[63];
-        compute_sync();
 
         // ---- S_pre = S_hi + S_lo in place (bf16, N-contiguous, 64-column atoms) ----
         ok &= mbar_wait(&bar[BAR_S], 0, kWaitNs);
@@ -352,152 +549,71 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         fence_proxy_async_smem();
         mbar_arrive(&bar[BAR_CONV]);
 
-        // ---- Gram epilogue: compact G and C (Lemma 2 / Lemma 1 read-out), written
-        //      into the [Q;K] buffer once the state products have consumed it ----
-        ok &= mbar_wait(&bar[BAR_GRAM], 0, kWaitNs);
+        // ---- state epilogue: rows 0..63 zero the [M; W] operand; rows 64..127
+        //      write R^T = (beta (v - P K S_pre))^T.  No tensor-memory stores:
+        //      Q S_pre stays in columns 0..127 and is scaled by P at the output ----
         ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
         tc_fence_after();
-        {
-            // stage the Gram rows in the S buffer (free once the state products are
-            // done): [128 rows][64 + 1] f32, rows 0..63 q_i.k_j, rows 64..127 k_i.k_j
-            float *gram = reinterpret_cast<float *>(sbuf);
-            float g[32];
-            tmem_ld32(tmem + lane_base + 128 + half * 32, g);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) gram[m * 65 + half * 32 + t] = g[t];
-        }
-        compute_sync();
-        // one thread per (row, ancestor): C for rows 0..63, G (strict ancestors) for 64..127
-        {
-            const int r = tid >> 1, part = tid & 1; // two threads per operand row
-            const int i = r & 63;
-            if (i < T) {
-                const bool isG = r >= 64;
-                uint64_t bits = msk[i];
-                if (isG) bits &= ~(1ull << i);
-                const float *grow = reinterpret_cast<const float *>(sbuf) + r * 65;
-                float *dst = (isG ? Gc : Cc) + i * kLd;
-                const float Li = Ls[i], scale = isG ? Bs[i] : 1.f;
-                int n = 0;
-#pragma unroll 1
-                while (bits) {
-                    const int j = __ffsll((long long)bits) - 1;
-                    bits &= bits - 1;
-                    if ((n++ & 1) == part) dst[Ds[j]] = scale * __expf(Li - Ls[j]) * grow[j];
-                }
-            }
-        }
-        // Neumann start Z^(0) = W = identity (the self entry sits at slot depth(i))
-        for (int p = tid; p < P; p += kComputeThreads) {
-            const int pr = pairs[p];
-            const int i = pr >> 8, t = pr & 255;
-            const float id = (t == Ds[i]) ? 1.f : 0.f;
-            Za[i * kLd + t] = id;
-            Wc[i * kLd + t] = id;
-        }
-        compute_sync();
-
-        // ---- W = sum_{m<=d} (-G)^m by Z <- -G Z, W += Z (Eq. (8) on the identity) ----
-        // Pair (i, t): row i's coefficient on its ancestor at depth t.  Z^(m)
-        // can be nonzero only where depth(i) - t >= m; one thread per pair.
-        {
-            float *Zc = Za, *Zn = Zb;
-            for (int step = 0; step < d; ++step) {
-                for (int p = tid; p < P; p += kComputeThreads) {
-                    const int pr = pairs[p];
-                    const int i = pr >> 8, t = pr & 255;
-                    const int di = Ds[i];
-                    if (t + step >= di) continue;
-                    const float *gi = Gc + i * kLd;
-                    const uint8_t *ai = ancat + i * kSlots;
-                    float v0 = 0.f, v1 = 0.f;
-                    int s2 = t + step;
-                    for (; s2 + 1 < di; s2 += 2) {
-                        v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
-                        v1 = fmaf(gi[s2 + 1], Zc[ai[s2 + 1] * kLd + t], v1);
-                    }
-                    if (s2 < di) v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
-                    const float val = -(v0 + v1);
-                    Zn[i * kLd + t] = val;
-                    Wc[i * kLd + t] += val;
-                }
-                compute_sync();
-                float *tmp = Zc; Zc = Zn; Zn = tmp;
-            }
-        }
-
-        // ---- state epilogue: B0 = P Q S_pre in place; R^T = (beta (v - P K S_pre))^T;
-        //      [M; W] operand zeroed ----
-        {
+        if (m < 64) {
             float4 *a2z = reinterpret_cast<float4 *>(sbuf);
+            const int zt = (half * 64 + m); // 0..127
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                a2z[tid + e * kComputeThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < 16; ++e) a2z[zt + e * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
             uint8_t *sB2 = sbuf + 32768;
-            const int i = m & 63;
+            uint8_t *dst = sB2 + (i >> 5) * 16384;
+            const uint8_t *vrow = sV + half * 8192 + i * 128; // 64 columns of row i
+            ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
                 tmem_ld32(tmem + lane_base + col0, x);
-                if (m < 64) {
-                    const float p = Ps[i];
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) x[t] *= p;
-                    tmem_st32(tmem + lane_base + col0, x);
-                } else {
-                    const float p = Ps[i], bt = Bs[i];
-                    uint8_t *dst = sB2 + (i >> 5) * 16384;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        v + ((size_t)(o + (i < T ? i : 0)) * H + h) * kD + col0);
+                for (int uu = 0; uu < 4; ++uu) {
+                    float f[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
 #pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        float f[8];
-                        bf16x8_to_f32(src[uu], f);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) {
-                            const int c = 8 * uu + t;
-                            const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
-                            *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i & 31)) = r;
-                        }
+                    for (int t = 0; t < 8; ++t) {
+                        const int c = 8 * uu + t;
+                        const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
+                        *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i & 31)) = r;
                     }
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) x[t] = 0.f;
-                    tmem_st32(tmem + lane_base + col0, x);
                 }
             }
         }
-        compute_sync(); // operand zeroed; W final
-        // ---- scatter M = C W (rows 0..63) and W (rows 64..127) into [M; W] ----
-        for (int p = tid; p < P; p += kComputeThreads) {
-            const int pr = pairs[p];
-            const int i = pr >> 8, t = pr & 255;
-            const int di = Ds[i];
-            const float *ci = Cc + i * kLd;
-            const uint8_t *ai = ancat + i * kSlots;
-            float mval = 0.f;
-            for (int s2 = t; s2 <= di; ++s2) mval = fmaf(ci[s2], Wc[ai[s2] * kLd + t], mval);
-            const int j = ai[t];
-            uint8_t *col = sbuf + (j >> 5) * 16384;
-            *reinterpret_cast<float *>(col + sw128_offset(i, j & 31)) = mval;
-            *reinterpret_cast<float *>(col + sw128_offset(64 + i, j & 31)) = Wc[i * kLd + t];
+        compute_sync(); // operand zeroed
+        // ---- [M; W] from the factor kernel's pair records ----
+#pragma unroll
+        for (int u = 0; u < kMaxPairs / kComputeThreads; ++u) {
+            if (tid + u * kComputeThreads < P) {
+                const PairRec r = rec[u];
+                uint8_t *col = sbuf + (r.j >> 5) * 16384;
+                *reinterpret_cast<float *>(col + sw128_offset(r.i, r.j & 31)) = r.m;
+                *reinterpret_cast<float *>(col + sw128_offset(64 + r.i, r.j & 31)) = r.w;
+            }
         }
         fence_proxy_async_smem();
-        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar[BAR_OPS]);
 
-        // ---- outputs: rows 0..63 O (bf16), rows 64..127 U (fp32) ----
+        // ---- outputs: O = P (Q S_pre) + M R (bf16), U = W R (fp32) ----
         ok &= mbar_wait(&bar[BAR_MMA2], 0, kWaitNs);
         tc_fence_after();
         {
-            const int i = m & 63;
             const bool store = ok && i < T;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
-                tmem_ld32(tmem + lane_base + col0, x);
+                tmem_ld32(tmem + 128 + lane_base + col0, x);
+                if (m < 64) {
+                    float y[32];
+                    tmem_ld32(tmem + lane_base + col0, y);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
+                }
                 if (!store) continue;
                 const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
                 if (m < 64) {
@@ -541,7 +657,8 @@ constexpr int CO_COEF = CO_PATH + 512;        // float[128]
 constexpr int CO_BAR = CO_COEF + 512;         // 2 mbarriers
 constexpr int CO_TSLOT = CO_BAR + 16;
 constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag
-constexpr int COMMIT_SMEM = CO_MISC + 16 + 1024;
+constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
+constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
 
 constexpr uint32_t IDESC_COMMIT = idesc_tf32(128, kHalf, false, false);
 
@@ -577,6 +694,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CO_TSLOT);
     int *plen = reinterpret_cast<int *>(sm + CO_MISC);
     int *flag = plen + 1;
+    int *spar = reinterpret_cast<int *>(sm + CO_PAR);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int unit = blockIdx.x, hv = blockIdx.y; // head unit, value half
@@ -608,12 +726,17 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         mbar_arrive_expect_tx(&bar[0], 2 * 16384);
         tma_load_2d(sS, &tmS, &bar[0], kHalf * hv, unit * kD);
         tma_load_2d(sS + 16384, &tmS, &bar[0], kHalf * hv + 32, unit * kD);
+    }
+    // stage the request's parent links (coalesced), then walk the accepted path
+    for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
+    __syncthreads();
+    if (tid == 0) {
         int L = 0, j = a;
         bool ok = true;
         while (j >= 0) {
             if (L >= kMaxTree) { ok = false; break; }
             path[L++] = j;
-            const int p = parent[o + j];
+            const int p = spar[j];
             if (p < -1 || p >= j) { ok = false; break; }
             j = p;
         }
@@ -762,6 +885,12 @@ bool tc_verify_supported(const VerifyArgs &a)
            a.max_depth < kSlots;
 }
 
+size_t tc_workspace_bytes(int B, int H, int max_T)
+{
+    const size_t recs = (size_t)B * max_T * H * kSlots * sizeof(PairRec);
+    return recs + (size_t)B * H * sizeof(int32_t);
+}
+
 // q or k [N][H][128] bf16 as a 3-D tensor, boxes of 64 elements x 1 head x 64 nodes.
 cudaError_t make_node_map(CUtensorMap *map, const void *x, int N, int H)
 {
@@ -781,17 +910,32 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
 {
     const int units = a.B * a.H;
     if (units == 0 || a.N == 0) return cudaSuccess;
-    CUtensorMap mS, mQ, mK;
+    CUtensorMap mS, mQ, mK, mV;
     cudaError_t e = make_state_map(&mS, a.S_pre, units);
     if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H);
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H);
+    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             VERIFY_SMEM);
+    PairRec *recs = static_cast<PairRec *>(a.ws);
+    int32_t *counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a.ws) +
+                                                  (size_t)a.B * a.max_T * a.H * kSlots * sizeof(PairRec));
+    e = cudaFuncSetAttribute(tc_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FACTOR_SMEM);
     if (e != cudaSuccess) return e;
-    tc_verify_kernel<<<units, kThreads, VERIFY_SMEM, s>>>(
-        mS, mQ, mK, static_cast<const __nv_bfloat16 *>(a.v), a.gamma, a.beta, a.offsets, a.depth,
-        a.anc, a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, a.st);
+    tc_factor_kernel<<<units, kFThreads, FACTOR_SMEM, s>>>(
+        mQ, mK, a.gamma, a.beta, a.offsets, a.depth, a.anc, a.req_depth, a.H, a.N, a.logP, recs,
+        counts, a.st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SOLVE_SMEM);
+    if (e != cudaSuccess) return e;
+    tc_solve_kernel<<<units, kThreads, SOLVE_SMEM, s>>>(
+        mS, mQ, mK, mV, a.beta, a.offsets, a.req_depth,
+        a.logP, recs, counts, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U, a.st);
     return cudaGetLastError();
 }
 
