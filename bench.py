@@ -104,7 +104,7 @@ def algorithmic(batch):
     return {"pack": topo_pack, "verify": verify, "commit": commit, "verify_flops": flops}
 
 
-VERIFY_KERNELS = ["tc_factor_kernel", "tc_solve_kernel"]
+VERIFY_KERNELS = ["tc_verify_kernel"]
 
 
 def recorded_traffic(kernels, config: int):
@@ -283,7 +283,7 @@ def main(argv=None):
                and batch.dv == 128 and batch.max_T <= 64
                and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
                                        batch.max_depth, torch.bfloat16, flags) == 0)
-    launches_per_step = 1 + 2 + 1  # pack, verify (factor + solve kernels), commit
+    launches_per_step = 1 + (1 if tc_used else 2) + 1  # pack, verify (1 or 2 kernels), commit
 
     def step(i, ev=None):
         db, rb = sets[i % n_sets]

@@ -2,32 +2,48 @@
 // d_k = d_v = 128 -- the Qwen3.5-shaped GDN head of the pages' evaluation.
 //
 // Verification, one CTA per (request, head), two CTAs per SM, trees of up to
-// 64 nodes and depth <= 15:
-//   1. TMA streams the head's S_pre (128 x 128 fp32, 128B-swizzled, four
-//      32-column boxes) into shared memory while the CTA stages [Q;K] of the
-//      tree as one 128 x 128 bf16 operand (rows 0..63 = q, 64..127 = k).
-//   2. S_pre is split exactly into bf16 S_hi + S_lo (S - S_hi rounds to bf16
-//      with ~2^-18 relative residue), and tcgen05 computes in tensor memory the
-//      Gram [Q;K] K^T and the state products [Q;K] (S_hi + S_lo), all with bf16
-//      products (exact) and fp32 accumulation.
-//   3. From the Gram the CTA forms the ancestor-masked factors
-//      G_ij = beta_i (P_i/P_j) k_i.k_j and C_ij = (P_i/P_j) q_i.k_j (Lemma 2,
-//      Lemma 1), stored compactly by ancestor depth, and runs the d-step
-//      Neumann recurrence Z <- -G Z, W += Z (Eq. (8)) on the identity, which
-//      yields W = (I+G)^{-1} (Lemma 3); M = C W follows.  All on chip.
-//   4. Epilogue of the state products: B0 = D_P Q S_pre stays in tensor
-//      memory, R = D_beta (V - D_P K S_pre) goes to shared memory (as R^T).
-//   5. One more tcgen05 product (tf32) [M; W] R accumulates M R onto B0
-//      (giving O) and writes W R (= U) in the other 64 rows.
-// Deviation from the pages' kernel: the Neumann recurrence runs on the
-// T x T identity instead of on each value tile's R.  The tree factor W does
-// not depend on the value columns, so the d dependent steps stay small and
-// off the state-streaming path, and propagation + read-out become one dense
-// tensor-core product per head.  The result is the same polynomial, Eq. (6).
+// 64 nodes and depth <= 15.  Everything between the inputs and (O, U, logP)
+// stays on chip:
+//   1. TMA streams the head's S_pre (128 x 128 fp32, four 32-column
+//      128B-swizzled boxes) and [Q;K] of the tree (one 128 x 128 bf16
+//      operand, rows 0..63 q, 64..127 k).
+//   2. While S_pre is in flight: the cumulative decay L_i = sum of log gamma
+//      over the ancestors-or-self of i (Lemma 1), the Gram [Q;K] K^T on
+//      tcgen05, the ancestor-masked factors
+//        C_ij = exp(L_i - L_j) q_i.k_j          (j an ancestor of i or i)
+//        G_ij = beta_i exp(L_i - L_j) k_i.k_j   (j a strict ancestor of i)
+//      stored compactly by ancestor depth, and the rows of W = (I+G)^{-1}
+//      and M = C W by backward substitution along each node's ancestor path
+//      (below).  The value rows follow by TMA once the factor scratch is free.
+//   3. S_pre is split exactly into bf16 S_hi + S_lo (S - S_hi rounds to bf16
+//      with ~2^-18 relative residue); tcgen05 computes [Q;K] (S_hi + S_lo)
+//      with bf16 products (exact) and fp32 accumulation.
+//   4. Epilogue: R = D_beta (V - D_P K S_pre) goes to shared memory as R^T,
+//      [M; W] is scattered into the other operand buffer.
+//   5. One tcgen05 product (tf32) [M; W] R gives M R and W R = U; the output
+//      adds D_P Q S_pre to M R (Eq. (6)), so O and U leave in one pass.
 //
-// Commit, one CTA per (request, head) with an accepted node: TMA loads S,
-// one tcgen05 product (D_a K_a)^T U_a over the accepted path (K chunks of 32
-// path nodes), the epilogue adds P_a S and TMA stores S in place (Eq. (10)).
+// Rows of W and M.  Restricted to the ancestor path a_0 (root), ..., a_d = i
+// of node i, I + G is the (d+1) x (d+1) unit lower-triangular matrix
+// L[u][t] = G(a_u, a_t) (u > t), and row i of the inverse only involves that
+// path (Lemma 3: every chain of G from i ends at an ancestor).  So row i of W
+// is the y with y^T L = e_d^T, and row i of M = C W is the z with
+// z^T L = c^T, c_t = C(i, a_t): both by backward substitution from t = d,
+//   y_t = [t = d] - sum_{u > t} y_u G(a_u, a_t),
+//   z_t = c_t     - sum_{u > t} z_u G(a_u, a_t),
+// which equals the d-step Neumann sum of Eq. (8) (nilpotent G, G^{d+1} = 0)
+// term by term, with one thread per node and no barrier between steps.
+//
+// Deviations from the pages' kernel: the inverse is formed once on the
+// T x T tree (not applied to each value tile's R by the recurrence), so the
+// dependent steps stay off the state-streaming path and propagation +
+// read-out become one dense tensor-core product per head.  The result is the
+// same polynomial, Eq. (6).
+//
+// Commit, one CTA per (request, head, 64-column half) with an accepted node:
+// TMA loads the half of S, one tcgen05 product (D_a K_a)^T U_a over the
+// accepted path (K chunks of 16 path nodes), the epilogue adds P_a S and TMA
+// stores S in place (Eq. (10)).
 #include <cudaTypedefs.h>
 #include <mutex>
 
@@ -45,44 +61,59 @@ constexpr int kSlots = 16;    // depth slots in the compact factors: depth <= 15
 constexpr int kLd = 17;       // padded row stride of the compact factors (bank spread)
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 200 ms bound on any device wait
 
-// ---- per-head pair records: the factor kernel's output, the solve kernel's input ----
-// For head (b, h) the records start at ((offsets[b] * H) + h * T_b) * kSlots and hold,
-// for every pair (node i, ancestor slot t <= depth(i)) with j the ancestor of i at
-// depth t: M_ij = (C W)_ij and W_ij.  At most T_b * kSlots records per head, so the
-// workspace is bounded by N * H * kSlots records (plus one count per head).
-struct PairRec {
-    float m, w;
-    int i, j;
-};
-static_assert(sizeof(PairRec) == 16, "16-byte records");
+// ---- verification shared-memory plan (bytes from a 1024-aligned base) ----
+//   S buffer (64 KB): four 16 KB boxes [128 rows x 128 B] of fp32 S_pre; the
+//     in-place split turns boxes (0,1) into (S_hi, S_lo) of columns 0..63 and
+//     boxes (2,3) into those of columns 64..127 (bf16, 128B-swizzled,
+//     N-contiguous); after the state products it holds [M;W] (first 32 KB)
+//     and R^T (second 32 KB), both tf32 K-major.
+//   A1 (32 KB): [Q;K] bf16 K-major, operand of the Gram and the state products.
+//   V (16 KB): first the factor scratch (compact C and G, ancestor table,
+//     decays, masks), then the head's value rows by TMA: two 128B-swizzled
+//     boxes [64 rows x 64 bf16], read by the epilogue from shared memory.
+// Tensor memory (256 columns, lane = operand row): columns 0..127 hold
+// [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R]; before the
+// propagation, 128..191 hold the Gram and 192..223 (lanes 0..63) the rows of
+// M and W.  The epilogues only read tensor memory.
+constexpr int OFF_SBUF = 0;
+constexpr int SBUF_BYTES = 65536;
+constexpr int OFF_A1 = SBUF_BYTES;
+constexpr int OFF_V = OFF_A1 + 32768;
+constexpr int OFF_BAR = OFF_V + 16384;        // mbarriers
+constexpr int OFF_MISC = OFF_BAR + 16 * 8;    // TMEM slot
+constexpr int VERIFY_END = OFF_MISC + 16;
+// factor scratch inside V
+constexpr int FAC_BYTES = kT * kLd * 4;       // one compact factor [64][17] f32
+constexpr int X_G = OFF_V;                    // G (row i, ancestor slot t < depth(i))
+constexpr int X_C = X_G + FAC_BYTES;          // C (row i, ancestor slot t <= depth(i))
+constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i at depth t
+constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
+constexpr int X_MASK = X_L + kT * 4;          // u64 ancestor-or-self masks
+constexpr int X_DEPTH = X_MASK + kT * 8;
+constexpr int X_RATIO = X_DEPTH + kT * 4;     // exp(L_i - L_j), j the ancestor of i at depth t
+static_assert(X_RATIO + FAC_BYTES <= OFF_V + 16384, "factor scratch fits the value buffer");
+static_assert(X_ANCAT % 16 == 0 && X_MASK % 8 == 0, "vector-aligned scratch rows");
+// Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
+// plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
+// dynamic base, which is aligned when the kernel has no static shared memory
+// (checked in the kernel).  A request at the 113 KB edge would drop to one CTA
+// per SM as soon as anything else claimed shared memory.
+constexpr int VERIFY_SMEM = VERIFY_END + 256;
+static_assert(2 * (VERIFY_SMEM + 1024) <= 228 * 1024, "two verification CTAs per SM");
+static_assert(3 * VERIFY_SMEM > 228 * 1024,
+              "at most two verification CTAs (2 x 256 TMEM columns) per SM");
 
-// =====================================================================
-// factor kernel: the per-(request, head) producer of the tree factors
-// =====================================================================
-// One CTA per (request, head), three CTAs per SM (58 KB shared memory, 64
-// tensor-memory columns).  It forms the cumulative decay, the Gram [Q;K] K^T
-// on tcgen05 (bf16 products, exact, fp32 accumulation), the ancestor-masked
-//   C_ij = exp(L_i - L_j) q_i.k_j        (j an ancestor of i or i itself)
-//   G_ij = beta_i exp(L_i - L_j) k_i.k_j (j a strict ancestor of i)
-// compactly by ancestor depth, runs the d-step Neumann recurrence
-// Z <- -G Z, W += Z on the identity (Eq. (8)), which gives W = (I+G)^{-1}
-// (Lemma 3), and writes M = C W and W as pair records.
-constexpr int kFThreads = 256;
-constexpr int kMaxPairs = kT * kSlots;
-constexpr int F_A1 = 0;                         // [Q;K] bf16 K-major, then the staged Gram
-constexpr int F_FAC = 32768;                    // G, C, Za, Zb, W: [64][17] f32 each
-constexpr int F_FAC_BYTES = kT * kLd * 4;
-constexpr int F_ANCAT = F_FAC + 5 * F_FAC_BYTES; // [64][16] u8
-constexpr int F_PAIRS = F_ANCAT + kT * kSlots;   // u16 (i << 8 | t)
-constexpr int F_L = F_PAIRS + kMaxPairs * 2;
-constexpr int F_BETA = F_L + kT * 4;
-constexpr int F_DEPTH = F_BETA + kT * 4;
-constexpr int F_BAR = F_DEPTH + kT * 4;         // mbarriers: A1, Gram
-constexpr int F_MISC = F_BAR + 16;              // TMEM slot, pair count
-constexpr int FACTOR_SMEM = F_MISC + 16 + 1024;
-static_assert(FACTOR_SMEM <= 75 * 1024, "three factor CTAs per SM");
+constexpr int kComputeThreads = 256;          // warps 0..7: factors, split, epilogues
+constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
 
 constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
+constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
+constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
+constexpr uint32_t TM_GRAM = 128, TM_MW = 192, TM_PROP = 128;      // tensor-memory columns
+
+// mbarrier slots
+constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE = 4, BAR_MMA2 = 5,
+              BAR_TOPO = 6, BAR_CONV = 7, BAR_OPS = 8;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
@@ -98,273 +129,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
                  : "memory");
 }
 
-__global__ void __launch_bounds__(kFThreads, 3)
-tc_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const float *__restrict__ gamma, const float *__restrict__ beta,
-                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
-                 const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth, int H,
-                 int N, float *__restrict__ logP, PairRec *__restrict__ recs,
-                 int32_t *__restrict__ counts, int32_t *st)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align1024(smem_raw);
-    uint8_t *sA1 = sm + F_A1;
-    float *gram = reinterpret_cast<float *>(sm + F_A1); // [128][64], column XOR row % 32
-    float *Gc = reinterpret_cast<float *>(sm + F_FAC);
-    float *Cc = Gc + kT * kLd;
-    float *Za = Cc + kT * kLd;
-    float *Zb = Za + kT * kLd;
-    float *Wc = Zb + kT * kLd;
-    uint8_t *ancat = sm + F_ANCAT;
-    uint16_t *pairs = reinterpret_cast<uint16_t *>(sm + F_PAIRS);
-    float *Ls = reinterpret_cast<float *>(sm + F_L);
-    float *Bs = reinterpret_cast<float *>(sm + F_BETA);
-    int *Ds = reinterpret_cast<int *>(sm + F_DEPTH);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + F_BAR); // A1, Gram
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + F_MISC);
-    int *npair = reinterpret_cast<int *>(sm + F_MISC + 4);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x;
-    const int b = unit / H, h = unit % H;
-    if (faulted(st)) return;
-    const int o = offsets[b], T = offsets[b + 1] - o;
-    if (T <= 0) return;
-    const int d = req_depth[b];
-    if (T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T) {
-        if (tid == 0)
-            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
-                   -1, T > kT ? T : d);
-        return;
-    }
-
-    if (tid == 32) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(tslot, 64);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    bool ok = true;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[0], 32768);
-#pragma unroll
-        for (int ka = 0; ka < 2; ++ka) {
-            tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[0], 64 * ka, h, o);
-            tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[0], 64 * ka, h, o);
-        }
-    }
-
-    // ---- topology, cumulative decay and the (node, ancestor slot) pair list ----
-    // Warps 0 and 1 own rows 0..63 (row = tid) and also read the partner row
-    // tid ^ 32, so each warp sees every row's gate and depth through shuffles:
-    // L_i = sum of log gamma over the ancestors-or-self of i (the prefix along
-    // parent links, Lemma 1), the ancestor-by-depth table, and the offsets of
-    // each row's pairs by a 64-row scan, without a barrier.
-    if (tid < kT) {
-        const int i = tid, ip = i ^ 32;
-        int di = -1, dp = -1;
-        uint64_t mi = 0;
-        float bi = 0.f, lgi = 0.f, lgp = 0.f;
-        if (i < T) {
-            const size_t nh = (size_t)(o + i) * H + h;
-            di = depth_g[o + i];
-            const uint2 m2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
-            mi = ((uint64_t)m2.y << 32) | m2.x;
-            bi = beta[nh];
-            lgi = logf(gamma[nh]);
-        }
-        if (ip < T) {
-            dp = depth_g[o + ip];
-            lgp = logf(gamma[(size_t)(o + ip) * H + h]);
-        }
-        const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
-        const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
-        const int cnt = di + 1;
-        int maxcnt = cnt;
-#pragma unroll
-        for (int sft = 16; sft > 0; sft >>= 1)
-            maxcnt = max(maxcnt, __shfl_xor_sync(0xffffffffu, maxcnt, sft));
-        float L = 0.f;
-        uint64_t mm = mi;
-        for (int t = 0; t < maxcnt; ++t) {
-            const int j = mm ? __ffsll((long long)mm) - 1 : 0;
-            const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
-            const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
-            if (mm) {
-                L += (j < 32) ? vlo : vhi;
-                ancat[i * kSlots + t] = (uint8_t)j;
-                mm &= mm - 1;
-            }
-        }
-        int c_lo = (i < 32) ? cnt : dp + 1, c_hi = (i < 32) ? dp + 1 : cnt;
-#pragma unroll
-        for (int sft = 1; sft < 32; sft <<= 1) {
-            const int ylo = __shfl_up_sync(0xffffffffu, c_lo, sft);
-            const int yhi = __shfl_up_sync(0xffffffffu, c_hi, sft);
-            if (lane >= sft) {
-                c_lo += ylo;
-                c_hi += yhi;
-            }
-        }
-        const int tot_lo = __shfl_sync(0xffffffffu, c_lo, 31);
-        const int tot_hi = __shfl_sync(0xffffffffu, c_hi, 31);
-        const int start = ((i < 32) ? c_lo : tot_lo + c_hi) - cnt;
-        for (int t = 0; t < cnt; ++t) {
-            pairs[start + t] = (uint16_t)((i << 8) | t);
-            const float id = (t == di) ? 1.f : 0.f; // Z^(0) = W = identity
-            Za[i * kLd + t] = id;
-            Wc[i * kLd + t] = id;
-        }
-        Ds[i] = di;
-        Bs[i] = bi;
-        Ls[i] = L;
-        if (i < T) logP[(size_t)(o + i) * H + h] = L;
-        if (i == 0) *npair = tot_lo + tot_hi;
-    }
-
-    // ---- Gram [Q;K] K^T on the tensor core, staged back into the [Q;K] buffer ----
-    if (tid == 0) {
-        ok &= mbar_wait(&bar[0], 0, kWaitNs);
-        tc_fence_after();
-        const uint32_t a1 = smem_addr(sA1);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem, sdesc_sw128(a1 + off, 16, 1024),
-                        sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
-        }
-        mma_commit(&bar[1]);
-    }
-    ok &= mbar_wait(&bar[1], 0, kWaitNs);
-    tc_fence_after();
-    {
-        const int rowgrp = warp & 3, half = warp >> 2;
-        const int m = rowgrp * 32 + lane; // row 0..63 q_i.k_j, 64..127 k_i.k_j
-        float g[32];
-        tmem_ld32(tmem + ((uint32_t)(rowgrp * 32) << 16) + half * 32, g);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) gram[m * 64 + ((half * 32 + t) ^ (m & 31))] = g[t];
-    }
-    tc_fence_before();
-    __syncthreads();
-    const int P = *npair;
-
-    // ---- compact C and G, one thread per (node, ancestor slot) pair ----
-    for (int p = tid; p < P; p += kFThreads) {
-        const int pr = pairs[p];
-        const int i = pr >> 8, t = pr & 255;
-        const int j = ancat[i * kSlots + t];
-        const float ratio = __expf(Ls[i] - Ls[j]);
-        Cc[i * kLd + t] = ratio * gram[i * 64 + (j ^ (i & 31))];
-        if (t < Ds[i]) Gc[i * kLd + t] = Bs[i] * ratio * gram[(64 + i) * 64 + (j ^ (i & 31))];
-    }
-    __syncthreads();
-
-    // ---- W = sum_{m<=d} (-G)^m by Z <- -G Z, W += Z (Eq. (8) on the identity) ----
-    // Pair (i, t): row i's coefficient on its ancestor at depth t.  Z^(m) can be
-    // nonzero only where depth(i) - t >= m; one thread per pair.
-    {
-        float *Zc = Za, *Zn = Zb;
-        for (int step = 0; step < d; ++step) {
-            for (int p = tid; p < P; p += kFThreads) {
-                const int pr = pairs[p];
-                const int i = pr >> 8, t = pr & 255;
-                const int di = Ds[i];
-                if (t + step >= di) continue;
-                const float *gi = Gc + i * kLd;
-                const uint8_t *ai = ancat + i * kSlots;
-                float v0 = 0.f, v1 = 0.f;
-                int s2 = t + step;
-                for (; s2 + 1 < di; s2 += 2) {
-                    v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
-                    v1 = fmaf(gi[s2 + 1], Zc[ai[s2 + 1] * kLd + t], v1);
-                }
-                if (s2 < di) v0 = fmaf(gi[s2], Zc[ai[s2] * kLd + t], v0);
-                const float val = -(v0 + v1);
-                Zn[i * kLd + t] = val;
-                Wc[i * kLd + t] += val;
-            }
-            __syncthreads();
-            float *tmp = Zc; Zc = Zn; Zn = tmp;
-        }
-    }
-
-    // ---- M = C W and W as pair records ----
-    PairRec *out = recs + ((size_t)o * H + (size_t)h * T) * kSlots;
-    for (int p = tid; p < P; p += kFThreads) {
-        const int pr = pairs[p];
-        const int i = pr >> 8, t = pr & 255;
-        const int di = Ds[i];
-        const float *ci = Cc + i * kLd;
-        const uint8_t *ai = ancat + i * kSlots;
-        float mval = 0.f;
-        for (int s2 = t; s2 <= di; ++s2) mval = fmaf(ci[s2], Wc[ai[s2] * kLd + t], mval);
-        PairRec r;
-        r.m = mval;
-        r.w = Wc[i * kLd + t];
-        r.i = i;
-        r.j = ai[t];
-        out[p] = r;
-    }
-    if (tid == 0) {
-        counts[unit] = P;
-        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
-    }
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
-}
-
-// =====================================================================
-// solve kernel: value tile = the whole head (b_v = d_v = 128)
-// =====================================================================
-// Shared-memory plan (bytes from a 1024-aligned base), two CTAs per SM:
-//   S buffer (64 KB): four 16 KB boxes [128 rows x 128 B] of fp32 S_pre; the
-//     in-place split turns boxes (0,1) into (S_hi, S_lo) of columns 0..63 and
-//     boxes (2,3) into those of columns 64..127 (bf16, 128B-swizzled,
-//     N-contiguous); after the state products it holds [M;W] (first 32 KB,
-//     tf32 K-major) and R^T (second 32 KB, tf32 K-major).
-//   A1 (32 KB): [Q;K] bf16 K-major (rows 0..63 q, 64..127 k).
-//   V (16 KB): the head's value rows, two 128B-swizzled boxes [64 rows x 64
-//     bf16], loaded by TMA beside the state so the epilogue reads them from
-//     shared memory (row-per-thread global loads cost several microseconds).
-// Tensor memory (256 columns, 128 lanes = operand rows): columns 0..127 hold
-// [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R].  The
-// epilogues only read it, so no tensor-memory store sits between the state
-// products and the second MMA.
-constexpr int OFF_SBUF = 0;
-constexpr int SBUF_BYTES = 65536;
-constexpr int OFF_A1 = SBUF_BYTES;
-constexpr int OFF_V = OFF_A1 + 32768;
-constexpr int OFF_BAR = OFF_V + 16384;        // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 8 * 8;     // TMEM slot
-constexpr int SOLVE_END = OFF_MISC + 16;
-// Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
-// plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
-// dynamic base, which is aligned when the kernel has no static shared memory
-// (checked in the kernel).  A request at the 113 KB edge would drop to one CTA
-// per SM as soon as anything else claimed shared memory.
-constexpr int SOLVE_SMEM = SOLVE_END + 256;
-static_assert(2 * (SOLVE_SMEM + 1024) <= 228 * 1024, "two solve CTAs per SM");
-static_assert(3 * SOLVE_SMEM > 228 * 1024, "at most two solve CTAs (2 x 256 TMEM columns) per SM");
-
-constexpr int kComputeThreads = 256;          // warps 0..7: split, epilogues, scatter
-constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
-
-constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
-constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
-
-// mbarrier slots
-constexpr int BAR_S = 0, BAR_A1 = 1, BAR_STATE = 2, BAR_MMA2 = 3, BAR_CONV = 4, BAR_OPS = 5,
-              BAR_V = 6;
-
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
 {
     const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -376,40 +140,42 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
     }
 }
 
-
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Barrier among the compute warps only (the issue warp keeps running).
-__device__ __forceinline__ void compute_sync()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
-}
+// Named barriers (0 is __syncthreads): the factor warps 0..3, and the four
+// warps that own operand rows 0..63 (0, 1, 4, 5).
+__device__ __forceinline__ void factor_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// One CTA per (request, head): state products on tcgen05, R, and the
-// propagation + read-out product [M; W] R.  Warp 8 streams operands and
-// issues the tensor-core products; warps 0..7 do everything else.  All waits
-// are bounded.
+// Verification kernel: one CTA per (request, head).  Warp 8 streams operands
+// and issues the tensor-core products.  Warps 0..3 build the tree factors
+// while warps 4..7 split S_pre as soon as it lands, so the state products run
+// beside the factor work; all eight share the epilogues.  All waits are
+// bounded.
 __global__ void __launch_bounds__(kThreads, 2)
-tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
-                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                const float *__restrict__ beta, const int32_t *__restrict__ offsets,
-                const int32_t *__restrict__ req_depth, const float *__restrict__ logP,
-                const PairRec *__restrict__ recs, const int32_t *__restrict__ counts, int H, int N,
-                __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout, int32_t *st)
+tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const float *__restrict__ gamma, const float *__restrict__ beta,
+                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
+                 const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth, int H,
+                 int N, __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
+                 float *__restrict__ logP, int32_t *st)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sbuf = sm + OFF_SBUF;
     uint8_t *sA1 = sm + OFF_A1;
-    uint8_t *sV = sm + OFF_V;
+    uint8_t *sV = sm + OFF_A1; // the value rows reuse [Q;K] once the state products are done
+    float *Gc = reinterpret_cast<float *>(sm + X_G);
+    float *Cc = reinterpret_cast<float *>(sm + X_C);
+    uint8_t *ancat = sm + X_ANCAT;
+    float *Ls = reinterpret_cast<float *>(sm + X_L);
+    uint64_t *Ms = reinterpret_cast<uint64_t *>(sm + X_MASK);
+    int *Ds = reinterpret_cast<int *>(sm + X_DEPTH);
+    float *Rt = reinterpret_cast<float *>(sm + X_RATIO);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
 
@@ -417,24 +183,62 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
 
-    // Uniform early exits, before any barrier or tensor-memory allocation
-    // (the factor kernel reported any fault of this head).
-    if (faulted(st)) return;
-    const int o = offsets[b], T = offsets[b + 1] - o;
-    if (T <= 0) return;
-    const int d = req_depth[b];
-    if (T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T) return;
-    if (sm + SOLVE_END > smem_raw + SOLVE_SMEM) { // dynamic base too far from 1024 B
+    if (sm + VERIFY_END > smem_raw + VERIFY_SMEM) { // dynamic base too far from 1024 B
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
-
-    if (tid == 32) {
+    // The state tile depends on the head alone: it is requested first, by the
+    // thread that initialises the barriers, while the others read the tree.
+    const bool issuer = tid == kComputeThreads;
+    if (issuer) {
         for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
-        mbar_init(&bar[BAR_V], 1);
-        mbar_init(&bar[BAR_CONV], kComputeThreads);
+        mbar_init(&bar[BAR_TOPO], kT);
+        mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+    }
+    // The status word, the request's extent and its depth in one round trip;
+    // uniform early exits (the issuing thread drains the state copy first).
+    const int fault = *(const volatile int32_t *)st;
+    const int o = offsets[b], T = offsets[b + 1] - o, d = req_depth[b];
+    const bool bad = T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T;
+    if (fault != 0 || T <= 0 || bad) {
+        if (bad && T > 0 && tid == 0 && h == 0)
+            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
+                   -1, T > kT ? T : d);
+        if (issuer) mbar_wait(&bar[BAR_S], 0, kWaitNs);
+        return;
+    }
+    if (issuer) {
+        mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
+#pragma unroll
+        for (int ka = 0; ka < 2; ++ka) {
+            tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
+            tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[BAR_A1], 64 * ka, h, o);
+        }
+    }
+    // Per-thread tree inputs, requested before the CTA barrier.
+    const int rowgrp = warp & 3, half = warp >> 2;
+    const int m = rowgrp * 32 + lane; // TMEM lane = operand row
+    const int i = m & 63;             // this thread's node
+    float bt = 0.f;                   // beta_i (rows 64..127: K side)
+    int my_depth = -1;                // topology threads (rows 0..63, warps 0 and 1)
+    uint2 anc2 = make_uint2(0, 0);
+    float g_i = 1.f, g_p = 1.f;
+    if (warp < 8) {
+        if (m >= 64 && i < T) bt = beta[(size_t)(o + i) * H + h];
+        if (tid < kT) {
+            if (i < T) {
+                my_depth = depth_g[o + i];
+                anc2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
+                g_i = gamma[(size_t)(o + i) * H + h];
+            }
+            if ((i ^ 32) < T) g_p = gamma[(size_t)(o + (i ^ 32)) * H + h];
+        }
     }
     if (warp == 0) {
         tmem_alloc(tslot, 256);
@@ -444,31 +248,26 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
 
     if (warp == kComputeThreads / 32) {
         // =========================== issue warp ===========================
-        const uint32_t a1 = smem_addr(sA1), s0 = smem_addr(sbuf);
         bool ok = true;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+            const uint32_t a1 = smem_addr(sA1), s0 = smem_addr(sbuf);
+            // Gram [Q;K] K^T
+            ok &= mbar_wait(&bar[BAR_A1], 0, kWaitNs);
+            tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
-            mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
-#pragma unroll
-            for (int ka = 0; ka < 2; ++ka) {
-                tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
-                tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[BAR_A1], 64 * ka, h, o);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_bf16_ss(tmem + TM_GRAM, sdesc_sw128(a1 + off, 16, 1024),
+                            sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
             }
-            mbar_arrive_expect_tx(&bar[BAR_V], 16384);
-            tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
-            tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
-        }
-        // state products [Q;K] (S_hi + S_lo) once the split is in place
-        ok &= mbar_wait(&bar[BAR_A1], 0, kWaitNs);
-        ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
-        tc_fence_after();
-        if (lane == 0) {
+            mma_commit(&bar[BAR_GRAM]);
+            // state products [Q;K] (S_hi + S_lo) once the split is in place
+            ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
+            tc_fence_after();
             const uint32_t slo = s0 + 16384;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -477,103 +276,216 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 mma_bf16_ss(tmem, ad, sdesc_sw128(slo + kk * 2048, 32768, 1024), IDESC_STATE, 1);
             }
             mma_commit(&bar[BAR_STATE]);
-        }
-        __syncwarp();
-        // propagation + read-out: [M; W] R accumulated onto [B0; 0]
-        ok &= mbar_wait(&bar[BAR_OPS], 0, kWaitNs);
-        tc_fence_after();
-        if (lane == 0) {
+            // value rows into the [Q;K] buffer, which the products have released
+            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            mbar_arrive_expect_tx(&bar[BAR_V], 16384);
+            tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
+            tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
+            // propagation + read-out: [M; W] R into its own 128 columns
+            ok &= mbar_wait(&bar[BAR_OPS], 0, kWaitNs);
+            tc_fence_after();
             const uint32_t b2 = s0 + 32768;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_tf32_ss(tmem + 128, sdesc_sw128(s0 + off, 16, 1024),
+                mma_tf32_ss(tmem + TM_PROP, sdesc_sw128(s0 + off, 16, 1024),
                             sdesc_sw128(b2 + off, 16, 1024), IDESC_TF32, kk > 0);
             }
             mma_commit(&bar[BAR_MMA2]);
         }
         __syncwarp();
-        if (!ok && lane == 0) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
+        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
     } else {
         // ========================== compute warps =========================
-        const int rowgrp = warp & 3, half = warp >> 2;
-        const int m = rowgrp * 32 + lane;    // TMEM lane = operand row
-        const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
         bool ok = true;
-        // this thread's operand row: P_i for both halves, beta_i for the K half
-        const int i = m & 63;
-        const float p = (i < T) ? expf(logP[(size_t)(o + i) * H + h]) : 0.f;
-        const float bt = (m >= 64 && i < T) ? beta[(size_t)(o + i) * H + h] : 0.f;
-        // this thread's pair records (at most kMaxPairs / 256 = 4), fetched early
-        const int P = counts[unit];
-        const PairRec *rin = recs + ((size_t)o * H + (size_t)h * T) * kSlots;
-        PairRec rec[kMaxPairs / kComputeThreads];
+        uint4 a4 = make_uint4(0, 0, 0, 0); // rows 0..63: ancestor table, kept for the scatter
+        if (warp < 4) {
+            // ---------------- factor warps: C, G, then W and M ----------------
+            if (tid < kT) {
+                // Topology and cumulative decay (row = tid).  Each warp also holds
+                // the partner row tid ^ 32, so it sees every row's log gamma
+                // through shuffles: L_i = sum over the ancestors-or-self of i (the
+                // prefix along parent links, Lemma 1) and the ancestor-by-depth
+                // table, without a barrier.  The walk passes the ancestors in
+                // depth order, so the partial sums are their L_j, which give the
+                // row's decay ratios exp(L_i - L_j) by slot.
+                const uint64_t mi = ((uint64_t)anc2.y << 32) | anc2.x;
+                const float lgi = logf(g_i), lgp = logf(g_p);
+                const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
+                const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
+                float L = 0.f, pre[kSlots];
+                uint64_t mm = mi;
 #pragma unroll
-        for (int u = 0; u < kMaxPairs / kComputeThreads; ++u) {
-            const int p = tid + u * kComputeThreads;
-            if (p < P) rec[u] = rin[p];
-        }
-
-        // ---- S_pre = S_hi + S_lo in place (bf16, N-contiguous, 64-column atoms) ----
-        ok &= mbar_wait(&bar[BAR_S], 0, kWaitNs);
-        {
-            const int r = tid & 127, p = tid >> 7; // row r, columns 64p .. 64p+63
-            uint8_t *box0 = sbuf + (2 * p) * 16384, *box1 = box0 + 16384;
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(box0 + sw128_chunk(r, c));
-                const float4 a1v = *reinterpret_cast<const float4 *>(box1 + sw128_chunk(r, c));
-                x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z; x[4 * c + 3] = a0.w;
-                x[32 + 4 * c + 0] = a1v.x; x[32 + 4 * c + 1] = a1v.y;
-                x[32 + 4 * c + 2] = a1v.z; x[32 + 4 * c + 3] = a1v.w;
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-                    hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+                for (int t = 0; t < kSlots; ++t) {
+                    const int j = mm ? __ffsll((long long)mm) - 1 : 0;
+                    const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
+                    const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
+                    if (t <= my_depth) {
+                        L += (j < 32) ? vlo : vhi;
+                        ancat[i * kSlots + t] = (uint8_t)j;
+                        mm &= mm - 1;
+                    }
+                    pre[t] = L; // L_j of the ancestor at depth t
                 }
-                *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) =
-                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) =
-                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                float *rrow = Rt + i * kLd;
+#pragma unroll
+                for (int t = 0; t < kSlots; ++t)
+                    if (t <= my_depth) rrow[t] = __expf(L - pre[t]);
+                Ls[i] = L;
+                Ms[i] = mi;
+                Ds[i] = my_depth;
+                if (i < T) logP[(size_t)(o + i) * H + h] = L;
+                mbar_arrive(&bar[BAR_TOPO]);
             }
+            // Compact C (rows 0..63) and G (rows 64..127) from the Gram: each
+            // thread takes its row's ancestor columns, in depth order.
+            ok &= mbar_wait(&bar[BAR_GRAM], 0, kWaitNs);
+            ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs);
+            tc_fence_after();
+            __syncwarp();
+            {
+                float x[64];
+                tmem_ld32(tmem + TM_GRAM + lane_base, *reinterpret_cast<float(*)[32]>(x));
+                tmem_ld32(tmem + TM_GRAM + 32 + lane_base, *reinterpret_cast<float(*)[32]>(x + 32));
+                const uint64_t mask = Ms[i];
+                const int di = Ds[i];
+                float *dst = (m < 64) ? Cc + i * kLd : Gc + i * kLd;
+                const float *rrow = Rt + i * kLd;
+                const float scale = (m < 64) ? 1.f : bt;
+                const int tmax = (m < 64) ? di : di - 1; // C keeps the diagonal, G does not
+                // Branch-free: every column is evaluated and only the stores
+                // are predicated, so the steps overlap.
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int t = __popcll(mask & ((1ull << c) - 1ull));
+                    const float val = scale * rrow[min(t, kSlots - 1)] * x[c];
+                    if (((mask >> c) & 1ull) && t <= tmax) dst[t] = val;
+                }
+            }
+            factor_sync(); // compact C and G complete
+            if (warp < 2) {
+                // Rows of W and M by backward substitution along the ancestor
+                // path (row = tid), parked in tensor memory until the
+                // propagation operand is free.
+                float mw[2 * kSlots]; // slots 0..15 M (z), 16..31 W (y)
+#pragma unroll
+                for (int t = 0; t < 2 * kSlots; ++t) mw[t] = 0.f;
+                if (i < T) {
+                    const int di = my_depth;
+                    a4 = *reinterpret_cast<const uint4 *>(ancat + i * kSlots);
+                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                    const float *ci = Cc + i * kLd;
+                    float ay[kSlots], az[kSlots]; // sum_{u > t} y_u G(a_u, a_t), same for z
+#pragma unroll
+                    for (int t = 0; t < kSlots; ++t) ay[t] = az[t] = 0.f;
+#pragma unroll
+                    for (int u = kSlots - 1; u >= 0; --u) {
+                        if (u <= di) {
+                            const float y = (u == di) ? 1.f : -ay[u];
+                            const float z = ci[u] - az[u];
+                            mw[u] = z;
+                            mw[kSlots + u] = y;
+                            const int au = (aw[u >> 2] >> (8 * (u & 3))) & 0xff;
+                            const float *gr = Gc + au * kLd;
+#pragma unroll
+                            for (int t = 0; t < u; ++t) {
+                                const float g = gr[t];
+                                ay[t] = fmaf(y, g, ay[t]);
+                                az[t] = fmaf(z, g, az[t]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                tmem_st32(tmem + TM_MW + lane_base, mw);
+                tmem_wait_st();
+            }
+        } else {
+            // --------- split warps: S_pre = S_hi + S_lo in place (row r) ---------
+            // bf16, N-contiguous, 64-column atoms: boxes (0,1) <- columns 0..63,
+            // boxes (2,3) <- columns 64..127.
+            const int r = tid - 128;
+            ok &= mbar_wait(&bar[BAR_S], 0, kWaitNs);
+#pragma unroll 1
+            for (int pc = 0; pc < 2; ++pc) {
+                uint8_t *box0 = sbuf + (2 * pc) * 16384, *box1 = box0 + 16384;
+                float x[64];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(box0 + sw128_chunk(r, c));
+                    const float4 a1v = *reinterpret_cast<const float4 *>(box1 + sw128_chunk(r, c));
+                    x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z; x[4 * c + 3] = a0.w;
+                    x[32 + 4 * c + 0] = a1v.x; x[32 + 4 * c + 1] = a1v.y;
+                    x[32 + 4 * c + 2] = a1v.z; x[32 + 4 * c + 3] = a1v.w;
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+                        hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+                    }
+                    *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) =
+                        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) =
+                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar[BAR_CONV]);
+            ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs); // L_i for P_i below
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar[BAR_CONV]);
+        const float p = (i < T) ? expf(Ls[i]) : 0.f; // P_i
 
-        // ---- state epilogue: rows 0..63 zero the [M; W] operand; rows 64..127
-        //      write R^T = (beta (v - P K S_pre))^T.  No tensor-memory stores:
-        //      Q S_pre stays in columns 0..127 and is scaled by P at the output ----
+        // ---- epilogue of the state products.  Rows 0..63 (warps 0, 1, 4, 5)
+        //      zero the [M; W] operand, then warps 0 and 1 scatter their rows;
+        //      warps 6 and 7 write R^T = (beta (v - P K S_pre))^T, all 128
+        //      columns of their rows ----
         ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
         tc_fence_after();
         if (m < 64) {
             float4 *a2z = reinterpret_cast<float4 *>(sbuf);
-            const int zt = (half * 64 + m); // 0..127
+            const int zt = half * 64 + m; // 0..127
 #pragma unroll
             for (int e = 0; e < 16; ++e) a2z[zt + e * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-            uint8_t *sB2 = sbuf + 32768;
-            uint8_t *dst = sB2 + (i >> 5) * 16384;
-            const uint8_t *vrow = sV + half * 8192 + i * 128; // 64 columns of row i
+            upper_sync();
+            if (warp < 2) {
+                float mw[2 * kSlots];
+                __syncwarp();
+                tmem_ld32(tmem + TM_MW + lane_base, mw);
+                if (i < T) {
+                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int t = 0; t < kSlots; ++t) {
+                        if (t <= my_depth) {
+                            const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
+                            uint8_t *col = sbuf + (j >> 5) * 16384;
+                            *reinterpret_cast<float *>(col + sw128_offset(i, j & 31)) = mw[t];
+                            *reinterpret_cast<float *>(col + sw128_offset(64 + i, j & 31)) =
+                                mw[kSlots + t];
+                        }
+                    }
+                }
+            }
+        } else if (warp >= 4) {
+            uint8_t *dst = sbuf + 32768 + (i >> 5) * 16384;
             ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col0 = half * 64 + cc * 32;
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col0 = cc * 32;
+                const uint8_t *vrow = sV + (cc >> 1) * 8192 + i * 128; // 64 columns of row i
                 float x[32];
                 tmem_ld32(tmem + lane_base + col0, x);
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     float f[8];
                     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
+                                      vrow + ((((cc & 1) * 4 + uu) ^ (i & 7)) << 4)), f);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         const int c = 8 * uu + t;
@@ -581,17 +493,6 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                         *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i & 31)) = r;
                     }
                 }
-            }
-        }
-        compute_sync(); // operand zeroed
-        // ---- [M; W] from the factor kernel's pair records ----
-#pragma unroll
-        for (int u = 0; u < kMaxPairs / kComputeThreads; ++u) {
-            if (tid + u * kComputeThreads < P) {
-                const PairRec r = rec[u];
-                uint8_t *col = sbuf + (r.j >> 5) * 16384;
-                *reinterpret_cast<float *>(col + sw128_offset(r.i, r.j & 31)) = r.m;
-                *reinterpret_cast<float *>(col + sw128_offset(64 + r.i, r.j & 31)) = r.w;
             }
         }
         fence_proxy_async_smem();
@@ -607,7 +508,7 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             for (int cc = 0; cc < 2; ++cc) {
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
-                tmem_ld32(tmem + 128 + lane_base + col0, x);
+                tmem_ld32(tmem + TM_PROP + lane_base + col0, x);
                 if (m < 64) {
                     float y[32];
                     tmem_ld32(tmem + lane_base + col0, y);
@@ -617,24 +518,24 @@ tc_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 if (!store) continue;
                 const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
                 if (m < 64) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(O + row);
+                    uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
 #pragma unroll
                     for (int uu = 0; uu < 4; ++uu) {
                         __nv_bfloat162 p2[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t)
                             p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
-                        dst[uu] = *reinterpret_cast<uint4 *>(p2);
+                        dsto[uu] = *reinterpret_cast<uint4 *>(p2);
                     }
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(Uout + row);
+                    float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
 #pragma unroll
                     for (int uu = 0; uu < 8; ++uu)
-                        dst[uu] = make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
+                        dstu[uu] = make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
                 }
             }
         }
-        if (!ok && tid == 0) report(st, BOLE_ERR_TIMEOUT, b, -1, 1);
+        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -885,11 +786,7 @@ bool tc_verify_supported(const VerifyArgs &a)
            a.max_depth < kSlots;
 }
 
-size_t tc_workspace_bytes(int B, int H, int max_T)
-{
-    const size_t recs = (size_t)B * max_T * H * kSlots * sizeof(PairRec);
-    return recs + (size_t)B * H * sizeof(int32_t);
-}
+size_t tc_workspace_bytes(int, int, int) { return 0; }
 
 // q or k [N][H][128] bf16 as a 3-D tensor, boxes of 64 elements x 1 head x 64 nodes.
 cudaError_t make_node_map(CUtensorMap *map, const void *x, int N, int H)
@@ -916,26 +813,15 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H);
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H);
     if (e != cudaSuccess) return e;
-    PairRec *recs = static_cast<PairRec *>(a.ws);
-    int32_t *counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a.ws) +
-                                                  (size_t)a.B * a.max_T * a.H * kSlots * sizeof(PairRec));
-    e = cudaFuncSetAttribute(tc_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             FACTOR_SMEM);
-    if (e != cudaSuccess) return e;
-    tc_factor_kernel<<<units, kFThreads, FACTOR_SMEM, s>>>(
-        mQ, mK, a.gamma, a.beta, a.offsets, a.depth, a.anc, a.req_depth, a.H, a.N, a.logP, recs,
-        counts, a.st);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SOLVE_SMEM);
+    e = cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             VERIFY_SMEM);
     if (e != cudaSuccess) return e;
-    tc_solve_kernel<<<units, kThreads, SOLVE_SMEM, s>>>(
-        mS, mQ, mK, mV, a.beta, a.offsets, a.req_depth,
-        a.logP, recs, counts, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U, a.st);
+    tc_verify_kernel<<<units, kThreads, VERIFY_SMEM, s>>>(
+        mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.depth, a.anc, a.req_depth, a.H, a.N,
+        static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, a.st);
     return cudaGetLastError();
 }
 

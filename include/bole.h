@@ -89,14 +89,14 @@ const char *bole_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int bole_version(void);
 
-/* Bytes of device workspace bole_tree_verify needs for these sizes.  max_T
- * bounds every tree's node count (1..128) and max_depth every tree's depth
- * (0..127); pass the same values, dtype and flags as to bole_tree_verify.
- * The workspace holds the short-lived tree factors of one call -- the
- * "verification scratch" of the pages' state lifecycle (Section IV-D): dense
- * G, C on the CUDA-core path, compact per-(node, ancestor) records of
- * M = C (I+G)^{-1} and (I+G)^{-1} on the tensor-core path -- and may be
- * reused by the next call once that call's kernels have finished. */
+/* Bytes of device workspace bole_tree_verify needs for these sizes (0 when
+ * the chosen kernel keeps every intermediate on chip, as the tensor-core
+ * kernel does).  max_T bounds every tree's node count (1..128) and max_depth
+ * every tree's depth (0..127); pass the same values, dtype and flags as to
+ * bole_tree_verify.  The workspace holds the short-lived tree factors (dense
+ * G, C) of one call on the CUDA-core path -- the "verification scratch" of the
+ * pages' state lifecycle (Section IV-D) -- and may be reused by the next call
+ * once that call's kernels have finished. */
 size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_depth,
                            bole_dtype qkv_dtype, unsigned flags);
 

@@ -53,9 +53,9 @@ def test_workspace_size_rules(lib):
     f.restype = ctypes.c_size_t
     # fp32 inputs use the CUDA-core path: two dense T x T factors per unit
     assert f(2, 3, 16, 16, 8, 3, 0, 0) == 2 * 4 * 2 * 3 * 8 * 8
-    # bf16, dk = dv = 128, trees <= 64 nodes of depth <= 15: tensor-core kernels, whose
-    # workspace holds 16 pair records of 16 bytes per node and head, plus a count per head
-    assert f(2, 3, 128, 128, 64, 15, 1, 0) == 2 * 64 * 3 * 16 * 16 + 2 * 3 * 4
+    # bf16, dk = dv = 128, trees <= 64 nodes of depth <= 15: tensor-core kernel, every
+    # intermediate on chip, no workspace
+    assert f(2, 3, 128, 128, 64, 15, 1, 0) == 0
     # deeper bound or forced CUDA-core path: workspace
     assert f(2, 3, 128, 128, 64, 16, 1, 0) == 2 * 4 * 2 * 3 * 64 * 64
     assert f(2, 3, 128, 128, 64, 8, 1, 1) == 2 * 4 * 2 * 3 * 64 * 64
