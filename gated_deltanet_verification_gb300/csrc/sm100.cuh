@@ -53,15 +53,33 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Bounded wait on an mbarrier phase: false once `limit_ns` has passed.
+// try_wait that may suspend the thread for up to `hint_ns` while the phase
+// is incomplete; the thread resumes as soon as the phase completes.  A
+// suspended warp issues nothing, so waiting warps leave the scheduler to the
+// warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: false once `limit_ns` has passed.  Each
+// try suspends for at most 20 us, and the bound is checked after every one.
 // Kept out of line: it is called from many places and is never hot.
 static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -65,34 +65,36 @@ constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 200 ms bound on any device
 //   S buffer (64 KB): four 16 KB boxes [128 rows x 128 B] of fp32 S_pre; the
 //     in-place split turns boxes (0,1) into (S_hi, S_lo) of columns 0..63 and
 //     boxes (2,3) into those of columns 64..127 (bf16, 128B-swizzled,
-//     N-contiguous); after the state products it holds [M;W] (first 32 KB)
-//     and R^T (second 32 KB), both tf32 K-major.
-//   A1 (32 KB): [Q;K] bf16 K-major, operand of the Gram and the state products.
-//   V (16 KB): first the factor scratch (compact C and G, ancestor table,
-//     decays, masks), then the head's value rows by TMA: two 128B-swizzled
-//     boxes [64 rows x 64 bf16], read by the epilogue from shared memory.
+//     N-contiguous).  Once the first d_k half of the state products has
+//     read rows 0..63 of every box, those rows (first 8 KB of each box) hold
+//     the staged Gram; after the whole product the first 32 KB hold [M;W]
+//     and the second 32 KB R^T, both tf32 K-major.
+//   A1 (32 KB): [Q;K] bf16 K-major, operand of the Gram and the state
+//     products; once the first d_k half is done, its first 16 KB take the
+//     head's value rows by TMA (two 128B-swizzled boxes [64 rows x 64 bf16]),
+//     read by the epilogue from shared memory.
+//   X (10 KB): the factor scratch (compact C and G, ancestor table, decays,
+//     depths).
 // Tensor memory (256 columns, lane = operand row): columns 0..127 hold
 // [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R]; before the
-// propagation, 128..191 hold the Gram and 192..223 (lanes 0..63) the rows of
-// M and W.  The epilogues only read tensor memory.
+// propagation, 128..191 hold the Gram.  The epilogues only read tensor memory.
 constexpr int OFF_SBUF = 0;
 constexpr int SBUF_BYTES = 65536;
 constexpr int OFF_A1 = SBUF_BYTES;
-constexpr int OFF_V = OFF_A1 + 32768;
-constexpr int OFF_BAR = OFF_V + 16384;        // mbarriers
+constexpr int OFF_X = OFF_A1 + 32768;         // factor scratch
+constexpr int X_BYTES = 10240;
+constexpr int OFF_BAR = OFF_X + X_BYTES;      // mbarriers
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;    // TMEM slot
 constexpr int VERIFY_END = OFF_MISC + 16;
-// factor scratch inside V
+// factor scratch
 constexpr int FAC_BYTES = kT * kLd * 4;       // one compact factor [64][17] f32
-constexpr int X_G = OFF_V;                    // G (row i, ancestor slot t < depth(i))
+constexpr int X_G = OFF_X;                    // G (row i, ancestor slot t < depth(i))
 constexpr int X_C = X_G + FAC_BYTES;          // C (row i, ancestor slot t <= depth(i))
 constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i at depth t
 constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
-constexpr int X_MASK = X_L + kT * 4;          // u64 ancestor-or-self masks
-constexpr int X_DEPTH = X_MASK + kT * 8;
-constexpr int X_RATIO = X_DEPTH + kT * 4;     // exp(L_i - L_j), j the ancestor of i at depth t
-static_assert(X_RATIO + FAC_BYTES <= OFF_V + 16384, "factor scratch fits the value buffer");
-static_assert(X_ANCAT % 16 == 0 && X_MASK % 8 == 0, "vector-aligned scratch rows");
+constexpr int X_DEPTH = X_L + kT * 4;
+static_assert(X_DEPTH + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
 // dynamic base, which is aligned when the kernel has no static shared memory
@@ -109,11 +111,11 @@ constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
 constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
 constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
 constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
-constexpr uint32_t TM_GRAM = 128, TM_MW = 192, TM_PROP = 128;      // tensor-memory columns
+constexpr uint32_t TM_GRAM = 128, TM_PROP = 128;                  // tensor-memory columns
 
 // mbarrier slots
-constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE = 4, BAR_MMA2 = 5,
-              BAR_TOPO = 6, BAR_CONV = 7, BAR_OPS = 8;
+constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, BAR_STATE = 5,
+              BAR_MMA2 = 6, BAR_TOPO = 7, BAR_STAGED = 8, BAR_CG = 9, BAR_CONV = 10, BAR_OPS = 11;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
@@ -145,15 +147,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Named barriers (0 is __syncthreads): the factor warps 0..3, and the four
-// warps that own operand rows 0..63 (0, 1, 4, 5).
-__device__ __forceinline__ void factor_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-
 // Verification kernel: one CTA per (request, head).  Warp 8 streams operands
-// and issues the tensor-core products.  Warps 0..3 build the tree factors
-// while warps 4..7 split S_pre as soon as it lands, so the state products run
-// beside the factor work; all eight share the epilogues.  All waits are
+// and issues the tensor-core products.  Warps 0..7 share the rest:
+//   warps 0, 1  topology, decay ratios, staging the q.k Gram rows, gathering
+//               the compact C and G, the rows of W;
+//   warps 2, 3  staging the k.k Gram rows, then R^T for columns 0..63;
+//   warps 4..7  splitting S_pre as soon as it lands; then warps 4, 5 the
+//               rows of M, warps 6, 7 R^T for columns 64..127.
+// The state products run in two halves of d_k: the first half releases the
+// [Q;K] columns that the value rows then overwrite and the S_pre rows where
+// the Gram is staged, so neither waits for the whole product.  All waits are
 // bounded.
 __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
@@ -168,14 +171,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sbuf = sm + OFF_SBUF;
     uint8_t *sA1 = sm + OFF_A1;
-    uint8_t *sV = sm + OFF_A1; // the value rows reuse [Q;K] once the state products are done
+    uint8_t *sV = sm + OFF_A1; // value rows over the first d_k half of [Q;K]
     float *Gc = reinterpret_cast<float *>(sm + X_G);
     float *Cc = reinterpret_cast<float *>(sm + X_C);
     uint8_t *ancat = sm + X_ANCAT;
     float *Ls = reinterpret_cast<float *>(sm + X_L);
-    uint64_t *Ms = reinterpret_cast<uint64_t *>(sm + X_MASK);
     int *Ds = reinterpret_cast<int *>(sm + X_DEPTH);
-    float *Rt = reinterpret_cast<float *>(sm + X_RATIO);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
 
@@ -187,22 +188,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
-    // The state tile depends on the head alone: it is requested first, by the
-    // thread that initialises the barriers, while the others read the tree.
-    const bool issuer = tid == kComputeThreads;
-    if (issuer) {
-        for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
-        mbar_init(&bar[BAR_TOPO], kT);
-        mbar_init(&bar[BAR_CONV], 128);
-        mbar_init(&bar[BAR_OPS], kComputeThreads);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
-    }
     // The status word, the request's extent and its depth in one round trip;
-    // uniform early exits (the issuing thread drains the state copy first).
+    // uniform early exits.
     const int fault = *(const volatile int32_t *)st;
     const int o = offsets[b], T = offsets[b + 1] - o, d = req_depth[b];
     const bool bad = T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T;
@@ -210,10 +197,20 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (bad && T > 0 && tid == 0 && h == 0)
             report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
                    -1, T > kT ? T : d);
-        if (issuer) mbar_wait(&bar[BAR_S], 0, kWaitNs);
         return;
     }
+    // The small, latency-critical reads go out before the 64 KB state tile,
+    // which every CTA requests at once: [Q;K] and the per-thread tree inputs
+    // (below) first, S_pre last.
+    const bool issuer = tid == kComputeThreads;
     if (issuer) {
+        for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
+        mbar_init(&bar[BAR_TOPO], kT);
+        mbar_init(&bar[BAR_STAGED], 128);
+        mbar_init(&bar[BAR_CG], kT);
+        mbar_init(&bar[BAR_CONV], 128);
+        mbar_init(&bar[BAR_OPS], kComputeThreads);
+        fence_mbar_init();
         mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
 #pragma unroll
         for (int ka = 0; ka < 2; ++ka) {
@@ -225,13 +222,14 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const int rowgrp = warp & 3, half = warp >> 2;
     const int m = rowgrp * 32 + lane; // TMEM lane = operand row
     const int i = m & 63;             // this thread's node
-    float bt = 0.f;                   // beta_i (rows 64..127: K side)
-    int my_depth = -1;                // topology threads (rows 0..63, warps 0 and 1)
+    const bool topo = tid < kT;       // warps 0, 1: row i = tid
+    float bt = 0.f;                   // beta_i (topology rows and the K-side rows)
+    int my_depth = -1;
     uint2 anc2 = make_uint2(0, 0);
     float g_i = 1.f, g_p = 1.f;
     if (warp < 8) {
-        if (m >= 64 && i < T) bt = beta[(size_t)(o + i) * H + h];
-        if (tid < kT) {
+        if ((topo || m >= 64) && i < T) bt = beta[(size_t)(o + i) * H + h];
+        if (topo) {
             if (i < T) {
                 my_depth = depth_g[o + i];
                 anc2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
@@ -239,6 +237,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             }
             if ((i ^ 32) < T) g_p = gamma[(size_t)(o + (i ^ 32)) * H + h];
         }
+    }
+    if (issuer) {
+        mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 256);
@@ -265,7 +269,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                             sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
             }
             mma_commit(&bar[BAR_GRAM]);
-            // state products [Q;K] (S_hi + S_lo) once the split is in place
+            // state products [Q;K] (S_hi + S_lo) once the split is in place,
+            // in two halves of d_k (rows 0..63 of S_pre, then 64..127)
             ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
             tc_fence_after();
             const uint32_t slo = s0 + 16384;
@@ -274,19 +279,20 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 const uint64_t ad = sdesc_sw128(a1 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                 mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + kk * 2048, 32768, 1024), IDESC_STATE, kk > 0);
                 mma_bf16_ss(tmem, ad, sdesc_sw128(slo + kk * 2048, 32768, 1024), IDESC_STATE, 1);
+                if (kk == 3) mma_commit(&bar[BAR_STATE_A]);
             }
             mma_commit(&bar[BAR_STATE]);
-            // value rows into the [Q;K] buffer, which the products have released
-            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            // value rows over the [Q;K] columns the first half has released
+            ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
             mbar_arrive_expect_tx(&bar[BAR_V], 16384);
             tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
             tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
             // propagation + read-out: [M; W] R into its own 128 columns
+            // (the K extent is the tree: ceil(T / 8) steps of 8 nodes)
             ok &= mbar_wait(&bar[BAR_OPS], 0, kWaitNs);
             tc_fence_after();
             const uint32_t b2 = s0 + 32768;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < (T + 7) / 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                 mma_tf32_ss(tmem + TM_PROP, sdesc_sw128(s0 + off, 16, 1024),
                             sdesc_sw128(b2 + off, 16, 1024), IDESC_TF32, kk > 0);
@@ -298,109 +304,81 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     } else {
         // ========================== compute warps =========================
         bool ok = true;
-        uint4 a4 = make_uint4(0, 0, 0, 0); // rows 0..63: ancestor table, kept for the scatter
-        if (warp < 4) {
-            // ---------------- factor warps: C, G, then W and M ----------------
-            if (tid < kT) {
-                // Topology and cumulative decay (row = tid).  Each warp also holds
-                // the partner row tid ^ 32, so it sees every row's log gamma
-                // through shuffles: L_i = sum over the ancestors-or-self of i (the
-                // prefix along parent links, Lemma 1) and the ancestor-by-depth
-                // table, without a barrier.  The walk passes the ancestors in
-                // depth order, so the partial sums are their L_j, which give the
-                // row's decay ratios exp(L_i - L_j) by slot.
-                const uint64_t mi = ((uint64_t)anc2.y << 32) | anc2.x;
-                const float lgi = logf(g_i), lgp = logf(g_p);
-                const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
-                const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
-                float L = 0.f, pre[kSlots];
-                uint64_t mm = mi;
+        // Gram row m is staged in the S_pre rows the first d_k half released:
+        // rows 32p..32p+31 in the first 8 KB of box p, 256 B per row, 16-byte
+        // chunks XOR-swizzled by row.
+        auto staged_row = [&](int row) -> float * {
+            return reinterpret_cast<float *>(sbuf + (row >> 5) * 16384 + (row & 31) * 256);
+        };
+        float ratio[kSlots]; // topology rows: exp(L_i - L_j), j the ancestor at depth t
+        uint32_t aw[4] = {0, 0, 0, 0}; // topology rows: ancestor-by-depth table, packed bytes
+        if (topo) {
+            // Topology and cumulative decay (row = tid).  Each warp also holds
+            // the partner row tid ^ 32, so it sees every row's log gamma
+            // through shuffles: L_i = sum over the ancestors-or-self of i (the
+            // prefix along parent links, Lemma 1) and the ancestor-by-depth
+            // table, without a barrier.  The walk passes the ancestors in depth
+            // order, so the partial sums are their L_j.
+            const uint64_t mi = ((uint64_t)anc2.y << 32) | anc2.x;
+            const float lgi = logf(g_i), lgp = logf(g_p);
+            const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
+            const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
+            float L = 0.f;
+            uint64_t mm = mi;
 #pragma unroll
-                for (int t = 0; t < kSlots; ++t) {
-                    const int j = mm ? __ffsll((long long)mm) - 1 : 0;
-                    const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
-                    const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
-                    if (t <= my_depth) {
-                        L += (j < 32) ? vlo : vhi;
-                        ancat[i * kSlots + t] = (uint8_t)j;
-                        mm &= mm - 1;
-                    }
-                    pre[t] = L; // L_j of the ancestor at depth t
+            for (int t = 0; t < kSlots; ++t) {
+                const int j = mm ? __ffsll((long long)mm) - 1 : 0;
+                const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
+                const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
+                if (t <= my_depth) {
+                    L += (j < 32) ? vlo : vhi;
+                    aw[t >> 2] |= (uint32_t)j << (8 * (t & 3));
+                    mm &= mm - 1;
                 }
-                float *rrow = Rt + i * kLd;
-#pragma unroll
-                for (int t = 0; t < kSlots; ++t)
-                    if (t <= my_depth) rrow[t] = __expf(L - pre[t]);
-                Ls[i] = L;
-                Ms[i] = mi;
-                Ds[i] = my_depth;
-                if (i < T) logP[(size_t)(o + i) * H + h] = L;
-                mbar_arrive(&bar[BAR_TOPO]);
+                ratio[t] = L; // L_j of the ancestor at depth t
             }
-            // Compact C (rows 0..63) and G (rows 64..127) from the Gram: each
-            // thread takes its row's ancestor columns, in depth order.
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) ratio[t] = __expf(L - ratio[t]);
+            *reinterpret_cast<uint4 *>(ancat + i * kSlots) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+            Ls[i] = L;
+            Ds[i] = my_depth;
+            if (i < T) logP[(size_t)(o + i) * H + h] = L;
+            mbar_arrive(&bar[BAR_TOPO]);
+        }
+        if (warp < 4) {
+            // Stage the Gram rows (q.k for rows 0..63, k.k for 64..127).
             ok &= mbar_wait(&bar[BAR_GRAM], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs);
+            ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
             tc_fence_after();
             __syncwarp();
-            {
-                float x[64];
-                tmem_ld32(tmem + TM_GRAM + lane_base, *reinterpret_cast<float(*)[32]>(x));
-                tmem_ld32(tmem + TM_GRAM + 32 + lane_base, *reinterpret_cast<float(*)[32]>(x + 32));
-                const uint64_t mask = Ms[i];
-                const int di = Ds[i];
-                float *dst = (m < 64) ? Cc + i * kLd : Gc + i * kLd;
-                const float *rrow = Rt + i * kLd;
-                const float scale = (m < 64) ? 1.f : bt;
-                const int tmax = (m < 64) ? di : di - 1; // C keeps the diagonal, G does not
-                // Branch-free: every column is evaluated and only the stores
-                // are predicated, so the steps overlap.
+            float4 *srow = reinterpret_cast<float4 *>(staged_row(m));
+#pragma unroll 1
+            for (int hc = 0; hc < 2; ++hc) {
+                float x[32];
+                tmem_ld32(tmem + TM_GRAM + 32 * hc + lane_base, x);
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int t = __popcll(mask & ((1ull << c) - 1ull));
-                    const float val = scale * rrow[min(t, kSlots - 1)] * x[c];
-                    if (((mask >> c) & 1ull) && t <= tmax) dst[t] = val;
+                for (int c4 = 0; c4 < 8; ++c4)
+                    srow[(8 * hc + c4) ^ (m & 15)] =
+                        make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+            }
+            mbar_arrive(&bar[BAR_STAGED]);
+        }
+        if (topo) {
+            // Compact C and G of row i, gathered in depth order.
+            ok &= mbar_wait(&bar[BAR_STAGED], 0, kWaitNs);
+            const float *qk = staged_row(i), *kk = staged_row(64 + i);
+            float *crow = Cc + i * kLd, *grow = Gc + i * kLd;
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) {
+                if (t <= my_depth) {
+                    const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
+                    const int sw = (((j >> 2) ^ (i & 15)) << 2) | (j & 3);
+                    crow[t] = ratio[t] * qk[sw];
+                    if (t < my_depth) grow[t] = bt * ratio[t] * kk[sw];
                 }
             }
-            factor_sync(); // compact C and G complete
-            if (warp < 2) {
-                // Rows of W and M by backward substitution along the ancestor
-                // path (row = tid), parked in tensor memory until the
-                // propagation operand is free.
-                float mw[2 * kSlots]; // slots 0..15 M (z), 16..31 W (y)
-#pragma unroll
-                for (int t = 0; t < 2 * kSlots; ++t) mw[t] = 0.f;
-                if (i < T) {
-                    const int di = my_depth;
-                    a4 = *reinterpret_cast<const uint4 *>(ancat + i * kSlots);
-                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
-                    const float *ci = Cc + i * kLd;
-                    float ay[kSlots], az[kSlots]; // sum_{u > t} y_u G(a_u, a_t), same for z
-#pragma unroll
-                    for (int t = 0; t < kSlots; ++t) ay[t] = az[t] = 0.f;
-#pragma unroll
-                    for (int u = kSlots - 1; u >= 0; --u) {
-                        if (u <= di) {
-                            const float y = (u == di) ? 1.f : -ay[u];
-                            const float z = ci[u] - az[u];
-                            mw[u] = z;
-                            mw[kSlots + u] = y;
-                            const int au = (aw[u >> 2] >> (8 * (u & 3))) & 0xff;
-                            const float *gr = Gc + au * kLd;
-#pragma unroll
-                            for (int t = 0; t < u; ++t) {
-                                const float g = gr[t];
-                                ay[t] = fmaf(y, g, ay[t]);
-                                az[t] = fmaf(z, g, az[t]);
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                tmem_st32(tmem + TM_MW + lane_base, mw);
-                tmem_wait_st();
-            }
-        } else {
+            mbar_arrive(&bar[BAR_CG]);
+        } else if (warp >= 4) {
             // --------- split warps: S_pre = S_hi + S_lo in place (row r) ---------
             // bf16, N-contiguous, 64-column atoms: boxes (0,1) <- columns 0..63,
             // boxes (2,3) <- columns 64..127.
@@ -438,54 +416,66 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             }
             fence_proxy_async_smem();
             mbar_arrive(&bar[BAR_CONV]);
-            ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs); // L_i for P_i below
         }
+        ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs);
         const float p = (i < T) ? expf(Ls[i]) : 0.f; // P_i
 
-        // ---- epilogue of the state products.  Rows 0..63 (warps 0, 1, 4, 5)
-        //      zero the [M; W] operand, then warps 0 and 1 scatter their rows;
-        //      warps 6 and 7 write R^T = (beta (v - P K S_pre))^T, all 128
-        //      columns of their rows ----
-        ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
-        tc_fence_after();
-        if (m < 64) {
-            float4 *a2z = reinterpret_cast<float4 *>(sbuf);
-            const int zt = half * 64 + m; // 0..127
+        if (m < 64 && (topo || warp >= 4)) {
+            // Rows of W (warps 0, 1: y) and of M (warps 4, 5: z) by backward
+            // substitution along the ancestor path, written straight into the
+            // [M; W] operand (row i of M, row 64 + i of W, column = ancestor)
+            // once the gathers and the state products have released it.  Each
+            // thread zeroes its own row first (program order keeps the values).
+            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
+            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            const bool wrow = topo;
+            const int orow = wrow ? 64 + i : i;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) a2z[zt + e * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
-            upper_sync();
-            if (warp < 2) {
-                float mw[2 * kSlots];
-                __syncwarp();
-                tmem_ld32(tmem + TM_MW + lane_base, mw);
-                if (i < T) {
-                    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+            for (int c = 0; c < 16; ++c) // 2 K-atoms x 8 chunks of 16 B
+                *reinterpret_cast<float4 *>(sbuf + (c >> 3) * 16384 + sw128_chunk(orow, c & 7)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < T) {
+                const int di = Ds[i];
+                const uint4 a4 = *reinterpret_cast<const uint4 *>(ancat + i * kSlots);
+                const uint32_t aw4[4] = {a4.x, a4.y, a4.z, a4.w};
+                const float *ci = Cc + i * kLd;
+                float acc[kSlots]; // sum_{u > t} (y or z)_u G(a_u, a_t)
 #pragma unroll
-                    for (int t = 0; t < kSlots; ++t) {
-                        if (t <= my_depth) {
-                            const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
-                            uint8_t *col = sbuf + (j >> 5) * 16384;
-                            *reinterpret_cast<float *>(col + sw128_offset(i, j & 31)) = mw[t];
-                            *reinterpret_cast<float *>(col + sw128_offset(64 + i, j & 31)) =
-                                mw[kSlots + t];
-                        }
+                for (int t = 0; t < kSlots; ++t) acc[t] = 0.f;
+#pragma unroll
+                for (int u = kSlots - 1; u >= 0; --u) {
+                    if (u <= di) {
+                        const float val = wrow ? ((u == di) ? 1.f : -acc[u]) : ci[u] - acc[u];
+                        const int au = (aw4[u >> 2] >> (8 * (u & 3))) & 0xff;
+                        *reinterpret_cast<float *>(sbuf + (au >> 5) * 16384 +
+                                                   sw128_offset(orow, au & 31)) = val;
+                        const float *gr = Gc + au * kLd;
+#pragma unroll
+                        for (int t = 0; t < u; ++t) acc[t] = fmaf(val, gr[t], acc[t]);
                     }
                 }
             }
-        } else if (warp >= 4) {
-            uint8_t *dst = sbuf + 32768 + (i >> 5) * 16384;
+        } else if (m >= 64) {
+            // R^T = (beta (v - P K S_pre))^T for columns 64 half .. +63 of the
+            // rows 64..127 (warps 2, 3, 6, 7), once the staged Gram in this
+            // buffer has been gathered.
+            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
             ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
+            tc_fence_after();
+            __syncwarp();
+            uint8_t *dst = sbuf + 32768 + (i >> 5) * 16384;
+            const uint8_t *vrow = sV + half * 8192 + i * 128; // 64 columns of row i
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col0 = cc * 32;
-                const uint8_t *vrow = sV + (cc >> 1) * 8192 + i * 128; // 64 columns of row i
+            for (int cc = 0; cc < 2; ++cc) {
+                const int col0 = half * 64 + cc * 32;
                 float x[32];
                 tmem_ld32(tmem + lane_base + col0, x);
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     float f[8];
                     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + ((((cc & 1) * 4 + uu) ^ (i & 7)) << 4)), f);
+                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         const int c = 8 * uu + t;
@@ -502,6 +492,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         // ---- outputs: O = P (Q S_pre) + M R (bf16), U = W R (fp32) ----
         ok &= mbar_wait(&bar[BAR_MMA2], 0, kWaitNs);
         tc_fence_after();
+        __syncwarp();
         {
             const bool store = ok && i < T;
 #pragma unroll 1
@@ -778,6 +769,29 @@ cudaError_t make_state_map(CUtensorMap *map, const float *S, int units)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Kernel attributes are per device and per function: set them on the first
+// launch on each device only (they do not change), so later calls -- and
+// stream capture -- meet no attribute call.
+cudaError_t configure_once(const void *fn, int smem, bool carveout, int slot)
+{
+    static std::mutex mu;
+    static uint64_t done[4] = {0, 0, 0, 0}; // bit = device, word = slot
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (bit && (done[slot] & bit)) return cudaSuccess;
+    if (carveout) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) done[slot] |= bit;
+    return e;
+}
+
 } // namespace
 
 bool tc_verify_supported(const VerifyArgs &a)
@@ -813,11 +827,7 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H);
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             VERIFY_SMEM);
+    e = configure_once(reinterpret_cast<const void *>(tc_verify_kernel), VERIFY_SMEM, true, 0);
     if (e != cudaSuccess) return e;
     tc_verify_kernel<<<units, kThreads, VERIFY_SMEM, s>>>(
         mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.depth, a.anc, a.req_depth, a.H, a.N,
@@ -837,8 +847,7 @@ cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s)
     CUtensorMap map;
     cudaError_t e = make_state_map(&map, a.S, units);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             COMMIT_SMEM);
+    e = configure_once(reinterpret_cast<const void *>(tc_commit_kernel), COMMIT_SMEM, false, 1);
     if (e != cudaSuccess) return e;
     tc_commit_kernel<<<dim3(units, kD / kHalf), kCommitThreads, COMMIT_SMEM, s>>>(
         map, static_cast<const __nv_bfloat16 *>(a.k), a.U, a.logP, a.offsets, a.parent,
