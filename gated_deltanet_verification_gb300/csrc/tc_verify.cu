@@ -73,8 +73,8 @@ constexpr uint64_t kWaitNs = 200ull * 1000 * 1000; // 200 ms bound on any device
 //     products; once the first d_k half is done, its first 16 KB take the
 //     head's value rows by TMA (two 128B-swizzled boxes [64 rows x 64 bf16]),
 //     read by the epilogue from shared memory.
-//   X (10 KB): the factor scratch (compact C and G, ancestor table, decays,
-//     depths).
+//   X (11 KB): the factor scratch (compact C and G, ancestor table, decays,
+//     depths, log gammas).
 // Tensor memory (256 columns, lane = operand row): columns 0..127 hold
 // [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R]; before the
 // propagation, 128..191 hold the Gram.  The epilogues only read tensor memory.
@@ -82,7 +82,7 @@ constexpr int OFF_SBUF = 0;
 constexpr int SBUF_BYTES = 65536;
 constexpr int OFF_A1 = SBUF_BYTES;
 constexpr int OFF_X = OFF_A1 + 32768;         // factor scratch
-constexpr int X_BYTES = 10240;
+constexpr int X_BYTES = 11264;
 constexpr int OFF_BAR = OFF_X + X_BYTES;      // mbarriers
 constexpr int OFF_MISC = OFF_BAR + 16 * 8;    // TMEM slot
 constexpr int VERIFY_END = OFF_MISC + 16;
@@ -93,7 +93,8 @@ constexpr int X_C = X_G + FAC_BYTES;          // C (row i, ancestor slot t <= de
 constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i at depth t
 constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
 constexpr int X_DEPTH = X_L + kT * 4;
-static_assert(X_DEPTH + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+constexpr int X_LG = X_DEPTH + kT * 4;        // log gamma_i
+static_assert(X_LG + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
 static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
@@ -177,6 +178,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     uint8_t *ancat = sm + X_ANCAT;
     float *Ls = reinterpret_cast<float *>(sm + X_L);
     int *Ds = reinterpret_cast<int *>(sm + X_DEPTH);
+    float *LGs = reinterpret_cast<float *>(sm + X_LG);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
 
@@ -226,7 +228,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     float bt = 0.f;                   // beta_i (topology rows and the K-side rows)
     int my_depth = -1;
     uint2 anc2 = make_uint2(0, 0);
-    float g_i = 1.f, g_p = 1.f;
+    float g_i = 1.f;
     if (warp < 8) {
         if ((topo || m >= 64) && i < T) bt = beta[(size_t)(o + i) * H + h];
         if (topo) {
@@ -235,7 +237,6 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 anc2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
                 g_i = gamma[(size_t)(o + i) * H + h];
             }
-            if ((i ^ 32) < T) g_p = gamma[(size_t)(o + (i ^ 32)) * H + h];
         }
     }
     if (issuer) {
@@ -313,27 +314,31 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         float ratio[kSlots]; // topology rows: exp(L_i - L_j), j the ancestor at depth t
         uint32_t aw[4] = {0, 0, 0, 0}; // topology rows: ancestor-by-depth table, packed bytes
         if (topo) {
-            // Topology and cumulative decay (row = tid).  Each warp also holds
-            // the partner row tid ^ 32, so it sees every row's log gamma
-            // through shuffles: L_i = sum over the ancestors-or-self of i (the
-            // prefix along parent links, Lemma 1) and the ancestor-by-depth
-            // table, without a barrier.  The walk passes the ancestors in depth
-            // order, so the partial sums are their L_j.
+            // Topology and cumulative decay (row = tid).  L_i is the sum of log
+            // gamma over the ancestors-or-self of i (the prefix along parent
+            // links, Lemma 1).  The ancestors come out of the mask in depth
+            // order (parents precede children), so the partial sums are their
+            // L_j.  All log gammas are read in one batch after a barrier of
+            // the two topology warps.
             const uint64_t mi = ((uint64_t)anc2.y << 32) | anc2.x;
-            const float lgi = logf(g_i), lgp = logf(g_p);
-            const float lg_lo = (i < 32) ? lgi : lgp; // log gamma of row `lane`
-            const float lg_hi = (i < 32) ? lgp : lgi; // log gamma of row `lane` + 32
-            float L = 0.f;
+            LGs[i] = logf(g_i);
+            asm volatile("bar.sync 2, 64;" ::: "memory");
+            int jt[kSlots];
             uint64_t mm = mi;
 #pragma unroll
             for (int t = 0; t < kSlots; ++t) {
-                const int j = mm ? __ffsll((long long)mm) - 1 : 0;
-                const float vlo = __shfl_sync(0xffffffffu, lg_lo, j & 31);
-                const float vhi = __shfl_sync(0xffffffffu, lg_hi, j & 31);
+                jt[t] = mm ? __ffsll((long long)mm) - 1 : 0;
+                mm &= mm - 1;
+            }
+            float lgv[kSlots];
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) lgv[t] = LGs[jt[t]];
+            float L = 0.f;
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) {
                 if (t <= my_depth) {
-                    L += (j < 32) ? vlo : vhi;
-                    aw[t >> 2] |= (uint32_t)j << (8 * (t & 3));
-                    mm &= mm - 1;
+                    L += lgv[t];
+                    aw[t >> 2] |= (uint32_t)jt[t] << (8 * (t & 3));
                 }
                 ratio[t] = L; // L_j of the ancestor at depth t
             }
@@ -368,13 +373,19 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             ok &= mbar_wait(&bar[BAR_STAGED], 0, kWaitNs);
             const float *qk = staged_row(i), *kk = staged_row(64 + i);
             float *crow = Cc + i * kLd, *grow = Gc + i * kLd;
+            float qv[kSlots], kv[kSlots]; // every load first, then the products
+#pragma unroll
+            for (int t = 0; t < kSlots; ++t) {
+                const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
+                const int sw = (((j >> 2) ^ (i & 15)) << 2) | (j & 3);
+                qv[t] = qk[sw];
+                kv[t] = kk[sw];
+            }
 #pragma unroll
             for (int t = 0; t < kSlots; ++t) {
                 if (t <= my_depth) {
-                    const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
-                    const int sw = (((j >> 2) ^ (i & 15)) << 2) | (j & 3);
-                    crow[t] = ratio[t] * qk[sw];
-                    if (t < my_depth) grow[t] = bt * ratio[t] * kk[sw];
+                    crow[t] = ratio[t] * qv[t];
+                    if (t < my_depth) grow[t] = bt * ratio[t] * kv[t];
                 }
             }
             mbar_arrive(&bar[BAR_CG]);
@@ -439,19 +450,37 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 const uint4 a4 = *reinterpret_cast<const uint4 *>(ancat + i * kSlots);
                 const uint32_t aw4[4] = {a4.x, a4.y, a4.z, a4.w};
                 const float *ci = Cc + i * kLd;
+                float cv[kSlots];
+#pragma unroll
+                for (int t = 0; t < kSlots; ++t) cv[t] = wrow ? 0.f : ci[t];
                 float acc[kSlots]; // sum_{u > t} (y or z)_u G(a_u, a_t)
 #pragma unroll
                 for (int t = 0; t < kSlots; ++t) acc[t] = 0.f;
+                // G row of the ancestor at depth u, read one step ahead
+                float gcur[kSlots];
+                {
+                    const float *gr = Gc + i * kLd;
+#pragma unroll
+                    for (int t = 0; t < kSlots - 1; ++t) gcur[t] = gr[t];
+                }
 #pragma unroll
                 for (int u = kSlots - 1; u >= 0; --u) {
                     if (u <= di) {
-                        const float val = wrow ? ((u == di) ? 1.f : -acc[u]) : ci[u] - acc[u];
+                        float gnext[kSlots];
+                        if (u >= 1) {
+                            const int an = (aw4[(u - 1) >> 2] >> (8 * ((u - 1) & 3))) & 0xff;
+                            const float *gr = Gc + an * kLd;
+#pragma unroll
+                            for (int t = 0; t < u - 1; ++t) gnext[t] = gr[t];
+                        }
+                        const float val = wrow ? ((u == di) ? 1.f : -acc[u]) : cv[u] - acc[u];
                         const int au = (aw4[u >> 2] >> (8 * (u & 3))) & 0xff;
                         *reinterpret_cast<float *>(sbuf + (au >> 5) * 16384 +
                                                    sw128_offset(orow, au & 31)) = val;
-                        const float *gr = Gc + au * kLd;
 #pragma unroll
-                        for (int t = 0; t < u; ++t) acc[t] = fmaf(val, gr[t], acc[t]);
+                        for (int t = 0; t < u; ++t) acc[t] = fmaf(val, gcur[t], acc[t]);
+#pragma unroll
+                        for (int t = 0; t < u - 1; ++t) gcur[t] = gnext[t];
                     }
                 }
             }
@@ -537,22 +566,22 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 // ---- commit ----
 // One CTA per (request, head, 64-column half of the state): value tiling as in
 // the pages' kernel, so four CTAs fit on an SM and overlap their TMA load,
-// tensor-core product and TMA store.
+// tensor-core product and TMA store.  (Narrower tiles fit more CTAs but
+// repeat the path operand's gather and measured slower.)
 constexpr int kCommitThreads = 128;
 constexpr int kChunk = 16;                    // path nodes per MMA K chunk
-constexpr int kHalf = 64;                     // state columns per CTA
+constexpr int kTile = 64;                     // state columns per CTA
 constexpr int CO_S = 0;                       // S half: 2 boxes x [128 rows x 128 B] = 32 KB
 constexpr int CO_A = 32768;                   // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
 constexpr int CO_B = CO_A + 8192;             // U_a^T chunk: 64 rows x 16 tf32
 constexpr int CO_PATH = CO_B + 4096;          // int[128]
-constexpr int CO_COEF = CO_PATH + 512;        // float[128]
-constexpr int CO_BAR = CO_COEF + 512;         // 2 mbarriers
+constexpr int CO_BAR = CO_PATH + 512;         // 2 mbarriers
 constexpr int CO_TSLOT = CO_BAR + 16;
 constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag
 constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
 constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
 
-constexpr uint32_t IDESC_COMMIT = idesc_tf32(128, kHalf, false, false);
+constexpr uint32_t IDESC_COMMIT = idesc_tf32(128, kTile, false, false);
 
 // 64-byte-swizzled K-major operand with 64-byte rows (16 tf32): the 16-byte
 // chunk index (0..3) is XORed with (row / 2) % 4.
@@ -569,7 +598,7 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo)
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
-__global__ void __launch_bounds__(kCommitThreads)
+__global__ void __launch_bounds__(kCommitThreads, 4)
 tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *__restrict__ k,
                  const float *__restrict__ U, const float *__restrict__ logP,
                  const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
@@ -581,7 +610,6 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     uint8_t *sA = sm + CO_A;
     uint8_t *sB = sm + CO_B;
     int *path = reinterpret_cast<int *>(sm + CO_PATH);
-    float *coef = reinterpret_cast<float *>(sm + CO_COEF);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CO_BAR); // tma, mma
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CO_TSLOT);
     int *plen = reinterpret_cast<int *>(sm + CO_MISC);
@@ -589,39 +617,40 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     int *spar = reinterpret_cast<int *>(sm + CO_PAR);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int unit = blockIdx.x, hv = blockIdx.y; // head unit, value half
+    const int unit = blockIdx.x, hv = blockIdx.y; // head unit, value tile
     const int b = unit / H, h = unit % H;
-    if (faulted(st)) return;
+    // The state half depends on the block alone: it is requested first.
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmS);
+        mbar_arrive_expect_tx(&bar[0], 2 * 16384);
+        tma_load_2d(sS, &tmS, &bar[0], kTile * hv, unit * kD);
+        tma_load_2d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD);
+    }
+    // The status word, the accepted node and the request's extent in one
+    // round trip; uniform early exits (the issuing thread drains the copy).
+    const int fault = *(const volatile int32_t *)st;
     const int a = accepted[b];
-    if (a < 0) return;
     const int o = offsets[b], T = offsets[b + 1] - o;
-    if (a >= T || o < 0 || o + T > N || T > kMaxTree) {
-        if (tid == 0 && hv == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
+    const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
+    if (fault != 0 || a < 0 || bad) {
+        if (bad && fault == 0 && tid == 0 && hv == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
+        if (tid == 0) mbar_wait(&bar[0], 0, kWaitNs);
         return;
     }
     if (warp == 0) {
         tmem_alloc(tslot, 64);
         tmem_relinquish();
     }
-    if (tid == 32) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        *flag = 0;
-        fence_mbar_init();
-    }
+    // stage the request's parent links (coalesced), then walk the accepted path
+    for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
+    if (tid == 32) *flag = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (tid == 0) {
-        prefetch_tensormap(&tmS);
-        mbar_arrive_expect_tx(&bar[0], 2 * 16384);
-        tma_load_2d(sS, &tmS, &bar[0], kHalf * hv, unit * kD);
-        tma_load_2d(sS + 16384, &tmS, &bar[0], kHalf * hv + 32, unit * kD);
-    }
-    // stage the request's parent links (coalesced), then walk the accepted path
-    for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
-    __syncthreads();
     if (tid == 0) {
         int L = 0, j = a;
         bool ok = true;
@@ -641,42 +670,40 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     __syncthreads();
     const int L = *plen;
     const float La = logP[(size_t)(o + a) * H + h];
-    for (int t = tid; t < L; t += kCommitThreads)
-        coef[t] = expf(La - logP[(size_t)(o + path[t]) * H + h]);
-    __syncthreads();
 
     const uint32_t sa = smem_addr(sA), sb = smem_addr(sB);
     const int nchunks = (*(volatile int *)flag != 0) ? 0 : (L + kChunk - 1) / kChunk;
     for (int ch = 0; ch < nchunks; ++ch) {
+        // Every path-dependent read of the chunk in one batch: the decay of
+        // each path node (each thread forms its own coefficients), row r =
+        // tid of its key and, for c = tid < 64, column c of its U row.
+        const int tn = min(kChunk, L - ch * kChunk); // path nodes in this chunk
+        float lp[kChunk], kv[kChunk], uv[kChunk];
+#pragma unroll
+        for (int tt = 0; tt < kChunk; ++tt) {
+            const size_t nh = (size_t)(o + (tt < tn ? path[ch * kChunk + tt] : 0)) * H + h;
+            lp[tt] = (tt < tn) ? logP[nh] : 0.f;
+            kv[tt] = (tt < tn) ? __bfloat162float(k[nh * kD + tid]) : 0.f;
+            uv[tt] = (tt < tn && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
+        }
         // A[r][t] = coef_t k_{j_t}[r] (row r = tid), K-major, 64-byte rows
-        {
-            const int r = tid;
-            float av[kChunk];
 #pragma unroll
-            for (int tt = 0; tt < kChunk; ++tt) {
-                const int t = ch * kChunk + tt;
-                av[tt] = (t < L) ? coef[t] * __bfloat162float(k[((size_t)(o + path[t]) * H + h) * kD + r])
-                                 : 0.f;
+        for (int c4 = 0; c4 < kChunk / 4; ++c4) {
+            float av[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tt = 4 * c4 + e;
+                av[e] = (tt < tn) ? expf(La - lp[tt]) * kv[tt] : 0.f;
             }
-#pragma unroll
-            for (int c4 = 0; c4 < kChunk / 4; ++c4)
-                *reinterpret_cast<float4 *>(sA + sw64_offset(r, 4 * c4)) =
-                    make_float4(av[4 * c4], av[4 * c4 + 1], av[4 * c4 + 2], av[4 * c4 + 3]);
+            *reinterpret_cast<float4 *>(sA + sw64_offset(tid, 4 * c4)) =
+                make_float4(av[0], av[1], av[2], av[3]);
         }
         // B^T[c][t] = u_{j_t}[64 hv + c] (row c < 64), K-major, 64-byte rows
-        if (tid < kHalf) {
-            const int c = tid;
+        if (tid < kTile) {
 #pragma unroll
-            for (int t4 = 0; t4 < kChunk / 4; ++t4) {
-                float uv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = ch * kChunk + 4 * t4 + e;
-                    uv[e] = (t < L) ? U[((size_t)(o + path[t]) * H + h) * kD + kHalf * hv + c] : 0.f;
-                }
-                *reinterpret_cast<float4 *>(sB + sw64_offset(c, 4 * t4)) =
-                    make_float4(uv[0], uv[1], uv[2], uv[3]);
-            }
+            for (int t4 = 0; t4 < kChunk / 4; ++t4)
+                *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * t4)) =
+                    make_float4(uv[4 * t4], uv[4 * t4 + 1], uv[4 * t4 + 2], uv[4 * t4 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -727,8 +754,8 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     }
     __syncthreads();
     if (tid == 0 && ok && nchunks > 0) {
-        tma_store_2d(&tmS, sS, kHalf * hv, unit * kD);
-        tma_store_2d(&tmS, sS + 16384, kHalf * hv + 32, unit * kD);
+        tma_store_2d(&tmS, sS, kTile * hv, unit * kD);
+        tma_store_2d(&tmS, sS + 16384, kTile * hv + 32, unit * kD);
         bulk_commit_group();
         bulk_wait_group_read0();
     }
@@ -849,7 +876,7 @@ cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     e = configure_once(reinterpret_cast<const void *>(tc_commit_kernel), COMMIT_SMEM, false, 1);
     if (e != cudaSuccess) return e;
-    tc_commit_kernel<<<dim3(units, kD / kHalf), kCommitThreads, COMMIT_SMEM, s>>>(
+    tc_commit_kernel<<<dim3(units, kD / kTile), kCommitThreads, COMMIT_SMEM, s>>>(
         map, static_cast<const __nv_bfloat16 *>(a.k), a.U, a.logP, a.offsets, a.parent,
         a.accepted, a.H, a.N, a.st);
     return cudaGetLastError();
