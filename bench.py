@@ -286,10 +286,7 @@ def main(argv=None):
     launches_per_step = 1 + (1 if tc_used else 2) + 1  # pack, verify (1 or 2 kernels), commit
 
     def step(i):
-        db, rb = sets[i % n_sets]
-        device.pack(db, rb, stream)
-        device.verify(db, rb, flags, stream)
-        device.commit(db, rb, flags, stream)
+        device.run_round(*sets[i % n_sets], flags, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -304,11 +301,7 @@ def main(argv=None):
     for i in range(n_sets):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            db, rb = sets[i]
-            cs = torch.cuda.current_stream()
-            device.pack(db, rb, cs)
-            device.verify(db, rb, flags, cs)
-            device.commit(db, rb, flags, cs)
+            device.run_round(*sets[i], flags, torch.cuda.current_stream())
         graphs.append(g)
     for i in range(n_sets):
         graphs[i].replay()
@@ -337,8 +330,9 @@ def main(argv=None):
     elapsed_ms = start.elapsed_time(end)
 
     # ---- separate pass: per-kernel durations.  One graph per call kind runs
-    #      that call once on every input copy, back to back (the copies keep
-    #      the L2 cold between reuses); events bracket each replay ----
+    #      that call once on every input copy, back to back and without launch
+    #      overlap (the copies keep the L2 cold between reuses); events bracket
+    #      each replay ----
     ks = max(1, min(args.kernel_steps, args.steps))
     per_kernel = {"pack": [], "verify": [], "commit": []}
     calls = {"pack": lambda db, rb, cs: device.pack(db, rb, cs),

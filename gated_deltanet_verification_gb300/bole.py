@@ -29,6 +29,7 @@ ERR_TIMEOUT = 7
 F32 = 0
 BF16 = 1
 FLAG_FORCE_SIMT = 0x1
+FLAG_OVERLAP_LAUNCH = 0x2  # see bole.h: overlap with the previous library call on the stream
 MAX_TREE_NODES = 128
 STATUS_WORDS = 4
 
@@ -223,4 +224,5 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
 __all__ = ["lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
            "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
-           "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT"]
+           "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT",
+           "FLAG_OVERLAP_LAUNCH"]

@@ -110,7 +110,8 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
         return BOLE_ERR_WORKSPACE;
     if (B == 0 || N == 0) return BOLE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return from_cuda(tc ? launch_tc_verify(a, s) : launch_simt_verify(a, s));
+    return from_cuda(tc ? launch_tc_verify(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0)
+                        : launch_simt_verify(a, s));
 }
 
 bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const void *k,
@@ -174,7 +175,8 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.st = dev_status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool tc = !(flags & BOLE_FLAG_FORCE_SIMT) && tc_commit_supported(a);
-    return from_cuda(tc ? launch_tc_commit(a, s) : launch_simt_commit(a, s));
+    return from_cuda(tc ? launch_tc_commit(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0)
+                        : launch_simt_commit(a, s));
 }
 
 } // extern "C"

@@ -26,6 +26,16 @@ __device__ __forceinline__ bool faulted(const int32_t *st)
     return *(const volatile int32_t *)st != 0;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// (it still waits for this one before reading what this one writes), and
+// wait for the previous kernel's completion and memory.  Both are no-ops for
+// launches without a programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x)
@@ -79,8 +89,8 @@ cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
 
 bool tc_verify_supported(const VerifyArgs &a);
 size_t tc_workspace_bytes(int B, int H, int max_T);
-cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s);
+cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap);
 bool tc_commit_supported(const CommitArgs &a);
-cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s);
+cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap);
 
 } // namespace bole

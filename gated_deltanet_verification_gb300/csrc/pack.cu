@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
     int32_t *__restrict__ req_depth, int32_t *st)
 {
     __shared__ int sp[kPackWarps][kMaxTree];
+    pdl_launch_dependents(); // a verification launched to overlap may start its state reads
     const int wib = threadIdx.x >> 5;
     const int b = (int)blockIdx.x * kPackWarps + wib;
     const int lane = threadIdx.x & 31;

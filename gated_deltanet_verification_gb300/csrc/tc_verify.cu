@@ -94,7 +94,8 @@ constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i 
 constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
 constexpr int X_DEPTH = X_L + kT * 4;
 constexpr int X_LG = X_DEPTH + kT * 4;        // log gamma_i
-static_assert(X_LG + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+constexpr int X_PAR = X_LG + kT * 4;          // parent links of the request
+static_assert(X_PAR + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
 static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
@@ -163,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const float *__restrict__ gamma, const float *__restrict__ beta,
-                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
-                 const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth, int H,
-                 int N, __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
+                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
+                 const int32_t *__restrict__ req_depth, int H, int N,
+                 __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
                  float *__restrict__ logP, int32_t *st)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -179,6 +180,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     float *Ls = reinterpret_cast<float *>(sm + X_L);
     int *Ds = reinterpret_cast<int *>(sm + X_DEPTH);
     float *LGs = reinterpret_cast<float *>(sm + X_LG);
+    int *Ps_par = reinterpret_cast<int *>(sm + X_PAR);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
 
@@ -190,20 +192,13 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
-    // The status word, the request's extent and its depth in one round trip;
-    // uniform early exits.
-    const int fault = *(const volatile int32_t *)st;
-    const int o = offsets[b], T = offsets[b + 1] - o, d = req_depth[b];
-    const bool bad = T > kT || o < 0 || o + T > N || d < 0 || d >= kSlots || d >= T;
-    if (fault != 0 || T <= 0 || bad) {
-        if (bad && T > 0 && tid == 0 && h == 0)
-            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
-                   -1, T > kT ? T : d);
-        return;
-    }
-    // The small, latency-critical reads go out before the 64 KB state tile,
-    // which every CTA requests at once: [Q;K] and the per-thread tree inputs
-    // (below) first, S_pre last.
+    pdl_launch_dependents(); // an overlapped commit may start its state reads
+    // Caller inputs first (a launch that overlaps pack reads only these before
+    // it waits): the request's extent, then the small, latency-critical reads
+    // -- [Q;K] and the per-thread gamma, beta -- before the 64 KB state tile,
+    // which every CTA requests at once.
+    const int o = offsets[b], T = offsets[b + 1] - o;
+    const bool in_range = T > 0 && T <= kT && o >= 0 && o + T <= N;
     const bool issuer = tid == kComputeThreads;
     if (issuer) {
         for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
@@ -213,30 +208,27 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
+        if (in_range) {
+            mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
 #pragma unroll
-        for (int ka = 0; ka < 2; ++ka) {
-            tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
-            tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[BAR_A1], 64 * ka, h, o);
+            for (int ka = 0; ka < 2; ++ka) {
+                tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
+                tma_load_3d(sA1 + ka * 16384 + 8192, &tmK, &bar[BAR_A1], 64 * ka, h, o);
+            }
         }
     }
-    // Per-thread tree inputs, requested before the CTA barrier.
     const int rowgrp = warp & 3, half = warp >> 2;
     const int m = rowgrp * 32 + lane; // TMEM lane = operand row
     const int i = m & 63;             // this thread's node
     const bool topo = tid < kT;       // warps 0, 1: row i = tid
     float bt = 0.f;                   // beta_i (topology rows and the K-side rows)
-    int my_depth = -1;
-    uint2 anc2 = make_uint2(0, 0);
     float g_i = 1.f;
-    if (warp < 8) {
-        if ((topo || m >= 64) && i < T) bt = beta[(size_t)(o + i) * H + h];
+    int par_i = -1;
+    if (warp < 8 && in_range && i < T) {
+        if (topo || m >= 64) bt = beta[(size_t)(o + i) * H + h];
         if (topo) {
-            if (i < T) {
-                my_depth = depth_g[o + i];
-                anc2 = *reinterpret_cast<const uint2 *>(anc_g + (size_t)(o + i) * 4);
-                g_i = gamma[(size_t)(o + i) * H + h];
-            }
+            g_i = gamma[(size_t)(o + i) * H + h];
+            par_i = parent[o + i];
         }
     }
     if (issuer) {
@@ -244,6 +236,43 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+    }
+    // Depth and ancestor-or-self mask of each node from the request's parent
+    // links (a caller input), walked in shared memory by the topology warps:
+    // at most 16 steps, every link checked to point backwards, so the walk is
+    // bounded and in range whatever the input (invalid trees are reported by
+    // pack, and the wait below ends such a launch before any output).
+    int my_depth = -1;
+    uint64_t my_mask = 0;
+    if (topo) {
+        Ps_par[i] = par_i;
+        asm volatile("bar.sync 2, 64;" ::: "memory");
+        if (in_range && i < T) {
+            int j = i;
+            for (int step = 0; step < kSlots && j >= 0; ++step) {
+                my_mask |= 1ull << j;
+                ++my_depth;
+                const int pj = Ps_par[j];
+                j = (pj < j && pj >= -1) ? pj : -2; // a forward or bad link ends the walk
+            }
+            if (j != -1) my_depth = -1; // deeper than 15 or malformed: no work for this row
+        }
+    }
+    // What the previous call wrote (the status word pack reset, the
+    // per-request depth) is read after the wait.
+    pdl_wait();
+    const int fault = *(const volatile int32_t *)st;
+    const int d = req_depth[b];
+    const bool bad = !in_range || d < 0 || d >= kSlots || d >= T;
+    if (fault != 0 || T <= 0 || bad) {
+        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0)
+            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
+                   -1, T > kT ? T : d);
+        if (issuer) { // drain the copies in flight before the CTA retires
+            if (in_range) mbar_wait(&bar[BAR_A1], 0, kWaitNs);
+            mbar_wait(&bar[BAR_S], 0, kWaitNs);
+        }
+        return;
     }
     if (warp == 0) {
         tmem_alloc(tslot, 256);
@@ -320,7 +349,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // order (parents precede children), so the partial sums are their
             // L_j.  All log gammas are read in one batch after a barrier of
             // the two topology warps.
-            const uint64_t mi = ((uint64_t)anc2.y << 32) | anc2.x;
+            const uint64_t mi = my_depth >= 0 ? my_mask : 0ull;
             LGs[i] = logf(g_i);
             asm volatile("bar.sync 2, 64;" ::: "memory");
             int jt[kSlots];
@@ -629,8 +658,12 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         tma_load_2d(sS, &tmS, &bar[0], kTile * hv, unit * kD);
         tma_load_2d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD);
     }
-    // The status word, the accepted node and the request's extent in one
-    // round trip; uniform early exits (the issuing thread drains the copy).
+    // The state half is the caller's; everything the verification (or the
+    // sampler) wrote -- U, log P, the accepted node, the status -- is read
+    // after the wait.  The status word, the accepted node and the request's
+    // extent come in one round trip; uniform early exits (the issuing thread
+    // drains the copy).
+    pdl_wait();
     const int fault = *(const volatile int32_t *)st;
     const int a = accepted[b];
     const int o = offsets[b], T = offsets[b + 1] - o;
@@ -819,6 +852,23 @@ cudaError_t configure_once(const void *fn, int smem, bool carveout, int slot)
     return e;
 }
 
+// Launch configuration; with `overlap` the kernel may start while the previous
+// kernel on the stream drains (programmatic dependent launch).
+cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, int smem, cudaStream_t s, bool overlap,
+                                 cudaLaunchAttribute (&attr)[1])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cfg;
+}
+
 } // namespace
 
 bool tc_verify_supported(const VerifyArgs &a)
@@ -844,7 +894,7 @@ cudaError_t make_node_map(CUtensorMap *map, const void *x, int N, int H)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
+cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
 {
     const int units = a.B * a.H;
     if (units == 0 || a.N == 0) return cudaSuccess;
@@ -856,10 +906,12 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     e = configure_once(reinterpret_cast<const void *>(tc_verify_kernel), VERIFY_SMEM, true, 0);
     if (e != cudaSuccess) return e;
-    tc_verify_kernel<<<units, kThreads, VERIFY_SMEM, s>>>(
-        mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.depth, a.anc, a.req_depth, a.H, a.N,
-        static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, a.st);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
+                                                 overlap, attr);
+    return cudaLaunchKernelEx(&cfg, tc_verify_kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets,
+                              a.parent, a.req_depth, a.H, a.N,
+                              static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, a.st);
 }
 
 bool tc_commit_supported(const CommitArgs &a)
@@ -867,7 +919,7 @@ bool tc_commit_supported(const CommitArgs &a)
     return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD;
 }
 
-cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s)
+cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap)
 {
     const int units = a.B * a.H;
     if (units == 0 || a.N == 0) return cudaSuccess;
@@ -876,10 +928,12 @@ cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     e = configure_once(reinterpret_cast<const void *>(tc_commit_kernel), COMMIT_SMEM, false, 1);
     if (e != cudaSuccess) return e;
-    tc_commit_kernel<<<dim3(units, kD / kTile), kCommitThreads, COMMIT_SMEM, s>>>(
-        map, static_cast<const __nv_bfloat16 *>(a.k), a.U, a.logP, a.offsets, a.parent,
-        a.accepted, a.H, a.N, a.st);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(dim3(units, kD / kTile), dim3(kCommitThreads),
+                                                 COMMIT_SMEM, s, overlap, attr);
+    return cudaLaunchKernelEx(&cfg, tc_commit_kernel, map,
+                              static_cast<const __nv_bfloat16 *>(a.k), a.U, a.logP, a.offsets,
+                              a.parent, a.accepted, a.H, a.N, a.st);
 }
 
 } // namespace bole

@@ -92,7 +92,9 @@ def commit(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> No
 
 
 def run_round(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:
-    """pack -> verify -> commit, all asynchronous on one stream."""
+    """pack -> verify -> commit, all asynchronous on one stream.  Each call
+    directly follows the one it depends on, so verify and commit may overlap
+    their predecessor's tail (bole.FLAG_OVERLAP_LAUNCH)."""
     pack(db, rb, stream)
-    verify(db, rb, flags, stream)
-    commit(db, rb, flags, stream)
+    verify(db, rb, flags | bole.FLAG_OVERLAP_LAUNCH, stream)
+    commit(db, rb, flags | bole.FLAG_OVERLAP_LAUNCH, stream)

@@ -82,6 +82,17 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
 /* Flags for bole_tree_verify / bole_commit / bole_workspace_size. */
 #define BOLE_FLAG_FORCE_SIMT 0x1u /* use the FP32 CUDA-core kernels even where the
                                      tcgen05 tensor-core kernels apply */
+/* Overlap the launch with the kernel before it on the stream (programmatic
+ * dependent launch; tensor-core kernels only).  The caller asserts that the
+ * previous kernel on the stream is the round's bole_pack_forest (before
+ * bole_tree_verify) or bole_tree_verify (before bole_commit), or any kernel
+ * that does not let its dependents start early.  The kernel may then begin
+ * while that one drains: before waiting for it, it reads only caller-owned
+ * inputs that neither library call writes (S_pre / S, q, k, v, gamma, beta,
+ * offsets); the status word and everything the previous call produced are
+ * read after the wait.  Without the flag every launch starts only after the
+ * previous kernel has ended. */
+#define BOLE_FLAG_OVERLAP_LAUNCH 0x2u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *bole_status_string(int status);

@@ -158,3 +158,32 @@ def test_empty_batch():
     depth, anc, req, st = bole.pack_forest(offsets, parent, 3)
     torch.cuda.synchronize()
     assert st.cpu().tolist()[0] == 0
+
+
+def test_overlapped_round_matches_serial_launches():
+    """run_round overlaps verify with pack and commit with verify (programmatic
+    dependent launch); the results must equal those of fully serial launches
+    bit for bit, and match the oracle."""
+    from gated_deltanet_verification_gb300 import bole, device
+    for cfg in (2, 3):
+        b = I.config_batch(cfg)
+        db1, db2 = device.to_device(b), device.to_device(b)
+        rb1, rb2 = device.alloc_round(db1), device.alloc_round(db2)
+        device.pack(db1, rb1)
+        device.verify(db1, rb1)
+        device.commit(db1, rb1)
+        device.run_round(db2, rb2)
+        torch.cuda.synchronize()
+        bole.check_status(rb1.status)
+        bole.check_status(rb2.status)
+        assert torch.equal(rb1.O, rb2.O)
+        assert torch.equal(rb1.U, rb2.U)
+        assert torch.equal(rb1.logP, rb2.logP)
+        assert torch.equal(db1.S, db2.S)
+    got = dict(depth=rb2.depth.cpu().numpy(), anc=rb2.anc.cpu().numpy().view(np.uint32),
+               req=rb2.req_depth[:b.B].cpu().numpy(),
+               O=rb2.O.float().cpu().numpy().astype(np.float64),
+               U=rb2.U.cpu().numpy().astype(np.float64),
+               logP=rb2.logP.cpu().numpy().astype(np.float64),
+               S_new=db2.S.cpu().numpy().astype(np.float64))
+    _check(b, got, 1e-2)
