@@ -119,9 +119,13 @@ constexpr uint32_t TM_GRAM = 128, TM_PROP = 128;                  // tensor-memo
 constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, BAR_STATE = 5,
               BAR_MMA2 = 6, BAR_TOPO = 7, BAR_STAGED = 8, BAR_CG = 9, BAR_CONV = 10, BAR_OPS = 11;
 
+// The dynamic shared-memory base rounded up to 1024 bytes.  The offset comes
+// from the 32-bit shared address and is added to the __shared__ array
+// itself, so the compiler keeps every derived pointer in the shared window
+// (shared-memory instructions, not generic ones).
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+    return p + ((1024u - (smem_addr(p) & 1023u)) & 1023u);
 }
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
