@@ -279,11 +279,12 @@ def main(argv=None):
         rb = device.alloc_round(db, flags)
         sets.append((db, rb))
     stream = torch.cuda.current_stream()
-    tc_used = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
-               and batch.dv == 128 and batch.max_T <= 64
-               and bole.workspace_size(batch.B, batch.H, batch.dk, batch.dv, batch.max_T,
-                                       batch.max_depth, torch.bfloat16, flags) == 0)
-    launches_per_step = 1 + (1 if tc_used else 2) + 1  # pack, verify (1 or 2 kernels), commit
+    tc_shape = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
+                and batch.dv == 128)
+    fused = tc_shape and batch.max_T <= 64 and batch.max_depth < 16   # single-CTA kernel
+    big = tc_shape and not fused and batch.max_T <= 128              # factor + solve kernels
+    tc_used = fused or big
+    launches_per_step = 1 + (1 if fused else 2) + 1  # pack, verify (1 or 2 kernels), commit
 
     def step(i):
         device.run_round(*sets[i % n_sets], flags, stream)
@@ -378,7 +379,7 @@ def main(argv=None):
     dominant = max(("verify", "commit"), key=lambda k: avg[k])
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
     traffic = recorded_traffic(VERIFY_KERNELS if dominant == "verify" else ["tc_commit_kernel"],
-                               args.config) if tc_used else None
+                               args.config) if fused else None
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": kern_rf[dominant]["frac"], "traffic": traffic, "peak_source": peak_kind,
@@ -404,7 +405,9 @@ def main(argv=None):
                    + (f" [{args.shape}]" if args.config == 4 else ""),
                    "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
-                   "seed": seed, "kernels": "tcgen05" if tc_used else "cuda-core",
+                   "seed": seed,
+                   "kernels": ("tcgen05" if fused else "tcgen05 factor + solve (large trees)"
+                               if big else "cuda-core"),
                    "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
                    "launch": "CUDA graph replay, one graph per input copy",
                    "kernel_timing": f"separate pass: per call kind, a graph of one call on each "

@@ -16,9 +16,26 @@ bool valid_dtype(bole_dtype t) { return t == BOLE_F32 || t == BOLE_BF16; }
 
 bole_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BOLE_OK : BOLE_ERR_CUDA; }
 
-bool use_tc_verify(const VerifyArgs &a, unsigned flags)
+// Verification kernels: the single-CTA tensor-core kernel (trees of up to 64
+// nodes, depth <= 15), the two-kernel tensor-core path for larger or deeper
+// trees (up to 128 nodes), else the FP32 CUDA-core kernels.
+enum class VerifyPath { Fused, Big, Simt };
+
+VerifyPath verify_path(const VerifyArgs &a, unsigned flags)
 {
-    return !(flags & BOLE_FLAG_FORCE_SIMT) && tc_verify_supported(a);
+    if (flags & BOLE_FLAG_FORCE_SIMT) return VerifyPath::Simt;
+    if (tc_verify_supported(a)) return VerifyPath::Fused;
+    if (tc_big_supported(a)) return VerifyPath::Big;
+    return VerifyPath::Simt;
+}
+
+size_t verify_workspace(const VerifyArgs &a, unsigned flags)
+{
+    switch (verify_path(a, flags)) {
+    case VerifyPath::Fused: return tc_workspace_bytes(a.B, a.H, a.max_T);
+    case VerifyPath::Big: return tc_big_workspace_bytes(a.B, a.H);
+    default: return simt_workspace_bytes(a.B, a.H, a.max_T);
+    }
 }
 
 } // namespace
@@ -52,8 +69,7 @@ size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_dept
     VerifyArgs a = {};
     a.dtype = qkv_dtype;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T; a.max_depth = max_depth;
-    if (use_tc_verify(a, flags)) return tc_workspace_bytes(B, H, max_T);
-    return simt_workspace_bytes(B, H, max_T);
+    return verify_workspace(a, flags);
 }
 
 bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int B, int N,
@@ -104,14 +120,18 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
     a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.st = dev_status;
 
-    const bool tc = use_tc_verify(a, flags);
-    const size_t need = tc ? tc_workspace_bytes(B, H, max_T) : simt_workspace_bytes(B, H, max_T);
+    const VerifyPath path = verify_path(a, flags);
+    const size_t need = verify_workspace(a, flags);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return BOLE_ERR_WORKSPACE;
     if (B == 0 || N == 0) return BOLE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return from_cuda(tc ? launch_tc_verify(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0)
-                        : launch_simt_verify(a, s));
+    switch (path) {
+    case VerifyPath::Fused:
+        return from_cuda(launch_tc_verify(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0));
+    case VerifyPath::Big: return from_cuda(launch_tc_big_verify(a, s));
+    default: return from_cuda(launch_simt_verify(a, s));
+    }
 }
 
 bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const void *k,

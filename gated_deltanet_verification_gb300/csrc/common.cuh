@@ -90,6 +90,9 @@ cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
 bool tc_verify_supported(const VerifyArgs &a);
 size_t tc_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap);
+bool tc_big_supported(const VerifyArgs &a);
+size_t tc_big_workspace_bytes(int B, int H);
+cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s);
 bool tc_commit_supported(const CommitArgs &a);
 cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap);
 

@@ -187,3 +187,50 @@ def test_overlapped_round_matches_serial_launches():
                logP=rb2.logP.cpu().numpy().astype(np.float64),
                S_new=db2.S.cpu().numpy().astype(np.float64))
     _check(b, got, 1e-2)
+
+
+@pytest.mark.parametrize("seed,sizes,depth", [(31, [100, 70], 40), (32, [128], 127), (33, [48], 20)])
+def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
+    """The large-tree path's factor kernel leaves [M; W] = [C (I+G)^{-1}; (I+G)^{-1}]
+    in the workspace; compare with a library dense inverse of the same G and C
+    (Lemma 3: the log-depth product of (I + G^(2^k)) equals the finite Neumann sum)."""
+    from gated_deltanet_verification_gb300 import bole, device
+    import pins_lib
+    b = I.random_batch(seed=seed, B=len(sizes), H=2, dk=128, dv=128, sizes=sizes,
+                       max_depth=depth, dtype="bf16", sigma=0.05, shape="chain" if depth >= 100
+                       else "random")
+    db = device.to_device(b)
+    rb = device.alloc_round(db)
+    assert rb.workspace is not None and rb.workspace.numel() * rb.workspace.element_size() == \
+        b.B * b.H * 256 * 128 * 4
+    device.pack(db, rb)
+    device.verify(db, rb)
+    torch.cuda.synchronize()
+    bole.check_status(rb.status)
+    mw = rb.workspace.view(torch.float32).view(b.B, b.H, 256, 128).cpu().numpy()
+    for r in range(b.B):
+        o, e = int(b.offsets[r]), int(b.offsets[r + 1])
+        T = e - o
+        for hh in range(b.H):
+            # G, C with decay ratios taken in log space (a 128-node chain underflows P)
+            anc = pins_lib.ancestors_or_self(b.parent[o:e])
+            lg = np.log(b.gamma[o:e, hh].astype(np.float64))
+            L = np.array([sum(lg[j] for j in anc[i]) for i in range(T)])
+            q64 = b.q[o:e, hh].astype(np.float64)
+            k64 = b.k[o:e, hh].astype(np.float64)
+            G = np.zeros((T, T))
+            C = np.zeros((T, T))
+            for i in range(T):
+                for j in anc[i]:
+                    ratio = np.exp(L[i] - L[j])
+                    C[i, j] = ratio * (q64[i] @ k64[j])
+                    if j != i:
+                        G[i, j] = b.beta[o + i, hh] * ratio * (k64[i] @ k64[j])
+            W = np.linalg.inv(np.eye(T) + G)
+            M = C @ W
+            Wg = mw[r, hh, 128:128 + T, :T]
+            Mg = mw[r, hh, :T, :T]
+            assert rel_fro(Wg, W) < 5e-3, (r, hh, rel_fro(Wg, W))
+            assert rel_fro(Mg, M) < 5e-3, (r, hh, rel_fro(Mg, M))
+            # padding rows and columns stay exactly zero (W keeps its unit diagonal)
+            assert np.all(mw[r, hh, :T, T:] == 0) and np.all(mw[r, hh, 128:128 + T, T:] == 0)
