@@ -7,9 +7,14 @@ namespace bole {
 namespace {
 
 // One warp per request.  The request's parent array (at most 128 entries) is
-// staged in shared memory with coalesced loads, validated, and then every lane
-// walks its nodes' parent links there (at most 128 steps, guaranteed to end
-// because every parent index was checked to be smaller); depth = bits - 1.
+// staged in shared memory with coalesced loads and validated; then the
+// ancestor-or-self masks are built by pointer jumping: node i starts with
+// {i} and a jump to its parent, and each round ORs in the mask held at its
+// jump target and doubles the jump (jump <- jump of the jump), so after
+// ceil(log2 128) = 7 rounds every mask holds the whole path to the root (a
+// path of length l is covered after ceil(log2 l) rounds).  Rounds alternate
+// between two copies of the masks and jumps so a lane never reads a value
+// another lane is writing.  depth = bits - 1.
 constexpr int kPackWarps = 4;
 
 __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
@@ -17,7 +22,8 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
     int max_depth, int32_t *__restrict__ depth, uint32_t *__restrict__ anc,
     int32_t *__restrict__ req_depth, int32_t *st)
 {
-    __shared__ int sp[kPackWarps][kMaxTree];
+    __shared__ uint4 smask[2][kPackWarps][kMaxTree];
+    __shared__ int sjump[2][kPackWarps][kMaxTree];
     pdl_launch_dependents(); // a verification launched to overlap may start its state reads
     const int wib = threadIdx.x >> 5;
     const int b = (int)blockIdx.x * kPackWarps + wib;
@@ -34,37 +40,54 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
         }
         return;
     }
-    int *par = sp[wib];
-    int bad_i = -1;
+    int bad_i = -1, bad_p = 0;
     for (int i = lane; i < T; i += 32) {
         const int p = parent[o + i];
-        par[i] = p;
-        if ((p < -1 || p >= i) && bad_i < 0) bad_i = i;
+        if ((p < -1 || p >= i) && bad_i < 0) {
+            bad_i = i;
+            bad_p = p;
+        }
+        const uint32_t bit = 1u << (i & 31), w = (uint32_t)(i >> 5);
+        smask[0][wib][i] = make_uint4(w == 0 ? bit : 0u, w == 1 ? bit : 0u, w == 2 ? bit : 0u,
+                                      w == 3 ? bit : 0u);
+        sjump[0][wib][i] = p;
     }
     const unsigned badm = __ballot_sync(0xffffffffu, bad_i >= 0);
     if (badm) {
         const int src = __ffs(badm) - 1;
         const int bi = __shfl_sync(0xffffffffu, bad_i, src);
+        const int bp = __shfl_sync(0xffffffffu, bad_p, src);
         if (lane == 0) {
             req_depth[b] = 0;
-            report(st, BOLE_ERR_BAD_TOPOLOGY, b, bi, par[bi]);
+            report(st, BOLE_ERR_BAD_TOPOLOGY, b, bi, bp);
         }
         return;
     }
     __syncwarp();
+    // every link points backwards, so jumps stay in [-1, i) and the rounds
+    // only ever read indices below the one they write
+    int cur = 0;
+    for (int round = 0; (1 << round) < T; ++round) {
+        for (int i = lane; i < T; i += 32) {
+            uint4 mk = smask[cur][wib][i];
+            int j = sjump[cur][wib][i];
+            if (j >= 0) {
+                const uint4 mj = smask[cur][wib][j];
+                mk.x |= mj.x; mk.y |= mj.y; mk.z |= mj.z; mk.w |= mj.w;
+                j = sjump[cur][wib][j];
+            }
+            smask[cur ^ 1][wib][i] = mk;
+            sjump[cur ^ 1][wib][i] = j;
+        }
+        __syncwarp();
+        cur ^= 1;
+    }
     int dmax = 0;
     for (int i = lane; i < T; i += 32) {
-        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        for (int j = i; j >= 0; j = par[j]) {
-            const uint32_t bit = 1u << (j & 31);
-            if (j < 32) w0 |= bit;
-            else if (j < 64) w1 |= bit;
-            else if (j < 96) w2 |= bit;
-            else w3 |= bit;
-        }
-        const int d = __popc(w0) + __popc(w1) + __popc(w2) + __popc(w3) - 1;
+        const uint4 mk = smask[cur][wib][i];
+        const int d = __popc(mk.x) + __popc(mk.y) + __popc(mk.z) + __popc(mk.w) - 1;
         depth[o + i] = d;
-        *reinterpret_cast<uint4 *>(anc + (size_t)(o + i) * 4) = make_uint4(w0, w1, w2, w3);
+        *reinterpret_cast<uint4 *>(anc + (size_t)(o + i) * 4) = mk;
         dmax = max(dmax, d);
     }
 #pragma unroll
