@@ -618,21 +618,18 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const int tid = threadIdx.x, warp = tid >> 5;
     const int unit = blockIdx.x, hv = blockIdx.y; // head unit, value tile
     const int b = unit / H, h = unit % H;
-    // The state half depends on the block alone: it is requested first.
+    // The state half is requested once the first batch of path reads is in
+    // flight (below), so those small reads do not queue behind it.
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmS);
-        mbar_arrive_expect_tx(&bar[0], 2 * 16384);
-        tma_load_2d(sS, &tmS, &bar[0], kTile * hv, unit * kD);
-        tma_load_2d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD);
     }
-    // The state half is the caller's; everything the verification (or the
-    // sampler) wrote -- U, log P, the accepted node, the status -- is read
-    // after the wait.  The status word, the accepted node and the request's
-    // extent come in one round trip; uniform early exits (the issuing thread
-    // drains the copy).
+    // Everything the verification (or the sampler) wrote -- U, log P, the
+    // accepted node, the status -- is read after the wait.  The status word,
+    // the accepted node and the request's extent come in one round trip;
+    // uniform early exits.
     pdl_wait();
     const int fault = *(const volatile int32_t *)st;
     const int a = accepted[b];
@@ -640,7 +637,6 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
     if (fault != 0 || a < 0 || bad) {
         if (bad && fault == 0 && tid == 0 && hv == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
-        if (tid == 0) mbar_wait(&bar[0], 0, kWaitNs);
         return;
     }
     if (warp == 0) {
@@ -689,6 +685,11 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
             kv[tt] = (tt < tn) ? __bfloat162float(k[nh * kD + tid]) : 0.f;
             uv[tt] = (tt < tn && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
         }
+        if (ch == 0 && tid == 0) {
+            mbar_arrive_expect_tx(&bar[0], 2 * 16384);
+            tma_load_2d(sS, &tmS, &bar[0], kTile * hv, unit * kD);
+            tma_load_2d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD);
+        }
         // A[r][t] = coef_t k_{j_t}[r] (row r = tid), K-major, 64-byte rows
 #pragma unroll
         for (int c4 = 0; c4 < kChunk / 4; ++c4) {
@@ -728,7 +729,8 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     }
 
     // epilogue: S <- P_a S + D, in shared memory, then TMA store in place
-    if (!mbar_wait(&bar[0], 0, kWaitNs)) {
+    // (the state half was requested with the first chunk)
+    if (nchunks > 0 && !mbar_wait(&bar[0], 0, kWaitNs)) {
         report(st, BOLE_ERR_TIMEOUT, b, -1, 8);
         *flag = 1;
     }
