@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=8,
+                   help="layers of the unified cross-layer commit measurement (0 skips it)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--kernel-steps", type=int, default=200,
@@ -360,6 +362,7 @@ def main(argv=None):
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
+    layers = run_layers(args, batch, flags, stream) if args.layers > 0 else None
 
     if rank != 0:
         if world > 1:
@@ -414,6 +417,7 @@ def main(argv=None):
                                     f"of the {n_sets} input copies, replayed "
                                     f"{max(1, ks // n_sets)}x between events"},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
+        "commit_layers": layers,
         "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
     }
     print(json.dumps(out))
@@ -421,6 +425,82 @@ def main(argv=None):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def run_layers(args, batch, flags, stream):
+    """Unified cross-layer commit on this workload: `args.layers` GDN layers
+    (each its own S_pre and operands, one shared forest) verified into
+    contiguous [layers, ...] factor buffers, then committed by ONE
+    bole_commit_layers launch -- timed against the same layers committed by
+    one bole_commit launch each.  Both in the default [dk, dv] state layout
+    and in the slot layout [dv, dk] (BOLE_FLAG_STATE_VK).  The states of all
+    layers (layers x B x H x 64 KB) exceed L2 for the batched workloads; each
+    timing replays a CUDA graph of the launch(es)."""
+    import torch
+    from gated_deltanet_verification_gb300 import bole, inputs
+
+    L = args.layers
+    lbs = inputs.layer_batches(batch, L, seed=4242)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dt = torch.bfloat16 if batch.dtype == "bf16" else torch.float32
+
+    def t(a, d):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=d)
+
+    offsets, parent = t(batch.offsets, torch.int32), t(batch.parent, torch.int32)
+    accepted = t(batch.accepted, torch.int32)
+    depth, anc, req, st = bole.pack_forest(offsets, parent, batch.max_depth)
+    k_all = torch.stack([t(lb.k, dt) for lb in lbs])
+    U_all = torch.empty((L, batch.N, batch.H, batch.dv), dtype=torch.float32, device=dev)
+    lp_all = torch.empty((L, batch.N, batch.H), dtype=torch.float32, device=dev)
+    alg = 0
+    for lb in lbs:
+        alg += algorithmic(lb)["commit"]
+    out = {"layers": L, "alg_bytes": int(alg)}
+    hbm, _, _ = measured_peaks()
+    for layout in ("kv", "vk"):
+        f = flags | (bole.FLAG_STATE_VK if layout == "vk" else 0)
+        S_all = torch.stack([t(lb.S_pre if layout == "kv" else lb.S_pre.transpose(0, 1, 3, 2),
+                               torch.float32) for lb in lbs])
+        for li, lb in enumerate(lbs):
+            bole.tree_verify(S_all[li], t(lb.q, dt), k_all[li], t(lb.v, dt),
+                             t(lb.gamma, torch.float32), t(lb.beta, torch.float32), offsets,
+                             parent, depth, anc, req, max(batch.max_T, 1), batch.max_depth,
+                             U=U_all[li], logP=lp_all[li], status=st, flags=f)
+        torch.cuda.synchronize()
+        bole.check_status(st, "layered verify")
+
+        def one_launch():
+            bole.commit_layers(S_all, k_all, U_all, lp_all, offsets, parent, accepted,
+                               status=st, flags=f)
+
+        def per_layer():
+            for li in range(L):
+                bole.commit(S_all[li], k_all[li], U_all[li], lp_all[li], offsets, parent,
+                            accepted, status=st, flags=f)
+
+        res = {}
+        for name, fn in (("one_launch", one_launch), ("per_layer", per_layer)):
+            fn()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            g.replay()
+            reps = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) / reps
+        bole.check_status(st, "layered commit")
+        gbs = alg / (res["one_launch"] * 1e-3) / 1e9
+        out[layout] = {"ms_one_launch": round(res["one_launch"], 5),
+                       "ms_per_layer_launches": round(res["per_layer"], 5),
+                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    return out
 
 
 def run_e2e(args, batch, sets, flags, stream, world):

@@ -30,6 +30,7 @@ F32 = 0
 BF16 = 1
 FLAG_FORCE_SIMT = 0x1
 FLAG_OVERLAP_LAUNCH = 0x2  # see bole.h: overlap with the previous library call on the stream
+FLAG_STATE_VK = 0x4  # state slots stored [B, H, dv, dk] (the serving runtime's slot layout)
 MAX_TREE_NODES = 128
 STATUS_WORDS = 4
 
@@ -76,6 +77,10 @@ def lib() -> ctypes.CDLL:
             L.bole_tree_verify_noalloc.restype = I
             L.bole_commit.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I, P, U, P]
             L.bole_commit.restype = I
+            I64 = ctypes.c_int64
+            L.bole_commit_layers.argtypes = [P, I64, P, I64, I, P, I64, P, I64, P, P, P, I, I, I,
+                                             I, I, I, P, U, P]
+            L.bole_commit_layers.restype = I
             _lib = L
     return _lib
 
@@ -221,7 +226,38 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
     return S
 
 
-__all__ = ["lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
+def _layer_stride(t: torch.Tensor, n_layers: int) -> int:
+    """Element stride between the layers of a [layers, ...] tensor whose
+    per-layer slices are contiguous."""
+    if t.dim() < 2 or t.shape[0] != n_layers or not t[0].is_contiguous():
+        raise ValueError("expected a [layers, ...] tensor with contiguous layer slices")
+    return int(t.stride(0)) if n_layers > 1 else 0
+
+
+def commit_layers(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int = 0,
+                  stream=None) -> torch.Tensor:
+    """bole_commit_layers: one launch commits every layer of a round.
+
+    S [layers, B, H, dk, dv] (or [layers, B, H, dv, dk] with FLAG_STATE_VK),
+    k [layers, N, H, dk], U [layers, N, H, dv], logP [layers, N, H]; each
+    layer's slice contiguous, the layer strides taken from the tensors (a
+    slice of a larger preallocated pool works).  Overwrites S in place and
+    returns it."""
+    n_layers = S.shape[0]
+    B = offsets.numel() - 1
+    _, N, H, dk = k.shape
+    dv = U.shape[-1]
+    if status is None:
+        status = new_status(k.device)
+    _check(lib().bole_commit_layers(
+        S.data_ptr(), _layer_stride(S, n_layers), k.data_ptr(), _layer_stride(k, n_layers),
+        _dtype_code(k), U.data_ptr(), _layer_stride(U, n_layers), logP.data_ptr(),
+        _layer_stride(logP, n_layers), _ptr(offsets), _ptr(parent), _ptr(accepted), n_layers, B,
+        H, dk, dv, N, _ptr(status), int(flags), _stream(stream)), "bole_commit_layers")
+    return S
+
+
+__all__ = ["commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
            "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
            "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT",

@@ -68,6 +68,7 @@ size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_dept
         return 0;
     VerifyArgs a = {};
     a.dtype = qkv_dtype;
+    a.vk = (flags & BOLE_FLAG_STATE_VK) != 0;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.max_T = max_T; a.max_depth = max_depth;
     return verify_workspace(a, flags);
 }
@@ -119,6 +120,7 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
     a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.st = dev_status;
+    a.vk = (flags & BOLE_FLAG_STATE_VK) != 0;
 
     const VerifyPath path = verify_path(a, flags);
     const size_t need = verify_workspace(a, flags);
@@ -167,8 +169,53 @@ bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const vo
     a.gamma = gamma; a.beta = beta;
     a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
-    a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.st = dev_status;
+    a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.st = dev_status; a.vk = false;
     return from_cuda(launch_simt_verify_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
+                               int64_t k_layer_stride, bole_dtype k_dtype, const float *U,
+                               int64_t u_layer_stride, const float *logP, int64_t lp_layer_stride,
+                               const int32_t *offsets, const int32_t *parent,
+                               const int32_t *accepted, int n_layers, int B, int H, int dk, int dv,
+                               int N, int32_t *dev_status, unsigned flags, bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(k_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if (n_layers < 0 || n_layers > 65535) return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && n_layers > 0 && (!S || !accepted)))
+        return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && n_layers > 0 && (!k || !U || !logP || !parent)) return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {S, k, U, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {logP, offsets, parent, accepted};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+    // Layer strides: none negative; state slices disjoint (each layer writes
+    // its own in place); every slice as aligned as the first.
+    const int64_t ksize = k_dtype == BOLE_BF16 ? 2 : 4;
+    if (s_layer_stride < 0 || k_layer_stride < 0 || u_layer_stride < 0 || lp_layer_stride < 0)
+        return BOLE_ERR_INVALID_ARG;
+    if (n_layers > 1 && s_layer_stride < (int64_t)B * H * dk * dv) return BOLE_ERR_INVALID_ARG;
+    if ((s_layer_stride * 4) % 16 != 0 || (k_layer_stride * ksize) % 16 != 0 ||
+        (u_layer_stride * 4) % 16 != 0)
+        return BOLE_ERR_INVALID_ARG;
+    if (B == 0 || N == 0 || n_layers == 0) return BOLE_OK;
+
+    CommitArgs a;
+    a.S = S; a.k = k; a.dtype = k_dtype; a.U = U; a.logP = logP;
+    a.offsets = offsets; a.parent = parent; a.accepted = accepted;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.st = dev_status;
+    a.layers = n_layers;
+    a.s_ls = s_layer_stride; a.k_ls = k_layer_stride; a.u_ls = u_layer_stride;
+    a.lp_ls = lp_layer_stride;
+    a.vk = (flags & BOLE_FLAG_STATE_VK) != 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = !(flags & BOLE_FLAG_FORCE_SIMT) && tc_commit_supported(a);
+    return from_cuda(tc ? launch_tc_commit(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0)
+                        : launch_simt_commit(a, s));
 }
 
 bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
@@ -176,27 +223,8 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
                         const int32_t *accepted, int B, int H, int dk, int dv, int N,
                         int32_t *dev_status, unsigned flags, bole_stream_t stream)
 {
-    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(k_dtype))
-        return BOLE_ERR_INVALID_ARG;
-    if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
-    if (!offsets || !dev_status || (B > 0 && (!S || !accepted))) return BOLE_ERR_INVALID_ARG;
-    if (N > 0 && (!k || !U || !logP || !parent)) return BOLE_ERR_INVALID_ARG;
-    const void *p16[] = {S, k, U, dev_status};
-    for (const void *p : p16)
-        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
-    const void *p4[] = {logP, offsets, parent, accepted};
-    for (const void *p : p4)
-        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
-    if (B == 0 || N == 0) return BOLE_OK;
-
-    CommitArgs a;
-    a.S = S; a.k = k; a.dtype = k_dtype; a.U = U; a.logP = logP;
-    a.offsets = offsets; a.parent = parent; a.accepted = accepted;
-    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.st = dev_status;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool tc = !(flags & BOLE_FLAG_FORCE_SIMT) && tc_commit_supported(a);
-    return from_cuda(tc ? launch_tc_commit(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0)
-                        : launch_simt_commit(a, s));
+    return bole_commit_layers(S, 0, k, 0, k_dtype, U, 0, logP, 0, offsets, parent, accepted, 1, B,
+                              H, dk, dv, N, dev_status, flags, stream);
 }
 
 } // extern "C"

@@ -69,8 +69,11 @@ struct VerifyArgs {
     float *U, *logP;
     void *ws;
     int32_t *st;
+    bool vk; // state stored [B, H, dv, dk] (BOLE_FLAG_STATE_VK)
 };
 
+// One commit launch over `layers` GDN layers: layer l's S, k, U and logP start
+// l strides (in elements) after the pointers below.
 struct CommitArgs {
     float *S;
     const void *k;
@@ -79,6 +82,9 @@ struct CommitArgs {
     const int32_t *offsets, *parent, *accepted;
     int B, H, dk, dv, N;
     int32_t *st;
+    int layers;
+    int64_t s_ls, k_ls, u_ls, lp_ls;
+    bool vk; // state stored [B, H, dv, dk] (BOLE_FLAG_STATE_VK)
 };
 
 size_t simt_workspace_bytes(int B, int H, int max_T);

@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kThreads) simt_factor_kernel(
 // Lane = value column; warps stride over nodes.
 //   B0 = D_P (Q S_pre^(r)),  R = D_beta (V^(r) - D_P (K S_pre^(r)))   (Eq. (7))
 //   Z <- -G Z, U += Z for d steps (Eq. (8)), then O = B0 + C U.
-template <typename T>
+// VK: the state is stored transposed ([dv][dk] per head, the slot layout).
+template <typename T, bool VK>
 __global__ void __launch_bounds__(kThreads) simt_solve_kernel(
     const float *__restrict__ S_pre, const T *__restrict__ q, const T *__restrict__ k,
     const T *__restrict__ v, const float *__restrict__ beta, const int32_t *__restrict__ offsets,
@@ -154,8 +155,11 @@ __global__ void __launch_bounds__(kThreads) simt_solve_kernel(
         Gs[e] = G[(size_t)(e / Tn) * max_T + (e % Tn)];
     const float *S = S_pre + (size_t)unit * dk * dv;
     for (int e = threadIdx.x; e < dk * kTileV; e += blockDim.x) {
-        const int r = e / kTileV, c = e % kTileV;
-        Ss[e] = (c0 + c < dv) ? S[(size_t)r * dv + c0 + c] : 0.f;
+        // consecutive threads read consecutive addresses in either layout
+        const int r = VK ? e % dk : e / kTileV, c = VK ? e / dk : e % kTileV;
+        Ss[r * kTileV + c] = (c0 + c < dv)
+                                 ? S[VK ? (size_t)(c0 + c) * dk + r : (size_t)r * dv + c0 + c]
+                                 : 0.f;
     }
     for (int i = threadIdx.x; i < Tn; i += blockDim.x) {
         Pv[i] = expf(logP[(size_t)(o + i) * H + h]);
@@ -206,18 +210,20 @@ __global__ void __launch_bounds__(kThreads) simt_solve_kernel(
     }
 }
 
-// Commit (Eq. (10)): one CTA per (request, head, block of 32 state rows).
-// S[r][c] <- P_a S[r][c] + sum_t exp(L_a - L_{j_t}) k_{j_t}[r] u_{j_t}[c],
-// the sum running over the accepted path j_t (root child .. a).
+// Commit (Eq. (10)): one CTA per (request, head, block of 32 state rows,
+// layer).  S[r][c] <- P_a S[r][c] + sum_t exp(L_a - L_{j_t}) k_{j_t}[r] u_{j_t}[c],
+// the sum running over the accepted path j_t (root child .. a).  Layer l's
+// buffers start l strides after the base pointers; with VK the state is
+// stored transposed (element (r, c) at c * dk + r).
 constexpr int kCommitRows = 32;
 constexpr int kPathChunk = 32;
 
-template <typename T>
+template <typename T, bool VK>
 __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
     float *__restrict__ S, const T *__restrict__ k, const float *__restrict__ U,
     const float *__restrict__ logP, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ parent, const int32_t *__restrict__ accepted, int H, int dk,
-    int dv, int N, int32_t *st)
+    int dv, int N, int64_t s_ls, int64_t k_ls, int64_t u_ls, int64_t lp_ls, int32_t *st)
 {
     __shared__ int path[kMaxTree];
     __shared__ float coef[kMaxTree];
@@ -227,6 +233,11 @@ __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
     const int r0 = blockIdx.y * kCommitRows;
+    const int layer = blockIdx.z;
+    S += layer * s_ls;
+    k += layer * k_ls;
+    U += layer * u_ls;
+    logP += layer * lp_ls;
     if (faulted(st)) return;
     const int a = accepted[b];
     if (a < 0) return;
@@ -261,12 +272,21 @@ __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
     const int rows = min(kCommitRows, dk - r0);
     float *Su = S + (size_t)unit * dk * dv;
     constexpr int kPer = kCommitRows * 128 / kThreads; // 16 elements per thread
+    // element idx of the tile: (row rr, column c), consecutive threads on
+    // consecutive addresses in either layout
+    auto elem = [&](int idx, int &rr, int &c) {
+        rr = VK ? idx % kCommitRows : idx / dv;
+        c = VK ? idx / kCommitRows : idx % dv;
+        return rr < rows && c < dv;
+    };
+    auto at = [&](int rr, int c) -> size_t {
+        return VK ? (size_t)c * dk + r0 + rr : (size_t)(r0 + rr) * dv + c;
+    };
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-        const int idx = threadIdx.x + e * kThreads;
-        const int rr = idx / dv, c = idx % dv;
-        acc[e] = (rr < rows) ? Pa * Su[(size_t)(r0 + rr) * dv + c] : 0.f;
+        int rr, c;
+        acc[e] = elem(threadIdx.x + e * kThreads, rr, c) ? Pa * Su[at(rr, c)] : 0.f;
     }
     __syncthreads();
     for (int t0 = 0; t0 < L; t0 += kPathChunk) {
@@ -285,9 +305,8 @@ __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
-            const int idx = threadIdx.x + e * kThreads;
-            const int rr = idx / dv, c = idx % dv;
-            if (rr < rows) {
+            int rr, c;
+            if (elem(threadIdx.x + e * kThreads, rr, c)) {
                 float s = acc[e];
                 for (int t = 0; t < n; ++t) s = fmaf(ks[t][rr], us[t][c], s);
                 acc[e] = s;
@@ -297,9 +316,8 @@ __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
     }
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-        const int idx = threadIdx.x + e * kThreads;
-        const int rr = idx / dv, c = idx % dv;
-        if (rr < rows) Su[(size_t)(r0 + rr) * dv + c] = acc[e];
+        int rr, c;
+        if (elem(threadIdx.x + e * kThreads, rr, c)) Su[at(rr, c)] = acc[e];
     }
 }
 
@@ -308,7 +326,7 @@ size_t solve_smem_bytes(int Tn, int dk)
     return sizeof(float) * ((size_t)Tn * Tn + (size_t)dk * kTileV + 4 * (size_t)Tn * kTileV + 2 * Tn);
 }
 
-template <typename T> cudaError_t verify_typed(const VerifyArgs &a, cudaStream_t s)
+template <typename T, bool VK> cudaError_t verify_typed(const VerifyArgs &a, cudaStream_t s)
 {
     const size_t unit_ws = (size_t)a.max_T * a.max_T;
     float *wsG = static_cast<float *>(a.ws);
@@ -320,23 +338,23 @@ template <typename T> cudaError_t verify_typed(const VerifyArgs &a, cudaStream_t
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = solve_smem_bytes(a.max_T, a.dk);
-    e = cudaFuncSetAttribute(simt_solve_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    e = cudaFuncSetAttribute(simt_solve_kernel<T, VK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(units, (a.dv + kTileV - 1) / kTileV);
-    simt_solve_kernel<T><<<grid, kThreads, smem, s>>>(
+    simt_solve_kernel<T, VK><<<grid, kThreads, smem, s>>>(
         a.S_pre, static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.beta, a.offsets, a.req_depth, a.H, a.dk, a.dv, a.N, a.max_T,
         a.logP, wsG, wsC, static_cast<T *>(a.O), a.U, a.st);
     return cudaGetLastError();
 }
 
-template <typename T> cudaError_t commit_typed(const CommitArgs &a, cudaStream_t s)
+template <typename T, bool VK> cudaError_t commit_typed(const CommitArgs &a, cudaStream_t s)
 {
-    dim3 grid(a.B * a.H, (a.dk + kCommitRows - 1) / kCommitRows);
-    simt_commit_kernel<T><<<grid, kThreads, 0, s>>>(a.S, static_cast<const T *>(a.k), a.U, a.logP,
-                                                     a.offsets, a.parent, a.accepted, a.H, a.dk,
-                                                     a.dv, a.N, a.st);
+    dim3 grid(a.B * a.H, (a.dk + kCommitRows - 1) / kCommitRows, a.layers);
+    simt_commit_kernel<T, VK><<<grid, kThreads, 0, s>>>(
+        a.S, static_cast<const T *>(a.k), a.U, a.logP, a.offsets, a.parent, a.accepted, a.H, a.dk,
+        a.dv, a.N, a.s_ls, a.k_ls, a.u_ls, a.lp_ls, a.st);
     return cudaGetLastError();
 }
 
@@ -350,13 +368,17 @@ size_t simt_workspace_bytes(int B, int H, int max_T)
 cudaError_t launch_simt_verify(const VerifyArgs &a, cudaStream_t s)
 {
     if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
-    return a.dtype == BOLE_BF16 ? verify_typed<__nv_bfloat16>(a, s) : verify_typed<float>(a, s);
+    if (a.dtype == BOLE_BF16)
+        return a.vk ? verify_typed<__nv_bfloat16, true>(a, s) : verify_typed<__nv_bfloat16, false>(a, s);
+    return a.vk ? verify_typed<float, true>(a, s) : verify_typed<float, false>(a, s);
 }
 
 cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s)
 {
-    if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
-    return a.dtype == BOLE_BF16 ? commit_typed<__nv_bfloat16>(a, s) : commit_typed<float>(a, s);
+    if (a.B * a.H == 0 || a.N == 0 || a.layers == 0) return cudaSuccess;
+    if (a.dtype == BOLE_BF16)
+        return a.vk ? commit_typed<__nv_bfloat16, true>(a, s) : commit_typed<__nv_bfloat16, false>(a, s);
+    return a.vk ? commit_typed<float, true>(a, s) : commit_typed<float, false>(a, s);
 }
 
 // ---- verification without any allocation ----

@@ -31,6 +31,7 @@ using namespace tc;
 constexpr int kTB = 128; // padded tree extent of this path
 constexpr uint32_t IDESC_G128 = idesc_bf16(128, 128, false, false);  // X K^T, both K-major
 constexpr uint32_t IDESC_S128 = idesc_bf16(128, 128, false, true);   // X S, S N-contiguous
+constexpr uint32_t IDESC_S128_VK = idesc_bf16(128, 128, false, false); // S stored [dv][dk]
 constexpr uint32_t IDESC_T128 = idesc_tf32(128, 128, false, false);  // tf32, both K-major
 
 // tcgen05 kind::tf32 with A read from tensor memory (lane = row, one fp32
@@ -333,6 +334,10 @@ constexpr int kSBThreads = kSBCompute + 32;
 constexpr int BS_S = 0, BS_QK = 1, BS_V = 2, BS_STATE = 3, BS_MW0 = 4, BS_MW1 = 5, BS_DONE0 = 6,
               BS_DONE1 = 7, BS_MMA2 = 8, BS_CONV = 9, BS_OPS = 10;
 
+// VK: the state is stored transposed ([dv][dk] per head, the slot layout);
+// the same boxes and split then hold K-major operand rows (row = value
+// column), read 32 B further along the rows per 16 d_k.
+template <bool VK>
 __global__ void __launch_bounds__(kSBThreads, 1)
 tc_big_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -401,19 +406,22 @@ tc_big_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             ok &= mbar_wait(&bar[BS_QK], 0, kWaitNs);
             ok &= mbar_wait(&bar[BS_CONV], 0, kWaitNs);
             tc_fence_after();
-            // Q S_pre -> R0, K S_pre -> R1 (S = S_hi + S_lo, N-contiguous)
+            // Q S_pre -> R0, K S_pre -> R1 (S = S_hi + S_lo)
             const uint32_t slo = s0 + 16384;
+            constexpr uint32_t idesc_s = VK ? IDESC_S128_VK : IDESC_S128;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint64_t bh = sdesc_sw128(s0 + kk * 2048, 32768, 1024);
-                const uint64_t bl = sdesc_sw128(slo + kk * 2048, 32768, 1024);
+                const uint32_t boff = VK ? (kk >> 2) * 32768 + (kk & 3) * 32 : kk * 2048;
+                const uint32_t lbo = VK ? 16 : 32768;
+                const uint64_t bh = sdesc_sw128(s0 + boff, lbo, 1024);
+                const uint64_t bl = sdesc_sw128(slo + boff, lbo, 1024);
                 const uint64_t aq = sdesc_sw128(qa + off, 16, 1024);
                 const uint64_t ak = sdesc_sw128(ka + off, 16, 1024);
-                mma_bf16_ss(R0, aq, bh, IDESC_S128, kk > 0);
-                mma_bf16_ss(R0, aq, bl, IDESC_S128, 1);
-                mma_bf16_ss(R1, ak, bh, IDESC_S128, kk > 0);
-                mma_bf16_ss(R1, ak, bl, IDESC_S128, 1);
+                mma_bf16_ss(R0, aq, bh, idesc_s, kk > 0);
+                mma_bf16_ss(R0, aq, bl, idesc_s, 1);
+                mma_bf16_ss(R1, ak, bh, idesc_s, kk > 0);
+                mma_bf16_ss(R1, ak, bl, idesc_s, 1);
             }
             mma_commit(&bar[BS_STATE]);
             // the [Q;K] buffer is free once the products are done: [M; W] chunks
@@ -604,12 +612,11 @@ cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s)
                                                              a.logP, mw, a.st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = configure_once(reinterpret_cast<const void *>(tc_big_solve_kernel), SB_SMEM, true, 3);
+    auto solve = a.vk ? tc_big_solve_kernel<true> : tc_big_solve_kernel<false>;
+    e = configure_once(reinterpret_cast<const void *>(solve), SB_SMEM, true, a.vk ? 6 : 3);
     if (e != cudaSuccess) return e;
-    tc_big_solve_kernel<<<units, kSBThreads, SB_SMEM, s>>>(mS, mQ, mK, mV, mMW, a.beta, a.offsets,
-                                                            a.logP, a.H, a.N,
-                                                            static_cast<__nv_bfloat16 *>(a.O), a.U,
-                                                            a.st);
+    solve<<<units, kSBThreads, SB_SMEM, s>>>(mS, mQ, mK, mV, mMW, a.beta, a.offsets, a.logP, a.H,
+                                             a.N, static_cast<__nv_bfloat16 *>(a.O), a.U, a.st);
     return cudaGetLastError();
 }
 

@@ -33,6 +33,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y,
+                                             int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
 {
     const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -81,12 +89,34 @@ inline cudaError_t make_state_map(CUtensorMap *map, const float *S, int units)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The states of `layers` GDN layers, layer l at S + l * layer_stride floats, as
+// a 3-D fp32 tensor [layers][B*H*128 rows][128 cols], boxes of 32 x 128 x 1.
+// One layer needs no stride (any valid value serves).
+inline cudaError_t make_layered_state_map(CUtensorMap *map, const float *S, int units, int layers,
+                                          int64_t layer_stride)
+{
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const uint64_t slice = (uint64_t)units * kD * kD * sizeof(float);
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)units * kD, (cuuint64_t)layers};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * sizeof(float),
+                             layers > 1 ? (cuuint64_t)layer_stride * sizeof(float) : slice};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(S), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Kernel attributes are per device and per function: set them on the first
 // launch on each device only (they do not change), so later calls -- and
 // stream capture -- meet no attribute call.
 inline cudaError_t configure_once(const void *fn, int smem, bool carveout, int slot)
 {
     static std::mutex mu;
+    // slots: 0 verify, 1 commit, 2 large-tree factor, 3 large-tree solve, and
+    // 4, 5, 6 the same kernels for the transposed state layout
     static uint64_t done[8] = {0, 0, 0, 0, 0, 0, 0, 0}; // bit = device, word = slot
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -112,6 +112,7 @@ constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
 
 constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
 constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
+constexpr uint32_t IDESC_STATE_VK = idesc_bf16(128, 128, false, false); // S stored [dv][dk]
 constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
 constexpr uint32_t TM_GRAM = 128, TM_PROP = 128;                  // tensor-memory columns
 
@@ -130,6 +131,12 @@ constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, B
 // [Q;K] columns that the value rows then overwrite and the S_pre rows where
 // the Gram is staged, so neither waits for the whole product.  All waits are
 // bounded.
+// VK: the state is stored transposed, [dv][dk] per head (the serving
+// runtime's slot layout).  The same TMA boxes and the same split then give
+// K-major operand rows (row = value column, 64 d_k entries per 128 B), the
+// first d_k half of the product reads the boxes (0, 1) whole, and the Gram
+// is staged in those 32 KB instead.
+template <bool VK>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -274,11 +281,16 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
             tc_fence_after();
             const uint32_t slo = s0 + 16384;
+            constexpr uint32_t idesc_s = VK ? IDESC_STATE_VK : IDESC_STATE;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = sdesc_sw128(a1 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + kk * 2048, 32768, 1024), IDESC_STATE, kk > 0);
-                mma_bf16_ss(tmem, ad, sdesc_sw128(slo + kk * 2048, 32768, 1024), IDESC_STATE, 1);
+                // 16 d_k rows of S: N-contiguous atoms 32 KB apart, or (VK) a
+                // 32 B step along the K-major rows of box pair kk / 4
+                const uint32_t boff = VK ? (kk >> 2) * 32768 + (kk & 3) * 32 : kk * 2048;
+                const uint32_t lbo = VK ? 16 : 32768;
+                mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + boff, lbo, 1024), idesc_s, kk > 0);
+                mma_bf16_ss(tmem, ad, sdesc_sw128(slo + boff, lbo, 1024), idesc_s, 1);
                 if (kk == 3) mma_commit(&bar[BAR_STATE_A]);
             }
             mma_commit(&bar[BAR_STATE]);
@@ -305,10 +317,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         // ========================== compute warps =========================
         bool ok = true;
         // Gram row m is staged in the S_pre rows the first d_k half released:
-        // rows 32p..32p+31 in the first 8 KB of box p, 256 B per row, 16-byte
-        // chunks XOR-swizzled by row.
+        // rows 32p..32p+31 in the first 8 KB of box p (VK: the first 32 KB,
+        // boxes 0 and 1), 256 B per row, 16-byte chunks XOR-swizzled by row.
         auto staged_row = [&](int row) -> float * {
-            return reinterpret_cast<float *>(sbuf + (row >> 5) * 16384 + (row & 31) * 256);
+            return reinterpret_cast<float *>(
+                sbuf + (VK ? row * 256 : (row >> 5) * 16384 + (row & 31) * 256));
         };
         float ratio[kSlots]; // topology rows: exp(L_i - L_j), j the ancestor at depth t
         uint32_t aw[4] = {0, 0, 0, 0}; // topology rows: ancestor-by-depth table, packed bytes
@@ -563,10 +576,17 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 }
 
 // ---- commit ----
-// One CTA per (request, head, 64-column half of the state): value tiling as in
-// the pages' kernel, so four CTAs fit on an SM and overlap their TMA load,
-// tensor-core product and TMA store.  (Narrower tiles fit more CTAs but
-// repeat the path operand's gather and measured slower.)
+// One CTA per (request, head, 64-column half of the state, layer): value
+// tiling as in the pages' kernel, so four CTAs fit on an SM and overlap their
+// TMA load, tensor-core product and TMA store.  (Narrower tiles fit more CTAs
+// but repeat the path operand's gather and measured slower.)  One launch
+// covers every layer of a unified cross-layer commit: layer l's state, keys,
+// deltas and decays start l strides after the base pointers.
+// The stored tile is always 128 rows x 64 columns.  [dk][dv] state: rows are
+// d_k (operand A = (D_a K_a)^T, 128 x path), columns a d_v half (operand B^T =
+// U_a^T of that half).  VK ([dv][dk], the slot layout): rows are d_v (A =
+// U_a^T), columns a d_k half (B^T = (D_a K_a)^T of that half) -- the same
+// product, transposed.
 constexpr int kCommitThreads = 128;
 constexpr int kChunk = 16;                    // path nodes per MMA K chunk
 constexpr int kTile = 64;                     // state columns per CTA
@@ -597,11 +617,13 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo)
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
+template <bool VK>
 __global__ void __launch_bounds__(kCommitThreads, 4)
 tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *__restrict__ k,
                  const float *__restrict__ U, const float *__restrict__ logP,
                  const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
-                 const int32_t *__restrict__ accepted, int H, int N, int32_t *st)
+                 const int32_t *__restrict__ accepted, int H, int N, int64_t k_ls, int64_t u_ls,
+                 int64_t lp_ls, int32_t *st)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -616,8 +638,12 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     int *spar = reinterpret_cast<int *>(sm + CO_PAR);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int unit = blockIdx.x, hv = blockIdx.y; // head unit, value tile
+    const int unit = blockIdx.x, hv = blockIdx.y; // head unit, column half
+    const int layer = blockIdx.z;
     const int b = unit / H, h = unit % H;
+    k += layer * k_ls;
+    U += layer * u_ls;
+    logP += layer * lp_ls;
     // The state half is requested once the first batch of path reads is in
     // flight (below), so those small reads do not queue behind it.
     if (tid == 0) {
@@ -636,7 +662,8 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const int o = offsets[b], T = offsets[b + 1] - o;
     const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
     if (fault != 0 || a < 0 || bad) {
-        if (bad && fault == 0 && tid == 0 && hv == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
+        if (bad && fault == 0 && tid == 0 && hv == 0 && layer == 0)
+            report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
         return;
     }
     if (warp == 0) {
@@ -661,7 +688,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
             j = p;
         }
         if (!ok) {
-            if (hv == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, j, -1);
+            if (hv == 0 && layer == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, j, -1);
             *flag = 1;
         }
         *plen = L;
@@ -674,40 +701,58 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const int nchunks = (*(volatile int *)flag != 0) ? 0 : (L + kChunk - 1) / kChunk;
     for (int ch = 0; ch < nchunks; ++ch) {
         // Every path-dependent read of the chunk in one batch: the decay of
-        // each path node (each thread forms its own coefficients), row r =
-        // tid of its key and, for c = tid < 64, column c of its U row.
+        // each path node (each thread forms its own coefficients), entry
+        // r = tid of the A-side row (key, or VK: U) and, for c = tid < 64,
+        // entry 64 hv + c of the B-side row (U, or VK: key).
         const int tn = min(kChunk, L - ch * kChunk); // path nodes in this chunk
-        float lp[kChunk], kv[kChunk], uv[kChunk];
+        float lp[kChunk], av_[kChunk], bv_[kChunk];
 #pragma unroll
         for (int tt = 0; tt < kChunk; ++tt) {
             const size_t nh = (size_t)(o + (tt < tn ? path[ch * kChunk + tt] : 0)) * H + h;
             lp[tt] = (tt < tn) ? logP[nh] : 0.f;
-            kv[tt] = (tt < tn) ? __bfloat162float(k[nh * kD + tid]) : 0.f;
-            uv[tt] = (tt < tn && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
+            if (VK) {
+                av_[tt] = (tt < tn) ? U[nh * kD + tid] : 0.f;
+                bv_[tt] = (tt < tn && tid < kTile)
+                              ? __bfloat162float(k[nh * kD + kTile * hv + tid]) : 0.f;
+            } else {
+                av_[tt] = (tt < tn) ? __bfloat162float(k[nh * kD + tid]) : 0.f;
+                bv_[tt] = (tt < tn && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
+            }
         }
         if (ch == 0 && tid == 0) {
             mbar_arrive_expect_tx(&bar[0], 2 * 16384);
-            tma_load_2d(sS, &tmS, &bar[0], kTile * hv, unit * kD);
-            tma_load_2d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD);
+            tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
+            tma_load_3d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD, layer);
         }
-        // A[r][t] = coef_t k_{j_t}[r] (row r = tid), K-major, 64-byte rows
+        // The key side carries the coefficients exp(L_a - L_j).
+        float coef[kChunk];
+#pragma unroll
+        for (int tt = 0; tt < kChunk; ++tt) coef[tt] = (tt < tn) ? expf(La - lp[tt]) : 0.f;
+        // A[r][t] (row r = tid), K-major, 64-byte rows
 #pragma unroll
         for (int c4 = 0; c4 < kChunk / 4; ++c4) {
             float av[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int tt = 4 * c4 + e;
-                av[e] = (tt < tn) ? expf(La - lp[tt]) * kv[tt] : 0.f;
+                av[e] = VK ? av_[tt] : coef[tt] * av_[tt];
             }
             *reinterpret_cast<float4 *>(sA + sw64_offset(tid, 4 * c4)) =
                 make_float4(av[0], av[1], av[2], av[3]);
         }
-        // B^T[c][t] = u_{j_t}[64 hv + c] (row c < 64), K-major, 64-byte rows
+        // B^T[c][t] (row c = tid < 64), K-major, 64-byte rows
         if (tid < kTile) {
 #pragma unroll
-            for (int t4 = 0; t4 < kChunk / 4; ++t4)
+            for (int t4 = 0; t4 < kChunk / 4; ++t4) {
+                float bv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tt = 4 * t4 + e;
+                    bv[e] = VK ? coef[tt] * bv_[tt] : bv_[tt];
+                }
                 *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * t4)) =
-                    make_float4(uv[4 * t4], uv[4 * t4 + 1], uv[4 * t4 + 2], uv[4 * t4 + 3]);
+                    make_float4(bv[0], bv[1], bv[2], bv[3]);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -759,8 +804,8 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     }
     __syncthreads();
     if (tid == 0 && ok && nchunks > 0) {
-        tma_store_2d(&tmS, sS, kTile * hv, unit * kD);
-        tma_store_2d(&tmS, sS + 16384, kTile * hv + 32, unit * kD);
+        tma_store_3d(&tmS, sS, kTile * hv, unit * kD, layer);
+        tma_store_3d(&tmS, sS + 16384, kTile * hv + 32, unit * kD, layer);
         bulk_commit_group();
         bulk_wait_group_read0();
     }
@@ -791,14 +836,15 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kT);
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kT);
     if (e != cudaSuccess) return e;
-    e = configure_once(reinterpret_cast<const void *>(tc_verify_kernel), VERIFY_SMEM, true, 0);
+    auto kernel = a.vk ? tc_verify_kernel<true> : tc_verify_kernel<false>;
+    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true, a.vk ? 4 : 0);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
                                                  overlap, attr);
-    return cudaLaunchKernelEx(&cfg, tc_verify_kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets,
-                              a.parent, a.req_depth, a.H, a.N,
-                              static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, a.st);
+    return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.parent,
+                              a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
+                              a.logP, a.st);
 }
 
 bool tc_commit_supported(const CommitArgs &a)
@@ -809,18 +855,20 @@ bool tc_commit_supported(const CommitArgs &a)
 cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap)
 {
     const int units = a.B * a.H;
-    if (units == 0 || a.N == 0) return cudaSuccess;
+    if (units == 0 || a.N == 0 || a.layers == 0) return cudaSuccess;
     CUtensorMap map;
-    cudaError_t e = make_state_map(&map, a.S, units);
+    cudaError_t e = make_layered_state_map(&map, a.S, units, a.layers, a.s_ls);
     if (e != cudaSuccess) return e;
-    e = configure_once(reinterpret_cast<const void *>(tc_commit_kernel), COMMIT_SMEM, false, 1);
+    auto kernel = a.vk ? tc_commit_kernel<true> : tc_commit_kernel<false>;
+    e = configure_once(reinterpret_cast<const void *>(kernel), COMMIT_SMEM, false, a.vk ? 5 : 1);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = launch_config(dim3(units, kD / kTile), dim3(kCommitThreads),
-                                                 COMMIT_SMEM, s, overlap, attr);
-    return cudaLaunchKernelEx(&cfg, tc_commit_kernel, map,
-                              static_cast<const __nv_bfloat16 *>(a.k), a.U, a.logP, a.offsets,
-                              a.parent, a.accepted, a.H, a.N, a.st);
+    const cudaLaunchConfig_t cfg = launch_config(dim3(units, kD / kTile, a.layers),
+                                                 dim3(kCommitThreads), COMMIT_SMEM, s, overlap,
+                                                 attr);
+    return cudaLaunchKernelEx(&cfg, kernel, map, static_cast<const __nv_bfloat16 *>(a.k), a.U,
+                              a.logP, a.offsets, a.parent, a.accepted, a.H, a.N, a.k_ls, a.u_ls,
+                              a.lp_ls, a.st);
 }
 
 } // namespace bole

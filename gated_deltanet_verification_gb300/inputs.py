@@ -323,8 +323,27 @@ def random_batch(seed: int, B: int, H: int, dk: int, dv: int, sizes, max_depth: 
     return make_batch(f"rand{seed}", rng, trees, H, dk, dv, dtype, max_depth, sigma, accept)
 
 
+def layer_batches(base: TreeBatch, n_layers: int, seed: int) -> List[TreeBatch]:
+    """`n_layers` GDN layers verifying one round's packed forest: layer 0 is
+    `base`; every further layer shares its offsets, parent links and accepted
+    nodes and draws its own S_pre, q, k, v, gamma, beta with the same
+    distributions (a layer's operands differ, the tree does not)."""
+    out = [base]
+    sigma = float(np.std(base.S_pre)) if base.S_pre.size else 0.05
+    sizes = base.tree_sizes()
+    trees = [base.parent[base.offsets[b]:base.offsets[b + 1]] for b in range(base.B)]
+    for layer in range(1, n_layers):
+        rng = np.random.Generator(np.random.PCG64([seed, layer]))
+        lb = make_batch(f"{base.name}-layer{layer}", rng, trees, base.H, base.dk, base.dv,
+                        base.dtype, base.max_depth, sigma, "none")
+        lb.accepted[:] = base.accepted
+        assert np.array_equal(lb.offsets, base.offsets) and len(sizes) == lb.B
+        out.append(lb)
+    return out
+
+
 __all__ = [
-    "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
+    "layer_batches", "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
     "kary_tree", "budgeted_forest", "make_batch", "config_batch", "random_batch",
     "CONFIG_NAMES", "SHAPES_CFG4", "MAX_TREE_NODES",
 ]

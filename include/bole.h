@@ -33,7 +33,8 @@
  *     kernels run exactly the per-request depth (extra Neumann steps would
  *     add exact zeros since G^(d+1) = 0).
  *   - Layouts (row-major, last index contiguous):
- *       S_pre / S     [B, H, dk, dv] float32 (one dk x dv state per head)
+ *       S_pre / S     [B, H, dk, dv] float32 (one dk x dv state per head);
+ *                     [B, H, dv, dk] with BOLE_FLAG_STATE_VK
  *       q, k          [N, H, dk]  bf16 or float32 (bole_dtype)
  *       v             [N, H, dv]  same dtype as q, k
  *       gamma, beta   [N, H] float32; gamma in (0, 1] (decay), beta = write gate
@@ -93,6 +94,13 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
  * read after the wait.  Without the flag every launch starts only after the
  * previous kernel has ended. */
 #define BOLE_FLAG_OVERLAP_LAUNCH 0x2u
+/* State slots in the serving runtime's canonical layout (Section IV-D, the
+ * state lifecycle of Fig. 6): S_pre / S stored [B, H, dv, dk] -- each head's
+ * state transposed, d_k contiguous -- instead of [B, H, dk, dv].  Accepted by
+ * bole_workspace_size, bole_tree_verify, bole_commit and bole_commit_layers;
+ * every kernel reads and writes that layout directly (no transposed copy).
+ * The results are the same numbers as with the default layout. */
+#define BOLE_FLAG_STATE_VK 0x4u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *bole_status_string(int status);
@@ -197,6 +205,36 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
                         const float *logP, const int32_t *offsets, const int32_t *parent,
                         const int32_t *accepted, int B, int H, int dk, int dv, int N,
                         int32_t *dev_status, unsigned flags, bole_stream_t stream);
+
+/* Unified cross-layer commit (Section IV-D and the integration notes of the
+ * SGLang page: every recurrent layer writes its P, K, U factors into one
+ * preallocated contiguous buffer and a single batched launch evaluates
+ * Eq. (10) for all of them).  One launch commits n_layers GDN layers that
+ * verified the same packed forest in this round: layer l's buffers are
+ *     S    + l * s_layer_stride    [B,H,dk,dv] (or [B,H,dv,dk]) float32, in/out
+ *     k    + l * k_layer_stride    [N,H,dk] k_dtype
+ *     U    + l * u_layer_stride    [N,H,dv] float32
+ *     logP + l * lp_layer_stride   [N,H]    float32
+ * (strides in ELEMENTS of each buffer), and offsets, parent, accepted are
+ * shared by all layers.  The result of each layer is exactly that of
+ * bole_commit on its slices; n_layers = 1 is bole_commit.
+ *   - n_layers in [0, 65535] (0 launches nothing).  With n_layers > 1 the
+ *     state slices must not overlap: s_layer_stride >= B*H*dk*dv (else
+ *     BOLE_ERR_INVALID_ARG); the read-only factor strides may be anything
+ *     >= 0 (0 shares one factor buffer between layers).
+ *   - Every stride times its element size is a multiple of 16 bytes, except
+ *     lp_layer_stride (4-byte elements, any value).
+ *   - flags: BOLE_FLAG_FORCE_SIMT, BOLE_FLAG_OVERLAP_LAUNCH (the previous
+ *     kernel on the stream is the last layer's bole_tree_verify, or does not
+ *     let dependents start early), BOLE_FLAG_STATE_VK.
+ *   - Device faults go to dev_status as for bole_commit (the first fault of
+ *     any layer wins; the fault record does not name the layer). */
+bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
+                               int64_t k_layer_stride, bole_dtype k_dtype, const float *U,
+                               int64_t u_layer_stride, const float *logP, int64_t lp_layer_stride,
+                               const int32_t *offsets, const int32_t *parent,
+                               const int32_t *accepted, int n_layers, int B, int H, int dk, int dv,
+                               int N, int32_t *dev_status, unsigned flags, bole_stream_t stream);
 
 #ifdef __cplusplus
 }

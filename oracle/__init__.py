@@ -150,5 +150,29 @@ def commit(batch, accepted=None, nthreads: Optional[int] = None, unit_begin: int
     return S_new
 
 
-__all__ = ["build", "load", "pack", "verify", "commit", "default_threads", "OK",
+def commit_layers(batches, accepted=None, state_layout: str = "kv",
+                  nthreads: Optional[int] = None, lib=None):
+    """Unified cross-layer commit (Section IV-D, state lifecycle; the SGLang
+    integration's single batched launch of Eq. (10) over every recurrent
+    layer's P, K, U): the layers of one round share the forest and the
+    accepted nodes, and layer l's committed state is that layer's own commit
+    (each layer's recurrence involves only its own S_pre and operands).
+
+    Returns [L, B, H, dk, dv], or with state_layout="vk" the serving runtime's
+    canonical slot layout [L, B, H, dv, dk] (Section IV-D: slots stored
+    [H, dv, dk])."""
+    if state_layout not in ("kv", "vk"):
+        raise ValueError(state_layout)
+    b0 = batches[0]
+    for b in batches[1:]:
+        if not (np.array_equal(b.offsets, b0.offsets) and np.array_equal(b.parent, b0.parent)):
+            raise ValueError("the layers of one round share the packed forest")
+    acc = b0.accepted if accepted is None else accepted
+    out = np.stack([commit(b, acc, nthreads, lib=lib) for b in batches])
+    if state_layout == "vk":
+        out = np.ascontiguousarray(out.transpose(0, 1, 2, 4, 3))
+    return out
+
+
+__all__ = ["build", "load", "pack", "verify", "commit", "commit_layers", "default_threads", "OK",
            "BAD_TOPOLOGY", "DEPTH"]

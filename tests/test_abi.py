@@ -96,3 +96,37 @@ def test_host_validation_without_gpu(lib):
     # commit: null accepted
     assert lib.bole_commit(fake, fake, 1, fake, fake, fake, fake, None, 1, 1, 128, 128, 4, fake,
                            0, None) == bole.ERR_INVALID_ARG
+
+
+def test_commit_layers_host_validation_without_gpu(lib):
+    """bole_commit_layers rejects layer strides that would overlap or misalign
+    the per-layer slices, before any launch."""
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake = c(1 << 20)
+    B, H, dk, dv, N = 2, 3, 128, 128, 8
+    slice_ = B * H * dk * dv
+
+    def call(n_layers, s_ls=slice_, k_ls=N * H * dk, u_ls=N * H * dv, lp_ls=N * H, S=fake,
+             flags=0):
+        return lib.bole_commit_layers(S, s_ls, fake, k_ls, 1, fake, u_ls, fake, lp_ls, fake,
+                                      fake, fake, n_layers, B, H, dk, dv, N, fake, flags, None)
+
+    assert call(2, s_ls=slice_ - 4) == bole.ERR_INVALID_ARG      # state slices overlap
+    assert call(2, s_ls=slice_ + 2) == bole.ERR_INVALID_ARG      # 8-byte layer stride step
+    assert call(2, k_ls=N * H * dk + 4) == bole.ERR_INVALID_ARG  # bf16 keys: 8 bytes
+    assert call(2, u_ls=-(N * H * dv)) == bole.ERR_INVALID_ARG   # negative stride
+    assert call(-1) == bole.ERR_INVALID_ARG
+    assert call(65536) == bole.ERR_INVALID_ARG
+    assert call(2, S=None) == bole.ERR_INVALID_ARG
+    # zero layers: valid, nothing launched
+    assert call(0) == bole.OK
+
+
+def test_state_layout_flag_keeps_the_workspace(lib):
+    f = lib.bole_workspace_size
+    f.restype = ctypes.c_size_t
+    from gated_deltanet_verification_gb300 import bole
+    vk = bole.FLAG_STATE_VK
+    for args in [(2, 3, 16, 16, 8, 3, 0), (2, 3, 128, 128, 64, 15, 1), (2, 3, 128, 128, 128, 127, 1)]:
+        assert f(*args, vk) == f(*args, 0)

@@ -244,3 +244,51 @@ def test_pack_rejects_bad_topology(bad):
         expected = oracle.DEPTH
     _, _, _, st = oracle.pack(offsets, parent, max_depth)
     assert st == expected
+
+
+def _slot_layout_path_replay(batch, b, h, a):
+    """The accepted node's state written straight in the slot layout [dv][dk]
+    (Section IV-D): walking the path root..a, each node applies Eq. (1) to the
+    TRANSPOSED state X = S^T,
+        X <- gamma X;  u = beta (v - X k);  X <- X + u k^T,
+    with X k = S^T k.  Independent of the oracle's [dk][dv] recurrence."""
+    o = batch.offsets[b]
+    path = []
+    j = a
+    while j >= 0:
+        path.append(j)
+        j = int(batch.parent[o + j])
+    X = batch.S_pre[b, h].astype(np.float64).T.copy()
+    for j in reversed(path):
+        kj = batch.k[o + j, h].astype(np.float64)
+        vj = batch.v[o + j, h].astype(np.float64)
+        X *= float(batch.gamma[o + j, h])
+        u = float(batch.beta[o + j, h]) * (vj - X @ kj)
+        X += np.outer(u, kj)
+    return X
+
+
+@pytest.mark.parametrize("layout", ["kv", "vk"])
+def test_commit_layers_is_each_layers_own_path(layout):
+    """Cross-layer commit of three layers sharing one forest: every layer's
+    committed slot equals that layer's own path replay (shapes dk=3, dv=5 make
+    a transposed layout fail by shape as well as by value); accepted = -1
+    leaves the slot at S_pre."""
+    base = I.random_batch(seed=41, B=3, H=2, dk=3, dv=5, sizes=[6, 4, 5], max_depth=4,
+                          dtype="f32", sigma=0.3, accept="uniform")
+    base.accepted[1] = -1
+    layers = I.layer_batches(base, 3, seed=9)
+    got = oracle.commit_layers(layers, state_layout=layout, nthreads=1)
+    assert got.shape == ((3, 3, 2, 3, 5) if layout == "kv" else (3, 3, 2, 5, 3))
+    for li, lb in enumerate(layers):
+        assert np.array_equal(lb.offsets, base.offsets) and np.array_equal(lb.parent, base.parent)
+        for b in range(base.B):
+            for h in range(base.H):
+                a = int(base.accepted[b])
+                exp = (_slot_layout_path_replay(lb, b, h, a) if a >= 0
+                       else lb.S_pre[b, h].astype(np.float64).T)
+                if layout == "kv":
+                    exp = exp.T
+                np.testing.assert_allclose(got[li, b, h], exp, rtol=1e-12, atol=1e-13)
+    # layers differ (each used its own operands)
+    assert not np.allclose(got[0], got[1])
