@@ -342,8 +342,56 @@ def layer_batches(base: TreeBatch, n_layers: int, seed: int) -> List[TreeBatch]:
     return out
 
 
+@dataclasses.dataclass
+class Stage1Inputs:
+    """Synthetic inputs of the tree-parallel convolution and gate stage for a
+    packed forest: x [N, C] in-projection channels (C = H (2 dk + dv): q of
+    every head, then k, then v), conv_state [B, W-1, C] (the committed
+    prefix's last W-1 tokens, row W-2 the most recent), conv_w [C, W] and
+    conv_b [C] (float32), gate pre-activations a, b [N, H] (float32), optional
+    per-head gate scale / bias [H].  x and conv_state are bf16-representable
+    float32 when dtype is "bf16"."""
+    W: int
+    dtype: str
+    x: np.ndarray
+    conv_state: np.ndarray
+    conv_w: np.ndarray
+    conv_b: np.ndarray
+    a: np.ndarray
+    b: np.ndarray
+    gate_scale: Optional[np.ndarray]
+    gate_bias: Optional[np.ndarray]
+
+
+def stage1_inputs(batch: TreeBatch, W: int = 4, seed: int = 0, dtype: Optional[str] = None,
+                  gate_terms: bool = False) -> Stage1Inputs:
+    """x, conv_state ~ N(0, 1); conv_w ~ N(0, 1/W); conv_b ~ N(0, 0.1^2);
+    a, b ~ N(0, 1), so that gamma = exp(-softplus(a)) and beta = sigmoid(b)
+    have the pages' workload distributions.  With gate_terms, per-head
+    gate scale ~ U(0.5, 2) and gate bias ~ N(0, 0.5^2)."""
+    dtype = dtype or batch.dtype
+    rng = np.random.Generator(np.random.PCG64([seed, 1]))
+    H, dk, dv, N, B = batch.H, batch.dk, batch.dv, batch.N, batch.B
+    C = H * (2 * dk + dv)
+    x = rng.standard_normal((N, C)).astype(np.float32)
+    st = rng.standard_normal((B, W - 1, C)).astype(np.float32)
+    if dtype == "bf16":
+        x, st = round_to_bf16(x), round_to_bf16(st)
+    elif dtype != "f32":
+        raise ValueError(dtype)
+    conv_w = (rng.standard_normal((C, W)) / np.sqrt(W)).astype(np.float32)
+    conv_b = (0.1 * rng.standard_normal(C)).astype(np.float32)
+    a = rng.standard_normal((N, H)).astype(np.float32)
+    b = rng.standard_normal((N, H)).astype(np.float32)
+    gs = gb = None
+    if gate_terms:
+        gs = rng.uniform(0.5, 2.0, H).astype(np.float32)
+        gb = (0.5 * rng.standard_normal(H)).astype(np.float32)
+    return Stage1Inputs(W, dtype, x, st, conv_w, conv_b, a, b, gs, gb)
+
+
 __all__ = [
-    "layer_batches", "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
+    "Stage1Inputs", "stage1_inputs", "layer_batches", "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
     "kary_tree", "budgeted_forest", "make_batch", "config_batch", "random_batch",
     "CONFIG_NAMES", "SHAPES_CFG4", "MAX_TREE_NODES",
 ]
