@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--conv-width", type=int, default=4,
+                   help="width of the stage-1 causal convolution measurement (0 skips it)")
     p.add_argument("--layers", type=int, default=8,
                    help="layers of the unified cross-layer commit measurement (0 skips it)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -363,6 +365,7 @@ def main(argv=None):
 
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
     layers = run_layers(args, batch, flags, stream) if args.layers > 0 else None
+    stage1 = run_stage1(args, batch, stream) if args.conv_width > 0 else None
 
     if rank != 0:
         if world > 1:
@@ -417,7 +420,7 @@ def main(argv=None):
                                     f"of the {n_sets} input copies, replayed "
                                     f"{max(1, ks // n_sets)}x between events"},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
-        "commit_layers": layers,
+        "commit_layers": layers, "stage1": stage1,
         "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
     }
     print(json.dumps(out))
@@ -425,6 +428,84 @@ def main(argv=None):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def stage1_bytes(batch, W: int):
+    """Algorithmic bytes of bole_conv_gates and bole_conv_commit per launch."""
+    B, H, dk, dv, N = batch.B, batch.H, batch.dk, batch.dv, batch.N
+    s_in = 2 if batch.dtype == "bf16" else 4
+    C = H * (2 * dk + dv)
+    topo = 4 * (B + 1) + 4 * N
+    gates = (2 * N * C * s_in + B * (W - 1) * C * s_in + C * W * 4 + C * 4 + 16 * N * H
+             + topo)
+    L = path_lengths(batch)
+    commit = int(np.sum(np.minimum(L, W - 1))) * C * s_in + 2 * int(np.sum(L > 0)) * (W - 1) * C \
+        * s_in + topo + 4 * B
+    return gates, commit
+
+
+def run_stage1(args, batch, stream):
+    """Stage 1 on this workload: bole_conv_gates (tree-parallel causal
+    convolution of width W, SiLU, q/k normalisation, gates) and
+    bole_conv_commit, each timed over input copies that rotate through more
+    than 3x L2, from a CUDA graph of one launch per copy."""
+    import torch
+    from gated_deltanet_verification_gb300 import bole, inputs
+
+    W = args.conv_width
+    s = inputs.stage1_inputs(batch, W=W, seed=77)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
+    gb, cb = stage1_bytes(batch, W)
+    n = max(2, int(np.ceil(3 * L2_BYTES / gb)) + 1)
+
+    def t(a, d):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=d)
+
+    offsets, parent = t(batch.offsets, torch.int32), t(batch.parent, torch.int32)
+    accepted = t(batch.accepted, torch.int32)
+    w, bias = t(s.conv_w, torch.float32), t(s.conv_b, torch.float32)
+    ga, gbt = t(s.a, torch.float32), t(s.b, torch.float32)
+    copies = [(t(s.x, dt), t(s.conv_state, dt)) for _ in range(n)]
+    outs = [(torch.empty((batch.N, batch.H, batch.dk), dtype=dt, device=dev),
+             torch.empty((batch.N, batch.H, batch.dk), dtype=dt, device=dev),
+             torch.empty((batch.N, batch.H, batch.dv), dtype=dt, device=dev),
+             torch.empty((batch.N, batch.H), dtype=torch.float32, device=dev),
+             torch.empty((batch.N, batch.H), dtype=torch.float32, device=dev)) for _ in range(n)]
+    st = bole.new_status(dev)
+
+    def gates_all():
+        for (x, cs), (q, k, v, g, bt) in zip(copies, outs):
+            bole.conv_gates(x, cs, w, bias, ga, gbt, offsets, parent, batch.H, batch.dk,
+                            batch.dv, max(batch.max_T, 1), q=q, k=k, v=v, gamma=g, beta=bt,
+                            status=st)
+
+    def commit_all():
+        for x, cs in copies:
+            bole.conv_commit(cs, x, offsets, parent, accepted, status=st)
+
+    hbm, _, _ = measured_peaks()
+    out = {"W": W, "copies": n}
+    for name, fn, nbytes in (("conv_gates", gates_all, gb), ("conv_commit", commit_all, cb)):
+        fn()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * n)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "alg_bytes": int(nbytes), "achieved_gbs": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4)}
+    bole.check_status(st, "stage 1")
+    return out
 
 
 def run_layers(args, batch, flags, stream):

@@ -81,6 +81,11 @@ def lib() -> ctypes.CDLL:
             L.bole_commit_layers.argtypes = [P, I64, P, I64, I, P, I64, P, I64, P, P, P, I, I, I,
                                              I, I, I, P, U, P]
             L.bole_commit_layers.restype = I
+            L.bole_conv_gates.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
+                                          P, P, P, P, P, P, U, P]
+            L.bole_conv_gates.restype = I
+            L.bole_conv_commit.argtypes = [P, P, I, P, P, P, I, I, I, I, P, U, P]
+            L.bole_conv_commit.restype = I
             _lib = L
     return _lib
 
@@ -226,6 +231,58 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
     return S
 
 
+MAX_CONV_WIDTH = 8
+
+
+def conv_gates(x, conv_state, conv_w, conv_b, a, b, offsets, parent, H: int, dk: int, dv: int,
+               max_T: int, *, gate_scale=None, gate_bias=None, q=None, k=None, v=None, gamma=None,
+               beta=None, status=None, flags: int = 0, stream=None):
+    """bole_conv_gates: stage 1 of a GDN layer on a packed forest.
+
+    x [N, C] (C = H (2 dk + dv); q channels, then k, then v), conv_state
+    [B, W-1, C] (same dtype), conv_w [C, W] float32, conv_b [C] float32 or
+    None, a, b [N, H] float32; max_T bounds the tree sizes.  Returns (q, k, v, gamma, beta) in the layouts
+    bole_tree_verify takes."""
+    B = offsets.numel() - 1
+    N, C = x.shape
+    W = conv_w.shape[1]
+    dev = x.device
+    code = _dtype_code(x)
+    if C != H * (2 * dk + dv):
+        raise ValueError("x must hold H (2 dk + dv) channels per node")
+    if conv_state is not None and conv_state.dtype != x.dtype:
+        raise TypeError("conv_state must have x's dtype")
+    q = torch.empty((N, H, dk), dtype=x.dtype, device=dev) if q is None else q
+    k = torch.empty((N, H, dk), dtype=x.dtype, device=dev) if k is None else k
+    v = torch.empty((N, H, dv), dtype=x.dtype, device=dev) if v is None else v
+    gamma = torch.empty((N, H), dtype=torch.float32, device=dev) if gamma is None else gamma
+    beta = torch.empty((N, H), dtype=torch.float32, device=dev) if beta is None else beta
+    if status is None:
+        status = new_status(dev)
+    _check(lib().bole_conv_gates(
+        _ptr(x), _ptr(conv_state), _ptr(conv_w), _ptr(conv_b), _ptr(a), _ptr(b),
+        _ptr(gate_scale), _ptr(gate_bias), code, _ptr(offsets), _ptr(parent), B, H, dk, dv, N,
+        int(max_T), W,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(beta), _ptr(status), int(flags),
+        _stream(stream)), "bole_conv_gates")
+    return q, k, v, gamma, beta
+
+
+def conv_commit(conv_state, x, offsets, parent, accepted, *, status=None, flags: int = 0,
+                stream=None):
+    """bole_conv_commit: conv_state [B, W-1, C] becomes, in place, the last
+    W-1 tokens ending at each request's accepted node.  Returns conv_state."""
+    B = offsets.numel() - 1
+    N, C = x.shape
+    W = conv_state.shape[1] + 1
+    if status is None:
+        status = new_status(x.device)
+    _check(lib().bole_conv_commit(_ptr(conv_state), _ptr(x), _dtype_code(x), _ptr(offsets),
+                                  _ptr(parent), _ptr(accepted), B, C, W, N, _ptr(status),
+                                  int(flags), _stream(stream)), "bole_conv_commit")
+    return conv_state
+
+
 def _layer_stride(t: torch.Tensor, n_layers: int) -> int:
     """Element stride between the layers of a [layers, ...] tensor whose
     per-layer slices are contiguous."""
@@ -257,7 +314,7 @@ def commit_layers(S, k, U, logP, offsets, parent, accepted, *, status=None, flag
     return S
 
 
-__all__ = ["commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
+__all__ = ["conv_gates", "conv_commit", "MAX_CONV_WIDTH", "commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
            "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
            "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT",

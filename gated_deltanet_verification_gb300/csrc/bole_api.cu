@@ -227,4 +227,62 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
                               H, dk, dv, N, dev_status, flags, stream);
 }
 
+bole_status bole_conv_gates(const void *x, const void *conv_state, const float *conv_w,
+                            const float *conv_b, const float *a, const float *b,
+                            const float *gate_scale, const float *gate_bias, bole_dtype x_dtype,
+                            const int32_t *offsets, const int32_t *parent, int B, int H, int dk,
+                            int dv, int N, int max_T, int W, void *q, void *k, void *v,
+                            float *gamma, float *beta, int32_t *dev_status, unsigned flags,
+                            bole_stream_t stream)
+{
+    (void)flags;
+    if (B < 0 || N < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) || !valid_dtype(x_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if (W < 1 || W > BOLE_MAX_CONV_WIDTH) return BOLE_ERR_INVALID_ARG;
+    if (max_T < 1 || max_T > BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * max_T) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status) return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!x || !conv_w || !a || !b || !parent || !q || !k || !v || !gamma || !beta ||
+                  (W > 1 && !conv_state)))
+        return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {x, conv_state, conv_w, q, k, v, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {conv_b, a, b, gate_scale, gate_bias, offsets, parent, gamma, beta};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+    if (B == 0 || N == 0) return BOLE_OK;
+    ConvGatesArgs g;
+    g.x = x; g.conv_state = conv_state; g.conv_w = conv_w; g.conv_b = conv_b; g.a = a; g.b = b;
+    g.gate_scale = gate_scale; g.gate_bias = gate_bias; g.dtype = x_dtype;
+    g.offsets = offsets; g.parent = parent;
+    g.B = B; g.H = H; g.dk = dk; g.dv = dv; g.N = N; g.W = W; g.max_T = max_T;
+    g.q = q; g.k = k; g.v = v; g.gamma = gamma; g.beta = beta; g.st = dev_status;
+    return from_cuda(launch_conv_gates(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+bole_status bole_conv_commit(void *conv_state, const void *x, bole_dtype x_dtype,
+                             const int32_t *offsets, const int32_t *parent,
+                             const int32_t *accepted, int B, int C, int W, int N,
+                             int32_t *dev_status, unsigned flags, bole_stream_t stream)
+{
+    (void)flags;
+    if (B < 0 || N < 0 || C < 1 || W < 1 || W > BOLE_MAX_CONV_WIDTH || !valid_dtype(x_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !dev_status || (B > 0 && W > 1 && (!conv_state || !accepted)))
+        return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && W > 1 && (!x || !parent)) return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {conv_state, x, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {offsets, parent, accepted};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+    if (B == 0 || N == 0 || W == 1) return BOLE_OK;
+    return from_cuda(launch_conv_commit(conv_state, x, x_dtype, offsets, parent, accepted, B, C,
+                                        W, N, dev_status,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 } // extern "C"

@@ -87,6 +87,23 @@ struct CommitArgs {
     bool vk; // state stored [B, H, dv, dk] (BOLE_FLAG_STATE_VK)
 };
 
+// Stage 1: tree-parallel convolution and gates.
+struct ConvGatesArgs {
+    const void *x, *conv_state;
+    const float *conv_w, *conv_b, *a, *b, *gate_scale, *gate_bias;
+    bole_dtype dtype;
+    const int32_t *offsets, *parent;
+    int B, H, dk, dv, N, W, max_T;
+    void *q, *k, *v;
+    float *gamma, *beta;
+    int32_t *st;
+};
+cudaError_t launch_conv_gates(const ConvGatesArgs &a, cudaStream_t s);
+cudaError_t launch_conv_commit(void *conv_state, const void *x, bole_dtype dtype,
+                               const int32_t *offsets, const int32_t *parent,
+                               const int32_t *accepted, int B, int C, int W, int N, int32_t *st,
+                               cudaStream_t s);
+
 size_t simt_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_simt_verify(const VerifyArgs &a, cudaStream_t s);
 bool simt_noalloc_fits(int B, int H, int max_T);

@@ -236,6 +236,54 @@ bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
                                const int32_t *accepted, int n_layers, int B, int H, int dk, int dv,
                                int N, int32_t *dev_status, unsigned flags, bole_stream_t stream);
 
+/* ---- Stage 1 of a GDN layer: tree-parallel convolution and gates ----
+ * (Section II-A: a GDN layer's short causal depthwise convolution and gates;
+ * Section IV-C, the fused pipeline: stage (1) fuses the convolution, its
+ * bias, SiLU and gate preparation per node along parent links, all nodes
+ * concurrently.)  For every node i of every request and every head h:
+ *   - window: i, its parent, grandparent, ... (nearest first); where the path
+ *     reaches the committed root, the committed prefix's last W-1 tokens
+ *     (conv_state rows W-2, W-3, ...);
+ *   - y[c] = conv_b[c] + sum_{d<W} conv_w[c][W-1-d] * (token at distance d)[c];
+ *   - SiLU; the q and k channels of each head L2-normalised (over d_k);
+ *   - gamma = exp(-s_h softplus(a + c_h)), beta = sigmoid(b), with
+ *     s_h = gate_scale[h] (1 if NULL) and c_h = gate_bias[h] (0 if NULL).
+ * Layouts:
+ *   x          [N, C] x_dtype, C = H (2 dk + dv): the q channels of every head
+ *              (head-major), then k, then v -- the in-projection output
+ *   conv_state [B, W-1, C] x_dtype (row W-2 the most recent committed token;
+ *              may be NULL when W = 1)
+ *   conv_w     [C, W] float32 (tap W-1 multiplies the current token)
+ *   conv_b     [C] float32 or NULL;  a, b [N, H] float32 gate pre-activations
+ *   q, k       [N, H, dk] x_dtype;  v [N, H, dv] x_dtype  (bole_tree_verify's
+ *              inputs);  gamma, beta [N, H] float32
+ * W in [1, 8]; dk, dv as elsewhere; max_T (1..128) bounds every tree's node
+ * count (it sizes the on-chip tile of one request).  offsets / parent: the
+ * packed forest (a malformed link or a tree larger than max_T is reported as
+ * BOLE_ERR_BAD_TOPOLOGY in dev_status, and that request is left unwritten).
+ * Stream-ordered after bole_pack_forest (which resets dev_status) and before
+ * bole_tree_verify. */
+#define BOLE_MAX_CONV_WIDTH 8
+bole_status bole_conv_gates(const void *x, const void *conv_state, const float *conv_w,
+                            const float *conv_b, const float *a, const float *b,
+                            const float *gate_scale, const float *gate_bias, bole_dtype x_dtype,
+                            const int32_t *offsets, const int32_t *parent, int B, int H, int dk,
+                            int dv, int N, int max_T, int W, void *q, void *k, void *v,
+                            float *gamma, float *beta, int32_t *dev_status, unsigned flags,
+                            bole_stream_t stream);
+
+/* Commit of the convolution state (the conv counterpart of bole_commit):
+ * for every request with accepted[b] = a >= 0, conv_state[b] ([W-1, C],
+ * in place) becomes the last W-1 tokens ending at a -- a's row of x in row
+ * W-2, its parent's in row W-3, ..., then the old rows, most recent first.
+ * accepted[b] = -1 leaves the request's state untouched.  x is the same
+ * buffer bole_conv_gates read.  Exact (rows are copied).  W = 1 launches
+ * nothing. */
+bole_status bole_conv_commit(void *conv_state, const void *x, bole_dtype x_dtype,
+                             const int32_t *offsets, const int32_t *parent,
+                             const int32_t *accepted, int B, int C, int W, int N,
+                             int32_t *dev_status, unsigned flags, bole_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,3 +130,34 @@ def test_state_layout_flag_keeps_the_workspace(lib):
     vk = bole.FLAG_STATE_VK
     for args in [(2, 3, 16, 16, 8, 3, 0), (2, 3, 128, 128, 64, 15, 1), (2, 3, 128, 128, 128, 127, 1)]:
         assert f(*args, vk) == f(*args, 0)
+
+
+def test_stage1_host_validation_without_gpu(lib):
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake = c(1 << 20)
+    B, H, dk, dv, N = 2, 3, 128, 128, 8
+
+    def gates(W=4, state=fake, dk=dk, x=fake, N=N, max_T=64):
+        return lib.bole_conv_gates(x, state, fake, None, fake, fake, None, None, 1, fake, fake,
+                                   B, H, dk, dv, N, max_T, W, fake, fake, fake, fake, fake, fake,
+                                   0, None)
+
+    assert gates(W=0) == bole.ERR_INVALID_ARG
+    assert gates(W=bole.MAX_CONV_WIDTH + 1) == bole.ERR_INVALID_ARG
+    assert gates(state=None) == bole.ERR_INVALID_ARG          # W > 1 needs the state
+    assert gates(dk=24) == bole.ERR_INVALID_ARG
+    assert gates(x=c((1 << 20) + 8)) == bole.ERR_INVALID_ARG  # 16-byte alignment
+    assert gates(N=B * 64 + 1) == bole.ERR_INVALID_ARG        # more nodes than B * max_T
+    assert gates(max_T=129) == bole.ERR_INVALID_ARG
+    assert gates(max_T=0) == bole.ERR_INVALID_ARG
+    assert gates(N=0) == bole.OK                              # nothing to launch
+
+    def commit(W=4, acc=fake, N=N):
+        return lib.bole_conv_commit(fake, fake, 1, fake, fake, acc, B, H * 384, W, N, fake, 0,
+                                    None)
+
+    assert commit(acc=None) == bole.ERR_INVALID_ARG
+    assert commit(W=9) == bole.ERR_INVALID_ARG
+    assert commit(W=1, acc=None) == bole.OK                   # no state to commit
+    assert commit(N=0) == bole.OK
