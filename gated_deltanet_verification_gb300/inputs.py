@@ -343,6 +343,63 @@ def layer_batches(base: TreeBatch, n_layers: int, seed: int) -> List[TreeBatch]:
 
 
 @dataclasses.dataclass
+class DraftCandidates:
+    """A drafter's proposal trees for B requests, packed candidate-major:
+    cand_offsets [B+1], cand_parent [M] (request-local, -1 = the committed
+    root, parent before child), p [M] float32 edge probabilities
+    p(v | parent(v)) (each node's children sum to 1), caps [B] per-request
+    node limits."""
+    cand_offsets: np.ndarray
+    cand_parent: np.ndarray
+    p: np.ndarray
+    caps: np.ndarray
+
+    @property
+    def B(self) -> int:
+        return len(self.cand_offsets) - 1
+
+    @property
+    def M(self) -> int:
+        return int(self.cand_offsets[-1])
+
+
+def draft_candidates(seed: int, B: int, m_lo: int, m_hi: int, max_depth: int,
+                     max_children: int = 4, cap_lo: int = 8, cap_hi: int = 64) -> DraftCandidates:
+    """Each request's proposal tree grows level by level (breadth first, so
+    parent before child): every node above max_depth gets 1..max_children
+    children with Dirichlet(1) edge probabilities, until the request has
+    M_b ~ U[m_lo, m_hi] candidates; caps ~ U[cap_lo, cap_hi]."""
+    rng = np.random.Generator(np.random.PCG64([seed, 2]))
+    offs = [0]
+    parents, probs = [], []
+    for _ in range(B):
+        m = int(rng.integers(m_lo, m_hi + 1))
+        par, pr, dep = [], [], []
+        frontier = [(-1, -1)]  # (node, depth)
+        while frontier and len(par) < m:
+            nxt = []
+            for node, d in frontier:
+                if d + 1 > max_depth or len(par) >= m:
+                    continue
+                c = int(rng.integers(1, max_children + 1))
+                ps = rng.dirichlet(np.ones(c))
+                for q in ps:
+                    if len(par) >= m:
+                        break
+                    par.append(node)
+                    pr.append(q)
+                    dep.append(d + 1)
+                    nxt.append((len(par) - 1, d + 1))
+            frontier = nxt
+        parents += par
+        probs += pr
+        offs.append(offs[-1] + len(par))
+    caps = rng.integers(cap_lo, cap_hi + 1, size=B).astype(np.int32)
+    return DraftCandidates(np.asarray(offs, np.int32), np.asarray(parents, np.int32),
+                           np.asarray(probs, np.float32), caps)
+
+
+@dataclasses.dataclass
 class Stage1Inputs:
     """Synthetic inputs of the tree-parallel convolution and gate stage for a
     packed forest: x [N, C] in-projection channels (C = H (2 dk + dv): q of
@@ -391,7 +448,7 @@ def stage1_inputs(batch: TreeBatch, W: int = 4, seed: int = 0, dtype: Optional[s
 
 
 __all__ = [
-    "Stage1Inputs", "stage1_inputs", "layer_batches", "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
+    "DraftCandidates", "draft_candidates", "Stage1Inputs", "stage1_inputs", "layer_batches", "TreeBatch", "round_to_bf16", "random_parent_tree", "chain_tree", "star_tree",
     "kary_tree", "budgeted_forest", "make_batch", "config_batch", "random_batch",
     "CONFIG_NAMES", "SHAPES_CFG4", "MAX_TREE_NODES",
 ]
