@@ -58,6 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--conv-width", type=int, default=4,
                    help="width of the stage-1 causal convolution measurement (0 skips it)")
+    p.add_argument("--no-selection", action="store_true",
+                   help="skip the device-side selection measurement")
     p.add_argument("--layers", type=int, default=8,
                    help="layers of the unified cross-layer commit measurement (0 skips it)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -366,6 +368,7 @@ def main(argv=None):
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
     layers = run_layers(args, batch, flags, stream) if args.layers > 0 else None
     stage1 = run_stage1(args, batch, stream) if args.conv_width > 0 else None
+    selection = run_selection(stream) if not args.no_selection else None
 
     if rank != 0:
         if world > 1:
@@ -420,7 +423,7 @@ def main(argv=None):
                                     f"of the {n_sets} input copies, replayed "
                                     f"{max(1, ks // n_sets)}x between events"},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
-        "commit_layers": layers, "stage1": stage1,
+        "commit_layers": layers, "stage1": stage1, "selection": selection,
         "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
     }
     print(json.dumps(out))
@@ -428,6 +431,55 @@ def main(argv=None):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def run_selection(stream):
+    """Device-side proposal selection + forest build on drafts shaped like the
+    ragged budgeted batch: 64 requests, 64..256 drafted candidates each (edge
+    probabilities Dirichlet(1) over 1..4 children, depth <= 12), per-request
+    caps U[8, 64], a budget of 2048 nodes.  Three small kernels, bound by
+    latency rather than bandwidth; timed from a CUDA graph."""
+    import torch
+    from gated_deltanet_verification_gb300 import bole, inputs
+
+    d = inputs.draft_candidates(2024, 64, 64, 256, 12)
+    budget = 2048
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def t(a, dt=torch.int32):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=dt)
+
+    p, co, cp, caps = t(d.p, torch.float32), t(d.cand_offsets), t(d.cand_parent), t(d.caps)
+    off = torch.empty(d.B + 1, dtype=torch.int32, device=dev)
+    par = torch.empty(budget, dtype=torch.int32, device=dev)
+    src = torch.empty(budget, dtype=torch.int32, device=dev)
+    rho = torch.empty(d.M, dtype=torch.float32, device=dev)
+    ws = torch.empty(bole.lib().bole_select_workspace_size(d.B), dtype=torch.uint8, device=dev)
+    st = bole.new_status(dev)
+
+    def run():
+        bole.select_forest(p, co, cp, budget, caps=caps, offsets=off, parent=par, src=src,
+                           rho=rho, workspace=ws, status=st)
+
+    run()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    g.replay()
+    reps = 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bole.check_status(st, "selection")
+    ms = e0.elapsed_time(e1) / reps
+    return {"requests": d.B, "candidates": d.M, "budget": budget,
+            "nodes": int(off[-1].item()), "ms": round(ms, 5),
+            "candidates_per_s": round(d.M / (ms * 1e-3), 1), "bound": "latency",
+            "launches": 3}
 
 
 def stage1_bytes(batch, W: int):

@@ -86,6 +86,10 @@ def lib() -> ctypes.CDLL:
             L.bole_conv_gates.restype = I
             L.bole_conv_commit.argtypes = [P, P, I, P, P, P, I, I, I, I, P, U, P]
             L.bole_conv_commit.restype = I
+            L.bole_select_workspace_size.argtypes = [I]
+            L.bole_select_workspace_size.restype = S
+            L.bole_select_forest.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P, S, P, U, P]
+            L.bole_select_forest.restype = I
             _lib = L
     return _lib
 
@@ -232,6 +236,35 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
 
 
 MAX_CONV_WIDTH = 8
+MAX_CANDIDATES = 1024
+SELECT_MAX_REQUESTS = 4096
+
+
+def select_forest(p, cand_offsets, cand_parent, budget: int, *, caps=None, offsets=None,
+                  parent=None, src=None, rho=None, workspace=None, status=None, flags: int = 0,
+                  stream=None):
+    """bole_select_forest: the round's proposal selection and forest build on
+    the device.  p [M] float32, cand_offsets [B+1], cand_parent [M] int32,
+    caps [B] int32 or None.  Returns (offsets [B+1], parent [budget],
+    src [budget], rho [M], status); offsets[B] (on the device) is the node
+    count -- the forest feeds pack_forest with N = budget."""
+    B = cand_offsets.numel() - 1
+    M = p.numel()
+    dev = p.device
+    i32 = torch.int32
+    offsets = torch.empty(B + 1, dtype=i32, device=dev) if offsets is None else offsets
+    parent = torch.empty(max(budget, 1), dtype=i32, device=dev) if parent is None else parent
+    src = torch.empty(max(budget, 1), dtype=i32, device=dev) if src is None else src
+    rho = torch.empty(max(M, 1), dtype=torch.float32, device=dev) if rho is None else rho
+    if workspace is None:
+        n = int(lib().bole_select_workspace_size(B))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    status = new_status(dev) if status is None else status
+    _check(lib().bole_select_forest(
+        _ptr(p), _ptr(cand_offsets), _ptr(cand_parent), _ptr(caps), B, M, int(budget),
+        _ptr(offsets), _ptr(parent), _ptr(src), _ptr(rho), _ptr(workspace), workspace.numel(),
+        _ptr(status), int(flags), _stream(stream)), "bole_select_forest")
+    return offsets, parent, src, rho, status
 
 
 def conv_gates(x, conv_state, conv_w, conv_b, a, b, offsets, parent, H: int, dk: int, dv: int,
@@ -314,7 +347,7 @@ def commit_layers(S, k, U, logP, offsets, parent, accepted, *, status=None, flag
     return S
 
 
-__all__ = ["conv_gates", "conv_commit", "MAX_CONV_WIDTH", "commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
+__all__ = ["select_forest", "MAX_CANDIDATES", "SELECT_MAX_REQUESTS", "conv_gates", "conv_commit", "MAX_CONV_WIDTH", "commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
            "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
            "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT",

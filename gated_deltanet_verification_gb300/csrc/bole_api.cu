@@ -227,6 +227,36 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
                               H, dk, dv, N, dev_status, flags, stream);
 }
 
+size_t bole_select_workspace_size(int B)
+{
+    if (B < 0 || B > BOLE_SELECT_MAX_REQUESTS) return 0;
+    return select_workspace_bytes(B);
+}
+
+bole_status bole_select_forest(const float *p, const int32_t *cand_offsets,
+                               const int32_t *cand_parent, const int32_t *caps, int B, int M,
+                               int budget, int32_t *offsets, int32_t *parent, int32_t *src,
+                               float *rho, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, unsigned flags, bole_stream_t stream)
+{
+    (void)flags;
+    if (B < 0 || B > BOLE_SELECT_MAX_REQUESTS || M < 0 || budget < 0)
+        return BOLE_ERR_INVALID_ARG;
+    if (!cand_offsets || !offsets || !dev_status) return BOLE_ERR_INVALID_ARG;
+    if (M > 0 && (!p || !cand_parent)) return BOLE_ERR_INVALID_ARG;
+    if (budget > 0 && (!parent || !src)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {p, cand_offsets, cand_parent, caps, offsets, parent, src, rho};
+    for (const void *q : p4)
+        if (!aligned(q, 4)) return BOLE_ERR_INVALID_ARG;
+    if (!aligned(dev_status, 16)) return BOLE_ERR_INVALID_ARG;
+    const size_t need = select_workspace_bytes(B);
+    if (B > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return BOLE_ERR_WORKSPACE;
+    return from_cuda(launch_select(p, cand_offsets, cand_parent, caps, B, M, budget, offsets,
+                                   parent, src, rho, workspace, dev_status,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bole_status bole_conv_gates(const void *x, const void *conv_state, const float *conv_w,
                             const float *conv_b, const float *a, const float *b,
                             const float *gate_scale, const float *gate_bias, bole_dtype x_dtype,

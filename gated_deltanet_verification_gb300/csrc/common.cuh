@@ -104,6 +104,13 @@ cudaError_t launch_conv_commit(void *conv_state, const void *x, bole_dtype dtype
                                const int32_t *accepted, int B, int C, int W, int N, int32_t *st,
                                cudaStream_t s);
 
+// Device-side selection and forest build.
+size_t select_workspace_bytes(int B);
+cudaError_t launch_select(const float *p, const int32_t *cand_offsets, const int32_t *cand_parent,
+                          const int32_t *caps, int B, int M, int budget, int32_t *offsets,
+                          int32_t *parent, int32_t *src, float *rho, void *ws, int32_t *st,
+                          cudaStream_t s);
+
 size_t simt_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_simt_verify(const VerifyArgs &a, cudaStream_t s);
 bool simt_noalloc_fits(int B, int H, int max_T);

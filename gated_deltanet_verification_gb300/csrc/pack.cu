@@ -31,8 +31,7 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
     if (b >= B) return;
     const int o = offsets[b], e = offsets[b + 1];
     const int T = e - o;
-    const bool bad_off = o < 0 || e > N || T < 0 || T > kMaxTree || (b == 0 && o != 0) ||
-                         (b == B - 1 && e != N);
+    const bool bad_off = o < 0 || e > N || T < 0 || T > kMaxTree || (b == 0 && o != 0);
     if (bad_off) {
         if (lane == 0) {
             req_depth[b] = 0;

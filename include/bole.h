@@ -24,8 +24,10 @@
  *     All calls are asynchronous on `stream` (a cudaStream_t; NULL selects
  *     the legacy default stream) and may be captured in CUDA graphs.
  *   - Packed forest: B requests' trees are concatenated node-major.
- *     offsets[B+1] (int32, offsets[0] = 0, non-decreasing, offsets[B] = N)
- *     delimits request b's nodes [offsets[b], offsets[b+1]).  parent[N]
+ *     offsets[B+1] (int32, offsets[0] = 0, non-decreasing, offsets[B] <= N)
+ *     delimits request b's nodes [offsets[b], offsets[b+1]); N is the
+ *     length (capacity) of the node arrays and nodes past offsets[B] are
+ *     ignored, so a forest built on the device needs no host round trip.  parent[N]
  *     (int32) holds request-LOCAL parent indices, -1 = the committed root,
  *     and parent[i] < i (parent before child).  At most 128 nodes per tree.
  *   - Depth of a node = number of strict proposal ancestors (a child of the
@@ -235,6 +237,49 @@ bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
                                const int32_t *offsets, const int32_t *parent,
                                const int32_t *accepted, int n_layers, int B, int H, int dk, int dv,
                                int N, int32_t *dev_status, unsigned flags, bole_stream_t stream);
+
+/* ---- Device-side proposal selection and forest build ----
+ * (Section IV, hardware-aware budget: at run time each drafted candidate v
+ * scores rho(v) = product over its path of the drafter's edge probabilities
+ * p(u | parent(u)), and the globally highest-scoring candidates fill the
+ * round's budget; a child never outscores its parent, so every request's
+ * selection is ancestor-closed.  The integration keeps selection and forest
+ * build on the GPU.)
+ *   p [M] float32 in [0, 1]        edge probability of each candidate
+ *   cand_offsets [B+1], cand_parent [M]   the drafter's trees, packed like a
+ *                                  forest (request-local parents, -1 = root,
+ *                                  parent before child), at most
+ *                                  BOLE_MAX_CANDIDATES per request
+ *   caps [B] int32 or NULL         per-request node limits (NULL: none); a
+ *                                  tree never exceeds BOLE_MAX_TREE_NODES
+ *   budget                         total nodes of the round
+ * Rule (every decision on float32 scores accumulated root-down,
+ * rho(v) = rho(parent) * p(v)): order = larger rho first, then smaller depth,
+ * request, candidate index; each request with a candidate first receives its
+ * best one (in that order while the budget lasts); the rest of the budget
+ * goes to the best remaining candidates, skipping requests at their limit.
+ * Outputs, all device:
+ *   offsets [B+1]                  the packed forest's extents (offsets[B] =
+ *                                  the node count, <= budget)
+ *   parent [budget], src [budget]  per forest node: request-local parent and
+ *                                  its candidate index (to gather its token /
+ *                                  hidden state); a request's nodes in
+ *                                  candidate order (parent before child)
+ *   rho [M] float32 or NULL        the scores
+ * The forest feeds bole_pack_forest directly with N = the node capacity
+ * (offsets[B] <= N), so no host round trip is needed.  dev_status is zeroed
+ * by this call (give the round's later calls their own status block, or
+ * check it first); malformed candidate trees are reported as
+ * BOLE_ERR_BAD_TOPOLOGY and that request gets no nodes.  B <= 4096.
+ * workspace: bole_select_workspace_size(B) bytes. */
+#define BOLE_MAX_CANDIDATES 1024
+#define BOLE_SELECT_MAX_REQUESTS 4096
+size_t bole_select_workspace_size(int B);
+bole_status bole_select_forest(const float *p, const int32_t *cand_offsets,
+                               const int32_t *cand_parent, const int32_t *caps, int B, int M,
+                               int budget, int32_t *offsets, int32_t *parent, int32_t *src,
+                               float *rho, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, unsigned flags, bole_stream_t stream);
 
 /* ---- Stage 1 of a GDN layer: tree-parallel convolution and gates ----
  * (Section II-A: a GDN layer's short causal depthwise convolution and gates;

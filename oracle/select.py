@@ -23,7 +23,8 @@ Points the pages leave open, and the readings taken:
   its child, even when p = 1), then smaller request index, then smaller
   candidate index.
 * Per-request caps cap[b] (the workload's per-request tree sizes; None = no
-  cap) and, since a request with no proposal cannot advance, each request
+  cap), never above 128 (a packed-forest tree holds at most 128 nodes), and,
+  since a request with no proposal cannot advance, each request
   with a candidate and cap >= 1 first receives its best candidate; the rest
   of the budget goes to the best remaining candidates in the global order,
   skipping requests at their cap.  With fewer budget slots than requests,
@@ -35,6 +36,8 @@ Points the pages leave open, and the readings taken:
 from __future__ import annotations
 
 import numpy as np
+
+MAX_TREE = 128  # nodes of one packed-forest tree
 
 
 def path_scores(p, cand_offsets, cand_parent):
@@ -66,7 +69,7 @@ def select_forest(p, cand_offsets, cand_parent, budget: int, caps=None):
     cand_offsets = np.asarray(cand_offsets)
     B = len(cand_offsets) - 1
     rho, depth = path_scores(p, cand_offsets, cand_parent)
-    cap = [None] * B if caps is None else [int(c) for c in caps]
+    cap = [MAX_TREE] * B if caps is None else [min(max(int(c), 0), MAX_TREE) for c in caps]
     items = []  # (-rho, depth, request, local index)
     for b in range(B):
         o, n = int(cand_offsets[b]), int(cand_offsets[b + 1] - cand_offsets[b])
@@ -79,7 +82,7 @@ def select_forest(p, cand_offsets, cand_parent, budget: int, caps=None):
     firsts = {}
     for it in items:
         b = it[2]
-        if b not in firsts and (cap[b] is None or cap[b] >= 1):
+        if b not in firsts and cap[b] >= 1:
             firsts[b] = it
     total = 0
     for it in sorted(firsts.values()):
@@ -92,7 +95,7 @@ def select_forest(p, cand_offsets, cand_parent, budget: int, caps=None):
         if total >= budget:
             break
         b = it[2]
-        if it in taken or (cap[b] is not None and len(chosen[b]) >= cap[b]):
+        if it in taken or len(chosen[b]) >= cap[b]:
             continue
         chosen[b].append(it[3])
         taken.add(it)

@@ -161,3 +161,23 @@ def test_stage1_host_validation_without_gpu(lib):
     assert commit(W=9) == bole.ERR_INVALID_ARG
     assert commit(W=1, acc=None) == bole.OK                   # no state to commit
     assert commit(N=0) == bole.OK
+
+
+def test_select_host_validation_without_gpu(lib):
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake = c(1 << 20)
+    ws = lib.bole_select_workspace_size
+    ws.restype = ctypes.c_size_t
+    assert ws(64) == 64 * 128 * 8 + 2 * 64 * 4
+    assert ws(bole.SELECT_MAX_REQUESTS + 1) == 0
+
+    def sel(B=4, M=40, budget=16, work=fake, nbytes=1 << 20, offsets=fake):
+        return lib.bole_select_forest(fake, fake, fake, None, B, M, budget, offsets, fake, fake,
+                                      None, work, nbytes, fake, 0, None)
+
+    assert sel(B=bole.SELECT_MAX_REQUESTS + 1) == bole.ERR_INVALID_ARG
+    assert sel(budget=-1) == bole.ERR_INVALID_ARG
+    assert sel(offsets=None) == bole.ERR_INVALID_ARG
+    assert sel(work=None) == bole.ERR_WORKSPACE
+    assert sel(nbytes=16) == bole.ERR_WORKSPACE

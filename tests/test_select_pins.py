@@ -140,8 +140,7 @@ MUTANTS = {
                            "items.append((-float(rho[o + i]), -int(depth[o + i]), b, i))"),
     "no_reserve": ("    for it in sorted(firsts.values()):\n        if total >= budget:",
                    "    for it in []:\n        if total >= budget:"),
-    "caps_ignored": ("if it in taken or (cap[b] is not None and len(chosen[b]) >= cap[b]):",
-                     "if it in taken:"),
+    "caps_ignored": ("if it in taken or len(chosen[b]) >= cap[b]:", "if it in taken:"),
     "score_is_sum": ("rho[o + i] = np.float32(rho[o + par] * p[o + i])",
                      "rho[o + i] = np.float32(rho[o + par] + p[o + i])"),
     "score_is_edge_only": ("rho[o + i] = np.float32(rho[o + par] * p[o + i])",
