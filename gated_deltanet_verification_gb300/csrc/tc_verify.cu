@@ -214,11 +214,17 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         for (int c = 0; c < 4; ++c)
             tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
     }
+    // What the previous call wrote (the status word pack reset, the
+    // per-request depth) is read after the wait; the reads above are already
+    // in flight, so without an overlapped launch both arrive in one round trip.
+    pdl_wait();
+    const int fault = *(const volatile int32_t *)st;
+    const int d = req_depth[b];
     // Depth and ancestor-or-self mask of each node from the request's parent
     // links (a caller input), walked in shared memory by the topology warps:
     // at most 16 steps, every link checked to point backwards, so the walk is
     // bounded and in range whatever the input (invalid trees are reported by
-    // pack, and the wait below ends such a launch before any output).
+    // pack, and the check below ends such a launch before any output).
     int my_depth = -1;
     uint64_t my_mask = 0;
     if (topo) {
@@ -235,11 +241,6 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             if (j != -1) my_depth = -1; // deeper than 15 or malformed: no work for this row
         }
     }
-    // What the previous call wrote (the status word pack reset, the
-    // per-request depth) is read after the wait.
-    pdl_wait();
-    const int fault = *(const volatile int32_t *)st;
-    const int d = req_depth[b];
     const bool bad = !in_range || d < 0 || d >= kSlots || d >= T;
     if (fault != 0 || T <= 0 || bad) {
         if (bad && T > 0 && fault == 0 && tid == 0 && h == 0)
