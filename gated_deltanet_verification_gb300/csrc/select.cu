@@ -12,12 +12,13 @@
 //      pointer jumping, the scores level by level, every candidate's 64-bit
 //      order key, a bitonic sort, and the request's best min(cap, 128, M_b)
 //      keys into a per-request list.
-//   2. select_global_kernel (one CTA per request): each request's best key
-//      is reserved (in global order while the budget lasts); every other
-//      listed key is selected when fewer than the remaining budget of the
-//      other lists' keys precede it -- its global rank, counted by binary
-//      search in every request's sorted list.  The selected keys of a
-//      request are a prefix of its list.
+//   2. select_global_kernel (one CTA per request, 8 threads per list entry):
+//      each request's best key is reserved (in global order while the
+//      budget lasts); every other listed key is selected when fewer than
+//      the remaining budget of the other lists' keys precede it -- its
+//      global rank, counted by binary search in every request's sorted list
+//      (an eighth of the lists per thread).  The selected keys of a request
+//      are a prefix of its list.
 //   3. build_forest_kernel (one CTA per request): the request's offset (sum
 //      of the earlier counts), its selected candidates in candidate order
 //      (parent before child), and their request-local parent links.
@@ -32,7 +33,9 @@ namespace {
 constexpr int kMaxCand = BOLE_MAX_CANDIDATES; // candidates per request
 constexpr int kListLen = kMaxTree;            // a request's tree holds at most 128 nodes
 constexpr int kSelThreads = 512;
-constexpr int kGlobThreads = kListLen;        // one thread per list entry
+constexpr int kGlobThreads = kListLen;        // build: one thread per list entry
+constexpr int kRankSplit = 8;                 // rank: list entry x eighth of the lists
+constexpr int kRankThreads = kListLen * kRankSplit;
 constexpr int kChunkLists = 40;               // lists staged per pass (40 KB)
 
 __device__ __forceinline__ uint64_t order_key(float rho, int depth, int b, int i)
@@ -154,23 +157,26 @@ __device__ __forceinline__ int block_sum(int v, int *red)
     return s;
 }
 
-__global__ void __launch_bounds__(kGlobThreads)
+// Thread (q, j): list entry j of this request against the staged lists r with
+// r % kRankSplit == q; the partial counts are summed in shared memory.
+__global__ void __launch_bounds__(kRankThreads)
 select_global_kernel(const uint64_t *__restrict__ lists, const int32_t *__restrict__ lens, int B,
                      int budget, int32_t *__restrict__ counts)
 {
     __shared__ uint64_t stage[kChunkLists][kListLen];
     __shared__ int32_t slen[kChunkLists];
-    __shared__ int red[kGlobThreads / 32];
-    const int b = blockIdx.x, j = threadIdx.x;
+    __shared__ int32_t part[kRankSplit][kListLen];
+    __shared__ int red[kRankThreads / 32];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int q = tid / kListLen, j = tid % kListLen;
     const int len = lens[b];
     const uint64_t first = len > 0 ? lists[(size_t)b * kListLen] : ~0ull;
     const bool has_x = j >= 1 && j < len; // a non-reserved entry of this list
     const uint64_t x = has_x ? lists[(size_t)b * kListLen + j] : 0ull;
     // requests with a list, and how many of their best keys precede this one's
     int nonempty = 0, ahead = 0;
-    for (int r = j; r < B; r += kGlobThreads) {
-        const int lr = lens[r];
-        if (lr > 0) {
+    for (int r = tid; r < B; r += kRankThreads) {
+        if (lens[r] > 0) {
             ++nonempty;
             ahead += lists[(size_t)r * kListLen] < first;
         }
@@ -184,17 +190,25 @@ select_global_kernel(const uint64_t *__restrict__ lists, const int32_t *__restri
     for (int c0 = 0; c0 < B; c0 += kChunkLists) {
         const int nl = min(kChunkLists, B - c0);
         __syncthreads();
-        if (j < nl) slen[j] = lens[c0 + j];
-        for (int e = j; e < nl * kListLen; e += kGlobThreads)
+        if (tid < nl) slen[tid] = lens[c0 + tid];
+        for (int e = tid; e < nl * kListLen; e += kRankThreads)
             stage[e / kListLen][e % kListLen] = lists[(size_t)c0 * kListLen + e];
         __syncthreads();
         if (has_x)
-            for (int r = 0; r < nl; ++r)
+            for (int r = q; r < nl; r += kRankSplit)
                 if (slen[r] > 1) rank += count_less(&stage[r][1], slen[r] - 1, x);
     }
-    const int mine = (has_x && rank < rest) ? 1 : 0;
+    part[q][j] = rank;
+    __syncthreads();
+    int mine = 0;
+    if (q == 0 && has_x) {
+        int tot = 0;
+#pragma unroll
+        for (int k = 0; k < kRankSplit; ++k) tot += part[k][j];
+        mine = tot < rest ? 1 : 0;
+    }
     const int n = block_sum(mine, red);
-    if (j == 0) counts[b] = (reserved ? 1 : 0) + (reserved ? n : 0);
+    if (tid == 0) counts[b] = (reserved ? 1 : 0) + n;
 }
 
 __global__ void __launch_bounds__(kGlobThreads)
@@ -271,7 +285,7 @@ cudaError_t launch_select(const float *p, const int32_t *cand_offsets, const int
     if (B == 0) return cudaSuccess;
     select_local_kernel<<<B, kSelThreads, 0, s>>>(p, cand_offsets, cand_parent, caps, M, rho,
                                                   lists, lens, st);
-    select_global_kernel<<<B, kGlobThreads, 0, s>>>(lists, lens, B, budget, counts);
+    select_global_kernel<<<B, kRankThreads, 0, s>>>(lists, lens, B, budget, counts);
     build_forest_kernel<<<B, kGlobThreads, 0, s>>>(lists, counts, cand_offsets, cand_parent, B,
                                                    offsets, parent, src, st);
     return cudaGetLastError();
