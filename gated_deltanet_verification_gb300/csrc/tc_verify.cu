@@ -578,11 +578,13 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 
 // ---- commit ----
 // One CTA per (request, head, 64-column half of the state, layer): value
-// tiling as in the pages' kernel, so four CTAs fit on an SM and overlap their
-// TMA load, tensor-core product and TMA store.  (Narrower tiles fit more CTAs
-// but repeat the path operand's gather and measured slower.)  One launch
-// covers every layer of a unified cross-layer commit: layer l's state, keys,
-// deltas and decays start l strides after the base pointers.
+// tiling as in the pages' kernel.  The half is staged one 32-column box at a
+// time through a 16 KB buffer (both boxes are prefetched into L2 at entry, so
+// the second load is an L2 hit), which lets seven CTAs share an SM and a
+// batch of 1024 tiles run in one wave.  (Narrower tiles fit more CTAs but
+// repeat the path operand's gather and measured slower.)  One launch covers
+// every layer of a unified cross-layer commit: layer l's state, keys, deltas
+// and decays start l strides after the base pointers.
 // The stored tile is always 128 rows x 64 columns.  [dk][dv] state: rows are
 // d_k (operand A = (D_a K_a)^T, 128 x path), columns a d_v half (operand B^T =
 // U_a^T of that half).  VK ([dv][dk], the slot layout): rows are d_v (A =
@@ -590,9 +592,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 // product, transposed.
 constexpr int kCommitThreads = 128;
 constexpr int kChunk = 16;                    // path nodes per MMA K chunk
+constexpr int kBatch = 8;                     // path nodes whose operands are read at once
 constexpr int kTile = 64;                     // state columns per CTA
-constexpr int CO_S = 0;                       // S half: 2 boxes x [128 rows x 128 B] = 32 KB
-constexpr int CO_A = 32768;                   // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
+constexpr int kCommitCTAs = 7;                // per SM (7 x 64 tensor memory columns)
+constexpr int CO_S = 0;                       // one box of the half: [128 rows x 128 B] = 16 KB
+constexpr int CO_A = 16384;                   // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
 constexpr int CO_B = CO_A + 8192;             // U_a^T chunk: 64 rows x 16 tf32
 constexpr int CO_PATH = CO_B + 4096;          // int[128]
 constexpr int CO_BAR = CO_PATH + 512;         // 2 mbarriers
@@ -600,6 +604,9 @@ constexpr int CO_TSLOT = CO_BAR + 16;
 constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag
 constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
 constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
+static_assert(kCommitCTAs * (COMMIT_SMEM + 1024) <= 228 * 1024, "seven commit CTAs per SM");
+static_assert((kCommitCTAs + 1) * (COMMIT_SMEM + 1024) > 228 * 1024,
+              "never eight (8 x 64 tensor memory columns would still fit, but keep the margin)");
 
 constexpr uint32_t IDESC_COMMIT = idesc_tf32(128, kTile, false, false);
 
@@ -619,7 +626,7 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo)
 }
 
 template <bool VK>
-__global__ void __launch_bounds__(kCommitThreads, 4)
+__global__ void __launch_bounds__(kCommitThreads, kCommitCTAs)
 tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *__restrict__ k,
                  const float *__restrict__ U, const float *__restrict__ logP,
                  const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
@@ -645,13 +652,16 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     k += layer * k_ls;
     U += layer * u_ls;
     logP += layer * lp_ls;
-    // The state half is requested once the first batch of path reads is in
-    // flight (below), so those small reads do not queue behind it.
+    // Both boxes of the half go to L2 now; the first is requested into shared
+    // memory once the first batch of path reads is in flight (below), so
+    // those small reads do not queue behind it.
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmS);
+        tma_prefetch_l2_3d(&tmS, kTile * hv, unit * kD, layer);
+        tma_prefetch_l2_3d(&tmS, kTile * hv + 32, unit * kD, layer);
     }
     // Everything the verification (or the sampler) wrote -- U, log P, the
     // accepted node, the status -- is read after the wait.  The status word,
@@ -701,58 +711,75 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const uint32_t sa = smem_addr(sA), sb = smem_addr(sB);
     const int nchunks = (*(volatile int *)flag != 0) ? 0 : (L + kChunk - 1) / kChunk;
     for (int ch = 0; ch < nchunks; ++ch) {
-        // Every path-dependent read of the chunk in one batch: the decay of
-        // each path node (each thread forms its own coefficients), entry
-        // r = tid of the A-side row (key, or VK: U) and, for c = tid < 64,
-        // entry 64 hv + c of the B-side row (U, or VK: key).
         const int tn = min(kChunk, L - ch * kChunk); // path nodes in this chunk
-        float lp[kChunk], av_[kChunk], bv_[kChunk];
+#pragma unroll 1
+        for (int t0 = 0; t0 < kChunk; t0 += kBatch) {
+            // Every path-dependent read of the batch at once: the decay of
+            // each path node (each thread forms its own coefficients), entry
+            // r = tid of the A-side row (key, or VK: U) and, for c = tid < 64,
+            // entry 64 hv + c of the B-side row (U, or VK: key).  Columns past
+            // the path are written as zeros.
+            float lp[kBatch], av_[kBatch], bv_[kBatch];
 #pragma unroll
-        for (int tt = 0; tt < kChunk; ++tt) {
-            const size_t nh = (size_t)(o + (tt < tn ? path[ch * kChunk + tt] : 0)) * H + h;
-            lp[tt] = (tt < tn) ? logP[nh] : 0.f;
-            if (VK) {
-                av_[tt] = (tt < tn) ? U[nh * kD + tid] : 0.f;
-                bv_[tt] = (tt < tn && tid < kTile)
-                              ? __bfloat162float(k[nh * kD + kTile * hv + tid]) : 0.f;
-            } else {
-                av_[tt] = (tt < tn) ? __bfloat162float(k[nh * kD + tid]) : 0.f;
-                bv_[tt] = (tt < tn && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
+            for (int tt = 0; tt < kBatch; ++tt) {
+                const bool on = t0 + tt < tn;
+                const size_t nh =
+                    (size_t)(o + (on ? path[ch * kChunk + t0 + tt] : 0)) * H + h;
+                lp[tt] = on ? logP[nh] : 0.f;
+                if (VK) {
+                    av_[tt] = on ? U[nh * kD + tid] : 0.f;
+                    bv_[tt] = (on && tid < kTile)
+                                  ? __bfloat162float(k[nh * kD + kTile * hv + tid]) : 0.f;
+                } else {
+                    av_[tt] = on ? __bfloat162float(k[nh * kD + tid]) : 0.f;
+                    bv_[tt] = (on && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
+                }
             }
-        }
-        if (ch == 0 && tid == 0) {
-            mbar_arrive_expect_tx(&bar[0], 2 * 16384);
-            tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
-            tma_load_3d(sS + 16384, &tmS, &bar[0], kTile * hv + 32, unit * kD, layer);
-        }
-        // The key side carries the coefficients exp(L_a - L_j).
-        float coef[kChunk];
-#pragma unroll
-        for (int tt = 0; tt < kChunk; ++tt) coef[tt] = (tt < tn) ? expf(La - lp[tt]) : 0.f;
-        // A[r][t] (row r = tid), K-major, 64-byte rows
-#pragma unroll
-        for (int c4 = 0; c4 < kChunk / 4; ++c4) {
-            float av[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tt = 4 * c4 + e;
-                av[e] = VK ? av_[tt] : coef[tt] * av_[tt];
+            if (ch == 0 && t0 == 0 && tid == 0) {
+                mbar_arrive_expect_tx(&bar[0], 16384);
+                tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
             }
-            *reinterpret_cast<float4 *>(sA + sw64_offset(tid, 4 * c4)) =
-                make_float4(av[0], av[1], av[2], av[3]);
-        }
-        // B^T[c][t] (row c = tid < 64), K-major, 64-byte rows
-        if (tid < kTile) {
+            // The key side carries the coefficients exp(L_a - L_j).
+            float coef[kBatch];
 #pragma unroll
-            for (int t4 = 0; t4 < kChunk / 4; ++t4) {
-                float bv[4];
+            for (int tt = 0; tt < kBatch; ++tt)
+                coef[tt] = (t0 + tt < tn) ? expf(La - lp[tt]) : 0.f;
+            // A[r][t] (row r = tid), K-major, 64-byte rows
+#pragma unroll
+            for (int c4 = 0; c4 < kBatch / 4; ++c4) {
+                float av[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int tt = 4 * t4 + e;
-                    bv[e] = VK ? coef[tt] * bv_[tt] : bv_[tt];
+                    const int tt = 4 * c4 + e;
+                    av[e] = VK ? av_[tt] : coef[tt] * av_[tt];
                 }
-                *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * t4)) =
-                    make_float4(bv[0], bv[1], bv[2], bv[3]);
+                *reinterpret_cast<float4 *>(sA + sw64_offset(tid, t0 + 4 * c4)) =
+                    make_float4(av[0], av[1], av[2], av[3]);
+            }
+            // B^T[c][t] (row c = tid < 64), K-major, 64-byte rows
+            if (tid < kTile) {
+#pragma unroll
+                for (int t4 = 0; t4 < kBatch / 4; ++t4) {
+                    float bv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tt = 4 * t4 + e;
+                        bv[e] = VK ? coef[tt] * bv_[tt] : bv_[tt];
+                    }
+                    *reinterpret_cast<float4 *>(sB + sw64_offset(tid, t0 + 4 * t4)) =
+                        make_float4(bv[0], bv[1], bv[2], bv[3]);
+                }
+            }
+            if (t0 + kBatch >= tn && t0 + kBatch < kChunk) { // the rest of the chunk is zero
+#pragma unroll
+                for (int c4 = kBatch / 4; c4 < kChunk / 4; ++c4) {
+                    *reinterpret_cast<float4 *>(sA + sw64_offset(tid, 4 * c4)) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (tid < kTile)
+                        *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * c4)) =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                break;
             }
         }
         fence_proxy_async_smem();
@@ -774,41 +801,54 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         __syncthreads();
     }
 
-    // epilogue: S <- P_a S + D, in shared memory, then TMA store in place
-    // (the state half was requested with the first chunk)
-    if (nchunks > 0 && !mbar_wait(&bar[0], 0, kWaitNs)) {
-        report(st, BOLE_ERR_TIMEOUT, b, -1, 8);
-        *flag = 1;
-    }
-    const bool ok = *(volatile int *)flag == 0;
-    if (ok && nchunks > 0) {
+    // epilogue, one 32-column box at a time: S <- P_a S + D in shared memory,
+    // then TMA store in place; the second box is requested into the buffer
+    // once the first one's store has read it (an L2 hit: prefetched at entry)
+    bool ok = *(volatile int *)flag == 0;
+    if (nchunks > 0) {
         const float Pa = expf(La);
         const int r = tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + cb * 32, x);
-            uint8_t *tile = sS + cb * 16384;
+            if (cb == 1 && tid == 0) {
+                bulk_wait_group_read0(); // the first box's store has read the buffer
+                if (ok) {
+                    mbar_arrive_expect_tx(&bar[0], 16384);
+                    tma_load_3d(sS, &tmS, &bar[0], kTile * hv + 32, unit * kD, layer);
+                }
+            }
+            if (cb == 1) {
+                __syncthreads();
+                if (!ok) break;
+            }
+            if (!mbar_wait(&bar[0], (uint32_t)cb, kWaitNs)) {
+                report(st, BOLE_ERR_TIMEOUT, b, -1, 8);
+                *flag = 1;
+            }
+            if (*(volatile int *)flag == 0) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + cb * 32, x);
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                float4 *p = reinterpret_cast<float4 *>(tile + sw128_offset(r, 4 * c4));
-                float4 s4 = *p;
-                s4.x = fmaf(Pa, s4.x, x[4 * c4 + 0]);
-                s4.y = fmaf(Pa, s4.y, x[4 * c4 + 1]);
-                s4.z = fmaf(Pa, s4.z, x[4 * c4 + 2]);
-                s4.w = fmaf(Pa, s4.w, x[4 * c4 + 3]);
-                *p = s4;
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    float4 *p = reinterpret_cast<float4 *>(sS + sw128_offset(r, 4 * c4));
+                    float4 s4 = *p;
+                    s4.x = fmaf(Pa, s4.x, x[4 * c4 + 0]);
+                    s4.y = fmaf(Pa, s4.y, x[4 * c4 + 1]);
+                    s4.z = fmaf(Pa, s4.z, x[4 * c4 + 2]);
+                    s4.w = fmaf(Pa, s4.w, x[4 * c4 + 3]);
+                    *p = s4;
+                }
+                fence_proxy_async_smem();
+            }
+            __syncthreads();
+            ok = *(volatile int *)flag == 0;
+            if (tid == 0 && ok) {
+                tma_store_3d(&tmS, sS, kTile * hv + 32 * cb, unit * kD, layer);
+                bulk_commit_group();
             }
         }
-        fence_proxy_async_smem();
-    }
-    __syncthreads();
-    if (tid == 0 && ok && nchunks > 0) {
-        tma_store_3d(&tmS, sS, kTile * hv, unit * kD, layer);
-        tma_store_3d(&tmS, sS + 16384, kTile * hv + 32, unit * kD, layer);
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        if (tid == 0) bulk_wait_group_read0();
     }
     tc_fence_before();
     __syncthreads();
