@@ -297,7 +297,8 @@ bole_status bole_conv_commit(void *conv_state, const void *x, bole_dtype x_dtype
                              int32_t *dev_status, unsigned flags, bole_stream_t stream)
 {
     (void)flags;
-    if (B < 0 || N < 0 || C < 1 || W < 1 || W > BOLE_MAX_CONV_WIDTH || !valid_dtype(x_dtype))
+    if (B < 0 || B > 65535 || N < 0 || C < 1 || C % 16 != 0 || W < 1 ||
+        W > BOLE_MAX_CONV_WIDTH || !valid_dtype(x_dtype))
         return BOLE_ERR_INVALID_ARG;
     if ((size_t)N > (size_t)B * BOLE_MAX_TREE_NODES) return BOLE_ERR_INVALID_ARG;
     if (!offsets || !dev_status || (B > 0 && W > 1 && (!conv_state || !accepted)))

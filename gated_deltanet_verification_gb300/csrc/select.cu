@@ -282,7 +282,7 @@ cudaError_t launch_select(const float *p, const int32_t *cand_offsets, const int
     int32_t *counts = lens + B;
     cudaError_t e = cudaMemsetAsync(st, 0, BOLE_STATUS_WORDS * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
-    if (B == 0) return cudaSuccess;
+    if (B == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t), s); // the empty forest
     select_local_kernel<<<B, kSelThreads, 0, s>>>(p, cand_offsets, cand_parent, caps, M, rho,
                                                   lists, lens, st);
     select_global_kernel<<<B, kRankThreads, 0, s>>>(lists, lens, B, budget, counts);

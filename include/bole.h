@@ -323,7 +323,7 @@ bole_status bole_conv_gates(const void *x, const void *conv_state, const float *
  * W-2, its parent's in row W-3, ..., then the old rows, most recent first.
  * accepted[b] = -1 leaves the request's state untouched.  x is the same
  * buffer bole_conv_gates read.  Exact (rows are copied).  W = 1 launches
- * nothing. */
+ * nothing.  C = H (2 dk + dv) (a multiple of 16); B <= 65535. */
 bole_status bole_conv_commit(void *conv_state, const void *x, bole_dtype x_dtype,
                              const int32_t *offsets, const int32_t *parent,
                              const int32_t *accepted, int B, int C, int W, int N,

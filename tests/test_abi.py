@@ -181,3 +181,13 @@ def test_select_host_validation_without_gpu(lib):
     assert sel(offsets=None) == bole.ERR_INVALID_ARG
     assert sel(work=None) == bole.ERR_WORKSPACE
     assert sel(nbytes=16) == bole.ERR_WORKSPACE
+
+
+def test_stage1_commit_rejects_bad_sizes_without_gpu(lib):
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake = c(1 << 20)
+    assert lib.bole_conv_commit(fake, fake, 1, fake, fake, fake, 70000, 384, 4, 8, fake, 0,
+                                None) == bole.ERR_INVALID_ARG      # B above the grid limit
+    assert lib.bole_conv_commit(fake, fake, 1, fake, fake, fake, 2, 100, 4, 8, fake, 0,
+                                None) == bole.ERR_INVALID_ARG      # C not a multiple of 16

@@ -189,3 +189,33 @@ def test_commit_layers_reports_a_bad_accepted_node_once():
     torch.cuda.synchronize()
     assert st.cpu().tolist() == [bole.ERR_BAD_TOPOLOGY, 2, 7, 7]
     assert torch.equal(S[:, 2], S0[:, 2])
+
+
+def test_commit_layers_overlapped_after_verify_matches_plain_launch():
+    """Launched to overlap the last verification (programmatic dependent
+    launch), the cross-layer commit gives bit-identical states."""
+    from gated_deltanet_verification_gb300 import bole
+    base = I.config_batch(2)
+    layers = I.layer_batches(base, 3, seed=77)
+    N, H = base.N, base.H
+    out = []
+    for flags in (0, bole.FLAG_OVERLAP_LAUNCH):
+        S = torch.stack([_t(lb.S_pre, torch.float32) for lb in layers])
+        k = torch.stack([_t(lb.k, torch.bfloat16) for lb in layers])
+        U = torch.empty((3, N, H, base.dv), dtype=torch.float32, device="cuda")
+        lp = torch.empty((3, N, H), dtype=torch.float32, device="cuda")
+        offsets, parent = _t(base.offsets, torch.int32), _t(base.parent, torch.int32)
+        depth, anc, req, st = bole.pack_forest(offsets, parent, base.max_depth)
+        for li, lb in enumerate(layers):
+            bole.tree_verify(S[li], _t(lb.q, torch.bfloat16), k[li], _t(lb.v, torch.bfloat16),
+                             _t(lb.gamma, torch.float32), _t(lb.beta, torch.float32), offsets,
+                             parent, depth, anc, req, base.max_T, base.max_depth, U=U[li],
+                             logP=lp[li], status=st, flags=flags)
+        bole.commit_layers(S, k, U, lp, offsets, parent, _t(base.accepted, torch.int32),
+                           status=st, flags=flags)
+        torch.cuda.synchronize()
+        bole.check_status(st)
+        out.append(S.cpu())
+    assert torch.equal(out[0], out[1])
+    ref = oracle.commit_layers(layers)
+    assert rel_fro(out[1].numpy().astype(np.float64), ref) <= TOL["bf16"]

@@ -122,3 +122,14 @@ def test_selected_forest_feeds_pack_and_verify_without_host_round_trip():
     Oe, Ue, _ = oracle.verify(b)
     assert rel_fro(O[:n].float().cpu().numpy(), Oe) <= 1e-2
     assert rel_fro(U[:n].cpu().numpy(), Ue) <= 1e-2
+
+
+def test_empty_batch_gives_the_empty_forest():
+    from gated_deltanet_verification_gb300 import bole
+    off = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    o, _, _, _, st = bole.select_forest(torch.zeros(1, dtype=torch.float32, device="cuda"),
+                                        torch.zeros(1, dtype=torch.int32, device="cuda"),
+                                        torch.zeros(1, dtype=torch.int32, device="cuda"), 10,
+                                        offsets=off)
+    torch.cuda.synchronize()
+    assert o.cpu().tolist() == [0] and st.cpu().tolist()[0] == 0
