@@ -88,13 +88,14 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
 /* Overlap the launch with the kernel before it on the stream (programmatic
  * dependent launch; tensor-core kernels only).  The caller asserts that the
  * previous kernel on the stream is the round's bole_pack_forest (before
- * bole_tree_verify) or bole_tree_verify (before bole_commit), or any kernel
- * that does not let its dependents start early.  The kernel may then begin
- * while that one drains: before waiting for it, it reads only caller-owned
- * inputs that neither library call writes (S_pre / S, q, k, v, gamma, beta,
- * offsets); the status word and everything the previous call produced are
- * read after the wait.  Without the flag every launch starts only after the
- * previous kernel has ended. */
+ * bole_tree_verify), a bole_tree_verify (before the next layer's
+ * bole_tree_verify, or before bole_commit / bole_commit_layers), or any
+ * kernel that does not let its dependents start early.  The kernel may then
+ * begin while that one drains: before waiting for it, it reads only
+ * caller-owned inputs that none of these calls writes (S_pre / S, q, k, v,
+ * gamma, beta, offsets); the status word and everything the previous call
+ * produced are read after the wait.  Without the flag every launch starts
+ * only after the previous kernel has ended. */
 #define BOLE_FLAG_OVERLAP_LAUNCH 0x2u
 /* State slots in the serving runtime's canonical layout (Section IV-D, the
  * state lifecycle of Fig. 6): S_pre / S stored [B, H, dv, dk] -- each head's
