@@ -50,6 +50,14 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
 {
     const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -124,9 +132,10 @@ inline cudaError_t make_layered_state_map(CUtensorMap *map, const float *S, int 
 inline cudaError_t configure_once(const void *fn, int smem, bool carveout, int slot)
 {
     static std::mutex mu;
-    // slots: 0 verify, 1 commit, 2 large-tree factor, 3 large-tree solve, and
-    // 4, 5, 6 the same kernels for the transposed state layout
-    static uint64_t done[8] = {0, 0, 0, 0, 0, 0, 0, 0}; // bit = device, word = slot
+    // slots: 0 verify, 1 commit, 2 large-tree factor, 3 large-tree solve,
+    // 4, 5, 6 the same kernels for the transposed state layout, 8 and 9 the
+    // small-tree verification (both layouts)
+    static uint64_t done[16] = {}; // bit = device, word = slot
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -78,6 +78,19 @@ constexpr int kLd = 17;       // padded row stride of the compact factors (bank 
 // Tensor memory (256 columns, lane = operand row): columns 0..127 hold
 // [Q S_pre; K S_pre], columns 128..255 the propagation [M R; W R]; before the
 // propagation, 128..191 hold the Gram.  The epilogues only read tensor memory.
+//
+// Trees of at most 32 nodes (the small variant) load q and k as 32-row boxes,
+// so rows 32..63 and 96..127 of each [Q;K] K-atom are padding that the
+// products read into tensor-memory lanes nobody reads.  Those 16 KB take the
+// value rows (TMA at entry, rows 32..63 of both atoms) and the staged Gram
+// (q.k rows 96..127 of atom 0, k.k rows 96..127 of atom 1, 128 B per row),
+// so the factor chain -- Gram, gather, substitution -- no longer waits for
+// the first d_k half of the state products and runs beside the S_pre
+// stream; the rows of W and M are held in registers until the state
+// products release the S buffer.
+constexpr int kTSmall = 32;
+constexpr int SM_V = 4096;                    // value rows: + 16384 for columns 64..127
+constexpr int SM_GQK = 12288, SM_GKK = 28672; // staged q.k and k.k Gram rows
 constexpr int OFF_SBUF = 0;
 constexpr int SBUF_BYTES = 65536;
 constexpr int OFF_A1 = SBUF_BYTES;
@@ -111,6 +124,7 @@ constexpr int kComputeThreads = 256;          // warps 0..7: factors, split, epi
 constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
 
 constexpr uint32_t IDESC_GRAM = idesc_bf16(128, 64, false, false);  // [Q;K] K^T
+constexpr uint32_t IDESC_GRAM_S = idesc_bf16(128, 32, false, false); // small trees
 constexpr uint32_t IDESC_STATE = idesc_bf16(128, 128, false, true); // [Q;K] S, S N-contiguous
 constexpr uint32_t IDESC_STATE_VK = idesc_bf16(128, 128, false, false); // S stored [dv][dk]
 constexpr uint32_t IDESC_TF32 = idesc_tf32(128, 128, false, false); // both K-major
@@ -136,7 +150,11 @@ constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, B
 // K-major operand rows (row = value column, 64 d_k entries per 128 B), the
 // first d_k half of the product reads the boxes (0, 1) whole, and the Gram
 // is staged in those 32 KB instead.
-template <bool VK>
+// SMALL (trees of at most 32 nodes): the Gram and the value rows live in the
+// [Q;K] padding; warps 0 and 2 stage the Gram, warp 0 gathers and forms the
+// rows of W, warp 1 those of M (both before the state products end); warps
+// 2 and 6 form R^T; only the lanes of rows 0..31 and 64..95 carry outputs.
+template <bool VK, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -144,7 +162,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                  const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
                  const int32_t *__restrict__ req_depth, int H, int N,
                  __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
-                 float *__restrict__ logP, int32_t *st)
+                 float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -169,24 +187,36 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
+    // Tensor memory: the SM starts the next CTA of a kernel that allocates
+    // tensor memory only once the resident one has given up its allocation
+    // permit.  A launch of its own allocates first, so the second CTA of each
+    // SM is not held back by the prologue; a launch overlapping the previous
+    // kernel allocates after the prologue (measured faster there: the CTAs
+    // that wait for the previous kernel then do not all start at once).
+    if (early_alloc && warp == 0) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
     pdl_launch_dependents(); // an overlapped commit may start its state reads
     // Caller inputs first (a launch that overlaps pack reads only these before
     // it waits): the request's extent, then the small, latency-critical reads
     // -- [Q;K] and the per-thread gamma, beta -- before the 64 KB state tile,
     // which every CTA requests at once.
     const int o = offsets[b], T = offsets[b + 1] - o;
-    const bool in_range = T > 0 && T <= kT && o >= 0 && o + T <= N;
+    constexpr int kTmax = SMALL ? kTSmall : kT;
+    const bool in_range = T > 0 && T <= kTmax && o >= 0 && o + T <= N;
     const bool issuer = tid == kComputeThreads;
     if (issuer) {
         for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
         mbar_init(&bar[BAR_TOPO], kT);
-        mbar_init(&bar[BAR_STAGED], 128);
+        mbar_init(&bar[BAR_STAGED], SMALL ? 64 : 128);
         mbar_init(&bar[BAR_CG], kT);
         mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
         fence_mbar_init();
         if (in_range) {
-            mbar_arrive_expect_tx(&bar[BAR_A1], 32768);
+            // q rows 0.., k rows 64.. of each K-atom (boxes of kTmax rows)
+            mbar_arrive_expect_tx(&bar[BAR_A1], SMALL ? 16384 : 32768);
 #pragma unroll
             for (int ka = 0; ka < 2; ++ka) {
                 tma_load_3d(sA1 + ka * 16384, &tmQ, &bar[BAR_A1], 64 * ka, h, o);
@@ -213,12 +243,18 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+        if (SMALL && in_range) { // value rows into the padding of the q boxes
+            mbar_arrive_expect_tx(&bar[BAR_V], 8192);
+            tma_load_3d(sA1 + SM_V, &tmV, &bar[BAR_V], 0, h, o);
+            tma_load_3d(sA1 + SM_V + 16384, &tmV, &bar[BAR_V], 64, h, o);
+        }
     }
     // What the previous call wrote (the status word pack reset, the
     // per-request depth) is read after the wait; the reads above are already
     // in flight, so without an overlapped launch both arrive in one round trip.
     pdl_wait();
-    const int fault = *(const volatile int32_t *)st;
+    int *sfault = reinterpret_cast<int *>(sm + OFF_MISC + 4);
+    if (tid == 0) *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
     const int d = req_depth[b];
     // Depth and ancestor-or-self mask of each node from the request's parent
     // links (a caller input), walked in shared memory by the topology warps:
@@ -241,18 +277,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             if (j != -1) my_depth = -1; // deeper than 15 or malformed: no work for this row
         }
     }
-    const bool bad = !in_range || d < 0 || d >= kSlots || d >= T;
-    if (fault != 0 || T <= 0 || bad) {
-        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0)
-            report(st, T > kT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH, b,
-                   -1, T > kT ? T : d);
-        if (issuer) { // drain the copies in flight before the CTA retires
-            if (in_range) mbar_wait(&bar[BAR_A1], 0, kWaitNs);
-            mbar_wait(&bar[BAR_S], 0, kWaitNs);
-        }
-        return;
-    }
-    if (warp == 0) {
+    if (!early_alloc && warp == 0) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
@@ -260,6 +285,20 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const int fault = *sfault;
+    const bool bad = !in_range || d < 0 || d >= kSlots || d >= T;
+    if (fault != 0 || T <= 0 || bad) {
+        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0)
+            report(st, T > kTmax || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH,
+                   b, -1, T > kTmax ? T : d);
+        if (issuer) { // drain the copies in flight before the CTA retires
+            if (in_range) mbar_wait(&bar[BAR_A1], 0, kWaitNs);
+            if (SMALL && in_range) mbar_wait(&bar[BAR_V], 0, kWaitNs);
+            mbar_wait(&bar[BAR_S], 0, kWaitNs);
+        }
+        if (warp == 0) tmem_dealloc(tmem, 256); // unused
+        return;
+    }
     const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
 
     if (warp == kComputeThreads / 32) {
@@ -274,7 +313,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                 mma_bf16_ss(tmem + TM_GRAM, sdesc_sw128(a1 + off, 16, 1024),
-                            sdesc_sw128(a1 + off + 8192, 16, 1024), IDESC_GRAM, kk > 0);
+                            sdesc_sw128(a1 + off + 8192, 16, 1024),
+                            SMALL ? IDESC_GRAM_S : IDESC_GRAM, kk > 0);
             }
             mma_commit(&bar[BAR_GRAM]);
             // state products [Q;K] (S_hi + S_lo) once the split is in place,
@@ -295,11 +335,22 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 if (kk == 3) mma_commit(&bar[BAR_STATE_A]);
             }
             mma_commit(&bar[BAR_STATE]);
+            // The state tile of the CTA one wave ahead (pf_stride = resident
+            // CTAs of the launch) goes to L2 now that this CTA's own tile has
+            // landed, so the next wave finds it there.
+            if (pf_stride > 0 && unit + pf_stride < (int)gridDim.x) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_prefetch_l2_2d(&tmS, 32 * c, (unit + pf_stride) * kD);
+            }
             // value rows over the [Q;K] columns the first half has released
-            ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
-            mbar_arrive_expect_tx(&bar[BAR_V], 16384);
-            tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
-            tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
+            // (small trees: loaded at entry)
+            if (!SMALL) {
+                ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
+                mbar_arrive_expect_tx(&bar[BAR_V], 16384);
+                tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
+                tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
+            }
             // propagation + read-out: [M; W] R into its own 128 columns
             // (the K extent is the tree: ceil(T / 8) steps of 8 nodes)
             ok &= mbar_wait(&bar[BAR_OPS], 0, kWaitNs);
@@ -320,7 +371,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         // Gram row m is staged in the S_pre rows the first d_k half released:
         // rows 32p..32p+31 in the first 8 KB of box p (VK: the first 32 KB,
         // boxes 0 and 1), 256 B per row, 16-byte chunks XOR-swizzled by row.
+        // Small trees: rows 0..31 and 64..95 in the [Q;K] padding, 128 B per
+        // row (32 columns), chunks XOR-swizzled by row & 7.
         auto staged_row = [&](int row) -> float * {
+            if (SMALL)
+                return reinterpret_cast<float *>(
+                    sA1 + (row < 64 ? SM_GQK + row * 128 : SM_GKK + (row - 64) * 128));
             return reinterpret_cast<float *>(
                 sbuf + (VK ? row * 256 : (row >> 5) * 16384 + (row & 31) * 256));
         };
@@ -363,26 +419,29 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             if (i < T) logP[(size_t)(o + i) * H + h] = L;
             mbar_arrive(&bar[BAR_TOPO]);
         }
-        if (warp < 4) {
-            // Stage the Gram rows (q.k for rows 0..63, k.k for 64..127).
+        if (SMALL ? (warp == 0 || warp == 2) : warp < 4) {
+            // Stage the Gram rows (q.k for rows 0..63, k.k for 64..127; small
+            // trees: rows 0..31 and 64..95, columns 0..31, with no wait for
+            // the state products).
             ok &= mbar_wait(&bar[BAR_GRAM], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
+            if (!SMALL) ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
             tc_fence_after();
             __syncwarp();
             float4 *srow = reinterpret_cast<float4 *>(staged_row(m));
 #pragma unroll 1
-            for (int hc = 0; hc < 2; ++hc) {
+            for (int hc = 0; hc < (SMALL ? 1 : 2); ++hc) {
                 float x[32];
                 tmem_ld32(tmem + TM_GRAM + 32 * hc + lane_base, x);
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4)
-                    srow[(8 * hc + c4) ^ (m & 15)] =
+                    srow[(8 * hc + c4) ^ (m & (SMALL ? 7 : 15))] =
                         make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
             }
             mbar_arrive(&bar[BAR_STAGED]);
         }
         if (topo) {
-            // Compact C and G of row i, gathered in depth order.
+            // Compact C and G of row i, gathered in depth order (small trees:
+            // warp 0 only, the rows of warp 1 are past the tree).
             ok &= mbar_wait(&bar[BAR_STAGED], 0, kWaitNs);
             const float *qk = staged_row(i), *kk = staged_row(64 + i);
             float *crow = Cc + i * kLd, *grow = Gc + i * kLd;
@@ -390,9 +449,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 #pragma unroll
             for (int t = 0; t < kSlots; ++t) {
                 const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
-                const int sw = (((j >> 2) ^ (i & 15)) << 2) | (j & 3);
-                qv[t] = qk[sw];
-                kv[t] = kk[sw];
+                const int sw = (((j >> 2) ^ (i & (SMALL ? 7 : 15))) << 2) | (j & 3);
+                qv[t] = (!SMALL || warp == 0) ? qk[sw] : 0.f;
+                kv[t] = (!SMALL || warp == 0) ? kk[sw] : 0.f;
             }
 #pragma unroll
             for (int t = 0; t < kSlots; ++t) {
@@ -444,7 +503,95 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs);
         const float p = (i < T) ? expf(Ls[i]) : 0.f; // P_i
 
-        if (m < 64 && (topo || warp >= 4)) {
+        if (SMALL && warp < 2) {
+            // Rows of W (warp 0: y) and M (warp 1: z) of node n = lane by the
+            // same backward substitution, formed while the state products
+            // run and written into the [M; W] operand once they are done.
+            const int n = lane;
+            const bool wrow = warp == 0;
+            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
+            float vals[kSlots];
+            uint32_t aw4[4] = {0, 0, 0, 0};
+            int di = -1;
+            if (n < T) {
+                di = Ds[n];
+                const uint4 a4 = *reinterpret_cast<const uint4 *>(ancat + n * kSlots);
+                aw4[0] = a4.x; aw4[1] = a4.y; aw4[2] = a4.z; aw4[3] = a4.w;
+                const float *ci = Cc + n * kLd;
+                float cv[kSlots], acc[kSlots], gcur[kSlots];
+#pragma unroll
+                for (int t = 0; t < kSlots; ++t) {
+                    cv[t] = wrow ? 0.f : ci[t];
+                    acc[t] = 0.f;
+                }
+                {
+                    const float *gr = Gc + n * kLd;
+#pragma unroll
+                    for (int t = 0; t < kSlots - 1; ++t) gcur[t] = gr[t];
+                }
+#pragma unroll
+                for (int u = kSlots - 1; u >= 0; --u) {
+                    vals[u] = 0.f;
+                    if (u <= di) {
+                        float gnext[kSlots];
+                        if (u >= 1) {
+                            const int an = (aw4[(u - 1) >> 2] >> (8 * ((u - 1) & 3))) & 0xff;
+                            const float *gr = Gc + an * kLd;
+#pragma unroll
+                            for (int t = 0; t < u - 1; ++t) gnext[t] = gr[t];
+                        }
+                        const float val = wrow ? ((u == di) ? 1.f : -acc[u]) : cv[u] - acc[u];
+                        vals[u] = val;
+#pragma unroll
+                        for (int t = 0; t < u; ++t) acc[t] = fmaf(val, gcur[t], acc[t]);
+#pragma unroll
+                        for (int t = 0; t < u - 1; ++t) gcur[t] = gnext[t];
+                    }
+                }
+            }
+            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            const int orow = wrow ? 64 + n : n;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) // K extent <= 32 nodes: the first K-atom
+                *reinterpret_cast<float4 *>(sbuf + sw128_chunk(orow, c)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < kSlots; ++u) {
+                if (u <= di) {
+                    const int au = (aw4[u >> 2] >> (8 * (u & 3))) & 0xff;
+                    *reinterpret_cast<float *>(sbuf + sw128_offset(orow, au)) = vals[u];
+                }
+            }
+        } else if (SMALL && rowgrp == 2) {
+            // R^T of nodes 0..31 (warp 2: columns 0..63, warp 6: 64..127),
+            // value rows from the [Q;K] padding.
+            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
+            tc_fence_after();
+            __syncwarp();
+            uint8_t *dst = sbuf + 32768;
+            const uint8_t *vrow = sA1 + SM_V + half * 16384 + i * 128;
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                const int col0 = half * 64 + cc * 32;
+                float x[32];
+                tmem_ld32(tmem + lane_base + col0, x);
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                    float f[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int c = 8 * uu + t;
+                        const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
+                        *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i)) = r;
+                    }
+                }
+            }
+        } else if (SMALL) {
+            // lanes of the padding rows: nothing to form
+        } else if (m < 64 && (topo || warp >= 4)) {
             // Rows of W (warps 0, 1: y) and of M (warps 4, 5: z) by backward
             // substitution along the ancestor path, written straight into the
             // [M; W] operand (row i of M, row 64 + i of W, column = ancestor)
@@ -535,7 +682,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         ok &= mbar_wait(&bar[BAR_MMA2], 0, kWaitNs);
         tc_fence_after();
         __syncwarp();
-        {
+        if (!SMALL || !(rowgrp & 1)) { // small trees: no output in the padding lanes
             const bool store = ok && i < T;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
@@ -601,7 +748,7 @@ constexpr int CO_B = CO_A + 8192;             // U_a^T chunk: 64 rows x 16 tf32
 constexpr int CO_PATH = CO_B + 4096;          // int[128]
 constexpr int CO_BAR = CO_PATH + 512;         // 2 mbarriers
 constexpr int CO_TSLOT = CO_BAR + 16;
-constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag
+constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag, status copy
 constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
 constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
 static_assert(kCommitCTAs * (COMMIT_SMEM + 1024) <= 228 * 1024, "seven commit CTAs per SM");
@@ -666,28 +813,37 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     // Everything the verification (or the sampler) wrote -- U, log P, the
     // accepted node, the status -- is read after the wait.  The status word,
     // the accepted node and the request's extent come in one round trip;
-    // uniform early exits.
+    // uniform early exit (the status is read by one thread).
     pdl_wait();
-    const int fault = *(const volatile int32_t *)st;
+    int *sfault = plen + 2;
+    if (tid == 0) *sfault = *(const volatile int32_t *)st;
     const int a = accepted[b];
     const int o = offsets[b], T = offsets[b + 1] - o;
     const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
-    if (fault != 0 || a < 0 || bad) {
-        if (bad && fault == 0 && tid == 0 && hv == 0 && layer == 0)
-            report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
-        return;
-    }
+    const bool work = a >= 0 && !bad;
+    // Tensor memory after this first round trip: the SM starts the next CTA
+    // once this one has given up its allocation permit, and staggering the
+    // seven CTAs of an SM by a round trip measured faster than starting them
+    // together.
     if (warp == 0) {
         tmem_alloc(tslot, 64);
         tmem_relinquish();
     }
     // stage the request's parent links (coalesced), then walk the accepted path
-    for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
+    if (work)
+        for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
     if (tid == 32) *flag = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const int fault = *sfault;
+    if (fault != 0 || !work) {
+        if (bad && fault == 0 && tid == 0 && hv == 0 && layer == 0)
+            report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, T);
+        if (warp == 0) tmem_dealloc(tmem, 64); // unused
+        return;
+    }
     if (tid == 0) {
         int L = 0, j = a;
         bool ok = true;
@@ -859,6 +1015,20 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
 
 } // namespace
 
+// CTAs of a launch resident at once (per_sm per SM), cached per device.
+static int resident_ctas(int per_sm)
+{
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = n;
+    }
+    return per_sm * sms[dev];
+}
+
 bool tc_verify_supported(const VerifyArgs &a)
 {
     return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && a.max_T <= kT &&
@@ -871,21 +1041,26 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
 {
     const int units = a.B * a.H;
     if (units == 0 || a.N == 0) return cudaSuccess;
+    // trees of at most 32 nodes take the small variant (q, k, v boxes of 32 rows)
+    const bool small = a.max_T <= kTSmall;
+    const int rows = small ? kTSmall : kT;
     CUtensorMap mS, mQ, mK, mV;
     cudaError_t e = make_state_map(&mS, a.S_pre, units);
-    if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, kT);
-    if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kT);
-    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kT);
+    if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, rows);
+    if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, rows);
+    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, rows);
     if (e != cudaSuccess) return e;
-    auto kernel = a.vk ? tc_verify_kernel<true> : tc_verify_kernel<false>;
-    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true, a.vk ? 4 : 0);
+    auto kernel = small ? (a.vk ? tc_verify_kernel<true, true> : tc_verify_kernel<false, true>)
+                        : (a.vk ? tc_verify_kernel<true, false> : tc_verify_kernel<false, false>);
+    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true,
+                       small ? (a.vk ? 9 : 8) : (a.vk ? 4 : 0));
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
                                                  overlap, attr);
     return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.parent,
                               a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
-                              a.logP, a.st);
+                              a.logP, a.st, resident_ctas(2), overlap ? 0 : 1);
 }
 
 bool tc_commit_supported(const CommitArgs &a)

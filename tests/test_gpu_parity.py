@@ -234,3 +234,49 @@ def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
             assert rel_fro(Mg, M) < 5e-3, (r, hh, rel_fro(Mg, M))
             # padding rows and columns stay exactly zero (W keeps its unit diagonal)
             assert np.all(mw[r, hh, :T, T:] == 0) and np.all(mw[r, hh, 128:128 + T, T:] == 0)
+
+
+def _verify_direct(b, max_T):
+    from gated_deltanet_verification_gb300 import bole
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device="cuda", dtype=dt)
+    offsets, parent = t(b.offsets, torch.int32), t(b.parent, torch.int32)
+    depth, anc, req, st = bole.pack_forest(offsets, parent, b.max_depth)
+    O, U, logP = bole.tree_verify(t(b.S_pre, torch.float32), t(b.q, torch.bfloat16),
+                                  t(b.k, torch.bfloat16), t(b.v, torch.bfloat16),
+                                  t(b.gamma, torch.float32), t(b.beta, torch.float32), offsets,
+                                  parent, depth, anc, req, max_T, b.max_depth, status=st)
+    torch.cuda.synchronize()
+    return (O.float().cpu().numpy().astype(np.float64), U.cpu().numpy().astype(np.float64),
+            logP.cpu().numpy().astype(np.float64), st.cpu().tolist())
+
+
+def test_small_tree_layout_matches_the_64_node_layout():
+    """A forest whose trees hold at most 32 nodes runs the small-tree layout of
+    the fused kernel (value rows and Gram in the [Q;K] padding, factors formed
+    beside the state products); declaring max_T = 64 runs the 64-node layout
+    on the same forest.  Both against the oracle, and against each other
+    (same products, same substitution order)."""
+    b = I.random_batch(seed=91, B=7, H=3, dk=128, dv=128, sizes=[32, 1, 17, 0, 32, 9, 25],
+                       max_depth=15, dtype="bf16", sigma=0.05, shape="random")
+    Oe, Ue, _ = oracle.verify(b)
+    got = []
+    for max_T in (32, 64):
+        O, U, logP, st = _verify_direct(b, max_T)
+        assert st[0] == 0, st
+        assert rel_fro(O, Oe) <= TOL["bf16"] and rel_fro(U, Ue) <= TOL["bf16"]
+        got.append((O, U, logP))
+    assert rel_fro(got[0][1], got[1][1]) <= 1e-5
+    assert rel_fro(got[0][0], got[1][0]) <= 1e-4  # bf16 rounding of equal fp32 values
+    assert np.array_equal(got[0][2], got[1][2])
+
+
+def test_tree_above_declared_max_T_is_reported():
+    """max_T bounds every tree: a 33-node tree declared as max_T = 32 is
+    reported as a topology error by the small-tree kernel, which then loads
+    none of its operands and writes no output."""
+    from gated_deltanet_verification_gb300 import bole
+    b = I.random_batch(seed=92, B=2, H=2, dk=128, dv=128, sizes=[5, 33], max_depth=6,
+                       dtype="bf16", sigma=0.05)
+    _, _, _, st = _verify_direct(b, 32)
+    assert st[0] == bole.ERR_BAD_TOPOLOGY and st[1] == 1, st
