@@ -726,8 +726,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 // ---- commit ----
 // One CTA per (request, head, 64-column half of the state, layer): value
 // tiling as in the pages' kernel.  The half is staged one 32-column box at a
-// time through a 16 KB buffer (both boxes are prefetched into L2 at entry, so
-// the second load is an L2 hit), which lets seven CTAs share an SM and a
+// time through a 16 KB buffer (both boxes are prefetched into L2 ahead of
+// use, so the second load is an L2 hit), which lets seven CTAs share an SM and a
 // batch of 1024 tiles run in one wave.  (Narrower tiles fit more CTAs but
 // repeat the path operand's gather and measured slower.)  One launch covers
 // every layer of a unified cross-layer commit: layer l's state, keys, deltas
@@ -799,16 +799,16 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     k += layer * k_ls;
     U += layer * u_ls;
     logP += layer * lp_ls;
-    // Both boxes of the half go to L2 now; the first is requested into shared
-    // memory once the first batch of path reads is in flight (below), so
-    // those small reads do not queue behind it.
+    // The first box of the half goes to L2 now, the second once the path
+    // reads are in flight (prefetching both at entry queued those small,
+    // dependent reads behind every CTA's state traffic); the first box is
+    // requested into shared memory beside the first batch of path reads.
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmS);
         tma_prefetch_l2_3d(&tmS, kTile * hv, unit * kD, layer);
-        tma_prefetch_l2_3d(&tmS, kTile * hv + 32, unit * kD, layer);
     }
     // Everything the verification (or the sampler) wrote -- U, log P, the
     // accepted node, the status -- is read after the wait.  The status word,
@@ -894,6 +894,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
             if (ch == 0 && t0 == 0 && tid == 0) {
                 mbar_arrive_expect_tx(&bar[0], 16384);
                 tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
+                tma_prefetch_l2_3d(&tmS, kTile * hv + 32, unit * kD, layer); // second box
             }
             // The key side carries the coefficients exp(L_a - L_j).
             float coef[kBatch];
