@@ -73,8 +73,9 @@ __global__ void __launch_bounds__(kThreads) simt_factor_kernel(
     __shared__ int up[kMaxTree];
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
-    if (faulted(st)) return;
+    const bool prior_fault = faulted(st);
     const int o = offsets[b], Tn = offsets[b + 1] - o;
+    if (__syncthreads_or(prior_fault)) return; // taken by the whole CTA
     if (Tn <= 0) return;
     if (Tn > max_T || o < 0 || o + Tn > N) {
         if (threadIdx.x == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, -1, Tn);
@@ -134,8 +135,9 @@ __global__ void __launch_bounds__(kThreads) simt_solve_kernel(
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
     const int c0 = blockIdx.y * kTileV;
-    if (faulted(st)) return;
+    const bool prior_fault = faulted(st);
     const int o = offsets[b], Tn = offsets[b + 1] - o;
+    if (__syncthreads_or(prior_fault)) return; // taken by the whole CTA
     if (Tn <= 0 || Tn > max_T || o < 0 || o + Tn > N) return; // reported by the producer
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool col_ok = c0 + lane < dv;
@@ -238,10 +240,11 @@ __global__ void __launch_bounds__(kThreads) simt_commit_kernel(
     k += layer * k_ls;
     U += layer * u_ls;
     logP += layer * lp_ls;
-    if (faulted(st)) return;
+    const bool prior_fault = faulted(st);
     const int a = accepted[b];
-    if (a < 0) return;
     const int o = offsets[b], Tn = offsets[b + 1] - o;
+    if (__syncthreads_or(prior_fault)) return; // taken by the whole CTA
+    if (a < 0) return;
     if (a >= Tn || o < 0 || o + Tn > N || Tn > kMaxTree) {
         if (threadIdx.x == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, Tn);
         return;

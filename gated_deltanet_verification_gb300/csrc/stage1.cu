@@ -16,6 +16,7 @@
 // products read shared memory.  No tensor-core work.
 #include "common.cuh"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace bole {
 namespace {
@@ -136,22 +137,25 @@ __device__ __forceinline__ float softplus(float x)
 
 // One CTA per (request, head, part), part 0 = q, 1 = k, 2 = v.  The CTA's
 // channel slice of every row it needs -- the request's T node rows and the
-// W-1 committed state rows -- arrives in shared memory by plain bulk copies
-// (one per row, 32..512 B, all in flight at once on one mbarrier), so each
-// row leaves DRAM once and the window products read shared memory.  The
+// W-1 committed state rows -- arrives in shared memory by TMA tiles (node
+// rows in boxes of 16, the state rows in one box, all on one mbarrier: a
+// handful of copies per CTA rather than one per row), so each row leaves
+// DRAM once and the window products read shared memory.  The
 // set-up reads (parent links, taps, bias, gate pre-activations) are issued
 // together, one item per thread (T, n <= 128 = the block).  Each warp pass
 // takes two nodes, 16 lanes per node and eight channels per lane.  The v
 // CTAs also form the gates.
 //   window[i][d], d = 0..W-1: the shared-memory row of the token at distance
-//   d before node i (d = 0 is i itself): row = node index < T, or T + s for
-//   state row s.
+//   d before node i (d = 0 is i itself): row = node index < T, or Tpad + s
+//   for state row s (Tpad = T rounded up to the 16-row box).
 constexpr uint64_t kS1WaitNs = 200ull * 1000 * 1000;
+constexpr int kRowBox = 16;          // node rows per TMA box
 static_assert(kS1Threads >= kMaxTree && kS1Threads >= kMaxChan, "one set-up item per thread");
 
 template <typename T, int MAXW>
 __global__ void __launch_bounds__(kS1Threads)
-conv_gates_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
+conv_gates_kernel(const __grid_constant__ CUtensorMap tmXqk, const __grid_constant__ CUtensorMap tmXv,
+                  const __grid_constant__ CUtensorMap tmCqk, const __grid_constant__ CUtensorMap tmCv,
                   const float *__restrict__ conv_w, const float *__restrict__ conv_b,
                   const float *__restrict__ ga, const float *__restrict__ gb,
                   const float *__restrict__ gate_scale, const float *__restrict__ gate_bias,
@@ -160,7 +164,7 @@ conv_gates_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
                   T *__restrict__ v, float *__restrict__ gamma, float *__restrict__ beta,
                   int32_t *st)
 {
-    extern __shared__ __align__(16) uint8_t rows_raw[]; // [max_T + W - 1][n] elements
+    extern __shared__ __align__(16) uint8_t rows_raw[]; // [Tpad(max_T) + W - 1][n] elements
     __shared__ int32_t spar[kMaxTree];
     __shared__ int32_t window[kMaxTree][MAXW];
     __shared__ __align__(16) float wts[MAXW][kMaxChan]; // tap-major
@@ -170,42 +174,43 @@ conv_gates_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
 
     const int unit = blockIdx.x, b = unit / H, h = unit % H, part = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (faulted(st)) return;
-    const int o = offsets[b], Tn = offsets[b + 1] - o;
-    if (Tn <= 0) return;
-    if (Tn > max_T || o < 0 || o + Tn > N) {
-        if (tid == 0 && h == 0 && part == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, -1, Tn);
-        return;
-    }
-    const int C = H * (2 * dk + dv);
     const int n = part < 2 ? dk : dv;
     const int cb = part == 0 ? h * dk : part == 1 ? (H + h) * dk : 2 * H * dk + h * dv;
-    T *rows = reinterpret_cast<T *>(rows_raw);
-    const int nrows = Tn + W - 1;
-    const uint32_t row_bytes = (uint32_t)n * sizeof(T);
-    if (tid == 0) {
-        bad = 0;
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (warp == 0) {
-        if (lane == 0) mbar_arrive_expect_tx(&bar, (uint32_t)nrows * row_bytes);
-        __syncwarp();
-        for (int r = lane; r < nrows; r += 32) {
-            const T *src = r < Tn ? x + (size_t)(o + r) * C + cb
-                                  : conv_state + ((size_t)b * (W - 1) + (r - Tn)) * C + cb;
-            bulk_load(rows + (size_t)r * n, src, row_bytes, &bar);
-        }
-    }
-    // set-up reads, all in flight together: thread tid = node tid, channel tid
-    const bool has_node = tid < Tn, has_chan = tid < n;
-    const int par_t = has_node ? parent[o + tid] : 0;
+    // One round trip for what needs nothing else: the status word, the
+    // request's extent and this slice's taps and bias (thread = channel).
+    // The exit on an earlier failure is taken by the whole CTA.
+    const bool has_chan = tid < n;
     float wv[MAXW];
 #pragma unroll
     for (int t = 0; t < MAXW; ++t)
         wv[t] = (has_chan && t < W) ? conv_w[(size_t)(cb + tid) * W + t] : 0.f;
     const float bv = (has_chan && conv_b) ? conv_b[cb + tid] : 0.f;
+    const bool prior_fault = faulted(st);
+    const int o = offsets[b], Tn = offsets[b + 1] - o;
+    if (__syncthreads_or(prior_fault)) return;
+    if (Tn <= 0) return;
+    if (Tn > max_T || o < 0 || o + Tn > N) {
+        if (tid == 0 && h == 0 && part == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, -1, Tn);
+        return;
+    }
+    // TMA destinations 128-byte aligned (the launch adds the slack)
+    T *rows = reinterpret_cast<T *>((reinterpret_cast<uintptr_t>(rows_raw) + 127) & ~(uintptr_t)127);
+    const int Tpad = (Tn + kRowBox - 1) / kRowBox * kRowBox;
+    const uint32_t row_bytes = (uint32_t)n * sizeof(T);
+    if (tid == 0) {
+        bad = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        const CUtensorMap *mx = part < 2 ? &tmXqk : &tmXv;
+        mbar_arrive_expect_tx(&bar, (uint32_t)(Tpad + W - 1) * row_bytes);
+        for (int r0 = 0; r0 < Tn; r0 += kRowBox) // rows past N arrive as zeros
+            tma_load_2d(rows + (size_t)r0 * n, mx, &bar, cb, o + r0);
+        if (W > 1)
+            tma_load_2d(rows + (size_t)Tpad * n, part < 2 ? &tmCqk : &tmCv, &bar, cb, b * (W - 1));
+    }
+    // request reads, in flight together with the rows: thread tid = node tid
+    const bool has_node = tid < Tn;
+    const int par_t = has_node ? parent[o + tid] : 0;
     const bool gates = part == 2 && has_node;
     const size_t nh_t = (size_t)(o + tid) * H + h;
     const float av = gates ? ga[nh_t] : 0.f, bgv = gates ? gb[nh_t] : 0.f;
@@ -237,7 +242,7 @@ conv_gates_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
             j = pj;
         }
         if (j < 0)
-            for (int s = W - 2; d < W; ++d, --s) window[tid][d] = Tn + s;
+            for (int s = W - 2; d < W; ++d, --s) window[tid][d] = Tpad + s;
     }
     __syncthreads();
     const bool ok = mbar_wait(&bar, 0, kS1WaitNs); // the copies end even when unused
@@ -310,10 +315,11 @@ conv_commit_kernel(T *__restrict__ conv_state, const T *__restrict__ x,
     __shared__ int32_t spar[kMaxTree];
     __shared__ int ok;
     const int b = blockIdx.y;
-    if (faulted(st)) return;
+    const bool prior_fault = faulted(st); // one round trip with the request's reads
     const int a = accepted[b];
-    if (a < 0) return;
     const int o = offsets[b], Tn = offsets[b + 1] - o;
+    if (__syncthreads_or(prior_fault)) return; // taken by the whole CTA
+    if (a < 0) return;
     if (a >= Tn || o < 0 || o + Tn > N || Tn > kMaxTree) {
         if (threadIdx.x == 0 && blockIdx.x == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, a, Tn);
         return;
@@ -365,18 +371,51 @@ conv_commit_kernel(T *__restrict__ conv_state, const T *__restrict__ x,
 
 size_t conv_rows_bytes(const ConvGatesArgs &a, size_t elem)
 {
-    return (size_t)(a.max_T + a.W - 1) * (size_t)(a.dk > a.dv ? a.dk : a.dv) * elem;
+    const size_t tpad = (size_t)(a.max_T + kRowBox - 1) / kRowBox * kRowBox;
+    return (tpad + a.W - 1) * (size_t)(a.dk > a.dv ? a.dk : a.dv) * elem + 128; // + alignment
+}
+
+// rows x C row-major (x: N rows, the convolution state: B (W-1) rows) as a
+// 2-D tensor whose boxes are `cols` channels x `box_rows` rows
+cudaError_t make_rows_map(CUtensorMap *map, const void *base, bole_dtype dt, int C, int rows,
+                          int cols, int box_rows)
+{
+    auto fn = tc::encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const size_t es = dt == BOLE_BF16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)C * es};
+    cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt == BOLE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <typename T, int MAXW> cudaError_t conv_gates_typed(const ConvGatesArgs &a, cudaStream_t s)
 {
     const size_t smem = conv_rows_bytes(a, sizeof(T));
+    const int C = a.H * (2 * a.dk + a.dv);
+    CUtensorMap xqk, xv, cqk, cv;
+    cudaError_t e = make_rows_map(&xqk, a.x, a.dtype, C, a.N, a.dk, kRowBox);
+    if (e == cudaSuccess) e = make_rows_map(&xv, a.x, a.dtype, C, a.N, a.dv, kRowBox);
+    if (e == cudaSuccess && a.W > 1) {
+        e = make_rows_map(&cqk, a.conv_state, a.dtype, C, a.B * (a.W - 1), a.dk, a.W - 1);
+        if (e == cudaSuccess)
+            e = make_rows_map(&cv, a.conv_state, a.dtype, C, a.B * (a.W - 1), a.dv, a.W - 1);
+    } else {
+        cqk = xqk; // unused: no state rows
+        cv = xv;
+    }
+    if (e != cudaSuccess) return e;
     auto kernel = conv_gates_kernel<T, MAXW>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kernel<<<dim3(a.B * a.H, 3), kS1Threads, smem, s>>>(
-        static_cast<const T *>(a.x), static_cast<const T *>(a.conv_state), a.conv_w, a.conv_b,
+        xqk, xv, cqk, cv, a.conv_w, a.conv_b,
         a.a, a.b, a.gate_scale, a.gate_bias, a.offsets, a.parent, a.H, a.dk, a.dv, a.N, a.W,
         a.max_T, static_cast<T *>(a.q), static_cast<T *>(a.k), static_cast<T *>(a.v), a.gamma,
         a.beta, a.st);

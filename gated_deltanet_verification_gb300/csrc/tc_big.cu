@@ -102,7 +102,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     const int fault = *(const volatile int32_t *)st;
     const int o = offsets[b], T = offsets[b + 1] - o, d = req_depth[b];
-    if (fault != 0 || T <= 0) return;
+    if (__syncthreads_or(fault != 0) || T <= 0) return; // taken by the whole CTA
     if (T > kTB || o < 0 || o + T > N || d < 0 || d >= T) {
         if (tid == 0 && h == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, -1, T);
         return;
@@ -363,7 +363,8 @@ tc_big_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     }
     const int fault = *(const volatile int32_t *)st;
     const int o = offsets[b], T = offsets[b + 1] - o;
-    if (fault != 0 || T <= 0 || T > kTB || o < 0 || o + T > N) return; // the factor kernel reported
+    if (__syncthreads_or(fault != 0) || T <= 0 || T > kTB || o < 0 || o + T > N)
+        return; // taken by the whole CTA; the factor kernel reported a bad tree
     const int nch = (T + 31) / 32; // [M; W] chunks of 32 nodes
     if (tid == kSBCompute) {
         for (int k = BS_S; k <= BS_MMA2; ++k) mbar_init(&bar[k], 1);
