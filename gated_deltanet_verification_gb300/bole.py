@@ -187,7 +187,8 @@ def tree_verify(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_de
     _check(lib().bole_tree_verify(
         _ptr(S_pre), _ptr(q), _ptr(k), _ptr(v), code, _ptr(gamma), _ptr(beta), _ptr(offsets),
         _ptr(parent), _ptr(depth), _ptr(anc), _ptr(req_depth), B, H, dk, dv, N, int(max_T),
-        int(max_depth), _ptr(O), _ptr(U), _ptr(logP), _ptr(workspace), workspace.numel(),
+        int(max_depth), _ptr(O), _ptr(U), _ptr(logP), _ptr(workspace),
+        workspace.numel() * workspace.element_size(),
         _ptr(status), int(flags), _stream(stream)), "bole_tree_verify")
     return O, U, logP
 
@@ -262,7 +263,8 @@ def select_forest(p, cand_offsets, cand_parent, budget: int, *, caps=None, offse
     status = new_status(dev) if status is None else status
     _check(lib().bole_select_forest(
         _ptr(p), _ptr(cand_offsets), _ptr(cand_parent), _ptr(caps), B, M, int(budget),
-        _ptr(offsets), _ptr(parent), _ptr(src), _ptr(rho), _ptr(workspace), workspace.numel(),
+        _ptr(offsets), _ptr(parent), _ptr(src), _ptr(rho), _ptr(workspace),
+        workspace.numel() * workspace.element_size(),
         _ptr(status), int(flags), _stream(stream)), "bole_select_forest")
     return offsets, parent, src, rho, status
 

@@ -33,7 +33,7 @@ size_t verify_workspace(const VerifyArgs &a, unsigned flags)
 {
     switch (verify_path(a, flags)) {
     case VerifyPath::Fused: return tc_workspace_bytes(a.B, a.H, a.max_T);
-    case VerifyPath::Big: return tc_big_workspace_bytes(a.B, a.H);
+    case VerifyPath::Big: return 0; // [M; W] stays on chip
     default: return simt_workspace_bytes(a.B, a.H, a.max_T);
     }
 }
@@ -119,7 +119,8 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     a.gamma = gamma; a.beta = beta;
     a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
-    a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.st = dev_status;
+    a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.ws_bytes = workspace ? workspace_bytes : 0;
+    a.st = dev_status;
     a.vk = (flags & BOLE_FLAG_STATE_VK) != 0;
 
     const VerifyPath path = verify_path(a, flags);
@@ -169,7 +170,8 @@ bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const vo
     a.gamma = gamma; a.beta = beta;
     a.offsets = offsets; a.parent = parent; a.depth = depth; a.anc = anc; a.req_depth = req_depth;
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
-    a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.st = dev_status; a.vk = false;
+    a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.ws_bytes = 0; a.st = dev_status;
+    a.vk = false;
     return from_cuda(launch_simt_verify_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -68,6 +68,7 @@ struct VerifyArgs {
     void *O;
     float *U, *logP;
     void *ws;
+    size_t ws_bytes;
     int32_t *st;
     bool vk; // state stored [B, H, dv, dk] (BOLE_FLAG_STATE_VK)
 };

@@ -2,8 +2,8 @@
 // 128, up to 128 nodes, any depth up to 127): the shapes the single-CTA
 // kernel's compact, depth-indexed factors cannot hold.
 //
-// Two kernels per call, one CTA per (request, head) each:
-//   1. factor: the Gram [Q;K] K^T on tcgen05, the dense ancestor-masked
+// One kernel, one CTA per (request, head), one CTA per SM:
+//   1. factors: the Gram [Q;K] K^T on tcgen05, the dense ancestor-masked
 //      C_ij = exp(L_i - L_j) q_i.k_j and G_ij = beta_i exp(L_i - L_j) k_i.k_j
 //      (Lemma 1, Lemma 2), then W = (I+G)^{-1} and M = C W by log-depth
 //      doubling: G is nilpotent with G^{d+1} = 0 (Lemma 3), so
@@ -13,11 +13,12 @@
 //      of 127 steps).  Each level squares P = G^(2^(k-1)) and multiplies W and
 //      M by (I + P); every product is one 128 x 128 x 128 tcgen05 kind::tf32
 //      MMA with A read from tensor memory and B (the transposed P) from
-//      shared memory.  [M; W] (256 x 128 fp32) goes to the workspace.
+//      shared memory.  S_pre streams in meanwhile.
 //   2. solve: S_pre split exactly into bf16 S_hi + S_lo, the state products
 //      Q S_pre and K S_pre on tcgen05, R = D_beta (V - D_P K S_pre) as R^T in
-//      shared memory, and the propagation [M; W] R streamed from the workspace
-//      in chunks of 32 nodes; O = D_P Q S_pre + M R (Eq. (6)), U = W R.
+//      shared memory, and the propagation with M and W read from tensor
+//      memory as A operands: O = D_P Q S_pre + M R (Eq. (6)), U = W R.
+// No factor leaves the SM (a caller may ask for a copy of [M; W]).
 #include "common.cuh"
 #include "sm100.cuh"
 #include "tc_common.cuh"
@@ -46,25 +47,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
                  : "memory");
 }
 
-// =====================================================================
-// factor kernel
-// =====================================================================
-// Shared memory: [Q;K] (64 KB: Q then K, each two 128B-swizzled boxes of
-// [128 rows x 64 bf16]); once the Gram is done the same 64 KB hold the
-// transposed B operand of the doubling (128 rows n x 128 k fp32, K-major,
-// four 32-column atoms of 16 KB).  Tensor memory (512 columns): R0 = C, then
-// M; R1 and R3 the powers P (ping-pong) and the products; R2 = W.
-constexpr int FB_QK = 0;
-constexpr int FB_L = 65536;             // L_i
-constexpr int FB_BETA = FB_L + 512;     // beta_i
-constexpr int FB_LG = FB_BETA + 512;    // log gamma_i
-constexpr int FB_MASK = FB_LG + 512;    // uint4 ancestor-or-self masks
-constexpr int FB_BAR = FB_MASK + 2048;  // TMA, MMA
-constexpr int FB_MISC = FB_BAR + 16;    // TMEM slot
-constexpr int FB_END = FB_MISC + 16;
-constexpr int FB_SMEM = FB_END + 1024;
-constexpr int kFBThreads = 256;
-
 // B operand, K-major tf32: element (row n, k) of a 128 x 128 matrix stored in
 // four 16 KB atoms of 32 k.
 __device__ __forceinline__ uint32_t kmaj_offset(int n, int k)
@@ -72,32 +54,66 @@ __device__ __forceinline__ uint32_t kmaj_offset(int n, int k)
     return (uint32_t)(k >> 5) * 16384u + sw128_offset(n, k & 31);
 }
 
-__global__ void __launch_bounds__(kFBThreads, 1)
-tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const float *__restrict__ gamma, const float *__restrict__ beta,
-                     const int32_t *__restrict__ offsets, const int32_t *__restrict__ depth_g,
-                     const uint32_t *__restrict__ anc_g, const int32_t *__restrict__ req_depth,
-                     int H, int N, float *__restrict__ logP, float *__restrict__ mw,
-                     int32_t *st)
+// =====================================================================
+// fused kernel: the factors and the solve in one CTA, [M; W] kept on chip
+// =====================================================================
+// The factor phase is the factor kernel's (Gram, dense C and G, log-depth
+// doubling), with the transposed power in a buffer of its own so that [Q;K]
+// survives for the state products; S_pre is requested at entry and lands
+// while the doubling runs.  M and W then stay in tensor memory as the A
+// operands of the propagation (tcgen05 kind::tf32 with A from tensor memory),
+// so no factor leaves the SM.
+// Shared memory (1 CTA per SM, ~197 KB):
+//   QK (64 KB): Q then K (two 128B-swizzled boxes of [128 rows x 64 bf16] each).
+//   PB (64 KB): the transposed power (tf32 K-major, four 32-column atoms);
+//     after the last doubling product, the value rows (two boxes).
+//   SB (64 KB): S_pre, split in place into bf16 hi/lo; after the state
+//     products R^T (tf32 K-major, four 32-node atoms).
+// Tensor memory (512 columns): R0 = C, then M; R1 = G and powers, then
+// P Q S_pre and finally O; R2 = W; R3 = products and powers, then K S_pre,
+// then U.
+constexpr int FU_QK = 0;
+constexpr int FU_PB = 65536;
+constexpr int FU_SB = 131072;
+constexpr int FU_L = 196608;            // L_i
+constexpr int FU_BETA = FU_L + 512;     // beta_i
+constexpr int FU_LG = FU_BETA + 512;    // log gamma_i
+constexpr int FU_MASK = FU_LG + 512;    // uint4 ancestor-or-self masks
+constexpr int FU_BAR = FU_MASK + 2048;  // [Q;K] TMA, MMA, S TMA, V TMA
+constexpr int FU_MISC = FU_BAR + 32;    // TMEM slot
+constexpr int FU_END = FU_MISC + 16;
+constexpr int FU_SMEM = FU_END + 1024;
+static_assert(FU_SMEM <= 227 * 1024, "one fused CTA fits an SM");
+constexpr int kFUThreads = 256;
+
+template <bool VK>
+__global__ void __launch_bounds__(kFUThreads, 1)
+tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const float *__restrict__ gamma, const float *__restrict__ beta,
+                    const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc_g,
+                    const int32_t *__restrict__ req_depth, int H, int N,
+                    __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
+                    float *__restrict__ logP, float *__restrict__ mw, int32_t *st)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sQK = sm + FB_QK;
-    float *Ls = reinterpret_cast<float *>(sm + FB_L);
-    float *Bs = reinterpret_cast<float *>(sm + FB_BETA);
-    float *LGs = reinterpret_cast<float *>(sm + FB_LG);
-    uint4 *Ms = reinterpret_cast<uint4 *>(sm + FB_MASK);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + FB_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FB_MISC);
+    uint8_t *sQK = sm + FU_QK, *sPB = sm + FU_PB, *sS = sm + FU_SB;
+    float *Ls = reinterpret_cast<float *>(sm + FU_L);
+    float *Bs = reinterpret_cast<float *>(sm + FU_BETA);
+    float *LGs = reinterpret_cast<float *>(sm + FU_LG);
+    uint4 *Ms = reinterpret_cast<uint4 *>(sm + FU_MASK);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + FU_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FU_MISC);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, b = unit / H, h = unit % H;
     const int q = warp & 3, hf = warp >> 2;
-    const int m = q * 32 + lane; // TMEM lane = matrix row
+    const int m = q * 32 + lane; // TMEM lane = matrix row = node
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
-    if (sm + FB_END > smem_raw + FB_SMEM) {
-        if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -2);
+    if (sm + FU_END > smem_raw + FU_SMEM) {
+        if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -4);
         return;
     }
     const int fault = *(const volatile int32_t *)st;
@@ -108,8 +124,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         return;
     }
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&bar[0], 65536);
 #pragma unroll
@@ -117,6 +132,9 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tma_load_3d(sQK + ka * 16384, &tmQ, &bar[0], 64 * ka, h, o);
             tma_load_3d(sQK + 32768 + ka * 16384, &tmK, &bar[0], 64 * ka, h, o);
         }
+        mbar_arrive_expect_tx(&bar[2], 65536); // the state, landing during the doubling
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_load_2d(sS + c * 16384, &tmS, &bar[2], 32 * c, unit * kD);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -164,10 +182,10 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
 
     // Gram: Q K^T -> R0, K K^T -> R1 (bf16 products, fp32 accumulation)
+    const uint32_t qa = smem_addr(sQK), ka = qa + 32768;
     if (tid == 0) {
         ok &= mbar_wait(&bar[0], 0, kWaitNs);
         tc_fence_after();
-        const uint32_t qa = smem_addr(sQK), ka = qa + 32768;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -184,7 +202,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     __syncwarp();
 
     // Dense C (R0, in place), G (R1, in place), W0 = I - G (R2) and G^T as the
-    // B operand (the [Q;K] buffer is free: the Gram has read it).
+    // B operand of the doubling.
     {
         const uint4 mk = Ms[m];
         const uint32_t w[4] = {mk.x, mk.y, mk.z, mk.w};
@@ -192,7 +210,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
             const int j0 = hf * 64 + cc * 32;
-            const uint32_t bits = w[j0 >> 5]; // ancestors-or-self among columns j0..j0+31
+            const uint32_t bits = w[j0 >> 5];
             float x[32], y[32];
             tmem_ld32(R0 + lane_base + j0, x);
             tmem_ld32(R1 + lane_base + j0, y);
@@ -203,7 +221,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const float r = anc ? __expf(Lm - Ls[j]) : 0.f;
                 x[t] = r * x[t];                               // C
                 y[t] = (anc && j != m) ? bm * r * y[t] : 0.f;  // G
-                *reinterpret_cast<float *>(sQK + kmaj_offset(j, m)) = y[t]; // G^T: row j, k = m
+                *reinterpret_cast<float *>(sPB + kmaj_offset(j, m)) = y[t]; // G^T
             }
             tmem_st32(R0 + lane_base + j0, x);
             tmem_st32(R1 + lane_base + j0, y);
@@ -212,9 +230,8 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tmem_st32(R2 + lane_base + j0, y);
         }
     }
-    const uint32_t bq = smem_addr(sQK);
-    // One 128 x 128 x 128 product D = A(tmem) B(smem: transposed, K-major).
-    auto product = [&](uint32_t d_reg, uint32_t a_reg) {
+    const uint32_t pb = smem_addr(sPB);
+    auto product = [&](uint32_t d_reg, uint32_t a_reg) { // D = A(tmem) B(PB), 128^3
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -224,8 +241,8 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
                 mma_tf32_ts(d_reg, a_reg + 8 * kk,
-                            sdesc_sw128(bq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), IDESC_T128,
-                            kk > 0);
+                            sdesc_sw128(pb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                            IDESC_T128, kk > 0);
             mma_commit(&bar[1]);
         }
         ok &= mbar_wait(&bar[1], mph, kWaitNs);
@@ -233,8 +250,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tc_fence_after();
         __syncwarp();
     };
-    // dst = dst + sign * src, row m, this thread's 64 columns
-    auto accumulate = [&](uint32_t dst, uint32_t src, float sign) {
+    auto accumulate = [&](uint32_t dst, uint32_t src, float sign) { // dst += sign src
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
             const int j0 = hf * 64 + cc * 32;
@@ -246,16 +262,14 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tmem_st32(dst + lane_base + j0, x);
         }
     };
-    // M0 = C - C G
+    // M0 = C - C G; levels: P <- P^2, W <- W + W P, M <- M + M P
     product(R3, R0);
     accumulate(R0, R3, -1.f);
-    // levels: P <- P^2, W <- W + W P, M <- M + M P
     int K = 0;
     while ((2 << K) <= d) ++K; // K = floor(log2 d) for d >= 1, 0 otherwise
     uint32_t Pp = R1, Pq = R3;
     for (int lev = 1; lev <= K; ++lev) {
-        product(Pq, Pp); // B still holds P^T of the previous power
-        // transpose the new power into the B operand
+        product(Pq, Pp);
         tmem_wait_st();
         tc_fence_before();
         __syncthreads(); // every thread is done with the previous B
@@ -267,7 +281,7 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tmem_ld32(Pq + lane_base + j0, x);
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-                *reinterpret_cast<float *>(sQK + kmaj_offset(j0 + t, m)) = x[t];
+                *reinterpret_cast<float *>(sPB + kmaj_offset(j0 + t, m)) = x[t];
         }
         product(Pp, R2); // W P
         accumulate(R2, Pp, 1.f);
@@ -279,10 +293,14 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
     tmem_wait_st();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads(); // M (R0) and W (R2) final; the PB buffer is free
     tc_fence_after();
-    // [M; W] rows to the workspace: unit-major, 256 rows of 128 fp32
-    {
+    if (tid == 0) { // the value rows into the freed PB buffer
+        mbar_arrive_expect_tx(&bar[3], 32768);
+        tma_load_3d(sPB, &tmV, &bar[3], 0, h, o);
+        tma_load_3d(sPB + 16384, &tmV, &bar[3], 64, h, o);
+    }
+    if (mw) { // optional copy of [M; W] for inspection: unit-major, 256 rows of 128
         float *rowM = mw + ((size_t)unit * 256 + m) * kTB;
         float *rowW = mw + ((size_t)unit * 256 + 128 + m) * kTB;
 #pragma unroll 1
@@ -301,288 +319,153 @@ tc_big_factor_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
         }
     }
-    if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 20);
+    // S_pre = S_hi + S_lo in place: thread = (row r, column half pc)
+    ok &= mbar_wait(&bar[2], 0, kWaitNs);
+    {
+        const int r = tid & 127, pc = tid >> 7;
+        uint8_t *box0 = sS + (2 * pc) * 16384, *box1 = box0 + 16384;
+        float x[64];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(box0 + sw128_chunk(r, c));
+            const float4 a1 = *reinterpret_cast<const float4 *>(box1 + sw128_chunk(r, c));
+            x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z; x[4 * c + 3] = a0.w;
+            x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
+            x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                const float2 hfv = __bfloat1622float2(h2);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hfv.x, x1 - hfv.y);
+                hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
+                lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+            }
+            *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
-
-// =====================================================================
-// solve kernel
-// =====================================================================
-// Shared memory (1 CTA per SM):
-//   SB (64 KB): S_pre fp32 (four 128B-swizzled boxes of 32 columns), split in
-//     place into bf16 hi/lo; after the state products R^T (tf32 K-major,
-//     128 rows n x 128 k, four 32-column atoms).
-//   QK (64 KB): Q then K (two boxes of [128 rows x 64 bf16] each); after the
-//     state products two 32 KB buffers of [M; W] chunks (256 rows x 32 k).
-//   V (32 KB): the value rows, two boxes of [128 rows x 64 bf16].
-// Tensor memory (512 columns): Q S_pre, K S_pre, M R, W R.
-constexpr int SB_S = 0;
-constexpr int SB_QK = 65536;
-constexpr int SB_V = SB_QK + 65536;
-constexpr int SB_P = SB_V + 32768;      // P_i
-constexpr int SB_BETA = SB_P + 512;     // beta_i
-constexpr int SB_BAR = SB_BETA + 512;   // mbarriers
-constexpr int SB_MISC = SB_BAR + 16 * 8;
-constexpr int SB_END = SB_MISC + 16;
-constexpr int SB_SMEM = SB_END + 1024;
-constexpr int kSBCompute = 256;
-constexpr int kSBThreads = kSBCompute + 32;
-constexpr int BS_S = 0, BS_QK = 1, BS_V = 2, BS_STATE = 3, BS_MW0 = 4, BS_MW1 = 5, BS_DONE0 = 6,
-              BS_DONE1 = 7, BS_MMA2 = 8, BS_CONV = 9, BS_OPS = 10;
-
-// VK: the state is stored transposed ([dv][dk] per head, the slot layout);
-// the same boxes and split then hold K-major operand rows (row = value
-// column), read 32 B further along the rows per 16 d_k.
-template <bool VK>
-__global__ void __launch_bounds__(kSBThreads, 1)
-tc_big_solve_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
-                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmMW, const float *__restrict__ beta,
-                    const int32_t *__restrict__ offsets, const float *__restrict__ logP, int H,
-                    int N, __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout, int32_t *st)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align1024(smem_raw);
-    uint8_t *sS = sm + SB_S;
-    uint8_t *sQK = sm + SB_QK;
-    uint8_t *sV = sm + SB_V;
-    float *Ps = reinterpret_cast<float *>(sm + SB_P);
-    float *Bs = reinterpret_cast<float *>(sm + SB_BETA);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SB_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SB_MISC);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x, b = unit / H, h = unit % H;
-    if (sm + SB_END > smem_raw + SB_SMEM) {
-        if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -3);
-        return;
-    }
-    const int fault = *(const volatile int32_t *)st;
-    const int o = offsets[b], T = offsets[b + 1] - o;
-    if (__syncthreads_or(fault != 0) || T <= 0 || T > kTB || o < 0 || o + T > N)
-        return; // taken by the whole CTA; the factor kernel reported a bad tree
-    const int nch = (T + 31) / 32; // [M; W] chunks of 32 nodes
-    if (tid == kSBCompute) {
-        for (int k = BS_S; k <= BS_MMA2; ++k) mbar_init(&bar[k], 1);
-        mbar_init(&bar[BS_CONV], kSBCompute);
-        mbar_init(&bar[BS_OPS], kSBCompute);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bar[BS_QK], 65536);
+    // state products: Q S_pre -> R1, K S_pre -> R3 (S = S_hi + S_lo)
+    const uint32_t s0 = smem_addr(sS);
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t slo = s0 + 16384;
+        constexpr uint32_t idesc_s = VK ? IDESC_S128_VK : IDESC_S128;
 #pragma unroll
-        for (int ka = 0; ka < 2; ++ka) {
-            tma_load_3d(sQK + ka * 16384, &tmQ, &bar[BS_QK], 64 * ka, h, o);
-            tma_load_3d(sQK + 32768 + ka * 16384, &tmK, &bar[BS_QK], 64 * ka, h, o);
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint32_t boff = VK ? (kk >> 2) * 32768 + (kk & 3) * 32 : kk * 2048;
+            const uint32_t lbo = VK ? 16 : 32768;
+            const uint64_t bh = sdesc_sw128(s0 + boff, lbo, 1024);
+            const uint64_t bl = sdesc_sw128(slo + boff, lbo, 1024);
+            const uint64_t aq = sdesc_sw128(qa + off, 16, 1024);
+            const uint64_t ak = sdesc_sw128(ka + off, 16, 1024);
+            mma_bf16_ss(R1, aq, bh, idesc_s, kk > 0);
+            mma_bf16_ss(R1, aq, bl, idesc_s, 1);
+            mma_bf16_ss(R3, ak, bh, idesc_s, kk > 0);
+            mma_bf16_ss(R3, ak, bl, idesc_s, 1);
         }
-        mbar_arrive_expect_tx(&bar[BS_S], 65536);
+        mma_commit(&bar[1]);
+    }
+    ok &= mbar_wait(&bar[1], mph, kWaitNs);
+    mph ^= 1u;
+    ok &= mbar_wait(&bar[3], 0, kWaitNs); // the value rows
+    tc_fence_after();
+    __syncwarp();
+    // R^T = (beta (v - P K S_pre))^T over the dead state buffer, and P Q S_pre
+    // in place, so that the propagation accumulates O onto it
+    {
+        const int i = m;
+        const bool live = i < T;
+        const float p = live ? expf(Ls[i]) : 0.f, bt = Bs[i];
+        const uint8_t *vrow = sPB + hf * 16384 + i * 128; // columns 64 hf .. 64 hf + 63
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            const int col0 = hf * 64 + cc * 32;
+            float x[32];
+            tmem_ld32(R3 + lane_base + col0, x);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tma_load_2d(sS + c * 16384, &tmS, &bar[BS_S], 32 * c, unit * kD);
-        mbar_arrive_expect_tx(&bar[BS_V], 32768);
-        tma_load_3d(sV, &tmV, &bar[BS_V], 0, h, o);
-        tma_load_3d(sV + 16384, &tmV, &bar[BS_V], 64, h, o);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                  vrow + (((cc * 4 + q4) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int n = col0 + 8 * q4 + t;
+                    const float r = live ? bt * (f[t] - p * x[8 * q4 + t]) : 0.f;
+                    *reinterpret_cast<float *>(sS + (i >> 5) * 16384 + sw128_offset(n, i & 31)) = r;
+                }
+            }
+            tmem_ld32(R1 + lane_base + col0, x);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] *= p;
+            tmem_st32(R1 + lane_base + col0, x);
+        }
     }
-    if (tid < kTB) {
-        const int i = tid;
-        Ps[i] = (i < T) ? expf(logP[(size_t)(o + i) * H + h]) : 0.f;
-        Bs[i] = (i < T) ? beta[(size_t)(o + i) * H + h] : 0.f;
-    }
-    if (warp == 0) {
-        tmem_alloc(tslot, 512);
-        tmem_relinquish();
-    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    // propagation + read-out over the tree's node steps: R1 += M R (O), R3 = W R (U)
+    if (tid == 0) {
+        tc_fence_after();
+        const int nk = (T + 7) / 8;
+        for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t bd = sdesc_sw128(s0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            mma_tf32_ts(R1, R0 + 8 * kk, bd, IDESC_T128, 1);
+            mma_tf32_ts(R3, R2 + 8 * kk, bd, IDESC_T128, kk > 0);
+        }
+        mma_commit(&bar[1]);
+    }
+    ok &= mbar_wait(&bar[1], mph, kWaitNs);
+    mph ^= 1u;
     tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
-
-    if (warp == kSBCompute / 32) {
-        // =========================== issue warp ===========================
-        bool ok = true;
-        if (lane == 0) {
-            const uint32_t s0 = smem_addr(sS), qa = smem_addr(sQK), ka = qa + 32768;
-            ok &= mbar_wait(&bar[BS_QK], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BS_CONV], 0, kWaitNs);
-            tc_fence_after();
-            // Q S_pre -> R0, K S_pre -> R1 (S = S_hi + S_lo)
-            const uint32_t slo = s0 + 16384;
-            constexpr uint32_t idesc_s = VK ? IDESC_S128_VK : IDESC_S128;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint32_t boff = VK ? (kk >> 2) * 32768 + (kk & 3) * 32 : kk * 2048;
-                const uint32_t lbo = VK ? 16 : 32768;
-                const uint64_t bh = sdesc_sw128(s0 + boff, lbo, 1024);
-                const uint64_t bl = sdesc_sw128(slo + boff, lbo, 1024);
-                const uint64_t aq = sdesc_sw128(qa + off, 16, 1024);
-                const uint64_t ak = sdesc_sw128(ka + off, 16, 1024);
-                mma_bf16_ss(R0, aq, bh, idesc_s, kk > 0);
-                mma_bf16_ss(R0, aq, bl, idesc_s, 1);
-                mma_bf16_ss(R1, ak, bh, idesc_s, kk > 0);
-                mma_bf16_ss(R1, ak, bl, idesc_s, 1);
-            }
-            mma_commit(&bar[BS_STATE]);
-            // the [Q;K] buffer is free once the products are done: [M; W] chunks
-            ok &= mbar_wait(&bar[BS_STATE], 0, kWaitNs);
-            for (int c = 0; c < nch && c < 2; ++c) {
-                mbar_arrive_expect_tx(&bar[BS_MW0 + c], 32768);
-                tma_load_2d(sQK + c * 32768, &tmMW, &bar[BS_MW0 + c], 32 * c, unit * 256);
-            }
-            // propagation: D_O += M_c R_c, D_U += W_c R_c over the chunks
-            ok &= mbar_wait(&bar[BS_OPS], 0, kWaitNs);
-            tc_fence_after();
-            for (int c = 0; c < nch; ++c) {
-                const int bi = c & 1;
-                ok &= mbar_wait(&bar[BS_MW0 + bi], (uint32_t)(c >> 1) & 1u, kWaitNs);
-                tc_fence_after();
-                const uint32_t am = qa + bi * 32768, aw = am + 16384, rb = s0 + c * 16384;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = sdesc_sw128(rb + kk * 32, 16, 1024);
-                    mma_tf32_ss(R2, sdesc_sw128(am + kk * 32, 16, 1024), bd, IDESC_T128,
-                                (c > 0 || kk > 0));
-                    mma_tf32_ss(R3, sdesc_sw128(aw + kk * 32, 16, 1024), bd, IDESC_T128,
-                                (c > 0 || kk > 0));
-                }
-                mma_commit(&bar[BS_DONE0 + bi]);
-                if (c + 2 < nch) { // refill this buffer once its products are done
-                    ok &= mbar_wait(&bar[BS_DONE0 + bi], (uint32_t)(c >> 1) & 1u, kWaitNs);
-                    mbar_arrive_expect_tx(&bar[BS_MW0 + bi], 32768);
-                    tma_load_2d(sQK + bi * 32768, &tmMW, &bar[BS_MW0 + bi], 32 * (c + 2),
-                                unit * 256);
-                }
-            }
-            mma_commit(&bar[BS_MMA2]);
-        }
-        __syncwarp();
-        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 21);
-    } else {
-        // ========================== compute warps =========================
-        bool ok = true;
-        const int q = warp & 3, hf = warp >> 2;
-        const int i = q * 32 + lane; // TMEM lane = node
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        // S_pre = S_hi + S_lo in place: thread = (row r, column half pc)
-        ok &= mbar_wait(&bar[BS_S], 0, kWaitNs);
-        {
-            const int r = tid & 127, pc = tid >> 7;
-            uint8_t *box0 = sS + (2 * pc) * 16384, *box1 = box0 + 16384;
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(box0 + sw128_chunk(r, c));
-                const float4 a1 = *reinterpret_cast<const float4 *>(box1 + sw128_chunk(r, c));
-                x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z; x[4 * c + 3] = a0.w;
-                x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
-                x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-                    const float2 hfv = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hfv.x, x1 - hfv.y);
-                    hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
-                }
-                *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar[BS_CONV]);
-        // R^T = (beta (v - P K S_pre))^T, K-major tf32 over the dead S buffer
-        ok &= mbar_wait(&bar[BS_STATE], 0, kWaitNs);
-        ok &= mbar_wait(&bar[BS_V], 0, kWaitNs);
-        tc_fence_after();
-        __syncwarp();
-        {
-            const float p = Ps[i], bt = Bs[i];
-            const bool live = i < T;
-            const uint8_t *vrow = sV + hf * 16384 + i * 128; // columns 64 hf .. 64 hf + 63
+    __syncwarp();
+    {
+        const int i = m;
+        const bool store = ok && i < T;
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col0 = hf * 64 + cc * 32;
-                float x[32];
-                tmem_ld32(R1 + lane_base + col0, x);
+        for (int cc = 0; cc < 2; ++cc) {
+            const int col0 = hf * 64 + cc * 32;
+            float x[32], y[32];
+            tmem_ld32(R1 + lane_base + col0, x);
+            tmem_ld32(R3 + lane_base + col0, y);
+            if (!store) continue;
+            const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
+            uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    float f[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + (((cc * 4 + q4) ^ (i & 7)) << 4)), f);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                __nv_bfloat162 p2[4];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const int n = col0 + 8 * q4 + t;
-                        const float r = live ? bt * (f[t] - p * x[8 * q4 + t]) : 0.f;
-                        *reinterpret_cast<float *>(sS + (i >> 5) * 16384 + sw128_offset(n, i & 31)) = r;
-                    }
-                }
+                for (int t = 0; t < 4; ++t)
+                    p2[t] = __floats2bfloat162_rn(x[8 * q4 + 2 * t], x[8 * q4 + 2 * t + 1]);
+                dsto[q4] = *reinterpret_cast<uint4 *>(p2);
             }
+            float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bar[BS_OPS]);
-        // outputs: O = P (Q S_pre) + M R (bf16), U = W R (fp32)
-        ok &= mbar_wait(&bar[BS_MMA2], 0, kWaitNs);
-        tc_fence_after();
-        __syncwarp();
-        {
-            const float p = Ps[i];
-            const bool store = ok && i < T;
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int col0 = hf * 64 + cc * 32;
-                float x[32], y[32];
-                tmem_ld32(R2 + lane_base + col0, x);
-                tmem_ld32(R0 + lane_base + col0, y);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
-                tmem_ld32(R3 + lane_base + col0, y);
-                if (!store) continue;
-                const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
-                uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    __nv_bfloat162 p2[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        p2[t] = __floats2bfloat162_rn(x[8 * q4 + 2 * t], x[8 * q4 + 2 * t + 1]);
-                    dsto[q4] = *reinterpret_cast<uint4 *>(p2);
-                }
-                float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
-            }
+    }
+    if (!ok) {
+        report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
+        if (tid == 0) { // the copies still in flight end before the CTA does
+            mbar_wait(&bar[0], 0, kWaitNs);
+            mbar_wait(&bar[2], 0, kWaitNs);
+            mbar_wait(&bar[3], 0, kWaitNs);
         }
-        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 22);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
-// [M; W] of every unit as a 2-D fp32 tensor [units * 256 rows][128 cols],
-// boxes of 32 columns x 256 rows (one chunk of 32 nodes, M rows then W rows).
-cudaError_t make_mw_map(CUtensorMap *map, const float *mw, int units)
-{
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {(cuuint64_t)kTB, (cuuint64_t)units * 256};
-    cuuint64_t strides[1] = {(cuuint64_t)kTB * sizeof(float)};
-    cuuint32_t box[2] = {32, 256};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(mw), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 } // namespace
@@ -598,26 +481,22 @@ cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s)
 {
     const int units = a.B * a.H;
     if (units == 0 || a.N == 0) return cudaSuccess;
-    float *mw = static_cast<float *>(a.ws);
-    CUtensorMap mS, mQ, mK, mV, mMW;
+    CUtensorMap mS, mQ, mK, mV;
     cudaError_t e = make_state_map(&mS, a.S_pre, units);
     if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, kTB);
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kTB);
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kTB);
-    if (e == cudaSuccess) e = make_mw_map(&mMW, mw, units);
     if (e != cudaSuccess) return e;
-    e = configure_once(reinterpret_cast<const void *>(tc_big_factor_kernel), FB_SMEM, true, 2);
+    auto kernel = a.vk ? tc_big_fused_kernel<true> : tc_big_fused_kernel<false>;
+    e = configure_once(reinterpret_cast<const void *>(kernel), FU_SMEM, true, a.vk ? 11 : 10);
     if (e != cudaSuccess) return e;
-    tc_big_factor_kernel<<<units, kFBThreads, FB_SMEM, s>>>(mQ, mK, a.gamma, a.beta, a.offsets,
-                                                             a.depth, a.anc, a.req_depth, a.H, a.N,
-                                                             a.logP, mw, a.st);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    auto solve = a.vk ? tc_big_solve_kernel<true> : tc_big_solve_kernel<false>;
-    e = configure_once(reinterpret_cast<const void *>(solve), SB_SMEM, true, a.vk ? 6 : 3);
-    if (e != cudaSuccess) return e;
-    solve<<<units, kSBThreads, SB_SMEM, s>>>(mS, mQ, mK, mV, mMW, a.beta, a.offsets, a.logP, a.H,
-                                             a.N, static_cast<__nv_bfloat16 *>(a.O), a.U, a.st);
+    // a workspace is not needed; one large enough receives a copy of [M; W]
+    float *mw = (a.ws && a.ws_bytes >= tc_big_workspace_bytes(a.B, a.H))
+                    ? static_cast<float *>(a.ws) : nullptr;
+    kernel<<<units, kFUThreads, FU_SMEM, s>>>(mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
+                                              a.req_depth, a.H, a.N,
+                                              static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, mw,
+                                              a.st);
     return cudaGetLastError();
 }
 

@@ -112,15 +112,13 @@ const char *bole_status_string(int status);
 int bole_version(void);
 
 /* Bytes of device workspace bole_tree_verify needs for these sizes (0 when
- * the chosen kernel keeps every intermediate on chip, as the single-CTA
- * tensor-core kernel does).  max_T bounds every tree's node count (1..128) and
- * max_depth every tree's depth (0..127); pass the same values, dtype and flags
- * as to bole_tree_verify.  The workspace holds the short-lived tree factors of
- * one call -- the "verification scratch" of the pages' state lifecycle
- * (Section IV-D): [M; W] = [C (I+G)^{-1}; (I+G)^{-1}] (256 x 128 floats per
- * request and head) on the large-tree tensor-core path, dense G, C on the
- * CUDA-core path -- and may be reused by the next call once that call's
- * kernels have finished. */
+ * the chosen kernel keeps every intermediate on chip, as both tensor-core
+ * kernels do).  max_T bounds every tree's node count (1..128) and max_depth
+ * every tree's depth (0..127); pass the same values, dtype and flags as to
+ * bole_tree_verify.  The workspace holds the short-lived tree factors of one
+ * call -- the "verification scratch" of the pages' state lifecycle (Section
+ * IV-D): dense G, C on the CUDA-core path -- and may be reused by the next
+ * call once that call's kernels have finished. */
 size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_depth,
                            bole_dtype qkv_dtype, unsigned flags);
 
@@ -153,10 +151,13 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * max_depth <= 15 run the single-CTA TMA + tcgen05 kernel (state products on
  * an exact bf16 hi/lo split of S_pre, fp32 accumulation, every factor on
  * chip); bf16 inputs with dk = dv = 128 and larger or deeper trees (up to 128
- * nodes, any depth) run two tcgen05 kernels (the factors [M; W] by log-depth
- * doubling into the workspace, then the state products and propagation);
- * everything else, or flags & BOLE_FLAG_FORCE_SIMT, runs the FP32 CUDA-core
- * kernels (producer of G, C into the workspace + value-tiled solve). */
+ * nodes, any depth) run one tcgen05 kernel per (request, head) that forms the
+ * factors [M; W] by log-depth doubling and keeps them in tensor memory for the
+ * state products and the propagation (no workspace; when the caller passes
+ * one of at least B * H * 256 * 128 * 4 bytes anyway, [M; W] is also written
+ * there, unit-major, 256 rows of 128 floats, for inspection); everything
+ * else, or flags & BOLE_FLAG_FORCE_SIMT, runs the FP32 CUDA-core kernels
+ * (producer of G, C into the workspace + value-tiled solve). */
 bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, const void *v,
                              bole_dtype qkv_dtype, const float *gamma, const float *beta,
                              const int32_t *offsets, const int32_t *parent, const int32_t *depth,

@@ -56,10 +56,10 @@ def test_workspace_size_rules(lib):
     # bf16, dk = dv = 128, trees <= 64 nodes of depth <= 15: tensor-core kernel, every
     # intermediate on chip, no workspace
     assert f(2, 3, 128, 128, 64, 15, 1, 0) == 0
-    # deeper or larger trees (up to 128 nodes): the two-kernel tensor-core path, whose
-    # workspace holds [M; W] = 256 x 128 floats per (request, head)
-    assert f(2, 3, 128, 128, 64, 16, 1, 0) == 2 * 3 * 256 * 128 * 4
-    assert f(2, 3, 128, 128, 128, 127, 1, 0) == 2 * 3 * 256 * 128 * 4
+    # deeper or larger trees (up to 128 nodes): the large-tree tensor-core kernel keeps
+    # [M; W] in tensor memory, no workspace either
+    assert f(2, 3, 128, 128, 64, 16, 1, 0) == 0
+    assert f(2, 3, 128, 128, 128, 127, 1, 0) == 0
     # forced CUDA-core path: two dense T x T factors per unit
     assert f(2, 3, 128, 128, 64, 8, 1, 1) == 2 * 4 * 2 * 3 * 64 * 64
     # invalid sizes report 0

@@ -191,9 +191,11 @@ def test_overlapped_round_matches_serial_launches():
 
 @pytest.mark.parametrize("seed,sizes,depth", [(31, [100, 70], 40), (32, [128], 127), (33, [48], 20)])
 def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
-    """The large-tree path's factor kernel leaves [M; W] = [C (I+G)^{-1}; (I+G)^{-1}]
-    in the workspace; compare with a library dense inverse of the same G and C
-    (Lemma 3: the log-depth product of (I + G^(2^k)) equals the finite Neumann sum)."""
+    """The large-tree kernel keeps [M; W] = [C (I+G)^{-1}; (I+G)^{-1}] in tensor
+    memory and needs no workspace; given one of B H 256 128 floats it also
+    writes [M; W] there.  Compare with a library dense inverse of the same G
+    and C (Lemma 3: the log-depth product of (I + G^(2^k)) equals the finite
+    Neumann sum), and O, U with the oracle."""
     from gated_deltanet_verification_gb300 import bole, device
     import pins_lib
     b = I.random_batch(seed=seed, B=len(sizes), H=2, dk=128, dv=128, sizes=sizes,
@@ -201,13 +203,17 @@ def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
                        else "random")
     db = device.to_device(b)
     rb = device.alloc_round(db)
-    assert rb.workspace is not None and rb.workspace.numel() * rb.workspace.element_size() == \
-        b.B * b.H * 256 * 128 * 4
+    assert bole.workspace_size(b.B, b.H, 128, 128, b.max_T, b.max_depth, db.q.dtype, 0) == 0
+    rb.workspace = torch.full((b.B * b.H * 256 * 128,), float("nan"), dtype=torch.float32,
+                              device="cuda")
     device.pack(db, rb)
     device.verify(db, rb)
     torch.cuda.synchronize()
     bole.check_status(rb.status)
-    mw = rb.workspace.view(torch.float32).view(b.B, b.H, 256, 128).cpu().numpy()
+    Oe, Ue, _ = oracle.verify(b)
+    assert rel_fro(rb.O.float().cpu().numpy(), Oe) <= TOL["bf16"]
+    assert rel_fro(rb.U.cpu().numpy(), Ue) <= TOL["bf16"]
+    mw = rb.workspace.view(b.B, b.H, 256, 128).cpu().numpy()
     for r in range(b.B):
         o, e = int(b.offsets[r]), int(b.offsets[r + 1])
         T = e - o
