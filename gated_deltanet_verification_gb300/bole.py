@@ -90,8 +90,23 @@ def lib() -> ctypes.CDLL:
             L.bole_select_workspace_size.restype = S
             L.bole_select_forest.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P, S, P, U, P]
             L.bole_select_forest.restype = I
+            L.bole_selftest_wait.argtypes = [P, ctypes.c_uint64, P]
+            L.bole_selftest_wait.restype = I
             _lib = L
     return _lib
+
+
+SELFTEST_MAX_WAIT_NS = 1_000_000_000
+
+
+def selftest_wait(limit_ns: int, *, status=None, stream=None) -> torch.Tensor:
+    """bole_selftest_wait: one device thread waits on a barrier nothing
+    arrives on, for at most limit_ns; returns the status block, which then
+    holds (ERR_TIMEOUT, -1, -1, microseconds waited)."""
+    status = new_status() if status is None else status
+    _check(lib().bole_selftest_wait(_ptr(status), int(limit_ns), _stream(stream)),
+           "bole_selftest_wait")
+    return status
 
 
 def status_string(code: int) -> str:
@@ -349,7 +364,7 @@ def commit_layers(S, k, U, logP, offsets, parent, accepted, *, status=None, flag
     return S
 
 
-__all__ = ["select_forest", "MAX_CANDIDATES", "SELECT_MAX_REQUESTS", "conv_gates", "conv_commit", "MAX_CONV_WIDTH", "commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
+__all__ = ["selftest_wait", "SELFTEST_MAX_WAIT_NS", "select_forest", "MAX_CANDIDATES", "SELECT_MAX_REQUESTS", "conv_gates", "conv_commit", "MAX_CONV_WIDTH", "commit_layers", "FLAG_STATE_VK", "lib", "library_path", "status_string", "version", "workspace_size", "pack_forest",
            "tree_verify", "tree_verify_noalloc", "commit", "new_status", "check_status", "BoleError", "OK",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_BAD_TOPOLOGY", "ERR_DEPTH",
            "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT", "F32", "BF16", "FLAG_FORCE_SIMT",

@@ -59,6 +59,14 @@ const char *bole_status_string(int status)
 
 int bole_version(void) { return 100; }
 
+bole_status bole_selftest_wait(int32_t *dev_status, uint64_t limit_ns, bole_stream_t stream)
+{
+    if (!dev_status || !aligned(dev_status, 16) || limit_ns > BOLE_SELFTEST_MAX_WAIT_NS)
+        return BOLE_ERR_INVALID_ARG;
+    return from_cuda(
+        launch_selftest_wait(dev_status, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t bole_workspace_size(int B, int H, int dk, int dv, int max_T, int max_depth,
                            bole_dtype qkv_dtype, unsigned flags)
 {

@@ -52,6 +52,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 // ---- launchers (one per kernel family; each returns the launch error) ----
 
+cudaError_t launch_selftest_wait(int32_t *st, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_pack(const int32_t *offsets, const int32_t *parent, int B, int N, int max_depth,
                         int32_t *depth, uint32_t *anc, int32_t *req_depth, int32_t *st,
                         cudaStream_t s);

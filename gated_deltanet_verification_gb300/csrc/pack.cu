@@ -2,6 +2,7 @@
 // node's depth and ancestor-or-self bit mask ("Bole", Section IV-C, and the
 // flat-ragged packed forest of the review's Section 3).  Integer only.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace bole {
 namespace {
@@ -97,7 +98,28 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
     }
 }
 
+// Self-test of the bounded device wait every kernel uses: one thread waits on
+// an mbarrier that nothing arrives on, with the caller's limit; the wait gives
+// up and the timeout is reported with the time actually waited (microseconds).
+__global__ void selftest_wait_kernel(int32_t *st, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    sm100::mbar_init(&bar, 1);
+    sm100::fence_mbar_init();
+    const uint64_t t0 = sm100::global_ns();
+    const bool arrived = sm100::mbar_wait(&bar, 0, limit_ns);
+    const uint64_t us = (sm100::global_ns() - t0) / 1000;
+    if (!arrived) report(st, BOLE_ERR_TIMEOUT, -1, -1, (int)(us < 0x7fffffffu ? us : 0x7fffffffu));
+}
+
 } // namespace
+
+cudaError_t launch_selftest_wait(int32_t *st, uint64_t limit_ns, cudaStream_t s)
+{
+    selftest_wait_kernel<<<1, 32, 0, s>>>(st, limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const int32_t *offsets, const int32_t *parent, int B, int N, int max_depth,
                         int32_t *depth, uint32_t *anc, int32_t *req_depth, int32_t *st,

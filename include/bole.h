@@ -111,6 +111,18 @@ const char *bole_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int bole_version(void);
 
+/* Self-test of the bounded device waits.  Every device wait of the library
+ * (an mbarrier wait for a copy or a tensor-core product) gives up after a
+ * limit and reports BOLE_ERR_TIMEOUT in the status block instead of hanging;
+ * this call launches one thread that waits on an mbarrier nothing arrives
+ * on, with the given limit (at most BOLE_SELFTEST_MAX_WAIT_NS), so that the
+ * timeout path can be exercised without a fault: afterwards dev_status holds
+ * {BOLE_ERR_TIMEOUT, -1, -1, microseconds waited} (first error wins, as
+ * everywhere) and the context stays usable.  dev_status: device, 16-byte
+ * aligned, BOLE_STATUS_WORDS words, not cleared by this call. */
+#define BOLE_SELFTEST_MAX_WAIT_NS 1000000000ull
+bole_status bole_selftest_wait(int32_t *dev_status, uint64_t limit_ns, bole_stream_t stream);
+
 /* Bytes of device workspace bole_tree_verify needs for these sizes (0 when
  * the chosen kernel keeps every intermediate on chip, as both tensor-core
  * kernels do).  max_T bounds every tree's node count (1..128) and max_depth

@@ -40,6 +40,16 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_selftest_wait_host_validation(lib):
+    """Bad arguments are refused before anything is launched."""
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    f = lib.bole_selftest_wait
+    assert f(None, 1000, None) == bole.ERR_INVALID_ARG               # no status block
+    assert f(c((1 << 20) + 4), 1000, None) == bole.ERR_INVALID_ARG   # misaligned status
+    assert f(c(1 << 20), bole.SELFTEST_MAX_WAIT_NS + 1, None) == bole.ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     from gated_deltanet_verification_gb300 import bole
     assert bole.status_string(0) == "ok"

@@ -100,6 +100,8 @@ def test_fp32_inputs_parity(cfg):
     ([40, 33, 64], "random", "bf16", 128, 128, 12),
     ([64] * 20, "random", "bf16", 128, 128, 30),
     ([64] * 20, "random", "bf16", 128, 128, 15),
+    ([1, 32, 1, 7], "random", "bf16", 128, 128, 15),   # small-tree layout, 1-node trees
+    ([128, 1, 2], "chain", "bf16", 128, 128, 127),    # large-tree kernel, depths 127 and 0
 ])
 def test_ragged_and_edge_shapes(sizes, shape, dtype, dk, dv, max_depth):
     b = I.random_batch(seed=sum(sizes) + dk, B=len(sizes), H=3, dk=dk, dv=dv, sizes=sizes,
@@ -286,3 +288,22 @@ def test_tree_above_declared_max_T_is_reported():
                        dtype="bf16", sigma=0.05)
     _, _, _, st = _verify_direct(b, 32)
     assert st[0] == bole.ERR_BAD_TOPOLOGY and st[1] == 1, st
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """Failure detection without a fault: a device thread waits on a barrier
+    nothing arrives on; the bounded wait gives up after the limit, reports
+    BOLE_ERR_TIMEOUT with the time waited, and the next calls on the same
+    context run normally (a verification and commit against the oracle)."""
+    from gated_deltanet_verification_gb300 import bole
+    for limit_ms in (2, 20):
+        st = bole.selftest_wait(limit_ms * 1_000_000)
+        torch.cuda.synchronize()
+        code, req, node, waited_us = st.cpu().tolist()
+        assert (code, req, node) == (bole.ERR_TIMEOUT, -1, -1)
+        assert limit_ms * 1000 <= waited_us < limit_ms * 1000 + 50_000
+        with pytest.raises(bole.BoleError):
+            bole.check_status(st)
+    b = I.random_batch(seed=97, B=3, H=2, dk=128, dv=128, sizes=[20, 31, 9], max_depth=6,
+                       dtype="bf16", sigma=0.05, accept="uniform")
+    _check(b, _run(b), TOL["bf16"])
