@@ -288,9 +288,10 @@ def main(argv=None):
     tc_shape = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
                 and batch.dv == 128)
     fused = tc_shape and batch.max_T <= 64 and batch.max_depth < 16   # single-CTA kernel
-    big = tc_shape and not fused and batch.max_T <= 128              # factor + solve kernels
+    big = tc_shape and not fused and batch.max_T <= 128              # fused large-tree kernel
     tc_used = fused or big
-    launches_per_step = 1 + (1 if fused else 2) + 1  # pack, verify (1 or 2 kernels), commit
+    # pack, verify (one tensor-core kernel, or the CUDA-core producer + solve), commit
+    launches_per_step = 1 + (1 if tc_used else 2) + 1
 
     def step(i):
         device.run_round(*sets[i % n_sets], flags, stream)
@@ -415,7 +416,7 @@ def main(argv=None):
                    "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
                    "seed": seed,
-                   "kernels": ("tcgen05" if fused else "tcgen05 factor + solve (large trees)"
+                   "kernels": ("tcgen05" if fused else "tcgen05 fused large-tree kernel"
                                if big else "cuda-core"),
                    "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
                    "launch": "CUDA graph replay, one graph per input copy",

@@ -17,7 +17,7 @@ bool valid_dtype(bole_dtype t) { return t == BOLE_F32 || t == BOLE_BF16; }
 bole_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BOLE_OK : BOLE_ERR_CUDA; }
 
 // Verification kernels: the single-CTA tensor-core kernel (trees of up to 64
-// nodes, depth <= 15), the two-kernel tensor-core path for larger or deeper
+// nodes, depth <= 15), the large-tree tensor-core kernel for larger or deeper
 // trees (up to 128 nodes), else the FP32 CUDA-core kernels.
 enum class VerifyPath { Fused, Big, Simt };
 

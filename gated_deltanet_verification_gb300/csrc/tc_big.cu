@@ -57,9 +57,9 @@ __device__ __forceinline__ uint32_t kmaj_offset(int n, int k)
 // =====================================================================
 // fused kernel: the factors and the solve in one CTA, [M; W] kept on chip
 // =====================================================================
-// The factor phase is the factor kernel's (Gram, dense C and G, log-depth
-// doubling), with the transposed power in a buffer of its own so that [Q;K]
-// survives for the state products; S_pre is requested at entry and lands
+// The factor phase (Gram, dense C and G, log-depth doubling) keeps the
+// transposed power in a buffer of its own so that [Q;K] survives for the
+// state products; S_pre is requested at entry and lands
 // while the doubling runs.  M and W then stay in tensor memory as the A
 // operands of the propagation (tcgen05 kind::tf32 with A from tensor memory),
 // so no factor leaves the SM.
