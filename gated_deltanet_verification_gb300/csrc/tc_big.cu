@@ -94,7 +94,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                     const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc_g,
                     const int32_t *__restrict__ req_depth, int H, int N,
                     __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
-                    float *__restrict__ logP, float *__restrict__ mw, int32_t *st)
+                    float *__restrict__ logP, float *__restrict__ mw, int32_t *st,
+                    int pf_stride)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -262,9 +263,12 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             tmem_st32(dst + lane_base + j0, x);
         }
     };
-    // M0 = C - C G; levels: P <- P^2, W <- W + W P, M <- M + M P
-    product(R3, R0);
-    accumulate(R0, R3, -1.f);
+    // M0 = C - C G (G = 0 exactly when every tree of the request has depth 0:
+    // M = C, W = I); levels: P <- P^2, W <- W + W P, M <- M + M P
+    if (d > 0) {
+        product(R3, R0);
+        accumulate(R0, R3, -1.f);
+    }
     int K = 0;
     while ((2 << K) <= d) ++K; // K = floor(log2 d) for d >= 1, 0 otherwise
     uint32_t Pp = R1, Pq = R3;
@@ -355,6 +359,21 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     // state products: Q S_pre -> R1, K S_pre -> R3 (S = S_hi + S_lo)
     const uint32_t s0 = smem_addr(sS);
     if (tid == 0) {
+        // this CTA's inputs have landed: the CTA one wave later (pf_stride =
+        // resident CTAs) finds its state, q, k and v in L2
+        const int nu = unit + pf_stride;
+        if (pf_stride > 0 && nu < (int)gridDim.x) {
+            const int nb = nu / H, nhh = nu % H;
+            const int no = offsets[nb];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tmS, 32 * c, nu * kD);
+#pragma unroll
+            for (int ka = 0; ka < 2; ++ka) {
+                tma_prefetch_l2_3d(&tmQ, 64 * ka, nhh, no);
+                tma_prefetch_l2_3d(&tmK, 64 * ka, nhh, no);
+                tma_prefetch_l2_3d(&tmV, 64 * ka, nhh, no);
+            }
+        }
         tc_fence_after();
         const uint32_t slo = s0 + 16384;
         constexpr uint32_t idesc_s = VK ? IDESC_S128_VK : IDESC_S128;
@@ -470,6 +489,20 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
 
 } // namespace
 
+// streaming multiprocessors of the current device (cached), 0 if unknown
+static int sm_count()
+{
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = n;
+    }
+    return sms[dev];
+}
+
 bool tc_big_supported(const VerifyArgs &a)
 {
     return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && a.max_T <= kTB;
@@ -496,7 +529,7 @@ cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s)
     kernel<<<units, kFUThreads, FU_SMEM, s>>>(mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
                                               a.req_depth, a.H, a.N,
                                               static_cast<__nv_bfloat16 *>(a.O), a.U, a.logP, mw,
-                                              a.st);
+                                              a.st, sm_count());
     return cudaGetLastError();
 }
 
