@@ -16,19 +16,33 @@ namespace {
 // path of length l is covered after ceil(log2 l) rounds).  Rounds alternate
 // between two copies of the masks and jumps so a lane never reads a value
 // another lane is writing.  depth = bits - 1.
+// A batch of at most 32 requests runs as one CTA (one warp per request) that
+// also clears the status block before any warp can report, so no separate
+// reset is needed; larger batches run CTAs of four warps after a reset copy.
 constexpr int kPackWarps = 4;
+constexpr int kPackOneCTA = 32;
+constexpr int kPackWarpSmem = 2 * kMaxTree * (16 + 4); // masks and jumps, two copies
 
-__global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
+template <bool ONE_CTA>
+__global__ void __launch_bounds__(32 * (ONE_CTA ? kPackOneCTA : kPackWarps)) pack_kernel(
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent, int B, int N,
     int max_depth, int32_t *__restrict__ depth, uint32_t *__restrict__ anc,
     int32_t *__restrict__ req_depth, int32_t *st)
 {
-    __shared__ uint4 smask[2][kPackWarps][kMaxTree];
-    __shared__ int sjump[2][kPackWarps][kMaxTree];
+    extern __shared__ __align__(16) uint8_t pack_smem[];
     pdl_launch_dependents(); // a verification launched to overlap may start its state reads
+    const int warps = (int)blockDim.x >> 5;
     const int wib = threadIdx.x >> 5;
-    const int b = (int)blockIdx.x * kPackWarps + wib;
+    const int b = (int)blockIdx.x * warps + wib;
     const int lane = threadIdx.x & 31;
+    if (ONE_CTA) { // the status block is clear before anyone can report
+        if (threadIdx.x < BOLE_STATUS_WORDS) st[threadIdx.x] = 0;
+        __syncthreads();
+    }
+    // this warp's two copies of the masks and jumps
+    uint4 (*smask)[kMaxTree] = reinterpret_cast<uint4 (*)[kMaxTree]>(pack_smem + wib * kPackWarpSmem);
+    int (*sjump)[kMaxTree] =
+        reinterpret_cast<int (*)[kMaxTree]>(pack_smem + wib * kPackWarpSmem + 2 * kMaxTree * 16);
     if (b >= B) return;
     const int o = offsets[b], e = offsets[b + 1];
     const int T = e - o;
@@ -48,9 +62,9 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
             bad_p = p;
         }
         const uint32_t bit = 1u << (i & 31), w = (uint32_t)(i >> 5);
-        smask[0][wib][i] = make_uint4(w == 0 ? bit : 0u, w == 1 ? bit : 0u, w == 2 ? bit : 0u,
+        smask[0][i] = make_uint4(w == 0 ? bit : 0u, w == 1 ? bit : 0u, w == 2 ? bit : 0u,
                                       w == 3 ? bit : 0u);
-        sjump[0][wib][i] = p;
+        sjump[0][i] = p;
     }
     const unsigned badm = __ballot_sync(0xffffffffu, bad_i >= 0);
     if (badm) {
@@ -69,22 +83,22 @@ __global__ void __launch_bounds__(32 * kPackWarps) pack_kernel(
     int cur = 0;
     for (int round = 0; (1 << round) < T; ++round) {
         for (int i = lane; i < T; i += 32) {
-            uint4 mk = smask[cur][wib][i];
-            int j = sjump[cur][wib][i];
+            uint4 mk = smask[cur][i];
+            int j = sjump[cur][i];
             if (j >= 0) {
-                const uint4 mj = smask[cur][wib][j];
+                const uint4 mj = smask[cur][j];
                 mk.x |= mj.x; mk.y |= mj.y; mk.z |= mj.z; mk.w |= mj.w;
-                j = sjump[cur][wib][j];
+                j = sjump[cur][j];
             }
-            smask[cur ^ 1][wib][i] = mk;
-            sjump[cur ^ 1][wib][i] = j;
+            smask[cur ^ 1][i] = mk;
+            sjump[cur ^ 1][i] = j;
         }
         __syncwarp();
         cur ^= 1;
     }
     int dmax = 0;
     for (int i = lane; i < T; i += 32) {
-        const uint4 mk = smask[cur][wib][i];
+        const uint4 mk = smask[cur][i];
         const int d = __popc(mk.x) + __popc(mk.y) + __popc(mk.z) + __popc(mk.w) - 1;
         depth[o + i] = d;
         *reinterpret_cast<uint4 *>(anc + (size_t)(o + i) * 4) = mk;
@@ -125,12 +139,29 @@ cudaError_t launch_pack(const int32_t *offsets, const int32_t *parent, int B, in
                         int32_t *depth, uint32_t *anc, int32_t *req_depth, int32_t *st,
                         cudaStream_t s)
 {
+    if (B >= 1 && B <= kPackOneCTA) { // one CTA clears the status block itself
+        const size_t smem = (size_t)B * kPackWarpSmem;
+        static bool configured[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !configured[dev]) {
+            e = cudaFuncSetAttribute(pack_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPackOneCTA * kPackWarpSmem);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = true;
+        }
+        pack_kernel<true><<<1, 32 * B, smem, s>>>(offsets, parent, B, N, max_depth, depth, anc,
+                                                  req_depth, st);
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaMemsetAsync(st, 0, sizeof(int32_t) * BOLE_STATUS_WORDS, s);
     if (e != cudaSuccess) return e;
     if (B <= 0) return cudaSuccess;
     const int blocks = (B + kPackWarps - 1) / kPackWarps;
-    pack_kernel<<<blocks, 32 * kPackWarps, 0, s>>>(offsets, parent, B, N, max_depth, depth, anc,
-                                                   req_depth, st);
+    pack_kernel<false><<<blocks, 32 * kPackWarps, kPackWarps * kPackWarpSmem, s>>>(
+        offsets, parent, B, N, max_depth, depth, anc, req_depth, st);
     return cudaGetLastError();
 }
 
