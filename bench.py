@@ -9,11 +9,17 @@ batched packed forest (16 requests x 32 heads, 32-node trees of depth <= 8,
 dk = dv = 128, bf16 q/k/v, fp32 state).
 
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
-torch.cuda.synchronize(), CUDA events on the launching stream.  Inputs rotate
-over enough independent copies that the bytes touched between two uses of
-the same copy exceed 3x the L2 cache, so every step streams from HBM.  The
-committed state of a copy becomes that copy's next S_pre, as in a serving
-loop.  Per-kernel durations come from events around each launch.
+torch.cuda.synchronize(), CUDA events on the launching stream; the timed
+steps replay one CUDA graph per input copy (so the GPU, not the Python issue
+cost, is measured).  Inputs rotate over enough independent copies that the
+bytes touched between two uses of the same copy exceed 3x the L2 cache, so
+every step streams from HBM.  The committed state of a copy becomes that
+copy's next S_pre, as in a serving loop.  Per-kernel durations come from a
+separate pass: per call kind, a graph of that call on every input copy,
+replayed between events.  The JSON line also carries the roofline of the
+dominant kernel, the end-to-end throughput from pinned host buffers (e2e),
+the oracle on the host cores (cpu_baseline), the clocks seen, and the rows
+beyond the round (cross-layer commit, stage 1, device-side selection).
 
 --impl reference runs the CPU oracle (fp64, all host cores) on the same
 workload: the slow reference arm, not a target.
