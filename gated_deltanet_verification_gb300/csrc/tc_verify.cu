@@ -107,8 +107,7 @@ constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i 
 constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
 constexpr int X_DEPTH = X_L + kT * 4;
 constexpr int X_LG = X_DEPTH + kT * 4;        // log gamma_i
-constexpr int X_PAR = X_LG + kT * 4;          // parent links of the request
-static_assert(X_PAR + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+static_assert(X_LG + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
 static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
@@ -159,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const float *__restrict__ gamma, const float *__restrict__ beta,
-                 const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
+                 const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc,
                  const int32_t *__restrict__ req_depth, int H, int N,
                  __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
                  float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc)
@@ -175,7 +174,6 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     float *Ls = reinterpret_cast<float *>(sm + X_L);
     int *Ds = reinterpret_cast<int *>(sm + X_DEPTH);
     float *LGs = reinterpret_cast<float *>(sm + X_LG);
-    int *Ps_par = reinterpret_cast<int *>(sm + X_PAR);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
 
@@ -230,13 +228,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const bool topo = tid < kT;       // warps 0, 1: row i = tid
     float bt = 0.f;                   // beta_i (topology rows and the K-side rows)
     float g_i = 1.f;
-    int par_i = -1;
     if (warp < 8 && in_range && i < T) {
         if (topo || m >= 64) bt = beta[(size_t)(o + i) * H + h];
-        if (topo) {
-            g_i = gamma[(size_t)(o + i) * H + h];
-            par_i = parent[o + i];
-        }
+        if (topo) g_i = gamma[(size_t)(o + i) * H + h];
     }
     if (issuer) {
         mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
@@ -250,32 +244,25 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         }
     }
     // What the previous call wrote (the status word pack reset, the
-    // per-request depth) is read after the wait; the reads above are already
-    // in flight, so without an overlapped launch both arrive in one round trip.
+    // per-request depth, each node's ancestor-or-self mask) is read after the
+    // wait; the reads above are already in flight, so without an overlapped
+    // launch they all arrive in one round trip.
     pdl_wait();
     int *sfault = reinterpret_cast<int *>(sm + OFF_MISC + 4);
     if (tid == 0) *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
     const int d = req_depth[b];
-    // Depth and ancestor-or-self mask of each node from the request's parent
-    // links (a caller input), walked in shared memory by the topology warps:
-    // at most 16 steps, every link checked to point backwards, so the walk is
-    // bounded and in range whatever the input (invalid trees are reported by
-    // pack, and the check below ends such a launch before any output).
+    // Depth and ancestor-or-self mask of each node as pack built them (rows
+    // below 64: the first two words of the 128-bit mask).  A tree pack found
+    // malformed or too deep has set the status or a depth the check below
+    // refuses, so such a launch ends before any output; every bit indexes a
+    // row below 64 whatever the input.
     int my_depth = -1;
     uint64_t my_mask = 0;
-    if (topo) {
-        Ps_par[i] = par_i;
-        asm volatile("bar.sync 2, 64;" ::: "memory");
-        if (in_range && i < T) {
-            int j = i;
-            for (int step = 0; step < kSlots && j >= 0; ++step) {
-                my_mask |= 1ull << j;
-                ++my_depth;
-                const int pj = Ps_par[j];
-                j = (pj < j && pj >= -1) ? pj : -2; // a forward or bad link ends the walk
-            }
-            if (j != -1) my_depth = -1; // deeper than 15 or malformed: no work for this row
-        }
+    if (topo && in_range && i < T) {
+        const uint2 mk = *reinterpret_cast<const uint2 *>(anc + (size_t)(o + i) * 4);
+        my_mask = ((uint64_t)mk.y << 32) | mk.x;
+        my_depth = __popcll(my_mask) - 1;
+        if (my_depth >= kSlots) my_depth = -1; // no work for this row (the request is refused)
     }
     if (!early_alloc && warp == 0) {
         tmem_alloc(tslot, 256);
@@ -1059,7 +1046,7 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
                                                  overlap, attr);
-    return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.parent,
+    return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
                               a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
                               a.logP, a.st, resident_ctas(2), overlap ? 0 : 1);
 }
