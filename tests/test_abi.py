@@ -201,3 +201,27 @@ def test_stage1_commit_rejects_bad_sizes_without_gpu(lib):
                                 None) == bole.ERR_INVALID_ARG      # B above the grid limit
     assert lib.bole_conv_commit(fake, fake, 1, fake, fake, fake, 2, 100, 4, 8, fake, 0,
                                 None) == bole.ERR_INVALID_ARG      # C not a multiple of 16
+
+
+def test_binding_constants_match_the_header():
+    """Every numeric constant the binding mirrors has the header's value (the
+    #defines and the bole_status codes), so the two cannot drift apart."""
+    import re
+    from gated_deltanet_verification_gb300 import bole
+    text = open(os.path.join(os.path.dirname(__file__), "..", "include", "bole.h")).read()
+    defines = {}
+    for name, val in re.findall(r"#define BOLE_([A-Z_]+)\s+([0-9x()<u l]+)", text):
+        defines[name] = eval(val.replace("ull", "").replace("u", "").strip())
+    codes = dict((n, int(v)) for n, v in re.findall(r"BOLE_(OK|ERR_[A-Z_]+)\s*=\s*(\d+)", text))
+    pairs = {"MAX_TREE_NODES": bole.MAX_TREE_NODES, "STATUS_WORDS": bole.STATUS_WORDS,
+             "FLAG_FORCE_SIMT": bole.FLAG_FORCE_SIMT,
+             "FLAG_OVERLAP_LAUNCH": bole.FLAG_OVERLAP_LAUNCH,
+             "FLAG_STATE_VK": bole.FLAG_STATE_VK,
+             "SELFTEST_MAX_WAIT_NS": bole.SELFTEST_MAX_WAIT_NS,
+             "NOALLOC_MAX_FACTOR_ELEMS": bole.NOALLOC_MAX_FACTOR_ELEMS,
+             "MAX_CANDIDATES": bole.MAX_CANDIDATES,
+             "SELECT_MAX_REQUESTS": bole.SELECT_MAX_REQUESTS,
+             "MAX_CONV_WIDTH": bole.MAX_CONV_WIDTH}
+    for name, value in pairs.items():
+        assert defines[name] == value, name
+    assert codes and all(getattr(bole, n) == v for n, v in codes.items()), codes
