@@ -4,9 +4,13 @@ One step = one pass of the whole hot path over one batch: forest packing
 (bole_pack_forest), closed-form verification (bole_tree_verify) and the
 factorised commit of the accepted paths (bole_commit), all through the C ABI
 on one CUDA stream.  Inputs are seeded synthetic workloads (see
-gated_deltanet_verification_gb300/inputs.py); the default workload is the
-batched packed forest (16 requests x 32 heads, 32-node trees of depth <= 8,
-dk = dv = 128, bf16 q/k/v, fp32 state).
+gated_deltanet_verification_gb300/inputs.py); the headline workload is the
+ragged budgeted batch (64 requests x 32 heads, trees of 8..64 nodes selected
+greedily under a 2048-node budget, depth <= 12, dk = dv = 128, bf16 q/k/v,
+fp32 state) -- the largest workload on one GPU -- and the batched packed
+forest (16 requests x 32 heads, 32-node trees of depth <= 8) is measured in
+the same run and reported under "configs" with its own roofline, per-kernel
+times, e2e and oracle baseline.
 
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize(), CUDA events on the launching stream; the timed
@@ -57,9 +61,20 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="bole", choices=["bole", "reference"])
-    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--config", type=int, default=3,
+                   help="workload of the headline line (default: the ragged budgeted batch, "
+                        "the largest single-GPU workload)")
+    p.add_argument("--extra-configs", default="2",
+                   help="comma-separated workloads measured in the same run and reported "
+                        "under 'configs' (each with its own roofline, kernels, e2e and "
+                        "cpu_baseline); empty for none")
     p.add_argument("--shape", default="chain", help="tree shape for config 4")
     p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
+    p.add_argument("--one-tile-per-head", action="store_true",
+                   help="trees of up to 32 nodes: force one CTA per (request, head)")
+    p.add_argument("--value-tiles", action="store_true",
+                   help="trees of up to 32 nodes: force the value-tiled kernel (two CTAs "
+                        "per head)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--conv-width", type=int, default=4,
@@ -116,27 +131,39 @@ def algorithmic(batch):
     return {"pack": topo_pack, "verify": verify, "commit": commit, "verify_flops": flops}
 
 
-VERIFY_KERNELS = ["tc_verify_kernel"]
+# source file of each tensor-core kernel (a recorded DRAM figure is only
+# reported while that file is unchanged)
+KERNEL_SOURCES = {"tc_verify_kernel": "tc_verify.cu", "tc_commit_kernel": "tc_verify.cu",
+                  "tc_big_fused_kernel": "tc_big.cu", "tc_vtile_kernel": "tc_vtile.cu"}
 
 
-def recorded_traffic(kernels, config: int):
+def workload_key(config: int, shape: str) -> str:
+    return f"{config}{shape}" if config == 4 else str(config)
+
+
+def recorded_traffic(kernels, workload: str):
     """DRAM bytes of one call (the sum over its kernels' launches) from the
-    committed ncu summary, or None when the kernel source changed since the
-    capture (or a kernel has no capture)."""
+    committed ncu summary profiles/traffic.txt, or None when a kernel's source
+    changed since the capture (or a kernel has no capture).  Lines:
+    `source <file> <sha256>` and `<kernel> <workload> <bytes>`."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = os.path.join(ROOT, "gated_deltanet_verification_gb300", "csrc", "tc_verify.cu")
+    csrc = os.path.join(ROOT, "gated_deltanet_verification_gb300", "csrc")
+    if not kernels:
+        return None
     try:
         lines = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
-        want = dict((ln[0], ln[1]) for ln in lines if len(ln) == 2)
-        if hashlib.sha256(open(src, "rb").read()).hexdigest() != want.get("source_sha256"):
-            return None
-        got = {ln[0]: int(ln[2]) for ln in lines if len(ln) == 3 and int(ln[1]) == config}
-        if all(k in got for k in kernels):
-            return sum(got[k] for k in kernels)
+        shas = {ln[1]: ln[2] for ln in lines if len(ln) == 3 and ln[0] == "source"}
+        got = {ln[0]: int(ln[2]) for ln in lines
+               if len(ln) == 3 and ln[0] != "source" and ln[1] == workload}
+        for k in kernels:
+            f = KERNEL_SOURCES[k]
+            sha = hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()
+            if shas.get(f) != sha or k not in got:
+                return None
+        return sum(got[k] for k in kernels)
     except Exception:
         return None
-    return None
 
 
 def rank_seed(config: int, rank: int) -> int:
@@ -262,8 +289,6 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from gated_deltanet_verification_gb300 import inputs
-
     if args.impl == "reference":
         return reference_arm(args, world, rank)
 
@@ -275,12 +300,57 @@ def main(argv=None):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
 
-    from gated_deltanet_verification_gb300 import bole, build, device
+    from gated_deltanet_verification_gb300 import build
 
     build.build()
-    flags = bole.FLAG_FORCE_SIMT if args.force_simt else 0
-    seed = rank_seed(args.config, rank)
-    batch = inputs.config_batch(args.config, seed=seed, shape=args.shape)
+    head = measure_config(args, args.config, world, rank, local_rank, dev, args.steps)
+    extras = {}
+    for c in [int(x) for x in args.extra_configs.split(",") if x.strip()]:
+        if c == args.config:
+            continue
+        extras[str(c)] = measure_config(args, c, world, rank, local_rank, dev, args.steps)
+    stream = torch.cuda.current_stream()
+    layers = run_layers(args, head["_batch"], head["_flags"], stream) if args.layers > 0 else None
+    stage1 = run_stage1(args, head["_batch"], stream) if args.conv_width > 0 else None
+    selection = run_selection(stream) if not args.no_selection else None
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    out = {k: v for k, v in head.items() if not k.startswith("_")}
+    launches = head["_launches"]
+    if extras:
+        out["configs"] = {k: {kk: vv for kk, vv in v.items() if not kk.startswith("_")
+                              and kk not in ("metric", "n_gpus", "higher_is_better", "scaling",
+                                             "vs_baseline", "data")}
+                          for k, v in extras.items()}
+        launches += sum(v["_launches"] for v in extras.values())
+    out.update({"commit_layers": layers, "stage1": stage1, "selection": selection,
+                "gpu_launches": launches})
+    print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_config(args, cfg, world, rank, local_rank, dev, steps):
+    """One workload: warm-up, K timed graph-replayed steps (clocks sampled),
+    per-kernel durations, roofline, e2e and the oracle baseline.  Returns the
+    fields of the JSON line (keys starting with '_' are internal)."""
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_verification_gb300 import bole, device, inputs
+
+    flags = (bole.FLAG_FORCE_SIMT if args.force_simt else 0) | \
+        (bole.FLAG_ONE_TILE_PER_HEAD if args.one_tile_per_head else 0) | \
+        (bole.FLAG_VALUE_TILES if args.value_tiles else 0) | \
+        getattr(args, "verify_flags", 0)
+    seed = rank_seed(cfg, rank)
+    batch = inputs.config_batch(cfg, seed=seed, shape=args.shape)
     alg = algorithmic(batch)
     step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
     n_sets = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
@@ -293,6 +363,12 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
     tc_shape = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
                 and batch.dv == 128)
+    # value-tiled kernel: forced, or by default while the heads leave the
+    # one-CTA kernel (two CTAs per SM) short of one wave
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    vtile = (tc_shape and batch.max_T <= 32 and batch.max_depth < 16
+             and not args.one_tile_per_head
+             and (args.value_tiles or batch.B * batch.H < 2 * sms))
     fused = tc_shape and batch.max_T <= 64 and batch.max_depth < 16   # single-CTA kernel
     big = tc_shape and not fused and batch.max_T <= 128              # fused large-tree kernel
     tc_used = fused or big
@@ -332,7 +408,7 @@ def main(argv=None):
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         graphs[(args.warmup + i) % n_sets].replay()
     end.record(stream)
     torch.cuda.synchronize()
@@ -347,7 +423,7 @@ def main(argv=None):
     #      that call once on every input copy, back to back and without launch
     #      overlap (the copies keep the L2 cold between reuses); events bracket
     #      each replay ----
-    ks = max(1, min(args.kernel_steps, args.steps))
+    ks = max(1, min(args.kernel_steps, steps))
     per_kernel = {"pack": [], "verify": [], "commit": []}
     calls = {"pack": lambda db, rb, cs: device.pack(db, rb, cs),
              "verify": lambda db, rb, cs: device.verify(db, rb, flags, cs),
@@ -373,19 +449,13 @@ def main(argv=None):
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
-    layers = run_layers(args, batch, flags, stream) if args.layers > 0 else None
-    stage1 = run_stage1(args, batch, stream) if args.conv_width > 0 else None
-    selection = run_selection(stream) if not args.no_selection else None
-
+    res = {"_batch": batch, "_flags": flags, "_launches": launches_per_step * steps}
     if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return 0
+        return res
 
     hbm, tflops, peak_kind = measured_peaks()
-    ms_step = elapsed_ms / args.steps
-    value = job_throughput(batch.N, args.steps, world, elapsed_ms)
+    ms_step = elapsed_ms / steps
+    value = job_throughput(batch.N, steps, world, elapsed_ms)
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     kern_rf = {}
     for k in ("pack", "verify", "commit"):
@@ -394,8 +464,10 @@ def main(argv=None):
                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
     dominant = max(("verify", "commit"), key=lambda k: avg[k])
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
-    traffic = recorded_traffic(VERIFY_KERNELS if dominant == "verify" else ["tc_commit_kernel"],
-                               args.config) if fused else None
+    verify_kernels = (["tc_vtile_kernel"] if vtile else ["tc_verify_kernel"] if fused
+                      else ["tc_big_fused_kernel"] if big else [])
+    traffic = (recorded_traffic(verify_kernels if dominant == "verify" else ["tc_commit_kernel"],
+                                workload_key(cfg, args.shape)) if tc_used else None)
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": kern_rf[dominant]["frac"], "traffic": traffic, "peak_source": peak_kind,
@@ -411,33 +483,29 @@ def main(argv=None):
                "sample": f"{reps} full repetition(s) of the workload's verify + commit "
                          f"({batch.N} nodes x {batch.H} heads each), {el:.1f} s"}
 
-    out = {
+    res.update({
         "metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16x2+tf32 (f32 acc)" if tc_used else "f32", "io_dtype": batch.dtype,
         "data": "synthetic",
-        "config": {"workload": inputs.CONFIG_NAMES[args.config]
-                   + (f" [{args.shape}]" if args.config == 4 else ""),
-                   "config_index": args.config, "B": batch.B, "H": batch.H, "dk": batch.dk,
+        "config": {"workload": inputs.CONFIG_NAMES[cfg]
+                   + (f" [{args.shape}]" if cfg == 4 else ""),
+                   "config_index": cfg, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
                    "seed": seed,
-                   "kernels": ("tcgen05" if fused else "tcgen05 fused large-tree kernel"
-                               if big else "cuda-core"),
+                   "kernels": ("tcgen05 value-tiled (two CTAs per head)" if vtile
+                               else "tcgen05 (one CTA per head)" if fused
+                               else "tcgen05 fused large-tree kernel" if big else "cuda-core"),
                    "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
                    "launch": "CUDA graph replay, one graph per input copy",
                    "kernel_timing": f"separate pass: per call kind, a graph of one call on each "
                                     f"of the {n_sets} input copies, replayed "
                                     f"{max(1, ks // n_sets)}x between events"},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
-        "commit_layers": layers, "stage1": stage1, "selection": selection,
-        "gpu_launches": launches_per_step * args.steps, "clocks": clock_info,
-    }
-    print(json.dumps(out))
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+        "clocks": clock_info,
+    })
+    return res
 
 
 def run_selection(stream):

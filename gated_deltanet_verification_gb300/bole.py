@@ -31,6 +31,8 @@ BF16 = 1
 FLAG_FORCE_SIMT = 0x1
 FLAG_OVERLAP_LAUNCH = 0x2  # see bole.h: overlap with the previous library call on the stream
 FLAG_STATE_VK = 0x4  # state slots stored [B, H, dv, dk] (the serving runtime's slot layout)
+FLAG_ONE_TILE_PER_HEAD = 0x8  # small trees: one CTA per (request, head), not two value tiles
+FLAG_VALUE_TILES = 0x10  # small trees: two value-tile CTAs per (request, head)
 MAX_TREE_NODES = 128
 STATUS_WORDS = 4
 
@@ -41,7 +43,10 @@ _lib: Optional[ctypes.CDLL] = None
 class BoleError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = int(code)
-        super().__init__(f"{what}: {status_string(code)} ({code})")
+        msg = f"{what}: {status_string(code)} ({code})"
+        if self.code == ERR_CUDA:
+            msg += f" [CUDA error {last_cuda_error()}: {last_cuda_error_string()}]"
+        super().__init__(msg)
 
 
 def library_path() -> str:
@@ -65,6 +70,10 @@ def lib() -> ctypes.CDLL:
             L.bole_status_string.restype = ctypes.c_char_p
             L.bole_version.argtypes = []
             L.bole_version.restype = I
+            L.bole_last_cuda_error.argtypes = []
+            L.bole_last_cuda_error.restype = I
+            L.bole_last_cuda_error_string.argtypes = []
+            L.bole_last_cuda_error_string.restype = ctypes.c_char_p
             L.bole_workspace_size.argtypes = [I, I, I, I, I, I, I, U]
             L.bole_workspace_size.restype = S
             L.bole_pack_forest.argtypes = [P, P, I, I, I, P, P, P, P, P]
@@ -115,6 +124,15 @@ def status_string(code: int) -> str:
 
 def version() -> int:
     return lib().bole_version()
+
+
+def last_cuda_error() -> int:
+    """cudaError_t behind this thread's last ERR_CUDA (0 if none)."""
+    return lib().bole_last_cuda_error()
+
+
+def last_cuda_error_string() -> str:
+    return lib().bole_last_cuda_error_string().decode()
 
 
 def _dtype_code(t: torch.Tensor) -> int:

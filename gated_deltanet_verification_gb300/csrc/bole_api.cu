@@ -14,16 +14,29 @@ bool valid_dim(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
 
 bool valid_dtype(bole_dtype t) { return t == BOLE_F32 || t == BOLE_BF16; }
 
-bole_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BOLE_OK : BOLE_ERR_CUDA; }
+// The CUDA error behind the calling thread's last BOLE_ERR_CUDA.
+thread_local int g_last_cuda_error = 0;
 
-// Verification kernels: the single-CTA tensor-core kernel (trees of up to 64
-// nodes, depth <= 15), the large-tree tensor-core kernel for larger or deeper
-// trees (up to 128 nodes), else the FP32 CUDA-core kernels.
-enum class VerifyPath { Fused, Big, Simt };
+bole_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return BOLE_OK;
+    g_last_cuda_error = (int)e;
+    return BOLE_ERR_CUDA;
+}
+
+// Verification kernels: the value-tiled tensor-core kernel (trees of up to
+// 32 nodes, depth <= 15, two CTAs per head), the single-CTA tensor-core
+// kernel (trees of up to 64 nodes, depth <= 15), the large-tree tensor-core
+// kernel for larger or deeper trees (up to 128 nodes), else the FP32
+// CUDA-core kernels.
+enum class VerifyPath { VTile, Fused, Big, Simt };
 
 VerifyPath verify_path(const VerifyArgs &a, unsigned flags)
 {
     if (flags & BOLE_FLAG_FORCE_SIMT) return VerifyPath::Simt;
+    if (!(flags & BOLE_FLAG_ONE_TILE_PER_HEAD) && tc_vtile_supported(a) &&
+        ((flags & BOLE_FLAG_VALUE_TILES) || tc_vtile_preferred(a)))
+        return VerifyPath::VTile;
     if (tc_verify_supported(a)) return VerifyPath::Fused;
     if (tc_big_supported(a)) return VerifyPath::Big;
     return VerifyPath::Simt;
@@ -32,6 +45,7 @@ VerifyPath verify_path(const VerifyArgs &a, unsigned flags)
 size_t verify_workspace(const VerifyArgs &a, unsigned flags)
 {
     switch (verify_path(a, flags)) {
+    case VerifyPath::VTile: return 0; // every factor stays on chip
     case VerifyPath::Fused: return tc_workspace_bytes(a.B, a.H, a.max_T);
     case VerifyPath::Big: return 0; // [M; W] stays on chip
     default: return simt_workspace_bytes(a.B, a.H, a.max_T);
@@ -58,6 +72,13 @@ const char *bole_status_string(int status)
 }
 
 int bole_version(void) { return 100; }
+
+int bole_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *bole_last_cuda_error_string(void)
+{
+    return g_last_cuda_error ? cudaGetErrorString((cudaError_t)g_last_cuda_error) : "no error";
+}
 
 bole_status bole_selftest_wait(int32_t *dev_status, uint64_t limit_ns, bole_stream_t stream)
 {
@@ -138,6 +159,8 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     if (B == 0 || N == 0) return BOLE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (path) {
+    case VerifyPath::VTile:
+        return from_cuda(launch_tc_vtile_verify(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0));
     case VerifyPath::Fused:
         return from_cuda(launch_tc_verify(a, s, (flags & BOLE_FLAG_OVERLAP_LAUNCH) != 0));
     case VerifyPath::Big: return from_cuda(launch_tc_big_verify(a, s));

@@ -119,6 +119,9 @@ bool simt_noalloc_fits(int B, int H, int max_T);
 cudaError_t launch_simt_verify_noalloc(const VerifyArgs &a, cudaStream_t s);
 cudaError_t launch_simt_commit(const CommitArgs &a, cudaStream_t s);
 
+bool tc_vtile_supported(const VerifyArgs &a);
+bool tc_vtile_preferred(const VerifyArgs &a);
+cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool overlap);
 bool tc_verify_supported(const VerifyArgs &a);
 size_t tc_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap);

@@ -79,8 +79,8 @@ constexpr int FU_L = 196608;            // L_i
 constexpr int FU_BETA = FU_L + 512;     // beta_i
 constexpr int FU_LG = FU_BETA + 512;    // log gamma_i
 constexpr int FU_MASK = FU_LG + 512;    // uint4 ancestor-or-self masks
-constexpr int FU_BAR = FU_MASK + 2048;  // [Q;K] TMA, MMA, S TMA, V TMA
-constexpr int FU_MISC = FU_BAR + 32;    // TMEM slot
+constexpr int FU_BAR = FU_MASK + 2048;  // [Q;K] TMA, MMA, S TMA, V TMA, drain
+constexpr int FU_MISC = FU_BAR + 48;    // TMEM slot
 constexpr int FU_END = FU_MISC + 16;
 constexpr int FU_SMEM = FU_END + 1024;
 static_assert(FU_SMEM <= 227 * 1024, "one fused CTA fits an SM");
@@ -125,7 +125,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         return;
     }
     if (tid == 0) {
-        for (int k = 0; k < 4; ++k) mbar_init(&bar[k], 1);
+        for (int k = 0; k < 5; ++k) mbar_init(&bar[k], 1); // 4: drain after a timeout
         fence_mbar_init();
         mbar_arrive_expect_tx(&bar[0], 65536);
 #pragma unroll
@@ -182,10 +182,16 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         if (i < T) logP[(size_t)(o + i) * H + h] = L;
     }
 
-    // Gram: Q K^T -> R0, K K^T -> R1 (bf16 products, fp32 accumulation)
+    // Gram: Q K^T -> R0, K K^T -> R1 (bf16 products, fp32 accumulation).
+    // Thread 0 issues every product between CTA barriers; once any thread's
+    // bounded wait has given up (`go` false after a barrier), nothing more is
+    // issued and nobody waits for a product.
     const uint32_t qa = smem_addr(sQK), ka = qa + 32768;
+    bool v_issued = false;
     if (tid == 0) {
         ok &= mbar_wait(&bar[0], 0, kWaitNs);
+    }
+    if (tid == 0 && ok) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -196,8 +202,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         }
         mma_commit(&bar[1]);
     }
-    __syncthreads(); // L visible
-    ok &= mbar_wait(&bar[1], mph, kWaitNs);
+    bool go = __syncthreads_and(ok); // L visible
+    if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
     mph ^= 1u;
     tc_fence_after();
     __syncwarp();
@@ -236,8 +242,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        go = __syncthreads_and(ok);
+        if (tid == 0 && go) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
@@ -246,7 +252,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                             IDESC_T128, kk > 0);
             mma_commit(&bar[1]);
         }
-        ok &= mbar_wait(&bar[1], mph, kWaitNs);
+        if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
         mph ^= 1u;
         tc_fence_after();
         __syncwarp();
@@ -297,9 +303,10 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     }
     tmem_wait_st();
     tc_fence_before();
-    __syncthreads(); // M (R0) and W (R2) final; the PB buffer is free
+    go = __syncthreads_and(ok); // M (R0) and W (R2) final; the PB buffer is free
     tc_fence_after();
-    if (tid == 0) { // the value rows into the freed PB buffer
+    if (go) v_issued = true;
+    if (tid == 0 && go) { // the value rows into the freed PB buffer
         mbar_arrive_expect_tx(&bar[3], 32768);
         tma_load_3d(sPB, &tmV, &bar[3], 0, h, o);
         tma_load_3d(sPB + 16384, &tmV, &bar[3], 64, h, o);
@@ -355,10 +362,10 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    go = __syncthreads_and(ok);
     // state products: Q S_pre -> R1, K S_pre -> R3 (S = S_hi + S_lo)
     const uint32_t s0 = smem_addr(sS);
-    if (tid == 0) {
+    if (tid == 0 && go) {
         // this CTA's inputs have landed: the CTA one wave later (pf_stride =
         // resident CTAs) finds its state, q, k and v in L2
         const int nu = unit + pf_stride;
@@ -393,9 +400,11 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         }
         mma_commit(&bar[1]);
     }
-    ok &= mbar_wait(&bar[1], mph, kWaitNs);
+    if (go) {
+        ok &= mbar_wait(&bar[1], mph, kWaitNs);
+        ok &= mbar_wait(&bar[3], 0, kWaitNs); // the value rows
+    }
     mph ^= 1u;
-    ok &= mbar_wait(&bar[3], 0, kWaitNs); // the value rows
     tc_fence_after();
     __syncwarp();
     // R^T = (beta (v - P K S_pre))^T over the dead state buffer, and P Q S_pre
@@ -431,9 +440,9 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    go = __syncthreads_and(ok);
     // propagation + read-out over the tree's node steps: R1 += M R (O), R3 = W R (U)
-    if (tid == 0) {
+    if (tid == 0 && go) {
         tc_fence_after();
         const int nk = (T + 7) / 8;
         for (int kk = 0; kk < nk; ++kk) {
@@ -443,13 +452,13 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         }
         mma_commit(&bar[1]);
     }
-    ok &= mbar_wait(&bar[1], mph, kWaitNs);
+    if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
     mph ^= 1u;
     tc_fence_after();
     __syncwarp();
     {
         const int i = m;
-        const bool store = ok && i < T;
+        const bool store = go && ok && i < T;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
             const int col0 = hf * 64 + cc * 32;
@@ -473,16 +482,20 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                 dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
         }
     }
-    if (!ok) {
-        report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
-        if (tid == 0) { // the copies still in flight end before the CTA does
+    if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
+    tc_fence_before();
+    if (!__syncthreads_and(ok)) {
+        // the products and copies still in flight end (bounded) before the
+        // CTA frees its tensor memory and leaves its shared memory to another
+        if (tid == 0) {
+            mma_commit(&bar[4]);
+            mbar_wait(&bar[4], 0, kWaitNs);
             mbar_wait(&bar[0], 0, kWaitNs);
             mbar_wait(&bar[2], 0, kWaitNs);
-            mbar_wait(&bar[3], 0, kWaitNs);
+            if (v_issued) mbar_wait(&bar[3], 0, kWaitNs);
         }
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
@@ -521,7 +534,7 @@ cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s)
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kTB);
     if (e != cudaSuccess) return e;
     auto kernel = a.vk ? tc_big_fused_kernel<true> : tc_big_fused_kernel<false>;
-    e = configure_once(reinterpret_cast<const void *>(kernel), FU_SMEM, true, a.vk ? 11 : 10);
+    e = configure_once(reinterpret_cast<const void *>(kernel), FU_SMEM, true);
     if (e != cudaSuccess) return e;
     // a workspace is not needed; one large enough receives a copy of [M; W]
     float *mw = (a.ws && a.ws_bytes >= tc_big_workspace_bytes(a.B, a.H))

@@ -127,28 +127,33 @@ inline cudaError_t make_layered_state_map(CUtensorMap *map, const float *S, int 
 }
 
 // Kernel attributes are per device and per function: set them on the first
-// launch on each device only (they do not change), so later calls -- and
-// stream capture -- meet no attribute call.
-inline cudaError_t configure_once(const void *fn, int smem, bool carveout, int slot)
+// launch of each kernel on each device only (they do not change), so later
+// calls -- and stream capture -- meet no attribute call.  Keyed by the
+// kernel's address.
+inline cudaError_t configure_once(const void *fn, int smem, bool carveout)
 {
     static std::mutex mu;
-    // slots: 0 verify, 1 commit, 2 large-tree factor, 3 large-tree solve,
-    // 4, 5, 6 the same kernels for the transposed state layout, 8 and 9 the
-    // small-tree verification (both layouts)
-    static uint64_t done[16] = {}; // bit = device, word = slot
+    constexpr int kMaxKernels = 64;
+    static const void *fns[kMaxKernels] = {};
+    static uint64_t done[kMaxKernels] = {}; // bit = device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (bit && (done[slot] & bit)) return cudaSuccess;
+    int slot = -1;
+    for (int i = 0; i < kMaxKernels; ++i) {
+        if (fns[i] == fn) { slot = i; break; }
+        if (fns[i] == nullptr) { fns[i] = fn; slot = i; break; }
+    }
+    if (slot >= 0 && bit && (done[slot] & bit)) return cudaSuccess;
     if (carveout) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
     }
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) done[slot] |= bit;
+    if (e == cudaSuccess && slot >= 0) done[slot] |= bit;
     return e;
 }
 

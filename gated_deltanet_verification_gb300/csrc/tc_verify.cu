@@ -131,7 +131,8 @@ constexpr uint32_t TM_GRAM = 128, TM_PROP = 128;                  // tensor-memo
 
 // mbarrier slots
 constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, BAR_STATE = 5,
-              BAR_MMA2 = 6, BAR_TOPO = 7, BAR_STAGED = 8, BAR_CG = 9, BAR_CONV = 10, BAR_OPS = 11;
+              BAR_MMA2 = 6, BAR_TOPO = 7, BAR_STAGED = 8, BAR_CG = 9, BAR_CONV = 10, BAR_OPS = 11,
+              BAR_DRAIN = 12;
 
 // Verification kernel: one CTA per (request, head).  Warp 8 streams operands
 // and issues the tensor-core products.  Warps 0..7 share the rest:
@@ -211,6 +212,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         mbar_init(&bar[BAR_CG], kT);
         mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
+        mbar_init(&bar[BAR_DRAIN], 1);
         fence_mbar_init();
         if (in_range) {
             // q rows 0.., k rows 64.. of each K-atom (boxes of kTmax rows)
@@ -249,7 +251,13 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     // launch they all arrive in one round trip.
     pdl_wait();
     int *sfault = reinterpret_cast<int *>(sm + OFF_MISC + 4);
-    if (tid == 0) *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
+    // Set by any thread whose bounded wait gave up; the issuing thread then
+    // issues no further copy or product.
+    volatile int *sfail = reinterpret_cast<volatile int *>(sm + OFF_MISC + 8);
+    if (tid == 0) {
+        *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
+        *sfail = 0;
+    }
     const int d = req_depth[b];
     // Depth and ancestor-or-self mask of each node as pack built them (rows
     // below 64: the first two words of the 128-bit mask).  A tree pack found
@@ -287,14 +295,23 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         return;
     }
     const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
+    // Bounded wait on phase 0 of barrier `i`; a timeout is recorded CTA-wide.
+    auto waitb = [&](int i) -> bool {
+        const bool r = mbar_wait(&bar[i], 0, kWaitNs);
+        if (!r) *sfail = 1;
+        return r;
+    };
+    bool v_issued = SMALL; // the value rows' copy (issued at entry for small trees)
 
     if (warp == kComputeThreads / 32) {
         // =========================== issue warp ===========================
         bool ok = true;
         if (lane == 0) {
             const uint32_t a1 = smem_addr(sA1), s0 = smem_addr(sbuf);
+            do { // every step ends the issue once a wait anywhere in the CTA gave up
             // Gram [Q;K] K^T
-            ok &= mbar_wait(&bar[BAR_A1], 0, kWaitNs);
+            ok &= waitb(BAR_A1);
+            if (!ok || *sfail) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -306,7 +323,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             mma_commit(&bar[BAR_GRAM]);
             // state products [Q;K] (S_hi + S_lo) once the split is in place,
             // in two halves of d_k (rows 0..63 of S_pre, then 64..127)
-            ok &= mbar_wait(&bar[BAR_CONV], 0, kWaitNs);
+            ok &= waitb(BAR_CONV);
+            if (!ok || *sfail) break;
             tc_fence_after();
             const uint32_t slo = s0 + 16384;
             constexpr uint32_t idesc_s = VK ? IDESC_STATE_VK : IDESC_STATE;
@@ -333,14 +351,17 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // value rows over the [Q;K] columns the first half has released
             // (small trees: loaded at entry)
             if (!SMALL) {
-                ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
+                ok &= waitb(BAR_STATE_A);
+                if (!ok || *sfail) break;
+                v_issued = true;
                 mbar_arrive_expect_tx(&bar[BAR_V], 16384);
                 tma_load_3d(sV, &tmV, &bar[BAR_V], 0, h, o);
                 tma_load_3d(sV + 8192, &tmV, &bar[BAR_V], 64, h, o);
             }
             // propagation + read-out: [M; W] R into its own 128 columns
             // (the K extent is the tree: ceil(T / 8) steps of 8 nodes)
-            ok &= mbar_wait(&bar[BAR_OPS], 0, kWaitNs);
+            ok &= waitb(BAR_OPS);
+            if (!ok || *sfail) break;
             tc_fence_after();
             const uint32_t b2 = s0 + 32768;
             for (int kk = 0; kk < (T + 7) / 8; ++kk) {
@@ -349,6 +370,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                             sdesc_sw128(b2 + off, 16, 1024), IDESC_TF32, kk > 0);
             }
             mma_commit(&bar[BAR_MMA2]);
+            } while (0);
         }
         __syncwarp();
         if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 0);
@@ -410,8 +432,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // Stage the Gram rows (q.k for rows 0..63, k.k for 64..127; small
             // trees: rows 0..31 and 64..95, columns 0..31, with no wait for
             // the state products).
-            ok &= mbar_wait(&bar[BAR_GRAM], 0, kWaitNs);
-            if (!SMALL) ok &= mbar_wait(&bar[BAR_STATE_A], 0, kWaitNs);
+            ok &= waitb(BAR_GRAM);
+            if (!SMALL) ok &= waitb(BAR_STATE_A);
             tc_fence_after();
             __syncwarp();
             float4 *srow = reinterpret_cast<float4 *>(staged_row(m));
@@ -429,7 +451,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (topo) {
             // Compact C and G of row i, gathered in depth order (small trees:
             // warp 0 only, the rows of warp 1 are past the tree).
-            ok &= mbar_wait(&bar[BAR_STAGED], 0, kWaitNs);
+            ok &= waitb(BAR_STAGED);
             const float *qk = staged_row(i), *kk = staged_row(64 + i);
             float *crow = Cc + i * kLd, *grow = Gc + i * kLd;
             float qv[kSlots], kv[kSlots]; // every load first, then the products
@@ -453,7 +475,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // bf16, N-contiguous, 64-column atoms: boxes (0,1) <- columns 0..63,
             // boxes (2,3) <- columns 64..127.
             const int r = tid - 128;
-            ok &= mbar_wait(&bar[BAR_S], 0, kWaitNs);
+            ok &= waitb(BAR_S);
 #pragma unroll 1
             for (int pc = 0; pc < 2; ++pc) {
                 uint8_t *box0 = sbuf + (2 * pc) * 16384, *box1 = box0 + 16384;
@@ -487,7 +509,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             fence_proxy_async_smem();
             mbar_arrive(&bar[BAR_CONV]);
         }
-        ok &= mbar_wait(&bar[BAR_TOPO], 0, kWaitNs);
+        ok &= waitb(BAR_TOPO);
         const float p = (i < T) ? expf(Ls[i]) : 0.f; // P_i
 
         if (SMALL && warp < 2) {
@@ -496,7 +518,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // run and written into the [M; W] operand once they are done.
             const int n = lane;
             const bool wrow = warp == 0;
-            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
+            ok &= waitb(BAR_CG);
             float vals[kSlots];
             uint32_t aw4[4] = {0, 0, 0, 0};
             int di = -1;
@@ -536,7 +558,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                     }
                 }
             }
-            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            ok &= waitb(BAR_STATE);
             const int orow = wrow ? 64 + n : n;
 #pragma unroll
             for (int c = 0; c < 8; ++c) // K extent <= 32 nodes: the first K-atom
@@ -552,8 +574,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         } else if (SMALL && rowgrp == 2) {
             // R^T of nodes 0..31 (warp 2: columns 0..63, warp 6: 64..127),
             // value rows from the [Q;K] padding.
-            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
+            ok &= waitb(BAR_STATE);
+            ok &= waitb(BAR_V);
             tc_fence_after();
             __syncwarp();
             uint8_t *dst = sbuf + 32768;
@@ -584,8 +606,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // [M; W] operand (row i of M, row 64 + i of W, column = ancestor)
             // once the gathers and the state products have released it.  Each
             // thread zeroes its own row first (program order keeps the values).
-            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
+            ok &= waitb(BAR_CG);
+            ok &= waitb(BAR_STATE);
             const bool wrow = topo;
             const int orow = wrow ? 64 + i : i;
 #pragma unroll
@@ -635,9 +657,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // R^T = (beta (v - P K S_pre))^T for columns 64 half .. +63 of the
             // rows 64..127 (warps 2, 3, 6, 7), once the staged Gram in this
             // buffer has been gathered.
-            ok &= mbar_wait(&bar[BAR_STATE], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_CG], 0, kWaitNs);
-            ok &= mbar_wait(&bar[BAR_V], 0, kWaitNs);
+            ok &= waitb(BAR_STATE);
+            ok &= waitb(BAR_CG);
+            ok &= waitb(BAR_V);
             tc_fence_after();
             __syncwarp();
             uint8_t *dst = sbuf + 32768 + (i >> 5) * 16384;
@@ -666,7 +688,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         mbar_arrive(&bar[BAR_OPS]);
 
         // ---- outputs: O = P (Q S_pre) + M R (bf16), U = W R (fp32) ----
-        ok &= mbar_wait(&bar[BAR_MMA2], 0, kWaitNs);
+        ok &= waitb(BAR_MMA2);
         tc_fence_after();
         __syncwarp();
         if (!SMALL || !(rowgrp & 1)) { // small trees: no output in the padding lanes
@@ -706,6 +728,19 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
+    if (*sfail) { // read after the barrier: the same value in every thread
+        // After a timeout the products and copies this CTA issued must end
+        // before its tensor memory and shared memory go to another CTA: wait
+        // (bounded) for every one of them.
+        if (issuer) {
+            mma_commit(&bar[BAR_DRAIN]);
+            mbar_wait(&bar[BAR_DRAIN], 0, kWaitNs);
+            mbar_wait(&bar[BAR_A1], 0, kWaitNs);
+            mbar_wait(&bar[BAR_S], 0, kWaitNs);
+            if (v_issued) mbar_wait(&bar[BAR_V], 0, kWaitNs);
+        }
+        __syncthreads();
+    }
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -733,8 +768,8 @@ constexpr int CO_S = 0;                       // one box of the half: [128 rows 
 constexpr int CO_A = 16384;                   // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
 constexpr int CO_B = CO_A + 8192;             // U_a^T chunk: 64 rows x 16 tf32
 constexpr int CO_PATH = CO_B + 4096;          // int[128]
-constexpr int CO_BAR = CO_PATH + 512;         // 2 mbarriers
-constexpr int CO_TSLOT = CO_BAR + 16;
+constexpr int CO_BAR = CO_PATH + 512;         // 3 mbarriers
+constexpr int CO_TSLOT = CO_BAR + 24;
 constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag, status copy
 constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
 constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
@@ -773,7 +808,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     uint8_t *sA = sm + CO_A;
     uint8_t *sB = sm + CO_B;
     int *path = reinterpret_cast<int *>(sm + CO_PATH);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CO_BAR); // tma, mma
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CO_BAR); // tma, mma, drain
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CO_TSLOT);
     int *plen = reinterpret_cast<int *>(sm + CO_MISC);
     int *flag = plen + 1;
@@ -793,6 +828,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmS);
         tma_prefetch_l2_3d(&tmS, kTile * hv, unit * kD, layer);
@@ -852,6 +888,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     const float La = logP[(size_t)(o + a) * H + h];
 
     const uint32_t sa = smem_addr(sA), sb = smem_addr(sB);
+    int nload = 0; // state boxes requested on bar[0] (thread 0)
     const int nchunks = (*(volatile int *)flag != 0) ? 0 : (L + kChunk - 1) / kChunk;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int tn = min(kChunk, L - ch * kChunk); // path nodes in this chunk
@@ -879,6 +916,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                 }
             }
             if (ch == 0 && t0 == 0 && tid == 0) {
+                ++nload;
                 mbar_arrive_expect_tx(&bar[0], 16384);
                 tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
                 tma_prefetch_l2_3d(&tmS, kTile * hv + 32, unit * kD, layer); // second box
@@ -943,6 +981,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         }
         tc_fence_after();
         __syncthreads();
+        if (*(volatile int *)flag != 0) break; // no further product after a timeout
     }
 
     // epilogue, one 32-column box at a time: S <- P_a S + D in shared memory,
@@ -958,6 +997,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
             if (cb == 1 && tid == 0) {
                 bulk_wait_group_read0(); // the first box's store has read the buffer
                 if (ok) {
+                    ++nload;
                     mbar_arrive_expect_tx(&bar[0], 16384);
                     tma_load_3d(sS, &tmS, &bar[0], kTile * hv + 32, unit * kD, layer);
                 }
@@ -996,6 +1036,16 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
     }
     tc_fence_before();
     __syncthreads();
+    if (*(volatile int *)flag != 0 && nchunks > 0) {
+        // after a timeout: the products and the state copy this CTA issued
+        // end (bounded) before its tensor and shared memory are released
+        if (tid == 0) {
+            mma_commit(&bar[2]);
+            mbar_wait(&bar[2], 0, kWaitNs);
+            if (nload > 0) mbar_wait(&bar[0], (uint32_t)(nload - 1) & 1u, kWaitNs);
+        }
+        __syncthreads();
+    }
     if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
@@ -1040,8 +1090,7 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
     if (e != cudaSuccess) return e;
     auto kernel = small ? (a.vk ? tc_verify_kernel<true, true> : tc_verify_kernel<false, true>)
                         : (a.vk ? tc_verify_kernel<true, false> : tc_verify_kernel<false, false>);
-    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true,
-                       small ? (a.vk ? 9 : 8) : (a.vk ? 4 : 0));
+    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
@@ -1064,7 +1113,7 @@ cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap)
     cudaError_t e = make_layered_state_map(&map, a.S, units, a.layers, a.s_ls);
     if (e != cudaSuccess) return e;
     auto kernel = a.vk ? tc_commit_kernel<true> : tc_commit_kernel<false>;
-    e = configure_once(reinterpret_cast<const void *>(kernel), COMMIT_SMEM, false, a.vk ? 5 : 1);
+    e = configure_once(reinterpret_cast<const void *>(kernel), COMMIT_SMEM, false);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units, kD / kTile, a.layers),

@@ -1,0 +1,596 @@
+// Value-tiled tensor-core verification for small trees: bf16 q/k/v,
+// d_k = d_v = 128, trees of up to 32 nodes, depth <= 15 (the batched
+// Qwen3.5-shaped workloads of the pages' evaluation).
+//
+// The pages' kernel splits d_v into N_v = d_v / b_v value tiles and gives each
+// (request, head, tile) its own CTA, so a request yields H * N_v
+// independently schedulable CTAs ("Bole", Section IV-B, value-tiled kernel).
+// Here b_v = 64, N_v = 2: each CTA streams its 128 x 64 tile of S_pre by TMA,
+// forms the tree factors of its head on chip (both tiles of a head repeat
+// that small T x T work instead of exchanging it), and writes its 64 columns
+// of O and U.  A CTA needs 66 KB of shared memory and 128 tensor-memory
+// columns, so three share an SM and one wave covers 456 tiles.  The library
+// runs it for batches whose heads would leave the one-CTA-per-head kernel
+// short of a wave (a single request's heads, say): there the extra CTAs add
+// parallelism, while on larger batches the one-CTA kernel keeps more state
+// bytes in flight per SM.
+//
+// Per CTA (T <= 32 nodes of one head, value columns c0 .. c0 + 63):
+//   1. TMA: [Q;K] of the tree (q rows 0..31, k rows 32..63 of each K-atom)
+//      and the value rows of the tile; once the per-node reads have returned,
+//      the two 32-column boxes of the S_pre tile.
+//   2. Warp 0: cumulative decay L_i along the ancestor-or-self mask (Lemma 1),
+//      the decay ratios exp(L_i - L_j) of each node's ancestors.
+//   3. tcgen05 Gram [Q;K] K^T (bf16 products, fp32 accumulation); warps 0, 1
+//      stage its rows in shared memory; warp 0 gathers the compact
+//        C_ij = exp(L_i - L_j) q_i.k_j          (j an ancestor of i, or i)
+//        G_ij = beta_i exp(L_i - L_j) k_i.k_j   (j a strict ancestor of i)
+//      by ancestor depth; rows of W = (I+G)^{-1} (warp 0) and M = C W
+//      (warp 5) by backward substitution along each node's ancestor path --
+//      the finite Neumann sum of Eq. (6), term for term.
+//   4. Warps 1..4 split the S_pre tile in place into bf16 S_hi + S_lo as soon
+//      as it lands (~2^-17 relative residue per element); tcgen05
+//      [Q;K] (S_hi + S_lo) with exact bf16 products and fp32 accumulation
+//      gives Q S_pre and K S_pre of the tile (Eq. (7)).
+//   5. Warps 1, 5: R^T = (beta (v - P K S_pre))^T of the tile; warps 0, 5
+//      write [M; W] -- both into the tile buffer the products released.
+//   6. One tcgen05 tf32 product [M; W] R (K = the tree's nodes) into the
+//      Gram's tensor-memory columns; warps 0, 4 write O = P Q S_pre + M R
+//      (bf16), warps 1, 5 U = W R (fp32).
+//
+// [Q;K] is stored without padding (64 rows per K-atom); the M = 128 products
+// read the 8 KB behind each atom as rows 64..127, whose results land in
+// tensor-memory lanes 64..127 that nothing reads.  The same holds for [M; W].
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+#include "tc_common.cuh"
+
+namespace bole {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kVT = 32;     // tree nodes per CTA
+constexpr int kVB = 64;     // b_v: value columns per CTA
+constexpr int kVSlots = 16; // depth slots of the compact factors: depth <= 15
+constexpr int kVLd = 17;    // padded row stride of the compact factors
+
+// ---- shared-memory plan (bytes from a 1024-aligned base) ----
+//   S (32 KB): the state tile as two fp32 boxes [128 rows x 32 columns],
+//     split in place into S_hi (first box) and S_lo (second box), bf16
+//     N-contiguous [128 d_k rows x 64 columns]; after the state products
+//     [M; W] (rows 0..63, tf32 K-major, 128 B per row) in the first 8 KB and
+//     R^T (64 value rows x 32 nodes, tf32 K-major) in 16..24 KB.
+//   QK (16 KB): two K-atoms [64 rows x 128 B] of bf16 q (rows 0..31) and k
+//     (rows 32..63); the M = 128 products read 8 KB past each atom.
+//   V (4 KB): the tile's value rows [32 nodes x 64 bf16], 128B-swizzled.
+//   G (8 KB): the staged Gram rows [64 x 32 fp32] (q.k rows 0..31, k.k rows
+//     32..63), 16-byte chunks XOR-swizzled by row.
+//   X: compact C, G [32][17], ancestor table [32][16] u8, L, depth, log gamma.
+constexpr int VT_S = 0;
+constexpr int VT_QK = 32768;
+constexpr int VT_V = VT_QK + 16384;
+constexpr int VT_G = VT_V + 4096;
+constexpr int VT_X = VT_G + 8192;
+constexpr int VT_FAC = kVT * kVLd * 4;
+constexpr int VT_GC = VT_X;
+constexpr int VT_CC = VT_GC + VT_FAC;
+constexpr int VT_ANCAT = VT_CC + VT_FAC;
+constexpr int VT_L = VT_ANCAT + kVT * kVSlots;
+constexpr int VT_DEPTH = VT_L + kVT * 4;
+constexpr int VT_LG = VT_DEPTH + kVT * 4;
+constexpr int VT_BAR = VT_LG + kVT * 4;
+constexpr int VT_MISC = VT_BAR + 16 * 8; // TMEM slot, status copy, wait-failure flag
+constexpr int VT_END = VT_MISC + 16;
+constexpr int VT_SMEM = VT_END + 1024;   // slack for the 1024-byte alignment of the base
+static_assert(VT_ANCAT % 16 == 0 && VT_BAR % 8 == 0, "aligned scratch");
+static_assert(VT_QK + 16384 + 8192 <= VT_X, "the products' reads past [Q;K] stay in V and G");
+static_assert(3 * (VT_SMEM + 1024) <= 228 * 1024, "three value-tile CTAs per SM");
+
+constexpr int kVTCompute = 192;               // warps 0..5
+constexpr int kVTThreads = kVTCompute + 32;   // warp 6: TMA and tcgen05 issue
+constexpr uint32_t TM_COLS = 128;             // tensor-memory columns per CTA
+constexpr uint32_t TM_GP = 64;                // Gram, then the propagation [M R; W R]
+
+constexpr uint32_t IDESC_VGRAM = idesc_bf16(128, 32, false, false);  // [Q;K] K^T
+constexpr uint32_t IDESC_VSTATE = idesc_bf16(128, kVB, false, true); // [Q;K] S, S N-contiguous
+constexpr uint32_t IDESC_VPROP = idesc_tf32(128, kVB, false, false); // [M; W] R
+
+// mbarrier slots
+constexpr int VB_S = 0, VB_QK = 1, VB_V = 2, VB_GRAM = 3, VB_STATE = 4, VB_PROP = 5,
+              VB_TOPO = 6, VB_STAGED = 7, VB_CG = 8, VB_CONV = 9, VB_OPS = 10, VB_DRAIN = 11;
+
+__global__ void __launch_bounds__(kVTThreads, 3)
+tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const float *__restrict__ gamma, const float *__restrict__ beta,
+                const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc,
+                const int32_t *__restrict__ req_depth, int H, int N,
+                __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
+                float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *sS = sm + VT_S, *sQK = sm + VT_QK, *sV = sm + VT_V, *sG = sm + VT_G;
+    float *Gc = reinterpret_cast<float *>(sm + VT_GC);
+    float *Cc = reinterpret_cast<float *>(sm + VT_CC);
+    uint8_t *ancat = sm + VT_ANCAT;
+    float *Ls = reinterpret_cast<float *>(sm + VT_L);
+    int *Ds = reinterpret_cast<int *>(sm + VT_DEPTH);
+    float *LGs = reinterpret_cast<float *>(sm + VT_LG);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + VT_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + VT_MISC);
+    int *sfault = reinterpret_cast<int *>(sm + VT_MISC + 4);
+    volatile int *sfail = reinterpret_cast<volatile int *>(sm + VT_MISC + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x >> 1, vh = blockIdx.x & 1; // (request, head), value tile
+    const int b = unit / H, h = unit % H;
+    const int c0 = vh * kVB; // first value column of the tile
+
+    if (sm + VT_END > smem_raw + VT_SMEM) { // dynamic base too far from 1024 B
+        if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -5);
+        return;
+    }
+    // A launch of its own allocates tensor memory first (the SM starts the
+    // next CTA once this one has given up its allocation permit); a launch
+    // overlapping the previous kernel allocates after its prologue.
+    if (early_alloc && warp == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    pdl_launch_dependents();
+    const int o = offsets[b], T = offsets[b + 1] - o;
+    const bool in_range = T > 0 && T <= kVT && o >= 0 && o + T <= N;
+    const bool issuer = tid == kVTCompute;
+    if (issuer) {
+        for (int k = VB_S; k <= VB_PROP; ++k) mbar_init(&bar[k], 1);
+        mbar_init(&bar[VB_TOPO], 32);
+        mbar_init(&bar[VB_STAGED], 64);
+        mbar_init(&bar[VB_CG], 32);
+        mbar_init(&bar[VB_CONV], 128);
+        mbar_init(&bar[VB_OPS], kVTCompute);
+        mbar_init(&bar[VB_DRAIN], 1);
+        fence_mbar_init();
+        if (in_range) {
+            // q rows 0..31 and k rows 32..63 of both K-atoms; the tile's value rows
+            mbar_arrive_expect_tx(&bar[VB_QK], 16384);
+#pragma unroll
+            for (int ka = 0; ka < 2; ++ka) {
+                tma_load_3d(sQK + ka * 8192, &tmQ, &bar[VB_QK], 64 * ka, h, o);
+                tma_load_3d(sQK + ka * 8192 + 4096, &tmK, &bar[VB_QK], 64 * ka, h, o);
+            }
+            mbar_arrive_expect_tx(&bar[VB_V], 4096);
+            tma_load_3d(sV, &tmV, &bar[VB_V], c0, h, o);
+        }
+    }
+    // per-thread tree inputs: warp 0 (node = lane) the gates of its row, warps
+    // 1 and 5 (node = lane, the K-side rows) beta for R^T
+    const int i = lane;
+    float bt = 0.f, g_i = 1.f;
+    if (in_range && i < T && (warp == 0 || warp == 1 || warp == 5)) {
+        bt = beta[(size_t)(o + i) * H + h];
+        if (warp == 0) g_i = gamma[(size_t)(o + i) * H + h];
+    }
+    // What the previous call wrote (the status word pack reset, the request's
+    // depth, each node's ancestor-or-self mask) is read after the wait.
+    pdl_wait();
+    if (tid == 0) {
+        *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
+        *sfail = 0;
+    }
+    const int d = req_depth[b];
+    int my_depth = -1;
+    uint32_t my_mask = 0;
+    if (warp == 0 && in_range && i < T) {
+        my_mask = anc[(size_t)(o + i) * 4]; // a tree of <= 32 nodes: the first word
+        my_depth = __popc(my_mask) - 1;
+        if (my_depth >= kVSlots) my_depth = -1; // the request is refused below
+    }
+    if (warp == 0) LGs[i] = logf(g_i); // consumes gamma before the barrier
+    if (!early_alloc && warp == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int fault = *sfault;
+    const bool bad = !in_range || d < 0 || d >= kVSlots || d >= T;
+    if (issuer && fault == 0 && T > 0 && !bad) {
+        // The state tile is requested once the small reads have returned:
+        // requested at entry it queued them behind every CTA's state burst
+        // (28.1 -> 26.3 us on the batched forest).
+        mbar_arrive_expect_tx(&bar[VB_S], 32768);
+        tma_load_2d(sS, &tmS, &bar[VB_S], c0, unit * kD);
+        tma_load_2d(sS + 16384, &tmS, &bar[VB_S], c0 + 32, unit * kD);
+    }
+    if (fault != 0 || T <= 0 || bad) {
+        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0 && vh == 0)
+            report(st, T > kVT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH,
+                   b, -1, T > kVT ? T : d);
+        if (issuer) { // the copies in flight end before the CTA retires
+            if (in_range) {
+                mbar_wait(&bar[VB_QK], 0, kWaitNs);
+                mbar_wait(&bar[VB_V], 0, kWaitNs);
+            }
+        }
+        if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+        return;
+    }
+    const int quad = warp & 3; // the tensor-memory lanes this warp reaches
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    auto waitb = [&](int k) -> bool {
+        const bool r = mbar_wait(&bar[k], 0, kWaitNs);
+        if (!r) *sfail = 1;
+        return r;
+    };
+    // staged Gram row r (0..63): 32 fp32, chunks XOR-swizzled by r & 7
+    auto staged = [&](int r) -> float * { return reinterpret_cast<float *>(sG + r * 128); };
+
+    if (warp == kVTCompute / 32) {
+        // =========================== issue warp ===========================
+        bool ok = true;
+        if (lane == 0) {
+            const uint32_t qk = smem_addr(sQK), s0 = smem_addr(sS);
+            do { // every step ends the issue once a wait anywhere in the CTA gave up
+                ok &= waitb(VB_QK);
+                if (!ok || *sfail) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) { // Gram [Q;K] K^T, 16 d_k per step
+                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + TM_GP, sdesc_sw128(qk + off, 16, 1024),
+                                sdesc_sw128(qk + off + 4096, 16, 1024), IDESC_VGRAM, kk > 0);
+                }
+                mma_commit(&bar[VB_GRAM]);
+                ok &= waitb(VB_CONV);
+                if (!ok || *sfail) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) { // [Q;K] (S_hi + S_lo), 16 d_k rows per step
+                    const uint64_t ad = sdesc_sw128(qk + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + kk * 2048, 16384, 1024), IDESC_VSTATE,
+                                kk > 0);
+                    mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + 16384 + kk * 2048, 16384, 1024),
+                                IDESC_VSTATE, 1);
+                }
+                mma_commit(&bar[VB_STATE]);
+                // the state tile of the CTA one wave later goes to L2 now that
+                // this CTA's own tile has landed
+                const int nx = (int)blockIdx.x + pf_stride;
+                if (pf_stride > 0 && nx < (int)gridDim.x) {
+                    tma_prefetch_l2_2d(&tmS, (nx & 1) * kVB, (nx >> 1) * kD);
+                    tma_prefetch_l2_2d(&tmS, (nx & 1) * kVB + 32, (nx >> 1) * kD);
+                }
+                ok &= waitb(VB_OPS);
+                if (!ok || *sfail) break;
+                tc_fence_after();
+                for (int kk = 0; kk < (T + 7) / 8; ++kk) // [M; W] R over the tree's nodes
+                    mma_tf32_ss(tmem + TM_GP, sdesc_sw128(s0 + kk * 32, 16, 1024),
+                                sdesc_sw128(s0 + 16384 + kk * 32, 16, 1024), IDESC_VPROP, kk > 0);
+                mma_commit(&bar[VB_PROP]);
+            } while (0);
+        }
+        __syncwarp();
+        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 30);
+    } else {
+        // ========================== compute warps =========================
+        bool ok = true;
+        float ratio[kVSlots];          // warp 0: exp(L_i - L_j), j the ancestor at depth t
+        uint32_t aw[4] = {0, 0, 0, 0}; // warp 0: ancestor-by-depth table, packed bytes
+        if (warp == 0) {
+            // Topology and cumulative decay (node i = lane): the ancestors come
+            // out of the mask in depth order (parents precede children), so the
+            // partial sums of log gamma are their L_j (Lemma 1).
+            __syncwarp();
+            int jt[kVSlots];
+            uint32_t mm = my_depth >= 0 ? my_mask : 0u;
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) {
+                jt[t] = mm ? __ffs(mm) - 1 : 0;
+                mm &= mm - 1;
+            }
+            float lgv[kVSlots];
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) lgv[t] = LGs[jt[t]];
+            float L = 0.f;
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) {
+                if (t <= my_depth) {
+                    L += lgv[t];
+                    aw[t >> 2] |= (uint32_t)jt[t] << (8 * (t & 3));
+                }
+                ratio[t] = L;
+            }
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) ratio[t] = __expf(L - ratio[t]);
+            *reinterpret_cast<uint4 *>(ancat + i * kVSlots) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+            Ls[i] = L;
+            Ds[i] = my_depth;
+            if (vh == 0 && i < T) logP[(size_t)(o + i) * H + h] = L;
+            mbar_arrive(&bar[VB_TOPO]);
+        }
+        if (warp < 2) {
+            // stage the Gram rows: q.k (warp 0, lanes 0..31), k.k (warp 1)
+            ok &= waitb(VB_GRAM);
+            tc_fence_after();
+            __syncwarp();
+            const int r = warp * 32 + lane;
+            float4 *srow = reinterpret_cast<float4 *>(staged(r));
+            float x[32];
+            tmem_ld32(tmem + TM_GP + lane_base, x);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                srow[c4 ^ (r & 7)] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2],
+                                                 x[4 * c4 + 3]);
+            mbar_arrive(&bar[VB_STAGED]);
+        }
+        if (warp == 0) {
+            // compact C and G of row i, gathered in depth order
+            ok &= waitb(VB_STAGED);
+            const float *qk = staged(i), *kk = staged(32 + i);
+            float *crow = Cc + i * kVLd, *grow = Gc + i * kVLd;
+            float qv[kVSlots], kv[kVSlots];
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) {
+                const int j = (aw[t >> 2] >> (8 * (t & 3))) & 0xff;
+                const int sw = (((j >> 2) ^ (i & 7)) << 2) | (j & 3);
+                qv[t] = qk[sw];
+                kv[t] = kk[sw];
+            }
+#pragma unroll
+            for (int t = 0; t < kVSlots; ++t) {
+                if (t <= my_depth) {
+                    crow[t] = ratio[t] * qv[t];
+                    if (t < my_depth) grow[t] = bt * ratio[t] * kv[t];
+                }
+            }
+            mbar_arrive(&bar[VB_CG]);
+        }
+        if (warp >= 1 && warp <= 4) {
+            // S_pre tile = S_hi + S_lo in place (row r): both boxes' row r
+            // (columns 0..31, 32..63) become 64 bf16 of S_hi (first box) and
+            // of S_lo (second box), N-contiguous and 128B-swizzled
+            const int r = tid - 32;
+            ok &= waitb(VB_S);
+            uint8_t *box0 = sS, *box1 = sS + 16384;
+            float x[64];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(box0 + sw128_chunk(r, c));
+                const float4 a1 = *reinterpret_cast<const float4 *>(box1 + sw128_chunk(r, c));
+                x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z; x[4 * c + 3] = a0.w;
+                x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
+                x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                    const float2 hf = __bfloat1622float2(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+                    hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
+                    lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+                }
+                *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) =
+                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) =
+                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar[VB_CONV]);
+        }
+        ok &= waitb(VB_TOPO);
+        const float p = (i < T) ? expf(Ls[i]) : 0.f; // P_i of node i = lane
+
+        if (warp == 0 || warp == 5) {
+            // Rows of W (warp 0: y) and M (warp 5: z) of node n = lane by
+            // backward substitution along its ancestor path a_0 .. a_d = n:
+            //   y_t = [t = d] - sum_{u > t} y_u G(a_u, a_t),
+            //   z_t = C(n, a_t) - sum_{u > t} z_u G(a_u, a_t),
+            // the finite Neumann sum of Eq. (6) restricted to the path (Lemma 3).
+            // Formed while the state products run; written into the [M; W]
+            // operand once they have released the tile buffer.
+            const int n = lane;
+            const bool wrow = warp == 0;
+            ok &= waitb(VB_CG);
+            float vals[kVSlots];
+            uint32_t aw4[4] = {0, 0, 0, 0};
+            int di = -1;
+            if (n < T) {
+                di = Ds[n];
+                const uint4 a4 = *reinterpret_cast<const uint4 *>(ancat + n * kVSlots);
+                aw4[0] = a4.x; aw4[1] = a4.y; aw4[2] = a4.z; aw4[3] = a4.w;
+                const float *ci = Cc + n * kVLd;
+                float cv[kVSlots], acc[kVSlots], gcur[kVSlots];
+#pragma unroll
+                for (int t = 0; t < kVSlots; ++t) {
+                    cv[t] = wrow ? 0.f : ci[t];
+                    acc[t] = 0.f;
+                }
+                {
+                    const float *gr = Gc + n * kVLd;
+#pragma unroll
+                    for (int t = 0; t < kVSlots - 1; ++t) gcur[t] = gr[t];
+                }
+#pragma unroll
+                for (int u = kVSlots - 1; u >= 0; --u) {
+                    vals[u] = 0.f;
+                    if (u <= di) {
+                        float gnext[kVSlots];
+                        if (u >= 1) { // G row of the ancestor at depth u - 1, one step ahead
+                            const int an = (aw4[(u - 1) >> 2] >> (8 * ((u - 1) & 3))) & 0xff;
+                            const float *gr = Gc + an * kVLd;
+#pragma unroll
+                            for (int t = 0; t < u - 1; ++t) gnext[t] = gr[t];
+                        }
+                        const float val = wrow ? ((u == di) ? 1.f : -acc[u]) : cv[u] - acc[u];
+                        vals[u] = val;
+#pragma unroll
+                        for (int t = 0; t < u; ++t) acc[t] = fmaf(val, gcur[t], acc[t]);
+#pragma unroll
+                        for (int t = 0; t < u - 1; ++t) gcur[t] = gnext[t];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kVSlots; ++u) vals[u] = 0.f;
+            }
+            ok &= waitb(VB_STATE);
+            const int orow = wrow ? 32 + n : n; // [M; W]: M rows 0..31, W rows 32..63
+#pragma unroll
+            for (int c = 0; c < 8; ++c) // K extent <= 32 nodes: one 128-byte row
+                *reinterpret_cast<float4 *>(sS + sw128_chunk(orow, c)) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < kVSlots; ++u) {
+                if (u <= di) {
+                    const int au = (aw4[u >> 2] >> (8 * (u & 3))) & 0xff;
+                    *reinterpret_cast<float *>(sS + sw128_offset(orow, au)) = vals[u];
+                }
+            }
+        }
+        if (warp == 1 || warp == 5) {
+            // R^T of the tile's columns 32 (warp / 5) .. + 31 for node i = lane:
+            // K S_pre from tensor-memory lanes 32..63, the value row from V.
+            ok &= waitb(VB_STATE);
+            ok &= waitb(VB_V);
+            tc_fence_after();
+            __syncwarp();
+            const int col0 = warp == 5 ? 32 : 0;
+            uint8_t *dst = sS + 16384;
+            const uint8_t *vrow = sV + i * 128;
+            float x[32];
+            tmem_ld32(tmem + lane_base + col0, x);
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                  vrow + ((((col0 >> 3) + uu) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int c = 8 * uu + t;
+                    const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
+                    *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i)) = r;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar[VB_OPS]);
+
+        // ---- outputs: O = P (Q S_pre) + M R (warps 0, 4), U = W R (warps 1, 5) ----
+        if (quad < 2) {
+            ok &= waitb(VB_PROP);
+            tc_fence_after();
+            __syncwarp();
+            const int col0 = warp >= 4 ? 32 : 0;
+            float x[32];
+            tmem_ld32(tmem + TM_GP + lane_base + col0, x);
+            const bool store = ok && !*sfail && i < T;
+            const size_t row = ((size_t)(o + i) * H + h) * kD + c0 + col0;
+            if (quad == 0) {
+                float y[32];
+                tmem_ld32(tmem + lane_base + col0, y);
+                if (store) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
+                    uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        __nv_bfloat162 p2[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
+                        dsto[uu] = *reinterpret_cast<uint4 *>(p2);
+                    }
+                }
+            } else if (store) {
+                float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu)
+                    dstu[uu] = make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
+            }
+        }
+        if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 31);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*sfail) { // read after the barrier: the same value in every thread
+        // after a timeout the products and copies this CTA issued end
+        // (bounded) before its tensor and shared memory go to another CTA
+        if (issuer) {
+            mma_commit(&bar[VB_DRAIN]);
+            mbar_wait(&bar[VB_DRAIN], 0, kWaitNs);
+            mbar_wait(&bar[VB_QK], 0, kWaitNs);
+            mbar_wait(&bar[VB_V], 0, kWaitNs);
+            mbar_wait(&bar[VB_S], 0, kWaitNs);
+        }
+        __syncthreads();
+    }
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+} // namespace
+
+// CTAs of a launch resident at once (per_sm per SM), 0 if unknown
+static int vtile_resident_ctas(int per_sm)
+{
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = n;
+    }
+    return per_sm * sms[dev];
+}
+
+bool tc_vtile_supported(const VerifyArgs &a)
+{
+    return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && a.max_T <= kVT &&
+           a.max_depth < kVSlots && !a.vk;
+}
+
+// Value tiles pay off while the heads of the batch leave the one-CTA
+// kernel (two CTAs per SM) short of one wave: measured on the 16-head
+// single request, 7.5 vs 7.8 us; on 512 heads, 28 vs 22 us (each CTA's
+// latency chain is as long as the one-CTA kernel's, so halving its state
+// bytes leaves fewer bytes in flight per SM).
+bool tc_vtile_preferred(const VerifyArgs &a)
+{
+    const int slots = vtile_resident_ctas(2);
+    return slots > 0 && a.B * a.H < slots;
+}
+
+cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
+{
+    const int units = a.B * a.H;
+    if (units == 0 || a.N == 0) return cudaSuccess;
+    CUtensorMap mS, mQ, mK, mV;
+    cudaError_t e = make_state_map(&mS, a.S_pre, units);
+    if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, kVT);
+    if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kVT);
+    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kVT);
+    if (e != cudaSuccess) return e;
+    e = configure_once(reinterpret_cast<const void *>(tc_vtile_kernel), VT_SMEM, true);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(dim3(2 * units), dim3(kVTThreads), VT_SMEM, s,
+                                                 overlap, attr);
+    return cudaLaunchKernelEx(&cfg, tc_vtile_kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets,
+                              a.anc, a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O),
+                              a.U, a.logP, a.st, vtile_resident_ctas(3), overlap ? 0 : 1);
+}
+
+} // namespace bole

@@ -13,16 +13,27 @@
  *     Eq. (4)), G_ij = beta_i (P_i/P_j) k_i.k_j for j in A(i) (Lemma 2,
  *     Eq. (5)), C_ij = (P_i/P_j) q_i.k_j for j in A(i) or j = i, and the
  *     inverse equal to the finite Neumann sum of (-G)^m, m <= d (Lemma 3,
- *     Eq. (6)), evaluated by the recurrence Z <- -G Z, U += Z (Eq. (8));
+ *     Eq. (6)).  The same finite polynomial is evaluated three ways: the
+ *     CUDA-core kernels run the pages' recurrence Z <- -G Z, U += Z
+ *     (Eq. (8)) on each value tile; the tensor-core kernel for trees of up
+ *     to 64 nodes forms each row of (I+G)^{-1} by backward substitution
+ *     along the node's ancestor path; the large-tree tensor-core kernel by
+ *     log-depth doubling, (I - G) prod_k (I + G^(2^k)).  Only the rounding
+ *     order differs;
  *   - the per-node factors (P, K, U) replace per-node state snapshots
  *     (Eq. (9)); after sampling, commit rebuilds the accepted node a's exact
  *     state S_new = P_a S_pre + (D_a K_a)^T U_a (Eq. (10)), in place.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
- *     library allocates no device memory and keeps no global mutable state.
- *     All calls are asynchronous on `stream` (a cudaStream_t; NULL selects
- *     the legacy default stream) and may be captured in CUDA graphs.
+ *     library allocates no device memory.  Its global state is limited to
+ *     set-up done once per device (kernel attributes, the tensor-map
+ *     encoder's entry point) and one exception: the fixed scratch array of
+ *     bole_tree_verify_noalloc, which every call of that entry point shares
+ *     (see there).  All calls are asynchronous on `stream` (a cudaStream_t;
+ *     NULL selects the legacy default stream); apart from
+ *     bole_tree_verify_noalloc (see there), they may be captured in CUDA
+ *     graphs.
  *   - Packed forest: B requests' trees are concatenated node-major.
  *     offsets[B+1] (int32, offsets[0] = 0, non-decreasing, offsets[B] <= N)
  *     delimits request b's nodes [offsets[b], offsets[b+1]); N is the
@@ -104,12 +115,30 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
  * every kernel reads and writes that layout directly (no transposed copy).
  * The results are the same numbers as with the default layout. */
 #define BOLE_FLAG_STATE_VK 0x4u
+/* Verification of bf16 trees of up to 32 nodes (depth <= 15, dk = dv = 128,
+ * default state layout) has two tensor-core kernels: one CTA per (request,
+ * head), or the value-tiled kernel -- two CTAs per head, 64 value columns
+ * each (Section IV-B: H * N_v independently schedulable CTAs per request).
+ * By default the value tiles serve batches whose B * H heads would not fill
+ * one wave of the one-CTA kernel (two CTAs per SM), where the extra CTAs
+ * add parallelism; larger batches run one CTA per head, which moves more
+ * state bytes per resident CTA.  These flags force either kernel (same
+ * results up to rounding order); they are ignored elsewhere. */
+#define BOLE_FLAG_ONE_TILE_PER_HEAD 0x8u
+#define BOLE_FLAG_VALUE_TILES 0x10u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *bole_status_string(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int bole_version(void);
+
+/* The cudaError_t behind the calling host thread's most recent BOLE_ERR_CUDA
+ * (0 if none yet), and its CUDA description (static storage, never NULL).
+ * A launch can also return the sticky error of an earlier kernel that
+ * faulted. */
+int bole_last_cuda_error(void);
+const char *bole_last_cuda_error_string(void);
 
 /* Self-test of the bounded device waits.  Every device wait of the library
  * (an mbarrier wait for a copy or a tensor-core product) gives up after a
@@ -149,10 +178,12 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
                              int max_depth, int32_t *depth, uint32_t *anc, int32_t *req_depth,
                              int32_t *dev_status, bole_stream_t stream);
 
-/* Closed-form verification of every node of every tree (Theorem 1, Eq. (2),
- * value-tiled as in Eq. (7), propagation by the finite Neumann recurrence of
- * Eq. (8)).  S_pre is read only (immutable during verification, Section
- * IV-D).  Inputs: S_pre, q, k, v, gamma, beta as laid out above; offsets and
+/* Closed-form verification of every node of every tree (Theorem 1, Eq. (2);
+ * state products as in Eq. (7); propagation by the finite Neumann sum of
+ * Eq. (6), evaluated per kernel as described at the top of this file: the
+ * recurrence of Eq. (8) on the CUDA-core path, backward substitution or
+ * log-depth doubling on the tensor-core paths).  S_pre is read only
+ * (immutable during verification, Section IV-D).  Inputs: S_pre, q, k, v, gamma, beta as laid out above; offsets and
  * parent of the packed forest; depth, anc, req_depth from bole_pack_forest.
  * max_T bounds the tree sizes (1..128), max_depth the depths (0..127).
  * Outputs: O (dtype of q/k/v), U (float32) and logP (float32) -- U, logP and
@@ -161,8 +192,9 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * bole_workspace_size(...) bytes (NULL allowed when that size is 0).
  * Kernel choice: bf16 inputs with dk = dv = 128, max_T <= 64 and
  * max_depth <= 15 run the single-CTA TMA + tcgen05 kernel (state products on
- * an exact bf16 hi/lo split of S_pre, fp32 accumulation, every factor on
- * chip); bf16 inputs with dk = dv = 128 and larger or deeper trees (up to 128
+ * a bf16 hi/lo split of S_pre -- the low part is itself rounded to bf16, so
+ * each state element keeps a relative residue of about 2^-17 -- with exact
+ * bf16 products and fp32 accumulation, every factor on chip); bf16 inputs with dk = dv = 128 and larger or deeper trees (up to 128
  * nodes, any depth) run one tcgen05 kernel per (request, head) that forms the
  * factors [M; W] by log-depth doubling and keeps them in tensor memory for the
  * state products and the propagation (no workspace; when the caller passes

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from conftest import rel_fro
+from conftest import assert_local_parity, rel_fro, state_unit_errors
 from gated_deltanet_verification_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +42,9 @@ def _run(batch, flags=0, dtype=None):
 
 
 def _check(batch, got, tol):
+    """Integers bit for bit; O, U and S_new within `tol` as whole tensors, per
+    (request, head) and per node row (Theorem 1 is an equality per node, so a
+    wrong node or head must not hide inside a large tensor's norm)."""
     depth, anc, req, st = oracle.pack(batch.offsets, batch.parent, batch.max_depth)
     assert st == oracle.OK
     assert np.array_equal(got["depth"], depth)
@@ -54,6 +57,13 @@ def _check(batch, got, tol):
     assert np.max(np.abs(got["logP"] - logP)) < 2e-4 * max(1.0, np.max(np.abs(logP)))
     for name, e in errs.items():
         assert e <= tol, f"{batch.name}: {name} rel err {e:.3e} > {tol}"
+    for name, ref in (("O", O), ("U", U)):
+        unit, row = assert_local_parity(batch.name, name, got[name], ref, batch.offsets, tol)
+        errs[name + "_worst_head"], errs[name + "_worst_row"] = unit, row
+    su = state_unit_errors(got["S_new"], S_new)
+    (wb, wh), worst = max(su.items(), key=lambda kv: kv[1])
+    assert worst <= tol, f"{batch.name}: S_new worst (request, head) = ({wb}, {wh}) {worst:.3e}"
+    errs["S_new_worst_head"] = worst
     return errs
 
 
@@ -118,6 +128,7 @@ def test_commit_edge_paths(which):
     got = _run(b)
     S_new = oracle.commit(b)
     assert rel_fro(got["S_new"], S_new) <= TOL["bf16"]
+    assert max(state_unit_errors(got["S_new"], S_new).values()) <= TOL["bf16"]
     if which == "none":
         assert np.array_equal(got["S_new"], b.S_pre.astype(np.float64))
 
@@ -215,6 +226,8 @@ def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
     Oe, Ue, _ = oracle.verify(b)
     assert rel_fro(rb.O.float().cpu().numpy(), Oe) <= TOL["bf16"]
     assert rel_fro(rb.U.cpu().numpy(), Ue) <= TOL["bf16"]
+    assert_local_parity(b.name, "O", rb.O.float().cpu().numpy(), Oe, b.offsets, TOL["bf16"])
+    assert_local_parity(b.name, "U", rb.U.cpu().numpy(), Ue, b.offsets, TOL["bf16"])
     mw = rb.workspace.view(b.B, b.H, 256, 128).cpu().numpy()
     for r in range(b.B):
         o, e = int(b.offsets[r]), int(b.offsets[r + 1])
@@ -273,6 +286,8 @@ def test_small_tree_layout_matches_the_64_node_layout():
         O, U, logP, st = _verify_direct(b, max_T)
         assert st[0] == 0, st
         assert rel_fro(O, Oe) <= TOL["bf16"] and rel_fro(U, Ue) <= TOL["bf16"]
+        assert_local_parity(b.name, "O", O, Oe, b.offsets, TOL["bf16"])
+        assert_local_parity(b.name, "U", U, Ue, b.offsets, TOL["bf16"])
         got.append((O, U, logP))
     assert rel_fro(got[0][1], got[1][1]) <= 1e-5
     assert rel_fro(got[0][0], got[1][0]) <= 1e-4  # bf16 rounding of equal fp32 values
@@ -307,3 +322,69 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     b = I.random_batch(seed=97, B=3, H=2, dk=128, dv=128, sizes=[20, 31, 9], max_depth=6,
                        dtype="bf16", sigma=0.05, accept="uniform")
     _check(b, _run(b), TOL["bf16"])
+
+
+def _verify_flags(b, flags, max_T=None):
+    from gated_deltanet_verification_gb300 import bole, device
+    db = device.to_device(b)
+    if max_T is not None:
+        db.max_T = max_T
+    rb = device.alloc_round(db, flags)
+    device.pack(db, rb)
+    device.verify(db, rb, flags)
+    torch.cuda.synchronize()
+    bole.check_status(rb.status)
+    return (rb.O.float().cpu().numpy().astype(np.float64), rb.U.cpu().numpy().astype(np.float64),
+            rb.logP.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("sizes,H,max_depth,shape", [
+    ([32] * 16, 32, 8, "random"),          # the batched forest's shape
+    ([1, 32, 0, 7, 0, 2], 3, 15, "random"),  # 1-node, empty and ragged trees, odd head count
+    ([16, 16, 9], 5, 15, "chain"),         # the deepest chains the kernel takes (depth 15)
+    ([32, 32], 2, 1, "star"),              # depth 0: no propagation
+])
+def test_value_tiled_kernel_matches_oracle_and_one_tile_per_head(sizes, H, max_depth, shape):
+    """Trees of up to 32 nodes: BOLE_FLAG_VALUE_TILES runs the value-tiled
+    kernel (two CTAs per head, 64 value columns each, Section IV-B),
+    BOLE_FLAG_ONE_TILE_PER_HEAD the one-CTA-per-head kernel on the same forest.  Both against the oracle per
+    tensor, per (request, head) and per node row, and against each other (the
+    same products; only the propagation's accumulation differs)."""
+    from gated_deltanet_verification_gb300 import bole
+    b = I.random_batch(seed=sum(sizes) + 7 * H, B=len(sizes), H=H, dk=128, dv=128, sizes=sizes,
+                       max_depth=max_depth, dtype="bf16", sigma=0.05, shape=shape)
+    Oe, Ue, Le = oracle.verify(b)
+    got = {}
+    for name, flags in (("vtile", bole.FLAG_VALUE_TILES), ("one_tile", bole.FLAG_ONE_TILE_PER_HEAD)):
+        O, U, logP = _verify_flags(b, flags, max_T=32)
+        assert rel_fro(O, Oe) <= TOL["bf16"] and rel_fro(U, Ue) <= TOL["bf16"], name
+        assert_local_parity(f"{b.name}/{name}", "O", O, Oe, b.offsets, TOL["bf16"])
+        assert_local_parity(f"{b.name}/{name}", "U", U, Ue, b.offsets, TOL["bf16"])
+        assert np.max(np.abs(logP - Le)) < 2e-4 * max(1.0, np.max(np.abs(Le)))
+        got[name] = (O, U, logP)
+    assert rel_fro(got["vtile"][1], got["one_tile"][1]) <= 1e-5
+    assert rel_fro(got["vtile"][0], got["one_tile"][0]) <= 1e-4
+    assert np.array_equal(got["vtile"][2], got["one_tile"][2])
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_value_tiled_round_matches_serial_and_one_tile_commit(cfg):
+    """A whole overlapped round (pack -> value-tiled verify -> commit with
+    programmatic dependent launch) equals serial launches bit for bit and
+    commits the oracle's state (config 1 takes the value tiles by default)."""
+    from gated_deltanet_verification_gb300 import bole, device
+    b = I.config_batch(cfg)
+    f = bole.FLAG_VALUE_TILES
+    db1, db2 = device.to_device(b), device.to_device(b)
+    rb1, rb2 = device.alloc_round(db1), device.alloc_round(db2)
+    device.pack(db1, rb1)
+    device.verify(db1, rb1, f)
+    device.commit(db1, rb1)
+    device.run_round(db2, rb2, f)
+    torch.cuda.synchronize()
+    bole.check_status(rb1.status)
+    bole.check_status(rb2.status)
+    assert torch.equal(rb1.O, rb2.O) and torch.equal(rb1.U, rb2.U)
+    assert torch.equal(db1.S, db2.S)
+    S_new = oracle.commit(b)
+    assert max(state_unit_errors(db2.S.cpu().numpy(), S_new).values()) <= TOL["bf16"]

@@ -3,14 +3,16 @@ nothing, for callers that cannot allocate device memory when they verify
 (hosts that hand over only their own tensors, serving loops that forbid
 allocation on the hot path).  Its G, C scratch is a fixed library-owned
 array; these tests call it through the C ABI and compare it with
-bole_tree_verify (same CUDA-core kernels, caller-allocated workspace) on two
-calls in a row of different sizes, so stale scratch from the first call must
-not leak into the second.  Collected last on purpose."""
+bole_tree_verify (same CUDA-core kernels, caller-allocated workspace) and with
+the fp64 CPU oracle, on two calls in a row of different sizes, so stale
+scratch from the first call must not leak into the second.  Collected last on
+purpose."""
 import numpy as np
 import pytest
 import torch
 
-from conftest import rel_fro
+import oracle
+from conftest import assert_local_parity, rel_fro
 from gated_deltanet_verification_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -52,6 +54,14 @@ def test_noalloc_matches_workspace_path_two_calls():
         ref, got = _both(batch)
         for r, g in zip(ref, got):
             assert rel_fro(g, r) <= TOL[batch.dtype]
+        # and against the oracle, so an error the two CUDA-core runs share
+        # cannot pass: O and U per tensor, per (request, head) and per node row
+        O, U, logP = oracle.verify(batch)
+        tol = TOL[batch.dtype]
+        assert rel_fro(got[0], O) <= tol and rel_fro(got[1], U) <= tol
+        assert_local_parity(batch.name, "O", got[0], O, batch.offsets, tol)
+        assert_local_parity(batch.name, "U", got[1], U, batch.offsets, tol)
+        assert np.max(np.abs(got[2] - logP)) < 2e-4 * max(1.0, np.max(np.abs(logP)))
 
 
 def test_noalloc_rejects_oversize():
