@@ -72,6 +72,9 @@ def parse_args(argv=None):
     p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
     p.add_argument("--one-tile-per-head", action="store_true",
                    help="trees of up to 32 nodes: force one CTA per (request, head)")
+    p.add_argument("--pack-round", action="store_true",
+                   help="run the round as pack -> verify -> commit even where the "
+                        "verification can form the topology itself")
     p.add_argument("--value-tiles", action="store_true",
                    help="trees of up to 32 nodes: force the value-tiled kernel (two CTAs "
                         "per head)")
@@ -107,13 +110,16 @@ def path_lengths(batch):
     return L
 
 
-def algorithmic(batch):
-    """Bytes each kernel must move at least once, and tensor flops of verify."""
+def algorithmic(batch, inline_topology=False):
+    """Bytes each kernel must move at least once, and tensor flops of verify.
+    With the topology formed in the verification there is no pack launch and
+    the verification reads the parent links instead of pack's outputs."""
     B, H, dk, dv, N = batch.B, batch.H, batch.dk, batch.dv, batch.N
     s_in = 2 if batch.dtype == "bf16" else 4
-    topo_pack = 4 * (B + 1) + 4 * N + 4 * N + 16 * N + 4 * B
+    topo_pack = 0 if inline_topology else 4 * (B + 1) + 4 * N + 4 * N + 16 * N + 4 * B
+    topo_verify = 4 * (B + 1) + (4 * N if inline_topology else 4 * N + 20 * N + 4 * B)
     verify = (B * H * dk * dv * 4 + N * H * (2 * dk + dv) * s_in + 8 * N * H
-              + N * H * dv * (s_in + 4) + 4 * N * H + 4 * (B + 1) + 4 * N + 20 * N + 4 * B)
+              + N * H * dv * (s_in + 4) + 4 * N * H + topo_verify)
     L = path_lengths(batch)
     committed = int(np.sum(L > 0))
     commit = (2 * committed * H * dk * dv * 4 + int(np.sum(L)) * H * (dk * s_in + 4 * dv + 4)
@@ -351,7 +357,13 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         getattr(args, "verify_flags", 0)
     seed = rank_seed(cfg, rank)
     batch = inputs.config_batch(cfg, seed=seed, shape=args.shape)
-    alg = algorithmic(batch)
+    probe_db = device.to_device(batch, device=dev)
+    # the topology step inside the verification where the kernels allow it
+    inline = (not args.pack_round) and device.inline_topology_supported(probe_db, flags)
+    del probe_db
+    if inline:
+        flags |= bole.FLAG_INLINE_TOPOLOGY
+    alg = algorithmic(batch, inline)
     step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
     n_sets = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
 
@@ -372,8 +384,9 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     fused = tc_shape and batch.max_T <= 64 and batch.max_depth < 16   # single-CTA kernel
     big = tc_shape and not fused and batch.max_T <= 128              # fused large-tree kernel
     tc_used = fused or big
-    # pack, verify (one tensor-core kernel, or the CUDA-core producer + solve), commit
-    launches_per_step = 1 + (1 if tc_used else 2) + 1
+    # pack (unless the verification forms the topology), verify (one tensor-core
+    # kernel, or the CUDA-core producer + solve), commit
+    launches_per_step = (0 if inline else 1) + (1 if tc_used else 2) + 1
 
     def step(i):
         device.run_round(*sets[i % n_sets], flags, stream)
@@ -425,9 +438,13 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     #      each replay ----
     ks = max(1, min(args.kernel_steps, steps))
     per_kernel = {"pack": [], "verify": [], "commit": []}
+    cflags = flags & ~bole.FLAG_INLINE_TOPOLOGY
     calls = {"pack": lambda db, rb, cs: device.pack(db, rb, cs),
              "verify": lambda db, rb, cs: device.verify(db, rb, flags, cs),
-             "commit": lambda db, rb, cs: device.commit(db, rb, flags, cs)}
+             "commit": lambda db, rb, cs: device.commit(db, rb, cflags, cs)}
+    if inline:
+        del calls["pack"]
+        per_kernel["pack"].append(0.0)
     for name, call in calls.items():
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -449,7 +466,8 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
-    res = {"_batch": batch, "_flags": flags, "_launches": launches_per_step * steps}
+    res = {"_batch": batch, "_flags": flags & ~bole.FLAG_INLINE_TOPOLOGY,
+           "_launches": launches_per_step * steps}
     if rank != 0:
         return res
 
@@ -459,6 +477,9 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     kern_rf = {}
     for k in ("pack", "verify", "commit"):
+        if k == "pack" and inline:
+            kern_rf[k] = {"ms": 0.0, "alg_bytes": 0, "note": "formed inside the verification"}
+            continue
         gbs = alg[k] / (avg[k] * 1e-3) / 1e9 if avg[k] > 0 else 0.0
         kern_rf[k] = {"ms": round(avg[k], 5), "alg_bytes": int(alg[k]),
                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
@@ -497,6 +518,8 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
                    "kernels": ("tcgen05 value-tiled (two CTAs per head)" if vtile
                                else "tcgen05 (one CTA per head)" if fused
                                else "tcgen05 fused large-tree kernel" if big else "cuda-core"),
+                   "round": ("verify (topology inside) -> commit" if inline
+                             else "pack -> verify -> commit"),
                    "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
                    "launch": "CUDA graph replay, one graph per input copy",
                    "kernel_timing": f"separate pass: per call kind, a graph of one call on each "

@@ -33,6 +33,7 @@ FLAG_OVERLAP_LAUNCH = 0x2  # see bole.h: overlap with the previous library call 
 FLAG_STATE_VK = 0x4  # state slots stored [B, H, dv, dk] (the serving runtime's slot layout)
 FLAG_ONE_TILE_PER_HEAD = 0x8  # small trees: one CTA per (request, head), not two value tiles
 FLAG_VALUE_TILES = 0x10  # small trees: two value-tile CTAs per (request, head)
+FLAG_INLINE_TOPOLOGY = 0x20  # tree_verify forms the topology itself (no pack_forest first)
 MAX_TREE_NODES = 128
 STATUS_WORDS = 4
 
@@ -201,7 +202,8 @@ def pack_forest(offsets: torch.Tensor, parent: torch.Tensor, max_depth: int, *,
 def tree_verify(S_pre, q, k, v, gamma, beta, offsets, parent, depth, anc, req_depth, max_T: int,
                 max_depth: int, *, O=None, U=None, logP=None, workspace=None, status=None,
                 flags: int = 0, stream=None):
-    """bole_tree_verify: returns (O, U, logP)."""
+    """bole_tree_verify: returns (O, U, logP).  With FLAG_INLINE_TOPOLOGY,
+    depth, anc and req_depth may be None."""
     B = offsets.numel() - 1
     N, H, dk = q.shape
     dv = v.shape[-1]

@@ -132,9 +132,12 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
         max_depth > BOLE_MAX_TREE_NODES - 1)
         return BOLE_ERR_INVALID_ARG;
     if ((size_t)N > (size_t)B * max_T) return BOLE_ERR_INVALID_ARG;
-    if (!offsets || !dev_status || (B > 0 && (!S_pre || !req_depth))) return BOLE_ERR_INVALID_ARG;
-    if (N > 0 && (!q || !k || !v || !gamma || !beta || !parent || !depth || !anc || !O || !U ||
-                  !logP))
+    // with the topology formed in the kernel, depth / anc / req_depth are unused
+    const bool inl = (flags & BOLE_FLAG_INLINE_TOPOLOGY) != 0;
+    if (!offsets || !dev_status || (B > 0 && (!S_pre || (!inl && !req_depth))))
+        return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !gamma || !beta || !parent || (!inl && (!depth || !anc)) ||
+                  !O || !U || !logP))
         return BOLE_ERR_INVALID_ARG;
     const void *p16[] = {S_pre, q, k, v, O, U, anc, dev_status};
     for (const void *p : p16)
@@ -151,8 +154,11 @@ bole_status bole_tree_verify(const float *S_pre, const void *q, const void *k, c
     a.O = O; a.U = U; a.logP = logP; a.ws = workspace; a.ws_bytes = workspace ? workspace_bytes : 0;
     a.st = dev_status;
     a.vk = (flags & BOLE_FLAG_STATE_VK) != 0;
+    a.inline_topo = inl;
 
     const VerifyPath path = verify_path(a, flags);
+    if (inl && path != VerifyPath::VTile && path != VerifyPath::Fused)
+        return BOLE_ERR_UNSUPPORTED; // these kernels read the masks bole_pack_forest builds
     const size_t need = verify_workspace(a, flags);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return BOLE_ERR_WORKSPACE;
@@ -203,6 +209,7 @@ bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const vo
     a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
     a.O = O; a.U = U; a.logP = logP; a.ws = nullptr; a.ws_bytes = 0; a.st = dev_status;
     a.vk = false;
+    a.inline_topo = false;
     return from_cuda(launch_simt_verify_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

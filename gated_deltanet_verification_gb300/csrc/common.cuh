@@ -72,6 +72,7 @@ struct VerifyArgs {
     size_t ws_bytes;
     int32_t *st;
     bool vk; // state stored [B, H, dv, dk] (BOLE_FLAG_STATE_VK)
+    bool inline_topo; // depth / anc / req_depth formed by the kernel from parent
 };
 
 // One commit launch over `layers` GDN layers: layer l's S, k, U and logP start

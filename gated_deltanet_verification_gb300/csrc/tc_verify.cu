@@ -107,7 +107,12 @@ constexpr int X_ANCAT = X_C + FAC_BYTES;      // [64][16] u8: ancestor of row i 
 constexpr int X_L = X_ANCAT + kT * kSlots;    // L_i
 constexpr int X_DEPTH = X_L + kT * 4;
 constexpr int X_LG = X_DEPTH + kT * 4;        // log gamma_i
-static_assert(X_LG + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+// topology formed in the kernel (no pack before it): ancestor masks and jumps
+constexpr int X_JMASK = X_LG + kT * 4;        // u64 [64]
+constexpr int X_JUMP = X_JMASK + kT * 8;      // int [64]
+static_assert(X_JUMP + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its region");
+static_assert(X_JMASK % 8 == 0, "aligned masks");
+constexpr int OFF_TOPO = OFF_BAR + 13 * 8;    // int [2]: first bad node, request depth
 static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
@@ -162,7 +167,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                  const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc,
                  const int32_t *__restrict__ req_depth, int H, int N,
                  __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
-                 float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc)
+                 float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc,
+                 const int32_t *__restrict__ parent, int max_depth, int inline_topo)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -230,9 +236,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const bool topo = tid < kT;       // warps 0, 1: row i = tid
     float bt = 0.f;                   // beta_i (topology rows and the K-side rows)
     float g_i = 1.f;
+    int my_par = -1;                  // topology rows, topology formed here: parent of i
     if (warp < 8 && in_range && i < T) {
         if (topo || m >= 64) bt = beta[(size_t)(o + i) * H + h];
         if (topo) g_i = gamma[(size_t)(o + i) * H + h];
+        if (topo && inline_topo) my_par = parent[o + i];
     }
     if (issuer) {
         mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
@@ -258,20 +266,66 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
         *sfail = 0;
     }
-    const int d = req_depth[b];
-    // Depth and ancestor-or-self mask of each node as pack built them (rows
-    // below 64: the first two words of the 128-bit mask).  A tree pack found
-    // malformed or too deep has set the status or a depth the check below
-    // refuses, so such a launch ends before any output; every bit indexes a
-    // row below 64 whatever the input.
+    int *stopo = reinterpret_cast<int *>(sm + OFF_TOPO);
+    const int d_read = inline_topo ? 0 : req_depth[b];
     int my_depth = -1;
     uint64_t my_mask = 0;
-    if (topo && in_range && i < T) {
-        const uint2 mk = *reinterpret_cast<const uint2 *>(anc + (size_t)(o + i) * 4);
-        my_mask = ((uint64_t)mk.y << 32) | mk.x;
-        my_depth = __popcll(my_mask) - 1;
-        if (my_depth >= kSlots) my_depth = -1; // no work for this row (the request is refused)
+    if (!inline_topo) {
+        // Depth and ancestor-or-self mask of each node as pack built them
+        // (rows below 64: the first two words of the 128-bit mask).  A tree
+        // pack found malformed or too deep has set the status or a depth the
+        // check below refuses, so such a launch ends before any output; every
+        // bit indexes a row below 64 whatever the input.
+        if (topo && in_range && i < T) {
+            const uint2 mk = *reinterpret_cast<const uint2 *>(anc + (size_t)(o + i) * 4);
+            my_mask = ((uint64_t)mk.y << 32) | mk.x;
+            my_depth = __popcll(my_mask) - 1;
+        }
+    } else if (topo) {
+        // The round's topology step in the kernel (Section IV-C): each node
+        // starts with itself and a jump to its parent, and every round ORs in
+        // the mask at its jump target and doubles the jump, so after
+        // log2(64) = 6 rounds the mask holds the whole path to the root.
+        // A link that does not point backwards is a fault (reported below)
+        // and is not followed, so every jump indexes an earlier node.
+        uint64_t *smk = reinterpret_cast<uint64_t *>(sm + X_JMASK);
+        int *sjp = reinterpret_cast<int *>(sm + X_JUMP);
+        const bool live = in_range && i < T;
+        const bool badp = live && (my_par < -1 || my_par >= i);
+        uint64_t mk = live ? (1ull << i) : 0ull;
+        int jp = (live && !badp) ? my_par : -1;
+        if (tid == 0) {
+            stopo[0] = kT;
+            stopo[1] = 0;
+        }
+        smk[i] = mk;
+        sjp[i] = jp;
+        asm volatile("bar.sync 3, 64;" ::: "memory");
+        if (badp) atomicMin(&stopo[0], i);
+#pragma unroll 1
+        for (int r = 0; r < 6; ++r) {
+            uint64_t m2 = 0;
+            int j2 = -1;
+            if (jp >= 0) {
+                m2 = smk[jp];
+                j2 = sjp[jp];
+            }
+            asm volatile("bar.sync 3, 64;" ::: "memory");
+            if (jp >= 0) {
+                mk |= m2;
+                jp = j2;
+            }
+            smk[i] = mk;
+            sjp[i] = jp;
+            asm volatile("bar.sync 3, 64;" ::: "memory");
+        }
+        if (live) {
+            my_mask = mk;
+            my_depth = __popcll(mk) - 1;
+            atomicMax(&stopo[1], my_depth);
+        }
     }
+    if (my_depth >= kSlots) my_depth = -1; // no work for this row (the request is refused)
     if (!early_alloc && warp == 0) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
@@ -281,11 +335,20 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int fault = *sfault;
-    const bool bad = !in_range || d < 0 || d >= kSlots || d >= T;
+    const int d = inline_topo ? stopo[1] : d_read;
+    const int bad_node = inline_topo && in_range ? stopo[0] : kT;
+    const bool bad = !in_range || d < 0 || d >= kSlots || d >= T || bad_node < kT ||
+                     (inline_topo && d > max_depth);
     if (fault != 0 || T <= 0 || bad) {
-        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0)
-            report(st, T > kTmax || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH,
-                   b, -1, T > kTmax ? T : d);
+        if (fault == 0 && h == 0 && (T > 0 || (inline_topo && T < 0))) {
+            if (bad_node < kT) { // the first node whose link does not point backwards
+                if (tid == bad_node) report(st, BOLE_ERR_BAD_TOPOLOGY, b, bad_node, my_par);
+            } else if (bad && tid == 0) {
+                report(st, T > kTmax || T < 0 || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY
+                                                                     : BOLE_ERR_DEPTH,
+                       b, -1, T > kTmax || T < 0 ? T : d);
+            }
+        }
         if (issuer) { // drain the copies in flight before the CTA retires
             if (in_range) mbar_wait(&bar[BAR_A1], 0, kWaitNs);
             if (SMALL && in_range) mbar_wait(&bar[BAR_V], 0, kWaitNs);
@@ -1097,7 +1160,8 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
                                                  overlap, attr);
     return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
                               a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
-                              a.logP, a.st, resident_ctas(2), overlap ? 0 : 1);
+                              a.logP, a.st, resident_ctas(2), overlap ? 0 : 1, a.parent,
+                              a.max_depth, a.inline_topo ? 1 : 0);
 }
 
 bool tc_commit_supported(const CommitArgs &a)

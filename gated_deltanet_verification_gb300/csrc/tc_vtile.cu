@@ -83,8 +83,9 @@ constexpr int VT_L = VT_ANCAT + kVT * kVSlots;
 constexpr int VT_DEPTH = VT_L + kVT * 4;
 constexpr int VT_LG = VT_DEPTH + kVT * 4;
 constexpr int VT_BAR = VT_LG + kVT * 4;
-constexpr int VT_MISC = VT_BAR + 16 * 8; // TMEM slot, status copy, wait-failure flag
-constexpr int VT_END = VT_MISC + 16;
+constexpr int VT_MISC = VT_BAR + 16 * 8; // TMEM slot, status copy, wait-failure flag,
+                                         // first bad node, request depth
+constexpr int VT_END = VT_MISC + 24;
 constexpr int VT_SMEM = VT_END + 1024;   // slack for the 1024-byte alignment of the base
 static_assert(VT_ANCAT % 16 == 0 && VT_BAR % 8 == 0, "aligned scratch");
 static_assert(VT_QK + 16384 + 8192 <= VT_X, "the products' reads past [Q;K] stay in V and G");
@@ -110,7 +111,8 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc,
                 const int32_t *__restrict__ req_depth, int H, int N,
                 __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
-                float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc)
+                float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc,
+                const int32_t *__restrict__ parent, int max_depth, int inline_topo)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
@@ -171,9 +173,11 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
     // 1 and 5 (node = lane, the K-side rows) beta for R^T
     const int i = lane;
     float bt = 0.f, g_i = 1.f;
+    int my_par = -1; // warp 0, topology formed here: the parent of node i
     if (in_range && i < T && (warp == 0 || warp == 1 || warp == 5)) {
         bt = beta[(size_t)(o + i) * H + h];
         if (warp == 0) g_i = gamma[(size_t)(o + i) * H + h];
+        if (warp == 0 && inline_topo) my_par = parent[o + i];
     }
     // What the previous call wrote (the status word pack reset, the request's
     // depth, each node's ancestor-or-self mask) is read after the wait.
@@ -182,14 +186,45 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
         *sfail = 0;
     }
-    const int d = req_depth[b];
+    int *stopo = reinterpret_cast<int *>(sm + VT_MISC + 12); // first bad node, depth
+    const int d_read = inline_topo ? 0 : req_depth[b];
     int my_depth = -1;
     uint32_t my_mask = 0;
-    if (warp == 0 && in_range && i < T) {
-        my_mask = anc[(size_t)(o + i) * 4]; // a tree of <= 32 nodes: the first word
-        my_depth = __popc(my_mask) - 1;
-        if (my_depth >= kVSlots) my_depth = -1; // the request is refused below
+    int wdepth = 0; // warp 0, topology formed here: the request's depth
+    if (!inline_topo) {
+        if (warp == 0 && in_range && i < T) {
+            my_mask = anc[(size_t)(o + i) * 4]; // a tree of <= 32 nodes: the first word
+            my_depth = __popc(my_mask) - 1;
+        }
+    } else if (warp == 0) {
+        // The round's topology step in the kernel (Section IV-C): pointer
+        // jumping over the lanes, so after log2(32) = 5 rounds each mask holds
+        // the node's whole path; a link that does not point backwards is a
+        // fault (reported below) and is not followed.
+        const bool live = in_range && i < T;
+        const bool badp = live && (my_par < -1 || my_par >= i);
+        uint32_t mk = live ? (1u << i) : 0u;
+        int jp = (live && !badp) ? my_par : -1;
+#pragma unroll
+        for (int r = 0; r < 5; ++r) {
+            const int src = jp >= 0 ? jp : i;
+            const uint32_t m2 = __shfl_sync(0xffffffffu, mk, src);
+            const int j2 = __shfl_sync(0xffffffffu, jp, src);
+            if (jp >= 0) {
+                mk |= m2;
+                jp = j2;
+            }
+        }
+        const unsigned badm = __ballot_sync(0xffffffffu, badp);
+        if (live) {
+            my_mask = mk;
+            my_depth = __popc(mk) - 1;
+        }
+        wdepth = __reduce_max_sync(0xffffffffu, live ? my_depth : 0);
+        if (lane == 0) stopo[0] = badm ? __ffs(badm) - 1 : kVT;
+        if (lane == 0) stopo[1] = wdepth;
     }
+    if (my_depth >= kVSlots) my_depth = -1; // the request is refused below
     if (warp == 0) LGs[i] = logf(g_i); // consumes gamma before the barrier
     if (!early_alloc && warp == 0) {
         tmem_alloc(tslot, TM_COLS);
@@ -200,7 +235,10 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int fault = *sfault;
-    const bool bad = !in_range || d < 0 || d >= kVSlots || d >= T;
+    const int d = inline_topo ? stopo[1] : d_read;
+    const int bad_node = inline_topo && in_range ? stopo[0] : kVT;
+    const bool bad = !in_range || d < 0 || d >= kVSlots || d >= T || bad_node < kVT ||
+                     (inline_topo && d > max_depth);
     if (issuer && fault == 0 && T > 0 && !bad) {
         // The state tile is requested once the small reads have returned:
         // requested at entry it queued them behind every CTA's state burst
@@ -210,9 +248,15 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         tma_load_2d(sS + 16384, &tmS, &bar[VB_S], c0 + 32, unit * kD);
     }
     if (fault != 0 || T <= 0 || bad) {
-        if (bad && T > 0 && fault == 0 && tid == 0 && h == 0 && vh == 0)
-            report(st, T > kVT || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY : BOLE_ERR_DEPTH,
-                   b, -1, T > kVT ? T : d);
+        if (fault == 0 && h == 0 && vh == 0 && (T > 0 || (inline_topo && T < 0))) {
+            if (bad_node < kVT) { // the first node whose link does not point backwards
+                if (tid == bad_node) report(st, BOLE_ERR_BAD_TOPOLOGY, b, bad_node, my_par);
+            } else if (bad && tid == 0) {
+                report(st, T > kVT || T < 0 || o < 0 || o + T > N ? BOLE_ERR_BAD_TOPOLOGY
+                                                                   : BOLE_ERR_DEPTH,
+                       b, -1, T > kVT || T < 0 ? T : d);
+            }
+        }
         if (issuer) { // the copies in flight end before the CTA retires
             if (in_range) {
                 mbar_wait(&bar[VB_QK], 0, kWaitNs);
@@ -590,7 +634,8 @@ cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool ove
                                                  overlap, attr);
     return cudaLaunchKernelEx(&cfg, tc_vtile_kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets,
                               a.anc, a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O),
-                              a.U, a.logP, a.st, vtile_resident_ctas(3), overlap ? 0 : 1);
+                              a.U, a.logP, a.st, vtile_resident_ctas(3), overlap ? 0 : 1,
+                              a.parent, a.max_depth, a.inline_topo ? 1 : 0);
 }
 
 } // namespace bole

@@ -91,10 +91,23 @@ def commit(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> No
                 status=rb.status, flags=flags, stream=stream)
 
 
+def inline_topology_supported(db: DeviceBatch, flags: int = 0) -> bool:
+    """Whether the verification can form the round's topology itself
+    (bole.FLAG_INLINE_TOPOLOGY): the tensor-core kernels for trees of up to 64
+    nodes and depth <= 15, bf16, dk = dv = 128, default state layout."""
+    return (db.q.dtype == torch.bfloat16 and db.dk == 128 and db.dv == 128
+            and db.max_T <= 64 and db.max_depth <= 15
+            and not flags & (bole.FLAG_FORCE_SIMT | bole.FLAG_STATE_VK))
+
+
 def run_round(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:
-    """pack -> verify -> commit, all asynchronous on one stream.  Each call
-    directly follows the one it depends on, so verify and commit may overlap
-    their predecessor's tail (bole.FLAG_OVERLAP_LAUNCH)."""
-    pack(db, rb, stream)
+    """One round, asynchronous on one stream.  With bole.FLAG_INLINE_TOPOLOGY
+    in `flags`: verify (which forms the topology itself) -> commit, the status
+    block left as the previous round left it (sticky: zeroed once by the
+    caller).  Otherwise pack -> verify -> commit, pack clearing the status
+    block.  Each call directly follows the one it depends on, so verify and
+    commit may overlap their predecessor's tail (bole.FLAG_OVERLAP_LAUNCH)."""
+    if not flags & bole.FLAG_INLINE_TOPOLOGY:
+        pack(db, rb, stream)
     verify(db, rb, flags | bole.FLAG_OVERLAP_LAUNCH, stream)
-    commit(db, rb, flags | bole.FLAG_OVERLAP_LAUNCH, stream)
+    commit(db, rb, (flags & ~bole.FLAG_INLINE_TOPOLOGY) | bole.FLAG_OVERLAP_LAUNCH, stream)

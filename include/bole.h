@@ -126,6 +126,22 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
  * results up to rounding order); they are ignored elsewhere. */
 #define BOLE_FLAG_ONE_TILE_PER_HEAD 0x8u
 #define BOLE_FLAG_VALUE_TILES 0x10u
+/* bole_tree_verify only: the round's topology step runs inside the
+ * verification (Section IV-C), so no bole_pack_forest precedes it.  Each CTA
+ * derives its tree's ancestor-or-self masks and depths from `parent` and
+ * validates the tree: a link that does not point backwards is reported as
+ * BOLE_ERR_BAD_TOPOLOGY {code, request, node, parent}, a tree deeper than
+ * max_depth as BOLE_ERR_DEPTH {code, request, -1, depth}, bad extents as
+ * bole_pack_forest reports them; that request's outputs are left unwritten
+ * (other requests' are written, and a later bole_commit of the round then
+ * writes nothing).  depth, anc and req_depth are not read and may be NULL.
+ * Nothing clears dev_status in this mode: zero it once, check it after the
+ * round, and zero it again after handling a fault (until then every later
+ * kernel sees the fault and writes nothing).  Supported where the
+ * tensor-core kernels for trees of up to 64 nodes apply (bf16, dk = dv =
+ * 128, max_T <= 64, max_depth <= 15, default state layout); elsewhere the
+ * call returns BOLE_ERR_UNSUPPORTED with nothing launched. */
+#define BOLE_FLAG_INLINE_TOPOLOGY 0x20u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *bole_status_string(int status);
@@ -185,6 +201,8 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * log-depth doubling on the tensor-core paths).  S_pre is read only
  * (immutable during verification, Section IV-D).  Inputs: S_pre, q, k, v, gamma, beta as laid out above; offsets and
  * parent of the packed forest; depth, anc, req_depth from bole_pack_forest.
+ * (With BOLE_FLAG_INLINE_TOPOLOGY the verification forms depth, anc and
+ * req_depth itself and they may be NULL; see the flag.)
  * max_T bounds the tree sizes (1..128), max_depth the depths (0..127).
  * Outputs: O (dtype of q/k/v), U (float32) and logP (float32) -- U, logP and
  * the caller's k buffer are the factors commit needs; keep them alive until

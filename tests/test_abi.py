@@ -219,6 +219,7 @@ def test_binding_constants_match_the_header():
              "FLAG_STATE_VK": bole.FLAG_STATE_VK,
              "FLAG_ONE_TILE_PER_HEAD": bole.FLAG_ONE_TILE_PER_HEAD,
              "FLAG_VALUE_TILES": bole.FLAG_VALUE_TILES,
+             "FLAG_INLINE_TOPOLOGY": bole.FLAG_INLINE_TOPOLOGY,
              "SELFTEST_MAX_WAIT_NS": bole.SELFTEST_MAX_WAIT_NS,
              "NOALLOC_MAX_FACTOR_ELEMS": bole.NOALLOC_MAX_FACTOR_ELEMS,
              "MAX_CANDIDATES": bole.MAX_CANDIDATES,

@@ -388,3 +388,105 @@ def test_value_tiled_round_matches_serial_and_one_tile_commit(cfg):
     assert torch.equal(db1.S, db2.S)
     S_new = oracle.commit(b)
     assert max(state_unit_errors(db2.S.cpu().numpy(), S_new).values()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("cfg,extra", [(1, 0), (2, 0), (3, 0), (2, "vt"), (3, "vk")])
+def test_inline_topology_round_matches_pack_round(cfg, extra):
+    """BOLE_FLAG_INLINE_TOPOLOGY: the verification forms each node's ancestor
+    mask and depth from the parent links itself (no bole_pack_forest); the
+    round's O, U, log P and committed state are bit-identical to the round
+    with pack, on both small-tree kernels and the [dv, dk] slot layout."""
+    from gated_deltanet_verification_gb300 import bole, device
+    b = I.config_batch(cfg)
+    f = bole.FLAG_VALUE_TILES if extra == "vt" else 0
+    db1, db2 = device.to_device(b), device.to_device(b)
+    if extra == "vk":
+        f = bole.FLAG_STATE_VK
+        for db in (db1, db2):
+            db.S = db.S.transpose(2, 3).contiguous()
+    rb1, rb2 = device.alloc_round(db1, f), device.alloc_round(db2, f)
+    device.run_round(db1, rb1, f)
+    device.pack(db2, rb2)  # the topology outputs are not used below: zero them
+    rb2.depth.zero_(); rb2.anc.zero_(); rb2.req_depth.zero_(); rb2.status.zero_()
+    bole.tree_verify(db2.S, db2.q, db2.k, db2.v, db2.gamma, db2.beta, db2.offsets, db2.parent,
+                     None, None, None, db2.max_T, db2.max_depth, O=rb2.O, U=rb2.U,
+                     logP=rb2.logP, status=rb2.status,
+                     flags=f | bole.FLAG_INLINE_TOPOLOGY | bole.FLAG_OVERLAP_LAUNCH)
+    device.commit(db2, rb2, f | bole.FLAG_OVERLAP_LAUNCH)
+    torch.cuda.synchronize()
+    bole.check_status(rb1.status)
+    bole.check_status(rb2.status)
+    assert torch.equal(rb1.O, rb2.O) and torch.equal(rb1.U, rb2.U)
+    assert torch.equal(rb1.logP, rb2.logP) and torch.equal(db1.S, db2.S)
+    if cfg == 3 and not extra:
+        got = dict(depth=rb1.depth.cpu().numpy(), anc=rb1.anc.cpu().numpy().view(np.uint32),
+                   req=rb1.req_depth[:b.B].cpu().numpy(),
+                   O=rb2.O.float().cpu().numpy().astype(np.float64),
+                   U=rb2.U.cpu().numpy().astype(np.float64),
+                   logP=rb2.logP.cpu().numpy().astype(np.float64),
+                   S_new=db2.S.cpu().numpy().astype(np.float64))
+        _check(b, got, TOL["bf16"])
+
+
+@pytest.mark.parametrize("vt", [False, True])
+def test_inline_topology_faults_and_sticky_status(vt):
+    """Faults found by the in-kernel topology step: a forward link is reported
+    with its request, node and parent and that request's outputs stay
+    unwritten (the commit then writes nothing); a tree deeper than max_depth
+    is reported as a depth error; the status block is not cleared by the next
+    round, which writes nothing until the caller zeroes it."""
+    from gated_deltanet_verification_gb300 import bole, device
+    f = bole.FLAG_INLINE_TOPOLOGY | (bole.FLAG_VALUE_TILES if vt else 0)
+    b = I.random_batch(seed=55, B=3, H=2, dk=128, dv=128, sizes=[12, 9, 20], max_depth=6,
+                       dtype="bf16", sigma=0.05, accept="uniform")
+    bad = b.parent.copy()
+    bad[12 + 5] = 8  # node 5 of request 1 points forward
+    db = device.to_device(b)
+    db.parent.copy_(torch.from_numpy(bad))
+    rb = device.alloc_round(db, f)
+    rb.O.fill_(3.0)
+    S0 = db.S.clone()
+    device.run_round(db, rb, f)
+    torch.cuda.synchronize()
+    assert rb.status.cpu().tolist() == [bole.ERR_BAD_TOPOLOGY, 1, 5, 8]
+    assert torch.all(rb.O[12:21].float() == 3.0)          # the bad request: untouched
+    assert not torch.all(rb.O[0:12].float() == 3.0)       # the others verified
+    assert torch.equal(db.S, S0)                          # the commit wrote nothing
+    # sticky: a clean forest verifies nothing until the status is zeroed
+    db.parent.copy_(torch.from_numpy(b.parent))
+    rb.O.fill_(3.0)
+    device.run_round(db, rb, f)
+    torch.cuda.synchronize()
+    assert rb.status.cpu().tolist()[0] == bole.ERR_BAD_TOPOLOGY
+    assert torch.all(rb.O.float() == 3.0) and torch.equal(db.S, S0)
+    rb.status.zero_()
+    device.run_round(db, rb, f)
+    torch.cuda.synchronize()
+    bole.check_status(rb.status)
+    S_new = oracle.commit(b)
+    assert max(state_unit_errors(db.S.cpu().numpy(), S_new).values()) <= TOL["bf16"]
+    # depth above the declared bound
+    db2 = device.to_device(b)
+    db2.max_depth = 2
+    rb2 = device.alloc_round(db2, f)
+    device.run_round(db2, rb2, f)
+    torch.cuda.synchronize()
+    st = rb2.status.cpu().tolist()
+    assert st[0] == bole.ERR_DEPTH and st[2] == -1 and st[3] > 2
+
+
+def test_inline_topology_unsupported_paths():
+    """Kernels that read the masks bole_pack_forest builds (the large-tree
+    kernel, the CUDA-core kernels) refuse the flag synchronously."""
+    from gated_deltanet_verification_gb300 import bole, device
+    b = I.random_batch(seed=56, B=2, H=2, dk=128, dv=128, sizes=[40, 70], max_depth=30,
+                       dtype="bf16", sigma=0.05)
+    db = device.to_device(b)
+    rb = device.alloc_round(db)
+    for flags in (bole.FLAG_INLINE_TOPOLOGY,
+                  bole.FLAG_INLINE_TOPOLOGY | bole.FLAG_FORCE_SIMT):
+        with pytest.raises(bole.BoleError) as e:
+            bole.tree_verify(db.S, db.q, db.k, db.v, db.gamma, db.beta, db.offsets, db.parent,
+                             None, None, None, db.max_T, db.max_depth, status=rb.status,
+                             workspace=rb.workspace, flags=flags)
+        assert e.value.code == bole.ERR_UNSUPPORTED
