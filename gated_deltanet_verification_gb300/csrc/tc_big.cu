@@ -198,7 +198,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
             const uint64_t kb = sdesc_sw128(ka + off, 16, 1024);
             mma_bf16_ss(R0, sdesc_sw128(qa + off, 16, 1024), kb, IDESC_G128, kk > 0);
-            mma_bf16_ss(R1, sdesc_sw128(ka + off, 16, 1024), kb, IDESC_G128, kk > 0);
+            if (d > 0) // K K^T feeds only G, which is zero at depth 0
+                mma_bf16_ss(R1, sdesc_sw128(ka + off, 16, 1024), kb, IDESC_G128, kk > 0);
         }
         mma_commit(&bar[1]);
     }
@@ -215,12 +216,32 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         const uint32_t w[4] = {mk.x, mk.y, mk.z, mk.w};
         const float Lm = Ls[m], bm = Bs[m];
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 2 && d == 0; ++cc) {
+            // every tree of the request has depth 0: G = 0 exactly, so W = I
+            // and only C is formed (no G, no transposed power for the doubling)
+            const int j0 = hf * 64 + cc * 32;
+            const uint32_t bits = w[j0 >> 5];
+            float x[32];
+            tmem_ld32(R0 + lane_base + j0, x);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                const bool anc = (bits >> t) & 1u;
+                x[t] = anc ? __expf(Lm - Ls[j0 + t]) * x[t] : 0.f;
+            }
+            tmem_st32(R0 + lane_base + j0, x);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = (j0 + t) == m ? 1.f : 0.f;
+            tmem_st32(R2 + lane_base + j0, x);
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < 2 && d > 0; ++cc) {
             const int j0 = hf * 64 + cc * 32;
             const uint32_t bits = w[j0 >> 5];
             float x[32], y[32];
-            tmem_ld32(R0 + lane_base + j0, x);
-            tmem_ld32(R1 + lane_base + j0, y);
+            tmem_ld32_async(R0 + lane_base + j0, x); // both loads in flight at once
+            tmem_ld32_async(R1 + lane_base + j0, y);
+            tmem_wait_ld32(x);
+            tmem_wait_ld32(y);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 const int j = j0 + t;
@@ -262,8 +283,10 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int cc = 0; cc < 2; ++cc) {
             const int j0 = hf * 64 + cc * 32;
             float x[32], y[32];
-            tmem_ld32(dst + lane_base + j0, x);
-            tmem_ld32(src + lane_base + j0, y);
+            tmem_ld32_async(dst + lane_base + j0, x);
+            tmem_ld32_async(src + lane_base + j0, y);
+            tmem_wait_ld32(x);
+            tmem_wait_ld32(y);
 #pragma unroll
             for (int t = 0; t < 32; ++t) x[t] = fmaf(sign, y[t], x[t]);
             tmem_st32(dst + lane_base + j0, x);
@@ -456,18 +479,24 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     mph ^= 1u;
     tc_fence_after();
     __syncwarp();
+    // Outputs: each thread puts its 64 columns of row i of O (bf16) and U
+    // (fp32) into shared memory freed by now ([Q;K] for O, the power and state
+    // buffers for U; rows padded by 16 B so the row-per-thread writes are
+    // conflict-free), and one bulk copy per node row and tensor writes them:
+    // row-per-thread global stores touched 32 cache lines per instruction.
+    constexpr int kORow = kD * 2 + 16, kURow = kD * 4 + 16; // padded staged rows
+    static_assert(kTB * kORow <= 65536 && kTB * kURow <= 131072, "staged outputs fit");
     {
         const int i = m;
-        const bool store = go && ok && i < T;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
             const int col0 = hf * 64 + cc * 32;
             float x[32], y[32];
-            tmem_ld32(R1 + lane_base + col0, x);
-            tmem_ld32(R3 + lane_base + col0, y);
-            if (!store) continue;
-            const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
-            uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
+            tmem_ld32_async(R1 + lane_base + col0, x);
+            tmem_ld32_async(R3 + lane_base + col0, y);
+            tmem_wait_ld32(x);
+            tmem_wait_ld32(y);
+            uint4 *dsto = reinterpret_cast<uint4 *>(sQK + i * kORow + col0 * 2);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 __nv_bfloat162 p2[4];
@@ -476,11 +505,20 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                     p2[t] = __floats2bfloat162_rn(x[8 * q4 + 2 * t], x[8 * q4 + 2 * t + 1]);
                 dsto[q4] = *reinterpret_cast<uint4 *>(p2);
             }
-            float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
+            float4 *dstu = reinterpret_cast<float4 *>(sPB + i * kURow + col0 * 4);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
                 dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
         }
+    }
+    fence_proxy_async_smem();
+    const bool store = __syncthreads_and(go && ok);
+    if (store && tid < T) { // thread i: node i's rows
+        const size_t row = ((size_t)(o + tid) * H + h) * kD;
+        bulk_store(O + row, sQK + tid * kORow, kD * 2);
+        bulk_store(Uout + row, sPB + tid * kURow, kD * 4);
+        bulk_commit_group();
+        bulk_wait_group_read0(); // the shared rows stay valid until read
     }
     if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
     tc_fence_before();

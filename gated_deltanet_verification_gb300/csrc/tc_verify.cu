@@ -760,12 +760,16 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             for (int cc = 0; cc < 2; ++cc) {
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
-                tmem_ld32(tmem + TM_PROP + lane_base + col0, x);
-                if (m < 64) {
+                if (m < 64) { // both loads in flight at once
                     float y[32];
-                    tmem_ld32(tmem + lane_base + col0, y);
+                    tmem_ld32_async(tmem + TM_PROP + lane_base + col0, x);
+                    tmem_ld32_async(tmem + lane_base + col0, y);
+                    tmem_wait_ld32(x);
+                    tmem_wait_ld32(y);
 #pragma unroll
                     for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
+                } else {
+                    tmem_ld32(tmem + TM_PROP + lane_base + col0, x);
                 }
                 if (!store) continue;
                 const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
