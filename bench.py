@@ -833,8 +833,9 @@ def run_e2e(args, batch, sets, flags, stream, world):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / args.steps, 5),
             "mode": "per step: one pinned-host -> device copy of the round's packed inputs on a "
-                    "copy stream (overlapping the previous round), pack + verify + commit, O and "
-                    "status back to pinned host memory",
+                    "copy stream (overlapping the previous round), the round (" +
+                    ("verify with the topology step inside, commit" if flags & bole.FLAG_INLINE_TOPOLOGY
+                     else "pack, verify, commit") + "), O and status back to pinned host memory",
             "plain": {"value": round(job_throughput(batch.N, plain_steps, world, ms_plain), 1),
                       "ms_per_step": round(ms_plain / plain_steps, 5),
                       "mode": "the same copies and calls, all on one stream"}}
