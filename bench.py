@@ -72,6 +72,9 @@ def parse_args(argv=None):
     p.add_argument("--force-simt", action="store_true", help="use the FP32 CUDA-core kernels")
     p.add_argument("--one-tile-per-head", action="store_true",
                    help="trees of up to 32 nodes: force one CTA per (request, head)")
+    p.add_argument("--io-dtype", default=None, choices=[None, "bf16", "f32"],
+                   help="override the workload's q/k/v (and O) dtype; float32 inputs run the "
+                        "CUDA-core kernels")
     p.add_argument("--pack-round", action="store_true",
                    help="run the round as pack -> verify -> commit even where the "
                         "verification can form the topology itself")
@@ -357,6 +360,8 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         getattr(args, "verify_flags", 0)
     seed = rank_seed(cfg, rank)
     batch = inputs.config_batch(cfg, seed=seed, shape=args.shape)
+    if args.io_dtype:
+        batch.dtype = args.io_dtype  # the drawn values are exact in either type
     probe_db = device.to_device(batch, device=dev)
     # the topology step inside the verification where the kernels allow it
     inline = (not args.pack_round) and device.inline_topology_supported(probe_db, flags)

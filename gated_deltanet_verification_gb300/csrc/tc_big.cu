@@ -482,7 +482,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     // Outputs: each thread puts its 64 columns of row i of O (bf16) and U
     // (fp32) into shared memory freed by now ([Q;K] for O, the power and state
     // buffers for U; rows padded by 16 B so the row-per-thread writes are
-    // conflict-free), and one bulk copy per node row and tensor writes them:
+    // conflict-free), and the CTA stores them row segment by row segment:
     // row-per-thread global stores touched 32 cache lines per instruction.
     constexpr int kORow = kD * 2 + 16, kURow = kD * 4 + 16; // padded staged rows
     static_assert(kTB * kORow <= 65536 && kTB * kURow <= 131072, "staged outputs fit");
@@ -511,14 +511,19 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                 dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
         }
     }
-    fence_proxy_async_smem();
-    const bool store = __syncthreads_and(go && ok);
-    if (store && tid < T) { // thread i: node i's rows
-        const size_t row = ((size_t)(o + tid) * H + h) * kD;
-        bulk_store(O + row, sQK + tid * kORow, kD * 2);
-        bulk_store(Uout + row, sPB + tid * kURow, kD * 4);
-        bulk_commit_group();
-        bulk_wait_group_read0(); // the shared rows stay valid until read
+    if (__syncthreads_and(go && ok)) {
+        // O: T rows of 16 chunks of 16 B, U: T rows of 32 (16 lanes per
+        // 256-byte row segment: four cache lines per store instruction)
+        for (int c = tid; c < T * 16; c += kFUThreads) {
+            const int r = c >> 4, q4 = c & 15;
+            *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + q4 * 8) =
+                *reinterpret_cast<const uint4 *>(sQK + r * kORow + q4 * 16);
+        }
+        for (int c = tid; c < T * 32; c += kFUThreads) {
+            const int r = c >> 5, q4 = c & 31;
+            *reinterpret_cast<float4 *>(Uout + ((size_t)(o + r) * H + h) * kD + q4 * 4) =
+                *reinterpret_cast<const float4 *>(sPB + r * kURow + q4 * 16);
+        }
     }
     if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
     tc_fence_before();

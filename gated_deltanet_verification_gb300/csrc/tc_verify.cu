@@ -124,6 +124,8 @@ static_assert(2 * (VERIFY_SMEM + 1024) <= 228 * 1024, "two verification CTAs per
 static_assert(3 * VERIFY_SMEM > 228 * 1024,
               "at most two verification CTAs (2 x 256 TMEM columns) per SM");
 
+constexpr int kORow = kD * 2 + 16, kURow = kD * 4 + 16; // staged output rows, padded
+static_assert(kT * kORow <= 32768 && kT * kURow <= SBUF_BYTES, "staged outputs fit");
 constexpr int kComputeThreads = 256;          // warps 0..7: factors, split, epilogues
 constexpr int kThreads = kComputeThreads + 32; // warp 8: TMA and tcgen05 issue
 
@@ -251,6 +253,14 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             mbar_arrive_expect_tx(&bar[BAR_V], 8192);
             tma_load_3d(sA1 + SM_V, &tmV, &bar[BAR_V], 0, h, o);
             tma_load_3d(sA1 + SM_V + 16384, &tmV, &bar[BAR_V], 64, h, o);
+        }
+        if (!SMALL && in_range) {
+            // 64-node layout: the value rows can only be loaded once the first
+            // d_k half of the state products has released their buffer, and
+            // R^T waits for them; requested into L2 now, that load is an L2 hit
+            // (first wave of config 3: R^T found them 5.7 K cycles late)
+            tma_prefetch_l2_3d(&tmV, 0, h, o);
+            tma_prefetch_l2_3d(&tmV, 64, h, o);
         }
     }
     // What the previous call wrote (the status word pack reset, the
@@ -754,8 +764,14 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         ok &= waitb(BAR_MMA2);
         tc_fence_after();
         __syncwarp();
+        // Each thread puts its 64 columns of row i of O (bf16, rows 0..63) or
+        // U (fp32, rows 64..127) into shared memory the propagation has
+        // released (O rows in the [Q;K] buffer, U rows in the state buffer,
+        // padded by 16 B so the row-per-thread writes are conflict-free);
+        // then the compute warps store the rows with 16 lanes per 256-byte
+        // row segment -- row-per-thread global stores touched 32 cache lines
+        // per instruction.
         if (!SMALL || !(rowgrp & 1)) { // small trees: no output in the padding lanes
-            const bool store = ok && i < T;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
                 const int col0 = half * 64 + cc * 32;
@@ -768,13 +784,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                     tmem_wait_ld32(y);
 #pragma unroll
                     for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
-                } else {
-                    tmem_ld32(tmem + TM_PROP + lane_base + col0, x);
-                }
-                if (!store) continue;
-                const size_t row = ((size_t)(o + i) * H + h) * kD + col0;
-                if (m < 64) {
-                    uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
+                    uint4 *dsto = reinterpret_cast<uint4 *>(sA1 + i * kORow + col0 * 2);
 #pragma unroll
                     for (int uu = 0; uu < 4; ++uu) {
                         __nv_bfloat162 p2[4];
@@ -784,11 +794,26 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                         dsto[uu] = *reinterpret_cast<uint4 *>(p2);
                     }
                 } else {
-                    float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
+                    tmem_ld32(tmem + TM_PROP + lane_base + col0, x);
+                    float4 *dstu = reinterpret_cast<float4 *>(sbuf + i * kURow + col0 * 4);
 #pragma unroll
                     for (int uu = 0; uu < 8; ++uu)
                         dstu[uu] = make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
                 }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kComputeThreads) : "memory");
+        if (ok && !*sfail) {
+            // O: T rows of 16 chunks of 16 B; U: T rows of 32 chunks
+            for (int c = tid; c < T * 16; c += kComputeThreads) {
+                const int r = c >> 4, q = c & 15;
+                *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + q * 8) =
+                    *reinterpret_cast<const uint4 *>(sA1 + r * kORow + q * 16);
+            }
+            for (int c = tid; c < T * 32; c += kComputeThreads) {
+                const int r = c >> 5, q = c & 31;
+                *reinterpret_cast<float4 *>(Uout + ((size_t)(o + r) * H + h) * kD + q * 4) =
+                    *reinterpret_cast<const float4 *>(sbuf + r * kURow + q * 16);
             }
         }
         if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 1);

@@ -532,36 +532,54 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         mbar_arrive(&bar[VB_OPS]);
 
         // ---- outputs: O = P (Q S_pre) + M R (warps 0, 4), U = W R (warps 1, 5) ----
+        // Each thread puts its 32 columns of row i into the tile buffer the
+        // propagation has released (rows padded by 16 B); then the compute
+        // warps store the tile's rows segment by segment (row-per-thread
+        // global stores touch 32 cache lines per instruction).
+        constexpr int kOR = kVB * 2 + 16, kUR = kVB * 4 + 16; // staged row strides
+        uint8_t *stO = sS, *stU = sS + kVT * kOR;
         if (quad < 2) {
             ok &= waitb(VB_PROP);
             tc_fence_after();
             __syncwarp();
             const int col0 = warp >= 4 ? 32 : 0;
             float x[32];
-            tmem_ld32(tmem + TM_GP + lane_base + col0, x);
-            const bool store = ok && !*sfail && i < T;
-            const size_t row = ((size_t)(o + i) * H + h) * kD + c0 + col0;
             if (quad == 0) {
                 float y[32];
-                tmem_ld32(tmem + lane_base + col0, y);
-                if (store) {
+                tmem_ld32_async(tmem + TM_GP + lane_base + col0, x);
+                tmem_ld32_async(tmem + lane_base + col0, y);
+                tmem_wait_ld32(x);
+                tmem_wait_ld32(y);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
-                    uint4 *dsto = reinterpret_cast<uint4 *>(O + row);
+                for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
+                uint4 *dsto = reinterpret_cast<uint4 *>(stO + i * kOR + col0 * 2);
 #pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        __nv_bfloat162 p2[4];
+                for (int uu = 0; uu < 4; ++uu) {
+                    __nv_bfloat162 p2[4];
 #pragma unroll
-                        for (int t = 0; t < 4; ++t)
-                            p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
-                        dsto[uu] = *reinterpret_cast<uint4 *>(p2);
-                    }
+                    for (int t = 0; t < 4; ++t)
+                        p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
+                    dsto[uu] = *reinterpret_cast<uint4 *>(p2);
                 }
-            } else if (store) {
-                float4 *dstu = reinterpret_cast<float4 *>(Uout + row);
+            } else {
+                tmem_ld32(tmem + TM_GP + lane_base + col0, x);
+                float4 *dstu = reinterpret_cast<float4 *>(stU + i * kUR + col0 * 4);
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu)
                     dstu[uu] = make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kVTCompute) : "memory");
+        if (ok && !*sfail) {
+            for (int c = tid; c < T * 8; c += kVTCompute) { // O: 8 chunks of 16 B per row
+                const int r = c >> 3, q = c & 7;
+                *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + c0 + q * 8) =
+                    *reinterpret_cast<const uint4 *>(stO + r * kOR + q * 16);
+            }
+            for (int c = tid; c < T * 16; c += kVTCompute) { // U: 16 chunks per row
+                const int r = c >> 4, q = c & 15;
+                *reinterpret_cast<float4 *>(Uout + ((size_t)(o + r) * H + h) * kD + c0 + q * 4) =
+                    *reinterpret_cast<const float4 *>(stU + r * kUR + q * 16);
             }
         }
         if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 31);
