@@ -73,8 +73,9 @@ def parse_args(argv=None):
     p.add_argument("--one-tile-per-head", action="store_true",
                    help="trees of up to 32 nodes: force one CTA per (request, head)")
     p.add_argument("--io-dtype", default=None, choices=[None, "bf16", "f32"],
-                   help="override the workload's q/k/v (and O) dtype; float32 inputs run the "
-                        "CUDA-core kernels")
+                   help="the workload's q/k/v (and O) dtype: f32 draws the same values at full "
+                        "float32 precision (tensor-core value tiles for trees of up to 32 "
+                        "nodes; commit on the CUDA cores)")
     p.add_argument("--pack-round", action="store_true",
                    help="run the round as pack -> verify -> commit even where the "
                         "verification can form the topology itself")
@@ -146,8 +147,9 @@ KERNEL_SOURCES = {"tc_verify_kernel": "tc_verify.cu", "tc_commit_kernel": "tc_ve
                   "tc_big_fused_kernel": "tc_big.cu", "tc_vtile_kernel": "tc_vtile.cu"}
 
 
-def workload_key(config: int, shape: str) -> str:
-    return f"{config}{shape}" if config == 4 else str(config)
+def workload_key(config: int, shape: str, io_dtype: str = "bf16") -> str:
+    key = f"{config}{shape}" if config == 4 else str(config)
+    return key if io_dtype == "bf16" or config == 0 else key + io_dtype
 
 
 def recorded_traffic(kernels, workload: str):
@@ -359,9 +361,12 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         (bole.FLAG_VALUE_TILES if args.value_tiles else 0) | \
         getattr(args, "verify_flags", 0)
     seed = rank_seed(cfg, rank)
-    batch = inputs.config_batch(cfg, seed=seed, shape=args.shape)
-    if args.io_dtype:
-        batch.dtype = args.io_dtype  # the drawn values are exact in either type
+    if cfg == 0:  # the float32 toy; its values are kept as drawn
+        batch = inputs.config_batch(cfg, seed=seed, shape=args.shape)
+        if args.io_dtype:
+            batch.dtype = args.io_dtype
+    else:  # f32: the same draws at full float32 precision
+        batch = inputs.config_batch(cfg, seed=seed, shape=args.shape, dtype=args.io_dtype)
     probe_db = device.to_device(batch, device=dev)
     # the topology step inside the verification where the kernels allow it
     inline = (not args.pack_round) and device.inline_topology_supported(probe_db, flags)
@@ -378,17 +383,17 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         rb = device.alloc_round(db, flags)
         sets.append((db, rb))
     stream = torch.cuda.current_stream()
-    tc_shape = (not args.force_simt and batch.dtype == "bf16" and batch.dk == 128
-                and batch.dv == 128)
-    # value-tiled kernel: forced, or by default while the heads leave the
-    # one-CTA kernel (two CTAs per SM) short of one wave
+    tc_dims = not args.force_simt and batch.dk == 128 and batch.dv == 128
+    tc_shape = tc_dims and batch.dtype == "bf16"
+    # value-tiled kernel: fp32 inputs always; bf16 forced, or by default while
+    # the heads leave the one-CTA kernel (two CTAs per SM) short of one wave
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    vtile = (tc_shape and batch.max_T <= 32 and batch.max_depth < 16
+    vtile = (tc_dims and batch.max_T <= 32 and batch.max_depth < 16
              and not args.one_tile_per_head
-             and (args.value_tiles or batch.B * batch.H < 2 * sms))
+             and (batch.dtype == "f32" or args.value_tiles or batch.B * batch.H < 2 * sms))
     fused = tc_shape and batch.max_T <= 64 and batch.max_depth < 16   # single-CTA kernel
     big = tc_shape and not fused and batch.max_T <= 128              # fused large-tree kernel
-    tc_used = fused or big
+    tc_used = fused or big or vtile
     # pack (unless the verification forms the topology), verify (one tensor-core
     # kernel, or the CUDA-core producer + solve), commit
     launches_per_step = (0 if inline else 1) + (1 if tc_used else 2) + 1
@@ -492,8 +497,9 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
     verify_kernels = (["tc_vtile_kernel"] if vtile else ["tc_verify_kernel"] if fused
                       else ["tc_big_fused_kernel"] if big else [])
-    traffic = (recorded_traffic(verify_kernels if dominant == "verify" else ["tc_commit_kernel"],
-                                workload_key(cfg, args.shape)) if tc_used else None)
+    commit_kernels = ["tc_commit_kernel"] if tc_shape else []
+    traffic = (recorded_traffic(verify_kernels if dominant == "verify" else commit_kernels,
+                                workload_key(cfg, args.shape, batch.dtype)) if tc_used else None)
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": kern_rf[dominant]["frac"], "traffic": traffic, "peak_source": peak_kind,
@@ -513,7 +519,9 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         "metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16x2+tf32 (f32 acc)" if tc_used else "f32", "io_dtype": batch.dtype,
+        "dtype": ("bf16x2+tf32 (f32 acc)" if tc_shape and tc_used
+                  else "f32 as bf16x3 (6 products) + tf32x2 (f32 acc)" if tc_used else "f32"),
+        "io_dtype": batch.dtype,
         "data": "synthetic",
         "config": {"workload": inputs.CONFIG_NAMES[cfg]
                    + (f" [{args.shape}]" if cfg == 4 else ""),

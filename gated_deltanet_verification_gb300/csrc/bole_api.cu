@@ -25,17 +25,18 @@ bole_status from_cuda(cudaError_t e)
 }
 
 // Verification kernels: the value-tiled tensor-core kernel (trees of up to
-// 32 nodes, depth <= 15, two CTAs per head), the single-CTA tensor-core
-// kernel (trees of up to 64 nodes, depth <= 15), the large-tree tensor-core
-// kernel for larger or deeper trees (up to 128 nodes), else the FP32
-// CUDA-core kernels.
+// 32 nodes, depth <= 15, two CTAs per head; bf16 where the batch's heads
+// would leave the one-CTA kernel short of a wave, fp32 always), the
+// single-CTA tensor-core kernel (bf16, trees of up to 64 nodes, depth <=
+// 15), the large-tree tensor-core kernel for larger or deeper bf16 trees (up
+// to 128 nodes), else the FP32 CUDA-core kernels.
 enum class VerifyPath { VTile, Fused, Big, Simt };
 
 VerifyPath verify_path(const VerifyArgs &a, unsigned flags)
 {
     if (flags & BOLE_FLAG_FORCE_SIMT) return VerifyPath::Simt;
     if (!(flags & BOLE_FLAG_ONE_TILE_PER_HEAD) && tc_vtile_supported(a) &&
-        ((flags & BOLE_FLAG_VALUE_TILES) || tc_vtile_preferred(a)))
+        ((flags & BOLE_FLAG_VALUE_TILES) || a.dtype == BOLE_F32 || tc_vtile_preferred(a)))
         return VerifyPath::VTile;
     if (tc_verify_supported(a)) return VerifyPath::Fused;
     if (tc_big_supported(a)) return VerifyPath::Big;

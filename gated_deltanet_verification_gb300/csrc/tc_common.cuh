@@ -174,17 +174,21 @@ inline cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, int smem, cudaStr
     return cfg;
 }
 
-// q, k or v [N][H][128] bf16 as a 3-D tensor, boxes of 64 elements x 1 head x
-// `rows` nodes.
-inline cudaError_t make_node_map(CUtensorMap *map, const void *x, int N, int H, int rows)
+// q, k or v [N][H][128] as a 3-D tensor: bf16 in boxes of 64 elements x 1
+// head x `rows` nodes, or (f32) fp32 in boxes of 32 elements x 1 x `rows` --
+// 128-byte box rows either way.
+inline cudaError_t make_node_map(CUtensorMap *map, const void *x, int N, int H, int rows,
+                                 bool f32 = false)
 {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)N};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * es, (cuuint64_t)H * kD * es};
+    cuuint32_t box[3] = {f32 ? 32u : 64u, 1, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims, strides,
+    CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void *>(x), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

@@ -1,6 +1,6 @@
-// Value-tiled tensor-core verification for small trees: bf16 q/k/v,
-// d_k = d_v = 128, trees of up to 32 nodes, depth <= 15 (the batched
-// Qwen3.5-shaped workloads of the pages' evaluation).
+// Value-tiled tensor-core verification for small trees: d_k = d_v = 128,
+// trees of up to 32 nodes, depth <= 15 (the batched Qwen3.5-shaped workloads
+// of the pages' evaluation), bf16 or fp32 q/k/v.
 //
 // The pages' kernel splits d_v into N_v = d_v / b_v value tiles and gives each
 // (request, head, tile) its own CTA, so a request yields H * N_v
@@ -8,17 +8,19 @@
 // Here b_v = 64, N_v = 2: each CTA streams its 128 x 64 tile of S_pre by TMA,
 // forms the tree factors of its head on chip (both tiles of a head repeat
 // that small T x T work instead of exchanging it), and writes its 64 columns
-// of O and U.  A CTA needs 66 KB of shared memory and 128 tensor-memory
-// columns, so three share an SM and one wave covers 456 tiles.  The library
-// runs it for batches whose heads would leave the one-CTA-per-head kernel
-// short of a wave (a single request's heads, say): there the extra CTAs add
-// parallelism, while on larger batches the one-CTA kernel keeps more state
-// bytes in flight per SM.
+// of O and U.  bf16 inputs: 66 KB of shared memory and 128 tensor-memory
+// columns, three CTAs per SM; the library runs this form for batches whose
+// heads would leave the one-CTA-per-head kernel short of a wave (a single
+// request's heads, say): there the extra CTAs add parallelism, while on
+// larger batches the one-CTA kernel keeps more state bytes in flight per SM.
+// fp32 inputs: 111 KB, two CTAs per SM, the tensor-core path for every fp32
+// batch it covers.
 //
 // Per CTA (T <= 32 nodes of one head, value columns c0 .. c0 + 63):
 //   1. TMA: [Q;K] of the tree (q rows 0..31, k rows 32..63 of each K-atom)
-//      and the value rows of the tile; once the per-node reads have returned,
-//      the two 32-column boxes of the S_pre tile.
+//      and (bf16) the value rows of the tile; once the per-node reads have
+//      returned, the two 32-column boxes of the S_pre tile.  fp32 value rows
+//      go straight to the registers of the threads that form R^T.
 //   2. Warp 0: cumulative decay L_i along the ancestor-or-self mask (Lemma 1),
 //      the decay ratios exp(L_i - L_j) of each node's ancestors.
 //   3. tcgen05 Gram [Q;K] K^T (bf16 products, fp32 accumulation); warps 0, 1
@@ -28,15 +30,26 @@
 //      by ancestor depth; rows of W = (I+G)^{-1} (warp 0) and M = C W
 //      (warp 5) by backward substitution along each node's ancestor path --
 //      the finite Neumann sum of Eq. (6), term for term.
-//   4. Warps 1..4 split the S_pre tile in place into bf16 S_hi + S_lo as soon
-//      as it lands (~2^-17 relative residue per element); tcgen05
-//      [Q;K] (S_hi + S_lo) with exact bf16 products and fp32 accumulation
-//      gives Q S_pre and K S_pre of the tile (Eq. (7)).
+//   4. Warps 1..4 split the S_pre tile in place as soon as it lands; tcgen05
+//      [Q;K] S_pre with exact bf16 products and fp32 accumulation gives
+//      Q S_pre and K S_pre of the tile (Eq. (7)).
 //   5. Warps 1, 5: R^T = (beta (v - P K S_pre))^T of the tile; warps 0, 5
 //      write [M; W] -- both into the tile buffer the products released.
-//   6. One tcgen05 tf32 product [M; W] R (K = the tree's nodes) into the
-//      Gram's tensor-memory columns; warps 0, 4 write O = P Q S_pre + M R
-//      (bf16), warps 1, 5 U = W R (fp32).
+//   6. tcgen05 tf32 [M; W] R (K = the tree's nodes) into the Gram's
+//      tensor-memory columns; warps 0, 4 write O = P Q S_pre + M R, warps
+//      1, 5 U = W R (fp32).
+//
+// Precision.  bf16 inputs: S_pre = S_hi + S_lo in bf16 (a relative residue
+// of about 2^-17 per element), q and k exact, [M; W] and R in tf32.  fp32
+// inputs (the 1e-5 bound): every fp32 operand x of the Gram and the state
+// products is written as x1 + x2 + x3 in bf16 (x1 = bf16(x), x2 = bf16(x -
+// x1), x3 = bf16(x - x1 - x2): 24 significant bits, x itself for normal
+// floats), and the product keeps the six terms of order up to 2^-16,
+//   sum_{i + j <= 4} x_i y_j   (i, j >= 1),
+// dropping terms of order 2^-24; [M; W] and R^T are written as hi + lo in
+// tf32 (rounded to nearest here, so the hardware's reading of an operand
+// is exact) and the propagation keeps hi hi + hi lo + lo hi (dropped term
+// ~2^-22).  Accumulation is fp32 throughout.
 //
 // [Q;K] is stored without padding (64 rows per K-atom); the M = 128 products
 // read the 8 KB behind each atom as rows 64..127, whose results land in
@@ -59,37 +72,49 @@ constexpr int kVSlots = 16; // depth slots of the compact factors: depth <= 15
 constexpr int kVLd = 17;    // padded row stride of the compact factors
 
 // ---- shared-memory plan (bytes from a 1024-aligned base) ----
-//   S (32 KB): the state tile as two fp32 boxes [128 rows x 32 columns],
-//     split in place into S_hi (first box) and S_lo (second box), bf16
-//     N-contiguous [128 d_k rows x 64 columns]; after the state products
-//     [M; W] (rows 0..63, tf32 K-major, 128 B per row) in the first 8 KB and
-//     R^T (64 value rows x 32 nodes, tf32 K-major) in 16..24 KB.
-//   QK (16 KB): two K-atoms [64 rows x 128 B] of bf16 q (rows 0..31) and k
-//     (rows 32..63); the M = 128 products read 8 KB past each atom.
-//   V (4 KB): the tile's value rows [32 nodes x 64 bf16], 128B-swizzled.
+//   S: the state tile lands as two fp32 boxes [128 rows x 32 columns]
+//     (32 KB) and is split in place into bf16 copies, N-contiguous [128 d_k
+//     rows x 64 columns], 16 KB each: S_hi, S_lo (bf16 inputs) or S_1, S_2,
+//     S_3 (fp32 inputs, 48 KB).  After the state products: [M; W] (rows
+//     0..63, tf32 K-major, 128 B per row) and R^T (64 value rows x 32 nodes,
+//     tf32 K-major): bf16 inputs [M; W] at 0, R^T at 16 KB; fp32 inputs
+//     [M; W] hi at 0, lo at 16 KB, R^T hi at 32 KB, lo at 40 KB.  After the
+//     propagation: the staged O and U rows.
+//   QK: K-atoms [64 rows x 128 B] of [Q;K] (q rows 0..31, k rows 32..63):
+//     bf16 inputs two atoms (16 KB) loaded as they are; fp32 inputs four fp32
+//     atoms (32 KB) loaded, then rewritten as three bf16 copies of two atoms
+//     each (48 KB, copy c atom a at (2 c + a) x 8 KB).  The M = 128 products
+//     read 8 KB past each atom.
+//   V (bf16 inputs, 4 KB): the tile's value rows [32 nodes x 64 bf16],
+//     128B-swizzled.
 //   G (8 KB): the staged Gram rows [64 x 32 fp32] (q.k rows 0..31, k.k rows
 //     32..63), 16-byte chunks XOR-swizzled by row.
 //   X: compact C, G [32][17], ancestor table [32][16] u8, L, depth, log gamma.
-constexpr int VT_S = 0;
-constexpr int VT_QK = 32768;
-constexpr int VT_V = VT_QK + 16384;
-constexpr int VT_G = VT_V + 4096;
-constexpr int VT_X = VT_G + 8192;
 constexpr int VT_FAC = kVT * kVLd * 4;
-constexpr int VT_GC = VT_X;
-constexpr int VT_CC = VT_GC + VT_FAC;
-constexpr int VT_ANCAT = VT_CC + VT_FAC;
-constexpr int VT_L = VT_ANCAT + kVT * kVSlots;
-constexpr int VT_DEPTH = VT_L + kVT * 4;
-constexpr int VT_LG = VT_DEPTH + kVT * 4;
-constexpr int VT_BAR = VT_LG + kVT * 4;
-constexpr int VT_MISC = VT_BAR + 16 * 8; // TMEM slot, status copy, wait-failure flag,
-                                         // first bad node, request depth
-constexpr int VT_END = VT_MISC + 24;
-constexpr int VT_SMEM = VT_END + 1024;   // slack for the 1024-byte alignment of the base
-static_assert(VT_ANCAT % 16 == 0 && VT_BAR % 8 == 0, "aligned scratch");
-static_assert(VT_QK + 16384 + 8192 <= VT_X, "the products' reads past [Q;K] stay in V and G");
-static_assert(3 * (VT_SMEM + 1024) <= 228 * 1024, "three value-tile CTAs per SM");
+template <bool F32> struct VtPlan {
+    static constexpr int S = 0;
+    static constexpr int QK = S + (F32 ? 3 : 2) * 16384;
+    static constexpr int QK_ATOMS = F32 ? 6 : 2; // 8 KB K-atoms after the split
+    static constexpr int V = QK + QK_ATOMS * 8192;
+    static constexpr int G = V + (F32 ? 0 : 4096);
+    static constexpr int X = G + 8192;
+    static constexpr int GC = X;
+    static constexpr int CC = GC + VT_FAC;
+    static constexpr int ANCAT = CC + VT_FAC;
+    static constexpr int L = ANCAT + kVT * kVSlots;
+    static constexpr int DEPTH = L + kVT * 4;
+    static constexpr int LG = DEPTH + kVT * 4;
+    static constexpr int BAR = LG + kVT * 4;
+    static constexpr int MISC = BAR + 16 * 8; // TMEM slot, status copy, wait-failure flag,
+                                              // first bad node, request depth
+    static constexpr int END = MISC + 24;
+    static constexpr int SMEM = END + 1024;   // slack for the 1024-byte alignment of the base
+    static constexpr int PER_SM = F32 ? 2 : 3;
+    static_assert(ANCAT % 16 == 0 && BAR % 8 == 0, "aligned scratch");
+    static_assert(QK + (QK_ATOMS - 1) * 8192 + 16384 <= X,
+                  "the products' reads past [Q;K] stay inside the CTA's buffers");
+    static_assert(PER_SM * (SMEM + 1024) <= 228 * 1024, "CTAs per SM");
+};
 
 constexpr int kVTCompute = 192;               // warps 0..5
 constexpr int kVTThreads = kVTCompute + 32;   // warp 6: TMA and tcgen05 issue
@@ -100,40 +125,78 @@ constexpr uint32_t IDESC_VGRAM = idesc_bf16(128, 32, false, false);  // [Q;K] K^
 constexpr uint32_t IDESC_VSTATE = idesc_bf16(128, kVB, false, true); // [Q;K] S, S N-contiguous
 constexpr uint32_t IDESC_VPROP = idesc_tf32(128, kVB, false, false); // [M; W] R
 
+// The six (x copy, y copy) pairs of the fp32 products, smallest first.
+__device__ constexpr int kSplitA[6] = {2, 1, 0, 1, 0, 0};
+__device__ constexpr int kSplitB[6] = {0, 1, 2, 0, 1, 0};
+
 // mbarrier slots
 constexpr int VB_S = 0, VB_QK = 1, VB_V = 2, VB_GRAM = 3, VB_STATE = 4, VB_PROP = 5,
-              VB_TOPO = 6, VB_STAGED = 7, VB_CG = 8, VB_CONV = 9, VB_OPS = 10, VB_DRAIN = 11;
+              VB_TOPO = 6, VB_STAGED = 7, VB_CG = 8, VB_CONV = 9, VB_OPS = 10, VB_DRAIN = 11,
+              VB_QKS = 12; // fp32: [Q;K] split into its bf16 copies
 
-__global__ void __launch_bounds__(kVTThreads, 3)
+// x -> x1 + x2 + x3 (bf16 each) for eight consecutive floats, packed as
+// three 16-byte chunks.
+__device__ __forceinline__ void split3_bf16x8(const float *x, uint4 &c1, uint4 &c2, uint4 &c3)
+{
+    uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float x0 = x[2 * t], x1 = x[2 * t + 1];
+        const __nv_bfloat162 b1 = __floats2bfloat162_rn(x0, x1);
+        const float2 f1 = __bfloat1622float2(b1);
+        const float r0 = x0 - f1.x, r1 = x1 - f1.y; // exact
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(r0, r1);
+        const float2 f2 = __bfloat1622float2(b2);
+        const __nv_bfloat162 b3 = __floats2bfloat162_rn(r0 - f2.x, r1 - f2.y);
+        w1[t] = *reinterpret_cast<const uint32_t *>(&b1);
+        w2[t] = *reinterpret_cast<const uint32_t *>(&b2);
+        w3[t] = *reinterpret_cast<const uint32_t *>(&b3);
+    }
+    c1 = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    c2 = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    c3 = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+}
+
+// x rounded to the nearest tf32 (10 explicit mantissa bits; ties away from
+// zero), so that a tf32 operand holds exactly this value.
+__device__ __forceinline__ float tf32_round(float x)
+{
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(kVTThreads, VtPlan<F32>::PER_SM)
 tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const float *__restrict__ gamma, const float *__restrict__ beta,
                 const int32_t *__restrict__ offsets, const uint32_t *__restrict__ anc,
                 const int32_t *__restrict__ req_depth, int H, int N,
-                __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
+                void *__restrict__ Oout, float *__restrict__ Uout,
                 float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc,
-                const int32_t *__restrict__ parent, int max_depth, int inline_topo)
+                const int32_t *__restrict__ parent, int max_depth, int inline_topo,
+                const float *__restrict__ vf32)
 {
+    using P = VtPlan<F32>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sS = sm + VT_S, *sQK = sm + VT_QK, *sV = sm + VT_V, *sG = sm + VT_G;
-    float *Gc = reinterpret_cast<float *>(sm + VT_GC);
-    float *Cc = reinterpret_cast<float *>(sm + VT_CC);
-    uint8_t *ancat = sm + VT_ANCAT;
-    float *Ls = reinterpret_cast<float *>(sm + VT_L);
-    int *Ds = reinterpret_cast<int *>(sm + VT_DEPTH);
-    float *LGs = reinterpret_cast<float *>(sm + VT_LG);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + VT_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + VT_MISC);
-    int *sfault = reinterpret_cast<int *>(sm + VT_MISC + 4);
-    volatile int *sfail = reinterpret_cast<volatile int *>(sm + VT_MISC + 8);
+    uint8_t *sS = sm + P::S, *sQK = sm + P::QK, *sV = sm + P::V, *sG = sm + P::G;
+    float *Gc = reinterpret_cast<float *>(sm + P::GC);
+    float *Cc = reinterpret_cast<float *>(sm + P::CC);
+    uint8_t *ancat = sm + P::ANCAT;
+    float *Ls = reinterpret_cast<float *>(sm + P::L);
+    int *Ds = reinterpret_cast<int *>(sm + P::DEPTH);
+    float *LGs = reinterpret_cast<float *>(sm + P::LG);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P::BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P::MISC);
+    int *sfault = reinterpret_cast<int *>(sm + P::MISC + 4);
+    volatile int *sfail = reinterpret_cast<volatile int *>(sm + P::MISC + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x >> 1, vh = blockIdx.x & 1; // (request, head), value tile
     const int b = unit / H, h = unit % H;
     const int c0 = vh * kVB; // first value column of the tile
 
-    if (sm + VT_END > smem_raw + VT_SMEM) { // dynamic base too far from 1024 B
+    if (sm + P::END > smem_raw + P::SMEM) { // dynamic base too far from 1024 B
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -5);
         return;
     }
@@ -156,17 +219,28 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         mbar_init(&bar[VB_CONV], 128);
         mbar_init(&bar[VB_OPS], kVTCompute);
         mbar_init(&bar[VB_DRAIN], 1);
+        mbar_init(&bar[VB_QKS], 128);
         fence_mbar_init();
         if (in_range) {
-            // q rows 0..31 and k rows 32..63 of both K-atoms; the tile's value rows
-            mbar_arrive_expect_tx(&bar[VB_QK], 16384);
+            if constexpr (F32) {
+                // q rows 0..31 and k rows 32..63 of the four fp32 K-atoms
+                mbar_arrive_expect_tx(&bar[VB_QK], 32768);
 #pragma unroll
-            for (int ka = 0; ka < 2; ++ka) {
-                tma_load_3d(sQK + ka * 8192, &tmQ, &bar[VB_QK], 64 * ka, h, o);
-                tma_load_3d(sQK + ka * 8192 + 4096, &tmK, &bar[VB_QK], 64 * ka, h, o);
+                for (int ka = 0; ka < 4; ++ka) {
+                    tma_load_3d(sQK + ka * 8192, &tmQ, &bar[VB_QK], 32 * ka, h, o);
+                    tma_load_3d(sQK + ka * 8192 + 4096, &tmK, &bar[VB_QK], 32 * ka, h, o);
+                }
+            } else {
+                // q rows 0..31 and k rows 32..63 of both K-atoms; the tile's value rows
+                mbar_arrive_expect_tx(&bar[VB_QK], 16384);
+#pragma unroll
+                for (int ka = 0; ka < 2; ++ka) {
+                    tma_load_3d(sQK + ka * 8192, &tmQ, &bar[VB_QK], 64 * ka, h, o);
+                    tma_load_3d(sQK + ka * 8192 + 4096, &tmK, &bar[VB_QK], 64 * ka, h, o);
+                }
+                mbar_arrive_expect_tx(&bar[VB_V], 4096);
+                tma_load_3d(sV, &tmV, &bar[VB_V], c0, h, o);
             }
-            mbar_arrive_expect_tx(&bar[VB_V], 4096);
-            tma_load_3d(sV, &tmV, &bar[VB_V], c0, h, o);
         }
     }
     // per-thread tree inputs: warp 0 (node = lane) the gates of its row, warps
@@ -174,10 +248,30 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
     const int i = lane;
     float bt = 0.f, g_i = 1.f;
     int my_par = -1; // warp 0, topology formed here: the parent of node i
+    // fp32 inputs: warps 1 and 5 hold the 32 value columns of node i they
+    // turn into R^T (columns c0 + 32 (warp / 5) ...), read now so the loads
+    // complete long before R^T is formed
+    float vreg[F32 ? 32 : 1];
+    if constexpr (F32) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) vreg[c] = 0.f;
+    }
     if (in_range && i < T && (warp == 0 || warp == 1 || warp == 5)) {
         bt = beta[(size_t)(o + i) * H + h];
         if (warp == 0) g_i = gamma[(size_t)(o + i) * H + h];
         if (warp == 0 && inline_topo) my_par = parent[o + i];
+        if constexpr (F32) {
+            if (warp != 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    vf32 + ((size_t)(o + i) * H + h) * kD + c0 + (warp == 5 ? 32 : 0));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 t4 = src[u];
+                    vreg[4 * u] = t4.x; vreg[4 * u + 1] = t4.y;
+                    vreg[4 * u + 2] = t4.z; vreg[4 * u + 3] = t4.w;
+                }
+            }
+        }
     }
     // What the previous call wrote (the status word pack reset, the request's
     // depth, each node's ancestor-or-self mask) is read after the wait.
@@ -186,7 +280,7 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         *sfault = *(const volatile int32_t *)st; // one read: a uniform exit
         *sfail = 0;
     }
-    int *stopo = reinterpret_cast<int *>(sm + VT_MISC + 12); // first bad node, depth
+    int *stopo = reinterpret_cast<int *>(sm + P::MISC + 12); // first bad node, depth
     const int d_read = inline_topo ? 0 : req_depth[b];
     int my_depth = -1;
     uint32_t my_mask = 0;
@@ -260,7 +354,7 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         if (issuer) { // the copies in flight end before the CTA retires
             if (in_range) {
                 mbar_wait(&bar[VB_QK], 0, kWaitNs);
-                mbar_wait(&bar[VB_V], 0, kWaitNs);
+                if (!F32) mbar_wait(&bar[VB_V], 0, kWaitNs);
             }
         }
         if (warp == 0) tmem_dealloc(tmem, TM_COLS);
@@ -282,26 +376,55 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         if (lane == 0) {
             const uint32_t qk = smem_addr(sQK), s0 = smem_addr(sS);
             do { // every step ends the issue once a wait anywhere in the CTA gave up
-                ok &= waitb(VB_QK);
+                ok &= waitb(F32 ? VB_QKS : VB_QK);
                 if (!ok || *sfail) break;
                 tc_fence_after();
+                if constexpr (F32) {
+                    // Gram from the bf16 copies: the six pairs, 16 d_k per step
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) { // Gram [Q;K] K^T, 16 d_k per step
-                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + TM_GP, sdesc_sw128(qk + off, 16, 1024),
-                                sdesc_sw128(qk + off + 4096, 16, 1024), IDESC_VGRAM, kk > 0);
+                    for (int t = 0; t < 6; ++t)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                            mma_bf16_ss(tmem + TM_GP,
+                                        sdesc_sw128(qk + kSplitA[t] * 16384 + off, 16, 1024),
+                                        sdesc_sw128(qk + kSplitB[t] * 16384 + off + 4096, 16, 1024),
+                                        IDESC_VGRAM, t > 0 || kk > 0);
+                        }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) { // Gram [Q;K] K^T, 16 d_k per step
+                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_bf16_ss(tmem + TM_GP, sdesc_sw128(qk + off, 16, 1024),
+                                    sdesc_sw128(qk + off + 4096, 16, 1024), IDESC_VGRAM, kk > 0);
+                    }
                 }
                 mma_commit(&bar[VB_GRAM]);
                 ok &= waitb(VB_CONV);
                 if (!ok || *sfail) break;
                 tc_fence_after();
+                if constexpr (F32) {
+                    // [Q;K] S_pre from the bf16 copies of both: the six pairs
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) { // [Q;K] (S_hi + S_lo), 16 d_k rows per step
-                    const uint64_t ad = sdesc_sw128(qk + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + kk * 2048, 16384, 1024), IDESC_VSTATE,
-                                kk > 0);
-                    mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + 16384 + kk * 2048, 16384, 1024),
-                                IDESC_VSTATE, 1);
+                    for (int t = 0; t < 6; ++t)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                            mma_bf16_ss(tmem, sdesc_sw128(qk + kSplitA[t] * 16384 + off, 16, 1024),
+                                        sdesc_sw128(s0 + kSplitB[t] * 16384 + kk * 2048, 16384,
+                                                    1024),
+                                        IDESC_VSTATE, t > 0 || kk > 0);
+                        }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) { // [Q;K] (S_hi + S_lo), 16 d_k rows per step
+                        const uint64_t ad =
+                            sdesc_sw128(qk + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + kk * 2048, 16384, 1024),
+                                    IDESC_VSTATE, kk > 0);
+                        mma_bf16_ss(tmem, ad, sdesc_sw128(s0 + 16384 + kk * 2048, 16384, 1024),
+                                    IDESC_VSTATE, 1);
+                    }
                 }
                 mma_commit(&bar[VB_STATE]);
                 // the state tile of the CTA one wave later goes to L2 now that
@@ -314,9 +437,23 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 ok &= waitb(VB_OPS);
                 if (!ok || *sfail) break;
                 tc_fence_after();
-                for (int kk = 0; kk < (T + 7) / 8; ++kk) // [M; W] R over the tree's nodes
-                    mma_tf32_ss(tmem + TM_GP, sdesc_sw128(s0 + kk * 32, 16, 1024),
-                                sdesc_sw128(s0 + 16384 + kk * 32, 16, 1024), IDESC_VPROP, kk > 0);
+                if constexpr (F32) {
+                    // [M; W] R as lo hi + hi lo + hi hi, over the tree's nodes
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const uint32_t a = s0 + (t == 0 ? 16384 : 0);
+                        const uint32_t bb = s0 + (t == 1 ? 40960 : 32768);
+                        for (int kk = 0; kk < (T + 7) / 8; ++kk)
+                            mma_tf32_ss(tmem + TM_GP, sdesc_sw128(a + kk * 32, 16, 1024),
+                                        sdesc_sw128(bb + kk * 32, 16, 1024), IDESC_VPROP,
+                                        t > 0 || kk > 0);
+                    }
+                } else {
+                    for (int kk = 0; kk < (T + 7) / 8; ++kk) // [M; W] R over the tree's nodes
+                        mma_tf32_ss(tmem + TM_GP, sdesc_sw128(s0 + kk * 32, 16, 1024),
+                                    sdesc_sw128(s0 + 16384 + kk * 32, 16, 1024), IDESC_VPROP,
+                                    kk > 0);
+                }
                 mma_commit(&bar[VB_PROP]);
             } while (0);
         }
@@ -352,12 +489,46 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 ratio[t] = L;
             }
 #pragma unroll
-            for (int t = 0; t < kVSlots; ++t) ratio[t] = __expf(L - ratio[t]);
+            for (int t = 0; t < kVSlots; ++t)
+                ratio[t] = F32 ? expf(L - ratio[t]) : __expf(L - ratio[t]);
             *reinterpret_cast<uint4 *>(ancat + i * kVSlots) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
             Ls[i] = L;
             Ds[i] = my_depth;
             if (vh == 0 && i < T) logP[(size_t)(o + i) * H + h] = L;
             mbar_arrive(&bar[VB_TOPO]);
+        }
+        if constexpr (F32) {
+            if (warp >= 1 && warp <= 4) {
+                // [Q;K] -> three bf16 copies: thread (row r, d_k half hf)
+                // reads its 64 floats from fp32 atoms 2 hf, 2 hf + 1, and
+                // once all 128 threads hold theirs, writes 64 bf16 of row r
+                // into atom hf of each copy.
+                const int t = tid - 32, r = t & 63, hf = t >> 6;
+                ok &= waitb(VB_QK);
+                float x[64];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(
+                        sQK + (2 * hf) * 8192 + sw128_chunk(r, c));
+                    const float4 a1 = *reinterpret_cast<const float4 *>(
+                        sQK + (2 * hf + 1) * 8192 + sw128_chunk(r, c));
+                    x[4 * c + 0] = a0.x; x[4 * c + 1] = a0.y; x[4 * c + 2] = a0.z;
+                    x[4 * c + 3] = a0.w;
+                    x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
+                    x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
+                }
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 c1, c2, c3;
+                    split3_bf16x8(x + 8 * c, c1, c2, c3);
+                    *reinterpret_cast<uint4 *>(sQK + hf * 8192 + sw128_chunk(r, c)) = c1;
+                    *reinterpret_cast<uint4 *>(sQK + (2 + hf) * 8192 + sw128_chunk(r, c)) = c2;
+                    *reinterpret_cast<uint4 *>(sQK + (4 + hf) * 8192 + sw128_chunk(r, c)) = c3;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bar[VB_QKS]);
+            }
         }
         if (warp < 2) {
             // stage the Gram rows: q.k (warp 0, lanes 0..31), k.k (warp 1)
@@ -397,9 +568,10 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             mbar_arrive(&bar[VB_CG]);
         }
         if (warp >= 1 && warp <= 4) {
-            // S_pre tile = S_hi + S_lo in place (row r): both boxes' row r
-            // (columns 0..31, 32..63) become 64 bf16 of S_hi (first box) and
-            // of S_lo (second box), N-contiguous and 128B-swizzled
+            // S_pre tile split in place (row r): both boxes' row r (columns
+            // 0..31, 32..63) become 64 bf16 of each copy, N-contiguous and
+            // 128B-swizzled -- S_hi in the first box and S_lo in the second
+            // (bf16 inputs), or S_1, S_2 there and S_3 after them (fp32)
             const int r = tid - 32;
             ok &= waitb(VB_S);
             uint8_t *box0 = sS, *box1 = sS + 16384;
@@ -412,22 +584,33 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
                 x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
             }
+            if constexpr (F32) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-                    hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+                for (int c = 0; c < 8; ++c) {
+                    uint4 c1, c2, c3;
+                    split3_bf16x8(x + 8 * c, c1, c2, c3);
+                    *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) = c1;
+                    *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) = c2;
+                    *reinterpret_cast<uint4 *>(sS + 32768 + sw128_chunk(r, c)) = c3;
                 }
-                *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) =
-                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) =
-                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float x0 = x[8 * c + 2 * t], x1 = x[8 * c + 2 * t + 1];
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+                        hw[t] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lw[t] = *reinterpret_cast<const uint32_t *>(&l2);
+                    }
+                    *reinterpret_cast<uint4 *>(box0 + sw128_chunk(r, c)) =
+                        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(box1 + sw128_chunk(r, c)) =
+                        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(&bar[VB_CONV]);
@@ -491,14 +674,25 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             ok &= waitb(VB_STATE);
             const int orow = wrow ? 32 + n : n; // [M; W]: M rows 0..31, W rows 32..63
 #pragma unroll
-            for (int c = 0; c < 8; ++c) // K extent <= 32 nodes: one 128-byte row
+            for (int c = 0; c < 8; ++c) { // K extent <= 32 nodes: one 128-byte row
                 *reinterpret_cast<float4 *>(sS + sw128_chunk(orow, c)) =
                     make_float4(0.f, 0.f, 0.f, 0.f);
+                if (F32) // the tf32 low part
+                    *reinterpret_cast<float4 *>(sS + 16384 + sw128_chunk(orow, c)) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
             for (int u = 0; u < kVSlots; ++u) {
                 if (u <= di) {
                     const int au = (aw4[u >> 2] >> (8 * (u & 3))) & 0xff;
-                    *reinterpret_cast<float *>(sS + sw128_offset(orow, au)) = vals[u];
+                    if constexpr (F32) {
+                        const float hi = tf32_round(vals[u]);
+                        *reinterpret_cast<float *>(sS + sw128_offset(orow, au)) = hi;
+                        *reinterpret_cast<float *>(sS + 16384 + sw128_offset(orow, au)) =
+                            tf32_round(vals[u] - hi);
+                    } else {
+                        *reinterpret_cast<float *>(sS + sw128_offset(orow, au)) = vals[u];
+                    }
                 }
             }
         }
@@ -506,24 +700,36 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             // R^T of the tile's columns 32 (warp / 5) .. + 31 for node i = lane:
             // K S_pre from tensor-memory lanes 32..63, the value row from V.
             ok &= waitb(VB_STATE);
-            ok &= waitb(VB_V);
+            if (!F32) ok &= waitb(VB_V);
             tc_fence_after();
             __syncwarp();
             const int col0 = warp == 5 ? 32 : 0;
-            uint8_t *dst = sS + 16384;
-            const uint8_t *vrow = sV + i * 128;
             float x[32];
             tmem_ld32(tmem + lane_base + col0, x);
+            if constexpr (F32) {
+                // R^T as tf32 hi (32 KB) + lo (40 KB); the value row from registers
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                float f[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                  vrow + ((((col0 >> 3) + uu) ^ (i & 7)) << 4)), f);
+                for (int c = 0; c < 32; ++c) {
+                    const float r = (i < T) ? bt * (vreg[c] - p * x[c]) : 0.f;
+                    const float hi = tf32_round(r);
+                    *reinterpret_cast<float *>(sS + 32768 + sw128_offset(col0 + c, i)) = hi;
+                    *reinterpret_cast<float *>(sS + 40960 + sw128_offset(col0 + c, i)) =
+                        tf32_round(r - hi);
+                }
+            } else {
+                uint8_t *dst = sS + 16384;
+                const uint8_t *vrow = sV + i * 128;
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int c = 8 * uu + t;
-                    const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
-                    *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i)) = r;
+                for (int uu = 0; uu < 4; ++uu) {
+                    float f[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                      vrow + ((((col0 >> 3) + uu) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int c = 8 * uu + t;
+                        const float r = (i < T) ? bt * (f[t] - p * x[c]) : 0.f;
+                        *reinterpret_cast<float *>(dst + sw128_offset(col0 + c, i)) = r;
+                    }
                 }
             }
         }
@@ -536,7 +742,7 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         // propagation has released (rows padded by 16 B); then the compute
         // warps store the tile's rows segment by segment (row-per-thread
         // global stores touch 32 cache lines per instruction).
-        constexpr int kOR = kVB * 2 + 16, kUR = kVB * 4 + 16; // staged row strides
+        constexpr int kOR = kVB * (F32 ? 4 : 2) + 16, kUR = kVB * 4 + 16; // staged row strides
         uint8_t *stO = sS, *stU = sS + kVT * kOR;
         if (quad < 2) {
             ok &= waitb(VB_PROP);
@@ -552,14 +758,22 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 tmem_wait_ld32(y);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) x[t] = fmaf(p, y[t], x[t]);
-                uint4 *dsto = reinterpret_cast<uint4 *>(stO + i * kOR + col0 * 2);
+                if constexpr (F32) {
+                    float4 *dsto = reinterpret_cast<float4 *>(stO + i * kOR + col0 * 4);
 #pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    __nv_bfloat162 p2[4];
+                    for (int uu = 0; uu < 8; ++uu)
+                        dsto[uu] =
+                            make_float4(x[4 * uu], x[4 * uu + 1], x[4 * uu + 2], x[4 * uu + 3]);
+                } else {
+                    uint4 *dsto = reinterpret_cast<uint4 *>(stO + i * kOR + col0 * 2);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
-                    dsto[uu] = *reinterpret_cast<uint4 *>(p2);
+                    for (int uu = 0; uu < 4; ++uu) {
+                        __nv_bfloat162 p2[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            p2[t] = __floats2bfloat162_rn(x[8 * uu + 2 * t], x[8 * uu + 2 * t + 1]);
+                        dsto[uu] = *reinterpret_cast<uint4 *>(p2);
+                    }
                 }
             } else {
                 tmem_ld32(tmem + TM_GP + lane_base + col0, x);
@@ -571,10 +785,20 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kVTCompute) : "memory");
         if (ok && !*sfail) {
-            for (int c = tid; c < T * 8; c += kVTCompute) { // O: 8 chunks of 16 B per row
-                const int r = c >> 3, q = c & 7;
-                *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + c0 + q * 8) =
-                    *reinterpret_cast<const uint4 *>(stO + r * kOR + q * 16);
+            if constexpr (F32) {
+                float *O = static_cast<float *>(Oout);
+                for (int c = tid; c < T * 16; c += kVTCompute) { // O: 16 chunks of 16 B per row
+                    const int r = c >> 4, q = c & 15;
+                    *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + c0 + q * 4) =
+                        *reinterpret_cast<const uint4 *>(stO + r * kOR + q * 16);
+                }
+            } else {
+                __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(Oout);
+                for (int c = tid; c < T * 8; c += kVTCompute) { // O: 8 chunks of 16 B per row
+                    const int r = c >> 3, q = c & 7;
+                    *reinterpret_cast<uint4 *>(O + ((size_t)(o + r) * H + h) * kD + c0 + q * 8) =
+                        *reinterpret_cast<const uint4 *>(stO + r * kOR + q * 16);
+                }
             }
             for (int c = tid; c < T * 16; c += kVTCompute) { // U: 16 chunks per row
                 const int r = c >> 4, q = c & 15;
@@ -593,7 +817,7 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             mma_commit(&bar[VB_DRAIN]);
             mbar_wait(&bar[VB_DRAIN], 0, kWaitNs);
             mbar_wait(&bar[VB_QK], 0, kWaitNs);
-            mbar_wait(&bar[VB_V], 0, kWaitNs);
+            if (!F32) mbar_wait(&bar[VB_V], 0, kWaitNs);
             mbar_wait(&bar[VB_S], 0, kWaitNs);
         }
         __syncthreads();
@@ -620,8 +844,8 @@ static int vtile_resident_ctas(int per_sm)
 
 bool tc_vtile_supported(const VerifyArgs &a)
 {
-    return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD && a.max_T <= kVT &&
-           a.max_depth < kVSlots && !a.vk;
+    return (a.dtype == BOLE_BF16 || a.dtype == BOLE_F32) && a.dk == kD && a.dv == kD &&
+           a.max_T <= kVT && a.max_depth < kVSlots && !a.vk;
 }
 
 // Value tiles pay off while the heads of the batch leave the one-CTA
@@ -635,25 +859,34 @@ bool tc_vtile_preferred(const VerifyArgs &a)
     return slots > 0 && a.B * a.H < slots;
 }
 
-cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
+template <bool F32>
+static cudaError_t launch_vtile(const VerifyArgs &a, cudaStream_t s, bool overlap)
 {
+    using P = VtPlan<F32>;
     const int units = a.B * a.H;
-    if (units == 0 || a.N == 0) return cudaSuccess;
     CUtensorMap mS, mQ, mK, mV;
     cudaError_t e = make_state_map(&mS, a.S_pre, units);
-    if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, kVT);
-    if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kVT);
-    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kVT);
+    if (e == cudaSuccess) e = make_node_map(&mQ, a.q, a.N, a.H, kVT, F32);
+    if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, kVT, F32);
+    if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, kVT, F32);
     if (e != cudaSuccess) return e;
-    e = configure_once(reinterpret_cast<const void *>(tc_vtile_kernel), VT_SMEM, true);
+    e = configure_once(reinterpret_cast<const void *>(tc_vtile_kernel<F32>), P::SMEM, true);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = launch_config(dim3(2 * units), dim3(kVTThreads), VT_SMEM, s,
+    const cudaLaunchConfig_t cfg = launch_config(dim3(2 * units), dim3(kVTThreads), P::SMEM, s,
                                                  overlap, attr);
-    return cudaLaunchKernelEx(&cfg, tc_vtile_kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets,
-                              a.anc, a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O),
-                              a.U, a.logP, a.st, vtile_resident_ctas(3), overlap ? 0 : 1,
-                              a.parent, a.max_depth, a.inline_topo ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, tc_vtile_kernel<F32>, mS, mQ, mK, mV, a.gamma, a.beta,
+                              a.offsets, a.anc, a.req_depth, a.H, a.N, a.O, a.U, a.logP, a.st,
+                              vtile_resident_ctas(P::PER_SM), overlap ? 0 : 1, a.parent,
+                              a.max_depth, a.inline_topo ? 1 : 0,
+                              static_cast<const float *>(F32 ? a.v : nullptr));
+}
+
+cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
+{
+    if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
+    return a.dtype == BOLE_F32 ? launch_vtile<true>(a, s, overlap)
+                               : launch_vtile<false>(a, s, overlap);
 }
 
 } // namespace bole

@@ -93,11 +93,16 @@ def commit(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> No
 
 def inline_topology_supported(db: DeviceBatch, flags: int = 0) -> bool:
     """Whether the verification can form the round's topology itself
-    (bole.FLAG_INLINE_TOPOLOGY): the tensor-core kernels for trees of up to 64
-    nodes and depth <= 15, bf16, dk = dv = 128, default state layout."""
-    return (db.q.dtype == torch.bfloat16 and db.dk == 128 and db.dv == 128
-            and db.max_T <= 64 and db.max_depth <= 15
-            and not flags & (bole.FLAG_FORCE_SIMT | bole.FLAG_STATE_VK))
+    (bole.FLAG_INLINE_TOPOLOGY): the tensor-core kernels for dk = dv = 128,
+    depth <= 15 and the default state layout -- bf16 trees of up to 64 nodes,
+    fp32 trees of up to 32 (the value-tiled kernel)."""
+    if (db.dk != 128 or db.dv != 128 or db.max_depth > 15
+            or flags & (bole.FLAG_FORCE_SIMT | bole.FLAG_STATE_VK)):
+        return False
+    if db.q.dtype == torch.bfloat16:
+        return db.max_T <= 64
+    return (db.q.dtype == torch.float32 and db.max_T <= 32
+            and not flags & bole.FLAG_ONE_TILE_PER_HEAD)
 
 
 def run_round(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:

@@ -269,23 +269,29 @@ CONFIG_NAMES = {
 SHAPES_CFG4 = ("chain", "star", "4ary")
 
 
-def config_batch(cfg: int, seed: Optional[int] = None, shape: str = "chain") -> TreeBatch:
-    """Build one of the five workloads.  Default seed = 1000 + cfg."""
+def config_batch(cfg: int, seed: Optional[int] = None, shape: str = "chain",
+                 dtype: Optional[str] = None) -> TreeBatch:
+    """Build one of the five workloads.  Default seed = 1000 + cfg.  dtype
+    "f32" keeps q, k, v of configs 1-4 at full float32 precision (the same
+    draws, not rounded to bf16)."""
     if seed is None:
         seed = 1000 + cfg
+    if dtype is not None and dtype not in ("f32", "bf16"):
+        raise ValueError(dtype)
+    qkv = dtype or "bf16"
     rng = np.random.Generator(np.random.PCG64(seed))
     if cfg == 0:
         trees = [random_parent_tree(rng, 8, 3)]
         return make_batch("cfg0", rng, trees, 1, 16, 16, "f32", 3, 0.1, "deepest")
     if cfg == 1:
         trees = [random_parent_tree(rng, 32, 6)]
-        return make_batch("cfg1", rng, trees, 16, 128, 128, "bf16", 6, 0.05, "leaf")
+        return make_batch("cfg1", rng, trees, 16, 128, 128, qkv, 6, 0.05, "leaf")
     if cfg == 2:
         trees = [random_parent_tree(rng, 32, 8) for _ in range(16)]
-        return make_batch("cfg2", rng, trees, 32, 128, 128, "bf16", 8, 0.05, "uniform")
+        return make_batch("cfg2", rng, trees, 32, 128, 128, qkv, 8, 0.05, "uniform")
     if cfg == 3:
         trees = budgeted_forest(rng, 64, 8, 64, 2048, 12)
-        return make_batch("cfg3", rng, trees, 32, 128, 128, "bf16", 12, 0.05, "uniform")
+        return make_batch("cfg3", rng, trees, 32, 128, 128, qkv, 12, 0.05, "uniform")
     if cfg == 4:
         if shape == "chain":
             tree, md = chain_tree(128), 127
@@ -296,7 +302,7 @@ def config_batch(cfg: int, seed: Optional[int] = None, shape: str = "chain") -> 
         else:
             raise ValueError(shape)
         trees = [tree.copy() for _ in range(8)]
-        return make_batch(f"cfg4-{shape}", rng, trees, 32, 128, 128, "bf16", md, 0.05,
+        return make_batch(f"cfg4-{shape}", rng, trees, 32, 128, 128, qkv, md, 0.05,
                           "deepest")
     raise ValueError(f"unknown config {cfg}")
 

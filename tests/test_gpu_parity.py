@@ -91,10 +91,39 @@ def test_cuda_core_path_parity(cfg):
 
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_fp32_inputs_parity(cfg):
-    """Same workloads with float32 q/k/v: float32 tolerance."""
-    b = I.config_batch(cfg)
-    b.dtype = "f32"
+    """Same workloads with full-precision float32 q/k/v (the tensor-core
+    value-tiled kernel, three-way bf16 operand split): float32 tolerance."""
+    b = I.config_batch(cfg, dtype="f32")
     _check(b, _run(b, dtype=torch.float32), TOL["f32"])
+
+
+@pytest.mark.parametrize("sizes,H,max_depth,shape,sigma", [
+    ([32] * 8, 8, 8, "random", 0.05),         # the batched forest's shape
+    ([1, 32, 0, 7, 0, 2], 3, 15, "random", 0.1),  # 1-node, empty and ragged trees
+    ([16, 16, 9], 5, 15, "chain", 0.1),        # the deepest chains the kernel takes
+    ([32, 32], 2, 1, "star", 0.1),             # depth 0
+    ([24, 31], 4, 15, "random", 0.5),          # large operands: the split's lower copies carry weight
+])
+def test_fp32_tensor_core_kernel_matches_oracle_and_cuda_core(sizes, H, max_depth, shape, sigma):
+    """fp32 q/k/v on the tensor cores: every fp32 operand of the Gram and the
+    state products as three bf16 parts (six products kept), the propagation
+    as tf32 hi + lo.  Against the oracle per tensor, per (request, head) and
+    per node row at the float32 bound, and against the FP32 CUDA-core kernels
+    (FLAG_FORCE_SIMT) on the same forest."""
+    from gated_deltanet_verification_gb300 import bole
+    b = I.random_batch(seed=sum(sizes) + 11 * H, B=len(sizes), H=H, dk=128, dv=128, sizes=sizes,
+                       max_depth=max_depth, dtype="f32", sigma=sigma, shape=shape)
+    Oe, Ue, Le = oracle.verify(b)
+    got = {}
+    for name, flags in (("tc", 0), ("simt", bole.FLAG_FORCE_SIMT)):
+        O, U, logP = _verify_flags(b, flags, max_T=32)
+        assert rel_fro(O, Oe) <= TOL["f32"] and rel_fro(U, Ue) <= TOL["f32"], name
+        assert_local_parity(f"{b.name}/{name}", "O", O, Oe, b.offsets, TOL["f32"])
+        assert_local_parity(f"{b.name}/{name}", "U", U, Ue, b.offsets, TOL["f32"])
+        assert np.max(np.abs(logP - Le)) < 2e-4 * max(1.0, np.max(np.abs(Le)))
+        got[name] = (O, U)
+    assert rel_fro(got["tc"][0], got["simt"][0]) <= 1e-5
+    assert rel_fro(got["tc"][1], got["simt"][1]) <= 1e-5
 
 
 @pytest.mark.parametrize("sizes,shape,dtype,dk,dv,max_depth", [
@@ -390,14 +419,15 @@ def test_value_tiled_round_matches_serial_and_one_tile_commit(cfg):
     assert max(state_unit_errors(db2.S.cpu().numpy(), S_new).values()) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("cfg,extra", [(1, 0), (2, 0), (3, 0), (2, "vt"), (3, "vk")])
+@pytest.mark.parametrize("cfg,extra", [(1, 0), (2, 0), (3, 0), (2, "vt"), (3, "vk"), (2, "f32")])
 def test_inline_topology_round_matches_pack_round(cfg, extra):
     """BOLE_FLAG_INLINE_TOPOLOGY: the verification forms each node's ancestor
     mask and depth from the parent links itself (no bole_pack_forest); the
     round's O, U, log P and committed state are bit-identical to the round
-    with pack, on both small-tree kernels and the [dv, dk] slot layout."""
+    with pack, on both small-tree kernels (bf16 and fp32 q/k/v) and the
+    [dv, dk] slot layout."""
     from gated_deltanet_verification_gb300 import bole, device
-    b = I.config_batch(cfg)
+    b = I.config_batch(cfg, dtype="f32" if extra == "f32" else None)
     f = bole.FLAG_VALUE_TILES if extra == "vt" else 0
     db1, db2 = device.to_device(b), device.to_device(b)
     if extra == "vk":
