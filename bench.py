@@ -497,7 +497,7 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
     verify_kernels = (["tc_vtile_kernel"] if vtile else ["tc_verify_kernel"] if fused
                       else ["tc_big_fused_kernel"] if big else [])
-    commit_kernels = ["tc_commit_kernel"] if tc_shape else []
+    commit_kernels = ["tc_commit_kernel"] if tc_dims else []
     traffic = (recorded_traffic(verify_kernels if dominant == "verify" else commit_kernels,
                                 workload_key(cfg, args.shape, batch.dtype)) if tc_used else None)
     roofline = {"bound": "hbm", "kernel": dominant,

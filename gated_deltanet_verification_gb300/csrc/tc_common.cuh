@@ -69,6 +69,15 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
     }
 }
 
+// x rounded to the nearest tf32 (10 explicit mantissa bits; ties away from
+// zero) by integer arithmetic on its IEEE-754 bits, so that a tf32 operand
+// holds exactly this value whatever rounding the tensor core applies.
+// Finite inputs below the largest float.
+__device__ __forceinline__ float tf32_round(float x)
+{
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");

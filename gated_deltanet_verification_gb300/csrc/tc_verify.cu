@@ -46,6 +46,7 @@
 // stores S in place (Eq. (10)).
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -851,23 +852,31 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 // U_a^T of that half).  VK ([dv][dk], the slot layout): rows are d_v (A =
 // U_a^T), columns a d_k half (B^T = (D_a K_a)^T of that half) -- the same
 // product, transposed.
+// Precision: bf16 keys are exact in tf32 and U_a is rounded to tf32.  fp32
+// keys (the 1e-5 bound): both operands are written as tf32 hi + lo (rounded
+// to nearest here, so the hardware reads them exactly) and each chunk keeps
+// lo hi + hi lo + hi hi (the dropped lo lo term is ~2^-22 relative).
 constexpr int kCommitThreads = 128;
 constexpr int kChunk = 16;                    // path nodes per MMA K chunk
 constexpr int kBatch = 8;                     // path nodes whose operands are read at once
 constexpr int kTile = 64;                     // state columns per CTA
-constexpr int kCommitCTAs = 7;                // per SM (7 x 64 tensor memory columns)
-constexpr int CO_S = 0;                       // one box of the half: [128 rows x 128 B] = 16 KB
-constexpr int CO_A = 16384;                   // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
-constexpr int CO_B = CO_A + 8192;             // U_a^T chunk: 64 rows x 16 tf32
-constexpr int CO_PATH = CO_B + 4096;          // int[128]
-constexpr int CO_BAR = CO_PATH + 512;         // 3 mbarriers
-constexpr int CO_TSLOT = CO_BAR + 24;
-constexpr int CO_MISC = CO_TSLOT + 4;         // path length, flag, status copy
-constexpr int CO_PAR = CO_MISC + 16;          // int[128]: the request's parent links
-constexpr int COMMIT_SMEM = CO_PAR + 512 + 1024;
-static_assert(kCommitCTAs * (COMMIT_SMEM + 1024) <= 228 * 1024, "seven commit CTAs per SM");
-static_assert((kCommitCTAs + 1) * (COMMIT_SMEM + 1024) > 228 * 1024,
-              "never eight (8 x 64 tensor memory columns would still fit, but keep the margin)");
+template <bool F32> struct CoPlan {
+    static constexpr int S = 0;               // one box of the half: [128 rows x 128 B] = 16 KB
+    static constexpr int A = 16384;           // (D_a K_a)^T chunk: 128 rows x 16 tf32 (64 B rows)
+    static constexpr int B = A + 8192;        // U_a^T chunk: 64 rows x 16 tf32
+    static constexpr int AL = B + 4096;       // fp32: the tf32 low parts of A and B
+    static constexpr int BL = AL + 8192;
+    static constexpr int PATH = F32 ? BL + 4096 : AL; // int[128]
+    static constexpr int BAR = PATH + 512;    // 3 mbarriers
+    static constexpr int TSLOT = BAR + 24;
+    static constexpr int MISC = TSLOT + 4;    // path length, flag, status copy
+    static constexpr int PAR = MISC + 16;     // int[128]: the request's parent links
+    static constexpr int SMEM = PAR + 512 + 1024;
+    static constexpr int CTAS = F32 ? 5 : 7;  // per SM (x 64 tensor memory columns)
+    static_assert(CTAS * (SMEM + 1024) <= 228 * 1024, "commit CTAs per SM");
+    static_assert((CTAS + 1) * (SMEM + 1024) > 228 * 1024,
+                  "never more (the tensor memory columns would still fit; keep the margin)");
+};
 
 constexpr uint32_t IDESC_COMMIT = idesc_tf32(128, kTile, false, false);
 
@@ -886,25 +895,29 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo)
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
-template <bool VK>
-__global__ void __launch_bounds__(kCommitThreads, kCommitCTAs)
-tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *__restrict__ k,
+template <bool VK, bool F32>
+__global__ void __launch_bounds__(kCommitThreads, CoPlan<F32>::CTAS)
+tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict__ kptr,
                  const float *__restrict__ U, const float *__restrict__ logP,
                  const int32_t *__restrict__ offsets, const int32_t *__restrict__ parent,
                  const int32_t *__restrict__ accepted, int H, int N, int64_t k_ls, int64_t u_ls,
                  int64_t lp_ls, int32_t *st)
 {
+    using P = CoPlan<F32>;
+    using KT = typename std::conditional<F32, float, __nv_bfloat16>::type;
+    const KT *k = static_cast<const KT *>(kptr);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    uint8_t *sS = sm + CO_S;
-    uint8_t *sA = sm + CO_A;
-    uint8_t *sB = sm + CO_B;
-    int *path = reinterpret_cast<int *>(sm + CO_PATH);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CO_BAR); // tma, mma, drain
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CO_TSLOT);
-    int *plen = reinterpret_cast<int *>(sm + CO_MISC);
+    uint8_t *sS = sm + P::S;
+    uint8_t *sA = sm + P::A;
+    uint8_t *sB = sm + P::B;
+    uint8_t *sAL = sm + P::AL, *sBL = sm + P::BL; // fp32 only
+    int *path = reinterpret_cast<int *>(sm + P::PATH);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P::BAR); // tma, mma, drain
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P::TSLOT);
+    int *plen = reinterpret_cast<int *>(sm + P::MISC);
     int *flag = plen + 1;
-    int *spar = reinterpret_cast<int *>(sm + CO_PAR);
+    int *spar = reinterpret_cast<int *>(sm + P::PAR);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int unit = blockIdx.x, hv = blockIdx.y; // head unit, column half
@@ -1000,10 +1013,9 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                 lp[tt] = on ? logP[nh] : 0.f;
                 if (VK) {
                     av_[tt] = on ? U[nh * kD + tid] : 0.f;
-                    bv_[tt] = (on && tid < kTile)
-                                  ? __bfloat162float(k[nh * kD + kTile * hv + tid]) : 0.f;
+                    bv_[tt] = (on && tid < kTile) ? to_f32(k[nh * kD + kTile * hv + tid]) : 0.f;
                 } else {
-                    av_[tt] = on ? __bfloat162float(k[nh * kD + tid]) : 0.f;
+                    av_[tt] = on ? to_f32(k[nh * kD + tid]) : 0.f;
                     bv_[tt] = (on && tid < kTile) ? U[nh * kD + kTile * hv + tid] : 0.f;
                 }
             }
@@ -1027,8 +1039,21 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                     const int tt = 4 * c4 + e;
                     av[e] = VK ? av_[tt] : coef[tt] * av_[tt];
                 }
-                *reinterpret_cast<float4 *>(sA + sw64_offset(tid, t0 + 4 * c4)) =
-                    make_float4(av[0], av[1], av[2], av[3]);
+                if constexpr (F32) {
+                    float hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hi[e] = tf32_round(av[e]);
+                        lo[e] = tf32_round(av[e] - hi[e]);
+                    }
+                    *reinterpret_cast<float4 *>(sA + sw64_offset(tid, t0 + 4 * c4)) =
+                        make_float4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<float4 *>(sAL + sw64_offset(tid, t0 + 4 * c4)) =
+                        make_float4(lo[0], lo[1], lo[2], lo[3]);
+                } else {
+                    *reinterpret_cast<float4 *>(sA + sw64_offset(tid, t0 + 4 * c4)) =
+                        make_float4(av[0], av[1], av[2], av[3]);
+                }
             }
             // B^T[c][t] (row c = tid < 64), K-major, 64-byte rows
             if (tid < kTile) {
@@ -1040,8 +1065,21 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                         const int tt = 4 * t4 + e;
                         bv[e] = VK ? coef[tt] * bv_[tt] : bv_[tt];
                     }
-                    *reinterpret_cast<float4 *>(sB + sw64_offset(tid, t0 + 4 * t4)) =
-                        make_float4(bv[0], bv[1], bv[2], bv[3]);
+                    if constexpr (F32) {
+                        float hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            hi[e] = tf32_round(bv[e]);
+                            lo[e] = tf32_round(bv[e] - hi[e]);
+                        }
+                        *reinterpret_cast<float4 *>(sB + sw64_offset(tid, t0 + 4 * t4)) =
+                            make_float4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<float4 *>(sBL + sw64_offset(tid, t0 + 4 * t4)) =
+                            make_float4(lo[0], lo[1], lo[2], lo[3]);
+                    } else {
+                        *reinterpret_cast<float4 *>(sB + sw64_offset(tid, t0 + 4 * t4)) =
+                            make_float4(bv[0], bv[1], bv[2], bv[3]);
+                    }
                 }
             }
             if (t0 + kBatch >= tn && t0 + kBatch < kChunk) { // the rest of the chunk is zero
@@ -1052,6 +1090,13 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
                     if (tid < kTile)
                         *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * c4)) =
                             make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (F32) {
+                        *reinterpret_cast<float4 *>(sAL + sw64_offset(tid, 4 * c4)) =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (tid < kTile)
+                            *reinterpret_cast<float4 *>(sBL + sw64_offset(tid, 4 * c4)) =
+                                make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
                 break;
             }
@@ -1061,10 +1106,21 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const __nv_bfloat16 *_
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
+            if constexpr (F32) {
+                const uint32_t sal = smem_addr(sAL), sbl = smem_addr(sBL);
 #pragma unroll
-            for (int kk = 0; kk < kChunk / 8; ++kk)
-                mma_tf32_ss(tmem, sdesc_sw64(sa + kk * 32, 512), sdesc_sw64(sb + kk * 32, 512),
-                            IDESC_COMMIT, (ch > 0 || kk > 0));
+                for (int t = 0; t < 3; ++t) // lo hi, hi lo, hi hi
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 8; ++kk)
+                        mma_tf32_ss(tmem, sdesc_sw64((t == 0 ? sal : sa) + kk * 32, 512),
+                                    sdesc_sw64((t == 1 ? sbl : sb) + kk * 32, 512), IDESC_COMMIT,
+                                    (ch > 0 || t > 0 || kk > 0));
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 8; ++kk)
+                    mma_tf32_ss(tmem, sdesc_sw64(sa + kk * 32, 512),
+                                sdesc_sw64(sb + kk * 32, 512), IDESC_COMMIT, (ch > 0 || kk > 0));
+            }
             mma_commit(&bar[1]);
         }
         if (!mbar_wait(&bar[1], ch & 1, kWaitNs)) {
@@ -1195,7 +1251,7 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
 
 bool tc_commit_supported(const CommitArgs &a)
 {
-    return a.dtype == BOLE_BF16 && a.dk == kD && a.dv == kD;
+    return (a.dtype == BOLE_BF16 || a.dtype == BOLE_F32) && a.dk == kD && a.dv == kD;
 }
 
 cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap)
@@ -1205,16 +1261,17 @@ cudaError_t launch_tc_commit(const CommitArgs &a, cudaStream_t s, bool overlap)
     CUtensorMap map;
     cudaError_t e = make_layered_state_map(&map, a.S, units, a.layers, a.s_ls);
     if (e != cudaSuccess) return e;
-    auto kernel = a.vk ? tc_commit_kernel<true> : tc_commit_kernel<false>;
-    e = configure_once(reinterpret_cast<const void *>(kernel), COMMIT_SMEM, false);
+    const bool f32 = a.dtype == BOLE_F32;
+    auto kernel = f32 ? (a.vk ? tc_commit_kernel<true, true> : tc_commit_kernel<false, true>)
+                      : (a.vk ? tc_commit_kernel<true, false> : tc_commit_kernel<false, false>);
+    const int smem = f32 ? CoPlan<true>::SMEM : CoPlan<false>::SMEM;
+    e = configure_once(reinterpret_cast<const void *>(kernel), smem, false);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(dim3(units, kD / kTile, a.layers),
-                                                 dim3(kCommitThreads), COMMIT_SMEM, s, overlap,
-                                                 attr);
-    return cudaLaunchKernelEx(&cfg, kernel, map, static_cast<const __nv_bfloat16 *>(a.k), a.U,
-                              a.logP, a.offsets, a.parent, a.accepted, a.H, a.N, a.k_ls, a.u_ls,
-                              a.lp_ls, a.st);
+                                                 dim3(kCommitThreads), smem, s, overlap, attr);
+    return cudaLaunchKernelEx(&cfg, kernel, map, a.k, a.U, a.logP, a.offsets, a.parent,
+                              a.accepted, a.H, a.N, a.k_ls, a.u_ls, a.lp_ls, a.st);
 }
 
 } // namespace bole

@@ -157,13 +157,6 @@ __device__ __forceinline__ void split3_bf16x8(const float *x, uint4 &c1, uint4 &
     c3 = make_uint4(w3[0], w3[1], w3[2], w3[3]);
 }
 
-// x rounded to the nearest tf32 (10 explicit mantissa bits; ties away from
-// zero), so that a tf32 operand holds exactly this value.
-__device__ __forceinline__ float tf32_round(float x)
-{
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
-}
-
 template <bool F32>
 __global__ void __launch_bounds__(kVTThreads, VtPlan<F32>::PER_SM)
 tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,

@@ -212,8 +212,14 @@ bole_status bole_pack_forest(const int32_t *offsets, const int32_t *parent, int 
  * max_depth <= 15 run the single-CTA TMA + tcgen05 kernel (state products on
  * a bf16 hi/lo split of S_pre -- the low part is itself rounded to bf16, so
  * each state element keeps a relative residue of about 2^-17 -- with exact
- * bf16 products and fp32 accumulation, every factor on chip); bf16 inputs with dk = dv = 128 and larger or deeper trees (up to 128
- * nodes, any depth) run one tcgen05 kernel per (request, head) that forms the
+ * bf16 products and fp32 accumulation, every factor on chip); fp32 inputs with
+ * dk = dv = 128, max_T <= 32 and max_depth <= 15 run the value-tiled tcgen05
+ * kernel (two CTAs per head) with every fp32 operand of the Gram and the state
+ * products written as three bf16 parts (24 significant bits) and the six
+ * products of order up to 2^-16 kept, the propagation as tf32 hi + lo (three
+ * products), fp32 accumulation -- within the float32 bound; bf16 inputs with
+ * dk = dv = 128 and larger or deeper trees (up to 128 nodes, any depth) run
+ * one tcgen05 kernel per (request, head) that forms the
  * factors [M; W] by log-depth doubling and keeps them in tensor memory for the
  * state products and the propagation (no workspace; when the caller passes
  * one of at least B * H * 256 * 128 * 4 bytes anyway, [M; W] is also written
@@ -263,9 +269,11 @@ bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const vo
  * written in place over S ([B,H,dk,dv] float32, which held S_pre during the
  * verification that produced U and logP).  accepted[b] = -1 leaves request b's
  * state untouched.  k is the same buffer verification read; U and logP are its
- * outputs.  bf16 k with dk = dv = 128 uses the TMA + tcgen05 kernel (one
- * tensor-core product per head over the accepted path); otherwise, or with
- * BOLE_FLAG_FORCE_SIMT, the FP32 CUDA-core kernel.  Must be stream-ordered after
+ * outputs.  dk = dv = 128 uses the TMA + tcgen05 kernel (one tensor-core
+ * product per 64-column half of each head's state over the accepted path, tf32
+ * operands; fp32 k writes both operands as tf32 hi + lo and keeps three
+ * products, for the float32 bound); otherwise, or with BOLE_FLAG_FORCE_SIMT,
+ * the FP32 CUDA-core kernel.  Must be stream-ordered after
  * the verification.  Device faults (accepted[b] >= tree size) go to dev_status. */
 bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
                         const float *logP, const int32_t *offsets, const int32_t *parent,

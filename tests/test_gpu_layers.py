@@ -74,6 +74,8 @@ CASES = [
     ("cfg1-simt", lambda: I.config_batch(1), 1),
     ("f32-simt", lambda: I.random_batch(seed=79, B=4, H=2, dk=32, dv=48, sizes=[9, 17, 1, 30],
                                         max_depth=9, dtype="f32", sigma=0.1), 0),
+    ("f32-tc", lambda: I.random_batch(seed=83, B=4, H=3, dk=128, dv=128, sizes=[32, 9, 1, 30],
+                                      max_depth=12, dtype="f32", sigma=0.1), 0),
 ]
 
 
@@ -121,6 +123,8 @@ LAYER_CASES = [
     ("cfg2-simt", lambda: I.config_batch(2), 1, 2),
     ("f32-simt", lambda: I.random_batch(seed=82, B=4, H=2, dk=32, dv=48, sizes=[9, 17, 1, 30],
                                         max_depth=9, dtype="f32", sigma=0.1), 0, 3),
+    ("f32-tc", lambda: I.random_batch(seed=84, B=4, H=3, dk=128, dv=128, sizes=[32, 9, 1, 30],
+                                      max_depth=12, dtype="f32", sigma=0.1), 0, 3),
 ]
 
 

@@ -112,18 +112,22 @@ def test_fp32_tensor_core_kernel_matches_oracle_and_cuda_core(sizes, H, max_dept
     (FLAG_FORCE_SIMT) on the same forest."""
     from gated_deltanet_verification_gb300 import bole
     b = I.random_batch(seed=sum(sizes) + 11 * H, B=len(sizes), H=H, dk=128, dv=128, sizes=sizes,
-                       max_depth=max_depth, dtype="f32", sigma=sigma, shape=shape)
+                       max_depth=max_depth, dtype="f32", sigma=sigma, shape=shape,
+                       accept="uniform")
     Oe, Ue, Le = oracle.verify(b)
+    Se = oracle.commit(b)
     got = {}
     for name, flags in (("tc", 0), ("simt", bole.FLAG_FORCE_SIMT)):
-        O, U, logP = _verify_flags(b, flags, max_T=32)
+        O, U, logP, S_new = _verify_flags(b, flags, max_T=32, commit=True)
         assert rel_fro(O, Oe) <= TOL["f32"] and rel_fro(U, Ue) <= TOL["f32"], name
         assert_local_parity(f"{b.name}/{name}", "O", O, Oe, b.offsets, TOL["f32"])
         assert_local_parity(f"{b.name}/{name}", "U", U, Ue, b.offsets, TOL["f32"])
         assert np.max(np.abs(logP - Le)) < 2e-4 * max(1.0, np.max(np.abs(Le)))
-        got[name] = (O, U)
-    assert rel_fro(got["tc"][0], got["simt"][0]) <= 1e-5
-    assert rel_fro(got["tc"][1], got["simt"][1]) <= 1e-5
+        # commit (fp32 keys: tf32 hi + lo operands on the tensor-core path)
+        assert max(state_unit_errors(S_new, Se).values()) <= TOL["f32"], name
+        got[name] = (O, U, S_new)
+    for t in range(3):
+        assert rel_fro(got["tc"][t], got["simt"][t]) <= 1e-5
 
 
 @pytest.mark.parametrize("sizes,shape,dtype,dk,dv,max_depth", [
@@ -353,7 +357,7 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     _check(b, _run(b), TOL["bf16"])
 
 
-def _verify_flags(b, flags, max_T=None):
+def _verify_flags(b, flags, max_T=None, commit=False):
     from gated_deltanet_verification_gb300 import bole, device
     db = device.to_device(b)
     if max_T is not None:
@@ -361,10 +365,13 @@ def _verify_flags(b, flags, max_T=None):
     rb = device.alloc_round(db, flags)
     device.pack(db, rb)
     device.verify(db, rb, flags)
+    if commit:
+        device.commit(db, rb, flags)
     torch.cuda.synchronize()
     bole.check_status(rb.status)
-    return (rb.O.float().cpu().numpy().astype(np.float64), rb.U.cpu().numpy().astype(np.float64),
-            rb.logP.cpu().numpy().astype(np.float64))
+    out = (rb.O.float().cpu().numpy().astype(np.float64), rb.U.cpu().numpy().astype(np.float64),
+           rb.logP.cpu().numpy().astype(np.float64))
+    return out + (db.S.cpu().numpy().astype(np.float64),) if commit else out
 
 
 @pytest.mark.parametrize("sizes,H,max_depth,shape", [
