@@ -23,7 +23,7 @@
 //      go straight to the registers of the threads that form R^T.
 //   2. Warp 0: cumulative decay L_i along the ancestor-or-self mask (Lemma 1),
 //      the decay ratios exp(L_i - L_j) of each node's ancestors.
-//   3. tcgen05 Gram [Q;K] K^T (bf16 products, fp32 accumulation); warps 0, 1
+//   3. tcgen05 Gram [Q;K] K^T (bf16 products, fp32 accumulation); warps 0, 5
 //      stage its rows in shared memory; warp 0 gathers the compact
 //        C_ij = exp(L_i - L_j) q_i.k_j          (j an ancestor of i, or i)
 //        G_ij = beta_i exp(L_i - L_j) k_i.k_j   (j a strict ancestor of i)
@@ -493,10 +493,12 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
         if constexpr (F32) {
             if (warp >= 1 && warp <= 4) {
                 // [Q;K] -> three bf16 copies: thread (row r, d_k half hf)
-                // reads its 64 floats from fp32 atoms 2 hf, 2 hf + 1, and
-                // once all 128 threads hold theirs, writes 64 bf16 of row r
-                // into atom hf of each copy.
-                const int t = tid - 32, r = t & 63, hf = t >> 6;
+                // reads its 64 floats from fp32 atoms 2 hf, 2 hf + 1 and
+                // writes 64 bf16 of row r into atom hf of each copy.  Row r's
+                // outputs overwrite only row r's inputs, and both halves of a
+                // row sit in one warp (adjacent lanes), so a warp-level sync
+                // orders the reads before the writes.
+                const int t = tid - 32, r = t >> 1, hf = t & 1;
                 ok &= waitb(VB_QK);
                 float x[64];
 #pragma unroll
@@ -510,7 +512,7 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                     x[32 + 4 * c + 0] = a1.x; x[32 + 4 * c + 1] = a1.y;
                     x[32 + 4 * c + 2] = a1.z; x[32 + 4 * c + 3] = a1.w;
                 }
-                asm volatile("bar.sync 2, 128;" ::: "memory");
+                __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 c1, c2, c3;
@@ -523,12 +525,14 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
                 mbar_arrive(&bar[VB_QKS]);
             }
         }
-        if (warp < 2) {
-            // stage the Gram rows: q.k (warp 0, lanes 0..31), k.k (warp 1)
+        if (warp == 0 || warp == 5) {
+            // stage the Gram rows: q.k (warp 0, lanes 0..31), k.k (warp 5,
+            // lanes 32..63 -- warp 1, which reaches the same lanes, is
+            // splitting the state tile meanwhile)
             ok &= waitb(VB_GRAM);
             tc_fence_after();
             __syncwarp();
-            const int r = warp * 32 + lane;
+            const int r = (warp == 0 ? 0 : 32) + lane;
             float4 *srow = reinterpret_cast<float4 *>(staged(r));
             float x[32];
             tmem_ld32(tmem + TM_GP + lane_base, x);
