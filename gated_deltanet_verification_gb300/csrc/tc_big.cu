@@ -79,7 +79,8 @@ constexpr int FU_L = 196608;            // L_i
 constexpr int FU_BETA = FU_L + 512;     // beta_i
 constexpr int FU_LG = FU_BETA + 512;    // log gamma_i
 constexpr int FU_MASK = FU_LG + 512;    // uint4 ancestor-or-self masks
-constexpr int FU_BAR = FU_MASK + 2048;  // [Q;K] TMA, MMA, S TMA, V TMA, drain
+constexpr int FU_JMP = FU_MASK + 2048;  // pointer-jumping links
+constexpr int FU_BAR = FU_JMP + 512;    // [Q;K] TMA, MMA, S TMA, V TMA, drain
 constexpr int FU_MISC = FU_BAR + 48;    // TMEM slot
 constexpr int FU_END = FU_MISC + 16;
 constexpr int FU_SMEM = FU_END + 1024;
@@ -104,6 +105,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     float *Bs = reinterpret_cast<float *>(sm + FU_BETA);
     float *LGs = reinterpret_cast<float *>(sm + FU_LG);
     uint4 *Ms = reinterpret_cast<uint4 *>(sm + FU_MASK);
+    int *Js = reinterpret_cast<int *>(sm + FU_JMP);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + FU_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FU_MISC);
 
@@ -133,9 +135,6 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             tma_load_3d(sQK + ka * 16384, &tmQ, &bar[0], 64 * ka, h, o);
             tma_load_3d(sQK + 32768 + ka * 16384, &tmK, &bar[0], 64 * ka, h, o);
         }
-        mbar_arrive_expect_tx(&bar[2], 65536); // the state, landing during the doubling
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tma_load_2d(sS + c * 16384, &tmS, &bar[2], 32 * c, unit * kD);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -158,27 +157,50 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+        // The state is requested once the per-node reads have returned
+        // (requested at entry, every CTA's 64 KB queued those reads behind a
+        // launch-wide burst); it lands while the factors are formed.
+        mbar_arrive_expect_tx(&bar[2], 65536);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_load_2d(sS + c * 16384, &tmS, &bar[2], 32 * c, unit * kD);
+    }
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     bool ok = true;
     uint32_t mph = 0; // MMA barrier phase
 
     // cumulative decay: L_i = sum of log gamma over the ancestors-or-self of i (Lemma 1)
+    // by pointer jumping over the parent links (the parent is the latest
+    // strict ancestor in the mask): after r rounds each node holds the sum
+    // over its 2^r nearest ancestors-or-self, so bits(d) rounds cover every
+    // path -- 7 rounds for a chain of 128 instead of 128 dependent steps
     if (tid < kTB) {
         const int i = tid;
         const uint4 mk = Ms[i];
-        const uint32_t w[4] = {mk.x, mk.y, mk.z, mk.w};
-        float L = 0.f;
+        uint32_t w[4] = {mk.x, mk.y, mk.z, mk.w};
+        w[i >> 5] &= ~(1u << (i & 31));
+        int par = -1;
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-            uint32_t bits = w[wi];
-            while (bits) {
-                const int j = wi * 32 + __ffs(bits) - 1;
-                L += LGs[j];
-                bits &= bits - 1;
-            }
-        }
+        for (int wi = 3; wi >= 0; --wi)
+            if (par < 0 && w[wi]) par = wi * 32 + 31 - __clz(w[wi]);
+        float L = LGs[i];
         Ls[i] = L;
+        Js[i] = par;
+        for (int span = 1; span <= d; span <<= 1) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            float Lp = 0.f;
+            int pp = -1;
+            if (par >= 0) {
+                Lp = Ls[par];
+                pp = Js[par];
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            L += Lp;
+            par = pp;
+            Ls[i] = L;
+            Js[i] = par;
+        }
         if (i < T) logP[(size_t)(o + i) * H + h] = L;
     }
 
