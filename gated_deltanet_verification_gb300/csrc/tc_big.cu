@@ -10,10 +10,11 @@
 //        (I+G)^{-1} = sum_{m<=d} (-G)^m = (I - G)(I + G^2)(I + G^4)...(I + G^(2^K)),
 //      2^(K+1) > d, i.e. K = floor(log2 d) squarings (the pages' d-step
 //      recurrence, Eq. (8), regrouped; a chain of 128 takes 6 levels instead
-//      of 127 steps).  Each level squares P = G^(2^(k-1)) and multiplies W and
-//      M by (I + P); every product is one 128 x 128 x 128 tcgen05 kind::tf32
-//      MMA with A read from tensor memory and B (the transposed P) from
-//      shared memory.  S_pre streams in meanwhile.
+//      of 127 steps).  Each level squares P = G^(2^(k-1)) and multiplies W by
+//      (I + P); M = C W is formed once W is final.  Every product is one
+//      128 x 128 x 128 tcgen05 kind::tf32 MMA with A read from tensor memory
+//      and B (the transposed right factor) from shared memory.  S_pre
+//      streams in meanwhile.
 //   2. solve: S_pre split exactly into bf16 S_hi + S_lo, the state products
 //      Q S_pre and K S_pre on tcgen05, R = D_beta (V - D_P K S_pre) as R^T in
 //      shared memory, and the propagation with M and W read from tensor
@@ -69,9 +70,10 @@ __device__ __forceinline__ uint32_t kmaj_offset(int n, int k)
 //     after the last doubling product, the value rows (two boxes).
 //   SB (64 KB): S_pre, split in place into bf16 hi/lo; after the state
 //     products R^T (tf32 K-major, four 32-node atoms).
-// Tensor memory (512 columns): R0 = C, then M; R1 = G and powers, then
-// P Q S_pre and finally O; R2 = W; R3 = products and powers, then K S_pre,
-// then U.
+// Tensor memory (512 columns): R0 = C; R1 = G and powers; R2 = W; R3 =
+// products and powers.  Depth 0: M = C stays in R0, R1 takes P Q S_pre and
+// then O, R3 K S_pre and then U.  Depth > 0: M = C W goes to R1, R0 takes
+// P Q S_pre and then O, R3 K S_pre and then U.
 constexpr int FU_QK = 0;
 constexpr int FU_PB = 65536;
 constexpr int FU_SB = 131072;
@@ -314,12 +316,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             tmem_st32(dst + lane_base + j0, x);
         }
     };
-    // M0 = C - C G (G = 0 exactly when every tree of the request has depth 0:
-    // M = C, W = I); levels: P <- P^2, W <- W + W P, M <- M + M P
-    if (d > 0) {
-        product(R3, R0);
-        accumulate(R0, R3, -1.f);
-    }
+    // W0 = I - G (G = 0 exactly when every tree of the request has depth 0:
+    // W = I, M = C); levels: P <- P^2, W <- W + W P
     int K = 0;
     while ((2 << K) <= d) ++K; // K = floor(log2 d) for d >= 1, 0 otherwise
     uint32_t Pp = R1, Pq = R3;
@@ -340,15 +338,34 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         }
         product(Pp, R2); // W P
         accumulate(R2, Pp, 1.f);
-        product(Pp, R0); // M P
-        accumulate(R0, Pp, 1.f);
         const uint32_t tmp = Pp;
         Pp = Pq;
         Pq = tmp;
     }
+    uint32_t regM = R0, regQS = R1, regKS = R3; // depth 0: M = C
+    if (d > 0) {
+        // M = C W: the transposed W into the B buffer (its last reader, the
+        // final W P product, has completed), then one product into R1
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            const int j0 = hf * 64 + cc * 32;
+            float x[32];
+            tmem_ld32(R2 + lane_base + j0, x);
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                *reinterpret_cast<float *>(sPB + kmaj_offset(j0 + t, m)) = x[t];
+        }
+        product(R1, R0);
+        regM = R1;
+        regQS = R0;
+    }
     tmem_wait_st();
     tc_fence_before();
-    go = __syncthreads_and(ok); // M (R0) and W (R2) final; the PB buffer is free
+    go = __syncthreads_and(ok); // M and W (R2) final; the PB buffer is free
     tc_fence_after();
     if (go) v_issued = true;
     if (tid == 0 && go) { // the value rows into the freed PB buffer
@@ -363,7 +380,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int cc = 0; cc < 2; ++cc) {
             const int j0 = hf * 64 + cc * 32;
             float x[32];
-            tmem_ld32(R0 + lane_base + j0, x);
+            tmem_ld32(regM + lane_base + j0, x);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 reinterpret_cast<float4 *>(rowM + j0)[c4] =
@@ -408,7 +425,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     fence_proxy_async_smem();
     tc_fence_before();
     go = __syncthreads_and(ok);
-    // state products: Q S_pre -> R1, K S_pre -> R3 (S = S_hi + S_lo)
+    // state products: Q S_pre -> regQS, K S_pre -> regKS (S = S_hi + S_lo)
     const uint32_t s0 = smem_addr(sS);
     if (tid == 0 && go) {
         // this CTA's inputs have landed: the CTA one wave later (pf_stride =
@@ -438,10 +455,10 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             const uint64_t bl = sdesc_sw128(slo + boff, lbo, 1024);
             const uint64_t aq = sdesc_sw128(qa + off, 16, 1024);
             const uint64_t ak = sdesc_sw128(ka + off, 16, 1024);
-            mma_bf16_ss(R1, aq, bh, idesc_s, kk > 0);
-            mma_bf16_ss(R1, aq, bl, idesc_s, 1);
-            mma_bf16_ss(R3, ak, bh, idesc_s, kk > 0);
-            mma_bf16_ss(R3, ak, bl, idesc_s, 1);
+            mma_bf16_ss(regQS, aq, bh, idesc_s, kk > 0);
+            mma_bf16_ss(regQS, aq, bl, idesc_s, 1);
+            mma_bf16_ss(regKS, ak, bh, idesc_s, kk > 0);
+            mma_bf16_ss(regKS, ak, bl, idesc_s, 1);
         }
         mma_commit(&bar[1]);
     }
@@ -463,7 +480,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int cc = 0; cc < 2; ++cc) {
             const int col0 = hf * 64 + cc * 32;
             float x[32];
-            tmem_ld32(R3 + lane_base + col0, x);
+            tmem_ld32(regKS + lane_base + col0, x);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float f[8];
@@ -476,24 +493,25 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
                     *reinterpret_cast<float *>(sS + (i >> 5) * 16384 + sw128_offset(n, i & 31)) = r;
                 }
             }
-            tmem_ld32(R1 + lane_base + col0, x);
+            tmem_ld32(regQS + lane_base + col0, x);
 #pragma unroll
             for (int t = 0; t < 32; ++t) x[t] *= p;
-            tmem_st32(R1 + lane_base + col0, x);
+            tmem_st32(regQS + lane_base + col0, x);
         }
     }
     tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();
     go = __syncthreads_and(ok);
-    // propagation + read-out over the tree's node steps: R1 += M R (O), R3 = W R (U)
+    // propagation + read-out over the tree's node steps: regQS += M R (O),
+    // regKS = W R (U)
     if (tid == 0 && go) {
         tc_fence_after();
         const int nk = (T + 7) / 8;
         for (int kk = 0; kk < nk; ++kk) {
             const uint64_t bd = sdesc_sw128(s0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            mma_tf32_ts(R1, R0 + 8 * kk, bd, IDESC_T128, 1);
-            mma_tf32_ts(R3, R2 + 8 * kk, bd, IDESC_T128, kk > 0);
+            mma_tf32_ts(regQS, regM + 8 * kk, bd, IDESC_T128, 1);
+            mma_tf32_ts(regKS, R2 + 8 * kk, bd, IDESC_T128, kk > 0);
         }
         mma_commit(&bar[1]);
     }
@@ -514,8 +532,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int cc = 0; cc < 2; ++cc) {
             const int col0 = hf * 64 + cc * 32;
             float x[32], y[32];
-            tmem_ld32_async(R1 + lane_base + col0, x);
-            tmem_ld32_async(R3 + lane_base + col0, y);
+            tmem_ld32_async(regQS + lane_base + col0, x);
+            tmem_ld32_async(regKS + lane_base + col0, y);
             tmem_wait_ld32(x);
             tmem_wait_ld32(y);
             uint4 *dsto = reinterpret_cast<uint4 *>(sQK + i * kORow + col0 * 2);
