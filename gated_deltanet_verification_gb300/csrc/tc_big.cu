@@ -82,7 +82,8 @@ constexpr int FU_BETA = FU_L + 512;     // beta_i
 constexpr int FU_LG = FU_BETA + 512;    // log gamma_i
 constexpr int FU_MASK = FU_LG + 512;    // uint4 ancestor-or-self masks
 constexpr int FU_JMP = FU_MASK + 2048;  // pointer-jumping links
-constexpr int FU_BAR = FU_JMP + 512;    // [Q;K] TMA, MMA, S TMA, V TMA, drain
+constexpr int FU_CD = FU_JMP + 512;     // depth 0: the diagonal of C
+constexpr int FU_BAR = FU_CD + 512;     // [Q;K] TMA, MMA, S TMA, V TMA, drain
 constexpr int FU_MISC = FU_BAR + 48;    // TMEM slot
 constexpr int FU_END = FU_MISC + 16;
 constexpr int FU_SMEM = FU_END + 1024;
@@ -108,6 +109,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     float *LGs = reinterpret_cast<float *>(sm + FU_LG);
     uint4 *Ms = reinterpret_cast<uint4 *>(sm + FU_MASK);
     int *Js = reinterpret_cast<int *>(sm + FU_JMP);
+    float *Cd = reinterpret_cast<float *>(sm + FU_CD);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + FU_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FU_MISC);
 
@@ -128,6 +130,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         if (tid == 0 && h == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, -1, T);
         return;
     }
+    bool v_issued = false; // thread 0: the value rows were requested
     if (tid == 0) {
         for (int k = 0; k < 5; ++k) mbar_init(&bar[k], 1); // 4: drain after a timeout
         fence_mbar_init();
@@ -136,6 +139,12 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int ka = 0; ka < 2; ++ka) {
             tma_load_3d(sQK + ka * 16384, &tmQ, &bar[0], 64 * ka, h, o);
             tma_load_3d(sQK + 32768 + ka * 16384, &tmK, &bar[0], 64 * ka, h, o);
+        }
+        if (d == 0) { // no factor phase uses the PB buffer: the value rows come now
+            v_issued = true;
+            mbar_arrive_expect_tx(&bar[3], 32768);
+            tma_load_3d(sPB, &tmV, &bar[3], 0, h, o);
+            tma_load_3d(sPB + 16384, &tmV, &bar[3], 64, h, o);
         }
     }
     if (warp == 0) {
@@ -211,27 +220,49 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     // bounded wait has given up (`go` false after a barrier), nothing more is
     // issued and nobody waits for a product.
     const uint32_t qa = smem_addr(sQK), ka = qa + 32768;
-    bool v_issued = false;
-    if (tid == 0) {
-        ok &= mbar_wait(&bar[0], 0, kWaitNs);
-    }
-    if (tid == 0 && ok) {
+    if (tid == 0 || (d == 0 && tid < kTB)) ok &= mbar_wait(&bar[0], 0, kWaitNs);
+    if (tid == 0 && ok && d > 0) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
             const uint64_t kb = sdesc_sw128(ka + off, 16, 1024);
             mma_bf16_ss(R0, sdesc_sw128(qa + off, 16, 1024), kb, IDESC_G128, kk > 0);
-            if (d > 0) // K K^T feeds only G, which is zero at depth 0
-                mma_bf16_ss(R1, sdesc_sw128(ka + off, 16, 1024), kb, IDESC_G128, kk > 0);
+            mma_bf16_ss(R1, sdesc_sw128(ka + off, 16, 1024), kb, IDESC_G128, kk > 0);
         }
         mma_commit(&bar[1]);
     }
-    bool go = __syncthreads_and(ok); // L visible
-    if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
-    mph ^= 1u;
-    tc_fence_after();
-    __syncwarp();
+    if (d == 0 && tid < kTB && ok) {
+        // Depth 0: every node's only ancestor-or-self is itself, so C is the
+        // diagonal c_i = q_i . k_i (exp(L_i - L_i) = 1), G = 0 and W = I.  The
+        // diagonal is formed here on the CUDA cores (exact bf16 products, fp32
+        // sums), and the propagation below reduces to O = P Q S_pre + c R,
+        // U = R: no Gram, no factor in tensor memory, no propagation product.
+        const int i = tid;
+        float c = 0.f;
+        if (i < T) {
+#pragma unroll
+            for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float fq[8], fk[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                      sQK + kb2 * 16384 + sw128_chunk(i, ch)), fq);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                      sQK + 32768 + kb2 * 16384 + sw128_chunk(i, ch)), fk);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) c = fmaf(fq[t], fk[t], c);
+                }
+        }
+        Cd[i] = c;
+    }
+    bool go = __syncthreads_and(ok); // L (and at depth 0 the diagonal) visible
+    if (d > 0) {
+        if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
+        mph ^= 1u;
+        tc_fence_after();
+        __syncwarp();
+    }
 
     // Dense C (R0, in place), G (R1, in place), W0 = I - G (R2) and G^T as the
     // B operand of the doubling.
@@ -239,24 +270,6 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         const uint4 mk = Ms[m];
         const uint32_t w[4] = {mk.x, mk.y, mk.z, mk.w};
         const float Lm = Ls[m], bm = Bs[m];
-#pragma unroll 1
-        for (int cc = 0; cc < 2 && d == 0; ++cc) {
-            // every tree of the request has depth 0: G = 0 exactly, so W = I
-            // and only C is formed (no G, no transposed power for the doubling)
-            const int j0 = hf * 64 + cc * 32;
-            const uint32_t bits = w[j0 >> 5];
-            float x[32];
-            tmem_ld32(R0 + lane_base + j0, x);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                const bool anc = (bits >> t) & 1u;
-                x[t] = anc ? __expf(Lm - Ls[j0 + t]) * x[t] : 0.f;
-            }
-            tmem_st32(R0 + lane_base + j0, x);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) x[t] = (j0 + t) == m ? 1.f : 0.f;
-            tmem_st32(R2 + lane_base + j0, x);
-        }
 #pragma unroll 1
         for (int cc = 0; cc < 2 && d > 0; ++cc) {
             const int j0 = hf * 64 + cc * 32;
@@ -367,8 +380,8 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     tc_fence_before();
     go = __syncthreads_and(ok); // M and W (R2) final; the PB buffer is free
     tc_fence_after();
-    if (go) v_issued = true;
-    if (tid == 0 && go) { // the value rows into the freed PB buffer
+    if (tid == 0 && go && d > 0) { // the value rows into the freed PB buffer
+        v_issued = true;
         mbar_arrive_expect_tx(&bar[3], 32768);
         tma_load_3d(sPB, &tmV, &bar[3], 0, h, o);
         tma_load_3d(sPB + 16384, &tmV, &bar[3], 64, h, o);
@@ -380,12 +393,22 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int cc = 0; cc < 2; ++cc) {
             const int j0 = hf * 64 + cc * 32;
             float x[32];
-            tmem_ld32(regM + lane_base + j0, x);
+            if (d > 0) {
+                tmem_ld32(regM + lane_base + j0, x);
+            } else { // depth 0: M = diag(c)
+#pragma unroll
+                for (int t = 0; t < 32; ++t) x[t] = (j0 + t) == m ? Cd[m] : 0.f;
+            }
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 reinterpret_cast<float4 *>(rowM + j0)[c4] =
                     make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
-            tmem_ld32(R2 + lane_base + j0, x);
+            if (d > 0) {
+                tmem_ld32(R2 + lane_base + j0, x);
+            } else { // W = I
+#pragma unroll
+                for (int t = 0; t < 32; ++t) x[t] = (j0 + t) == m ? 1.f : 0.f;
+            }
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 reinterpret_cast<float4 *>(rowW + j0)[c4] =
@@ -469,9 +492,62 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     mph ^= 1u;
     tc_fence_after();
     __syncwarp();
+    // Outputs are staged in shared memory freed by then -- O (bf16) in the
+    // [Q;K] buffer, rows padded by 16 B; U (fp32) in the state buffer, rows of
+    // 512 B whose 16-byte chunks are XOR-swizzled by row, so that the
+    // row-per-thread writes are conflict-free -- and the CTA stores them row
+    // segment by row segment (row-per-thread global stores touched 32 cache
+    // lines per instruction).
+    constexpr int kORow = kD * 2 + 16, kURow = kD * 4; // staged rows
+    static_assert(kTB * kORow <= 65536 && kTB * kURow <= 65536, "staged outputs fit");
+    auto stage_row = [&](int i, int col0, const float (&ov)[32], const float (&uv)[32]) {
+        uint4 *dsto = reinterpret_cast<uint4 *>(sQK + i * kORow + col0 * 2);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            __nv_bfloat162 p2[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                p2[t] = __floats2bfloat162_rn(ov[8 * q4 + 2 * t], ov[8 * q4 + 2 * t + 1]);
+            dsto[q4] = *reinterpret_cast<uint4 *>(p2);
+        }
+        uint8_t *urow = sS + i * kURow;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4 *>(urow + ((((col0 >> 2) + q4) ^ (i & 31)) << 4)) =
+                make_float4(uv[4 * q4], uv[4 * q4 + 1], uv[4 * q4 + 2], uv[4 * q4 + 3]);
+    };
     // R^T = (beta (v - P K S_pre))^T over the dead state buffer, and P Q S_pre
-    // in place, so that the propagation accumulates O onto it
-    {
+    // in place, so that the propagation accumulates O onto it.  Depth 0: the
+    // outputs themselves, O = P Q S_pre + c R and U = R, staged directly.
+    if (d == 0) {
+        const int i = m;
+        const bool live = i < T;
+        const float p = live ? expf(Ls[i]) : 0.f, bt = Bs[i], c = Cd[i];
+        const uint8_t *vrow = sPB + hf * 16384 + i * 128; // columns 64 hf .. 64 hf + 63
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            const int col0 = hf * 64 + cc * 32;
+            float x[32], y[32];
+            tmem_ld32_async(regKS + lane_base + col0, x);
+            tmem_ld32_async(regQS + lane_base + col0, y);
+            tmem_wait_ld32(x);
+            tmem_wait_ld32(y);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                                  vrow + (((cc * 4 + q4) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int e = 8 * q4 + t;
+                    const float r = live ? bt * (f[t] - p * x[e]) : 0.f;
+                    x[e] = r;                        // U = R
+                    y[e] = fmaf(p, y[e], c * r);     // O = P Q S_pre + c R
+                }
+            }
+            stage_row(i, col0, y, x);
+        }
+    } else {
         const int i = m;
         const bool live = i < T;
         const float p = live ? expf(Ls[i]) : 0.f, bt = Bs[i];
@@ -504,29 +580,25 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
     tc_fence_before();
     go = __syncthreads_and(ok);
     // propagation + read-out over the tree's node steps: regQS += M R (O),
-    // regKS = W R (U)
-    if (tid == 0 && go) {
-        tc_fence_after();
-        const int nk = (T + 7) / 8;
-        for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t bd = sdesc_sw128(s0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            mma_tf32_ts(regQS, regM + 8 * kk, bd, IDESC_T128, 1);
-            mma_tf32_ts(regKS, R2 + 8 * kk, bd, IDESC_T128, kk > 0);
+    // regKS = W R (U); depth 0 has none
+    if (d > 0) {
+        if (tid == 0 && go) {
+            tc_fence_after();
+            const int nk = (T + 7) / 8;
+            for (int kk = 0; kk < nk; ++kk) {
+                const uint64_t bd =
+                    sdesc_sw128(s0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                mma_tf32_ts(regQS, regM + 8 * kk, bd, IDESC_T128, 1);
+                mma_tf32_ts(regKS, R2 + 8 * kk, bd, IDESC_T128, kk > 0);
+            }
+            mma_commit(&bar[1]);
         }
-        mma_commit(&bar[1]);
-    }
-    if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
-    mph ^= 1u;
-    tc_fence_after();
-    __syncwarp();
-    // Outputs: each thread puts its 64 columns of row i of O (bf16) and U
-    // (fp32) into shared memory freed by now ([Q;K] for O, the power and state
-    // buffers for U; rows padded by 16 B so the row-per-thread writes are
-    // conflict-free), and the CTA stores them row segment by row segment:
-    // row-per-thread global stores touched 32 cache lines per instruction.
-    constexpr int kORow = kD * 2 + 16, kURow = kD * 4 + 16; // padded staged rows
-    static_assert(kTB * kORow <= 65536 && kTB * kURow <= 131072, "staged outputs fit");
-    {
+        if (go) ok &= mbar_wait(&bar[1], mph, kWaitNs);
+        mph ^= 1u;
+        tc_fence_after();
+        __syncwarp();
+        // each thread stages its 64 columns of row i of O and U (the
+        // propagation has read the state buffer's R^T by now)
         const int i = m;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
@@ -536,19 +608,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             tmem_ld32_async(regKS + lane_base + col0, y);
             tmem_wait_ld32(x);
             tmem_wait_ld32(y);
-            uint4 *dsto = reinterpret_cast<uint4 *>(sQK + i * kORow + col0 * 2);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                __nv_bfloat162 p2[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    p2[t] = __floats2bfloat162_rn(x[8 * q4 + 2 * t], x[8 * q4 + 2 * t + 1]);
-                dsto[q4] = *reinterpret_cast<uint4 *>(p2);
-            }
-            float4 *dstu = reinterpret_cast<float4 *>(sPB + i * kURow + col0 * 4);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                dstu[q4] = make_float4(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3]);
+            stage_row(i, col0, x, y);
         }
     }
     if (__syncthreads_and(go && ok)) {
@@ -562,7 +622,7 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
         for (int c = tid; c < T * 32; c += kFUThreads) {
             const int r = c >> 5, q4 = c & 31;
             *reinterpret_cast<float4 *>(Uout + ((size_t)(o + r) * H + h) * kD + q4 * 4) =
-                *reinterpret_cast<const float4 *>(sPB + r * kURow + q4 * 16);
+                *reinterpret_cast<const float4 *>(sS + r * kURow + ((q4 ^ (r & 31)) << 4));
         }
     }
     if (!ok) report(st, BOLE_ERR_TIMEOUT, b, -1, 23);
