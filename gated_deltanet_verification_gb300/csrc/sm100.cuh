@@ -112,6 +112,16 @@ __device__ __forceinline__ void bulk_wait_group_read0()
 }
 
 
+// Prefetch `bytes` (a multiple of 16; address 16-byte aligned) of global
+// memory into L2; nothing to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(gsrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

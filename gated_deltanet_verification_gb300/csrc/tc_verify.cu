@@ -990,6 +990,23 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
     }
     __syncthreads();
     const int L = *plen;
+    if (L > kBatch && *(volatile int *)flag == 0) {
+        // A path longer than one batch: every node's key and delta rows go
+        // to L2 now, so that the batches below, each a dependent round trip,
+        // meet L2 instead of DRAM.  A side: the row of 128 (key, or VK: U),
+        // B side: this CTA's 64-entry half (U, or VK: key).
+        constexpr uint32_t kRowK = kD * sizeof(KT), kHalfK = kTile * sizeof(KT);
+        for (int t = tid; t < L; t += kCommitThreads) {
+            const size_t nh = (size_t)(o + path[t]) * H + h;
+            if (VK) {
+                bulk_prefetch_l2(U + nh * kD, kD * 4);
+                bulk_prefetch_l2(k + nh * kD + kTile * hv, kHalfK);
+            } else {
+                bulk_prefetch_l2(k + nh * kD, kRowK);
+                bulk_prefetch_l2(U + nh * kD + kTile * hv, kTile * 4);
+            }
+        }
+    }
     const float La = logP[(size_t)(o + a) * H + h];
 
     const uint32_t sa = smem_addr(sA), sb = smem_addr(sB);
