@@ -51,6 +51,7 @@ if ROOT not in sys.path:
 METRIC = ("verified tree nodes/sec (GDN verify+commit, 1×GB300); "
           "achieved HBM GB/s vs peak")
 L2_BYTES = 129 * 1024 * 1024
+MAX_SETS = 64  # input copies at most; smaller workloads flush L2 before each step
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -375,7 +376,15 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         flags |= bole.FLAG_INLINE_TOPOLOGY
     alg = algorithmic(batch, inline)
     step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
-    n_sets = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
+    # L2 hygiene: rotate over enough input copies that > 3x L2 is touched
+    # between reuses; a workload too small for that (more than MAX_SETS
+    # copies) keeps two copies and writes a buffer of twice the L2 before
+    # every timed step instead, each step then timed on its own.
+    need = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
+    flush_mode = need > MAX_SETS
+    n_sets = 2 if flush_mode else need
+    flush_buf = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+                 if flush_mode else None)
 
     sets = []
     for _ in range(n_sets):
@@ -407,17 +416,24 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     for _, rb in sets:
         bole.check_status(rb.status, "warm-up")
 
-    # The steps are replayed from CUDA graphs (one per input copy), so the
-    # timed region measures the GPU work, not the Python and ctypes cost of
-    # issuing three launches (the end-to-end number below keeps that cost).
+    # The steps are replayed from CUDA graphs, so the timed region measures
+    # the GPU work, not the Python and ctypes cost of issuing the launches
+    # (the end-to-end number below keeps that cost): one graph holds a round
+    # on every input copy in turn (replayed while whole passes remain), one
+    # graph per copy serves the rest and the flushed steps.
     graphs = []
     for i in range(n_sets):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             device.run_round(*sets[i], flags, torch.cuda.current_stream())
         graphs.append(g)
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all):
+        for i in range(n_sets):
+            device.run_round(*sets[i], flags, torch.cuda.current_stream())
     for i in range(n_sets):
         graphs[i].replay()
+    g_all.replay()
     torch.cuda.synchronize()
     for _, rb in sets:
         bole.check_status(rb.status, "graph warm-up")
@@ -430,17 +446,29 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(steps):
-        graphs[(args.warmup + i) % n_sets].replay()
-    end.record(stream)
+    if flush_mode:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush_buf.fill_(float(i & 1))
+            evs[i][0].record(stream)
+            graphs[i % n_sets].replay()
+            evs[i][1].record(stream)
+    else:
+        start.record(stream)
+        for _ in range(steps // n_sets):
+            g_all.replay()
+        for i in range(steps % n_sets):
+            graphs[i].replay()
+        end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clock_info = clocks.stop()
     for _, rb in sets:
         bole.check_status(rb.status, "timed steps")
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = (sum(a.elapsed_time(b) for a, b in evs) if flush_mode
+                  else start.elapsed_time(end))
 
     # ---- separate pass: per-kernel durations.  One graph per call kind runs
     #      that call once on every input copy, back to back and without launch
@@ -459,12 +487,24 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream()
-            for db, rb in sets:
+            for db, rb in (sets[:1] if flush_mode else sets):
                 call(db, rb, cs)
         g.replay()
+        torch.cuda.synchronize()
+        if flush_mode:  # one call per flushed replay, each timed on its own
+            reps = max(1, ks)
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(reps)]
+            for a, b in pairs:
+                flush_buf.fill_(0.0)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_kernel[name].append(sum(a.elapsed_time(b) for a, b in pairs) / reps)
+            continue
         reps = max(1, ks // n_sets)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(reps):
             g.replay()
@@ -533,11 +573,21 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
                                else "tcgen05 fused large-tree kernel" if big else "cuda-core"),
                    "round": ("verify (topology inside) -> commit" if inline
                              else "pack -> verify -> commit"),
-                   "l2": f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)",
-                   "launch": "CUDA graph replay, one graph per input copy",
-                   "kernel_timing": f"separate pass: per call kind, a graph of one call on each "
-                                    f"of the {n_sets} input copies, replayed "
-                                    f"{max(1, ks // n_sets)}x between events"},
+                   "l2": (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB "
+                          f"write outside the events; the inputs would need {need} copies)"
+                          if flush_mode else
+                          f"inputs rotate over {n_sets} copies (> 3x L2 between reuses)"),
+                   "launch": ("CUDA graph replay: one graph per step, each step between its "
+                              "own events" if flush_mode else
+                              f"CUDA graph replay: one graph of {n_sets} rounds (one per input "
+                              "copy), replayed while whole passes remain, then one graph per "
+                              "remaining round"),
+                   "kernel_timing": (f"separate pass: per call kind, one call per flushed "
+                                     f"replay, {max(1, ks)} replays each between events"
+                                     if flush_mode else
+                                     f"separate pass: per call kind, a graph of one call on each "
+                                     f"of the {n_sets} input copies, replayed "
+                                     f"{max(1, ks // n_sets)}x between events")},
         "roofline": roofline, "kernels": kern_rf, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clock_info,
     })
