@@ -465,17 +465,19 @@ def test_inline_topology_round_matches_pack_round(cfg, extra):
         _check(b, got, TOL["bf16"])
 
 
-@pytest.mark.parametrize("vt", [False, True])
+@pytest.mark.parametrize("vt", [False, True, "f32"])
 def test_inline_topology_faults_and_sticky_status(vt):
     """Faults found by the in-kernel topology step: a forward link is reported
     with its request, node and parent and that request's outputs stay
     unwritten (the commit then writes nothing); a tree deeper than max_depth
     is reported as a depth error; the status block is not cleared by the next
-    round, which writes nothing until the caller zeroes it."""
+    round, which writes nothing until the caller zeroes it.  On the one-CTA
+    kernel, the value tiles and the fp32 value tiles."""
     from gated_deltanet_verification_gb300 import bole, device
-    f = bole.FLAG_INLINE_TOPOLOGY | (bole.FLAG_VALUE_TILES if vt else 0)
+    f = bole.FLAG_INLINE_TOPOLOGY | (bole.FLAG_VALUE_TILES if vt is True else 0)
+    dtype = "f32" if vt == "f32" else "bf16"
     b = I.random_batch(seed=55, B=3, H=2, dk=128, dv=128, sizes=[12, 9, 20], max_depth=6,
-                       dtype="bf16", sigma=0.05, accept="uniform")
+                       dtype=dtype, sigma=0.05, accept="uniform")
     bad = b.parent.copy()
     bad[12 + 5] = 8  # node 5 of request 1 points forward
     db = device.to_device(b)
@@ -501,7 +503,7 @@ def test_inline_topology_faults_and_sticky_status(vt):
     torch.cuda.synchronize()
     bole.check_status(rb.status)
     S_new = oracle.commit(b)
-    assert max(state_unit_errors(db.S.cpu().numpy(), S_new).values()) <= TOL["bf16"]
+    assert max(state_unit_errors(db.S.cpu().numpy(), S_new).values()) <= TOL[dtype]
     # depth above the declared bound
     db2 = device.to_device(b)
     db2.max_depth = 2
