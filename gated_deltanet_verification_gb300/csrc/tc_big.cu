@@ -277,13 +277,23 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             float x[32], y[32];
             tmem_ld32_async(R0 + lane_base + j0, x); // both loads in flight at once
             tmem_ld32_async(R1 + lane_base + j0, y);
+            // the 32 decays of this chunk's columns, read before the loop: its
+            // stores into the power buffer could alias them as far as the
+            // compiler knows, which kept each read behind the previous store
+            float lj[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(Ls + j0 + 4 * c4);
+                lj[4 * c4] = l4.x; lj[4 * c4 + 1] = l4.y; lj[4 * c4 + 2] = l4.z;
+                lj[4 * c4 + 3] = l4.w;
+            }
             tmem_wait_ld32(x);
             tmem_wait_ld32(y);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 const int j = j0 + t;
                 const bool anc = (bits >> t) & 1u;
-                const float r = anc ? __expf(Lm - Ls[j]) : 0.f;
+                const float r = anc ? __expf(Lm - lj[t]) : 0.f;
                 x[t] = r * x[t];                               // C
                 y[t] = (anc && j != m) ? bm * r * y[t] : 0.f;  // G
                 *reinterpret_cast<float *>(sPB + kmaj_offset(j, m)) = y[t]; // G^T
@@ -557,11 +567,14 @@ tc_big_fused_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_consta
             const int col0 = hf * 64 + cc * 32;
             float x[32];
             tmem_ld32(regKS + lane_base + col0, x);
+            uint4 vv[4]; // read ahead of the scattered stores below, which could alias
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                vv[q4] = *reinterpret_cast<const uint4 *>(vrow + (((cc * 4 + q4) ^ (i & 7)) << 4));
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float f[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                  vrow + (((cc * 4 + q4) ^ (i & 7)) << 4)), f);
+                bf16x8_to_f32(vv[q4], f);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int n = col0 + 8 * q4 + t;

@@ -659,11 +659,15 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
                 tmem_ld32(tmem + lane_base + col0, x);
+                uint4 vv[4]; // read ahead of the scattered stores below, which could alias
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu)
+                    vv[uu] = *reinterpret_cast<const uint4 *>(vrow +
+                                                              (((cc * 4 + uu) ^ (i & 7)) << 4));
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     float f[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
+                    bf16x8_to_f32(vv[uu], f);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         const int c = 8 * uu + t;
@@ -743,11 +747,15 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 const int col0 = half * 64 + cc * 32;
                 float x[32];
                 tmem_ld32(tmem + lane_base + col0, x);
+                uint4 vv[4]; // read ahead of the scattered stores below, which could alias
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu)
+                    vv[uu] = *reinterpret_cast<const uint4 *>(vrow +
+                                                              (((cc * 4 + uu) ^ (i & 7)) << 4));
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     float f[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + (((cc * 4 + uu) ^ (i & 7)) << 4)), f);
+                    bf16x8_to_f32(vv[uu], f);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         const int c = 8 * uu + t;
@@ -1178,15 +1186,18 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
             if (*(volatile int *)flag == 0) {
                 float x[32];
                 tmem_ld32(tmem + lane_base + cb * 32, x);
+                float4 s4[8]; // the row read whole before any of it is written back
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    s4[c4] = *reinterpret_cast<const float4 *>(sS + sw128_offset(r, 4 * c4));
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
-                    float4 *p = reinterpret_cast<float4 *>(sS + sw128_offset(r, 4 * c4));
-                    float4 s4 = *p;
-                    s4.x = fmaf(Pa, s4.x, x[4 * c4 + 0]);
-                    s4.y = fmaf(Pa, s4.y, x[4 * c4 + 1]);
-                    s4.z = fmaf(Pa, s4.z, x[4 * c4 + 2]);
-                    s4.w = fmaf(Pa, s4.w, x[4 * c4 + 3]);
-                    *p = s4;
+                    float4 v = s4[c4];
+                    v.x = fmaf(Pa, v.x, x[4 * c4 + 0]);
+                    v.y = fmaf(Pa, v.y, x[4 * c4 + 1]);
+                    v.z = fmaf(Pa, v.z, x[4 * c4 + 2]);
+                    v.w = fmaf(Pa, v.w, x[4 * c4 + 3]);
+                    *reinterpret_cast<float4 *>(sS + sw128_offset(r, 4 * c4)) = v;
                 }
                 fence_proxy_async_smem();
             }

@@ -716,11 +716,15 @@ tc_vtile_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__
             } else {
                 uint8_t *dst = sS + 16384;
                 const uint8_t *vrow = sV + i * 128;
+                uint4 vv[4]; // read ahead of the scattered stores below, which could alias
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu)
+                    vv[uu] = *reinterpret_cast<const uint4 *>(
+                        vrow + ((((col0 >> 3) + uu) ^ (i & 7)) << 4));
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
                     float f[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                                      vrow + ((((col0 >> 3) + uu) ^ (i & 7)) << 4)), f);
+                    bf16x8_to_f32(vv[uu], f);
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
                         const int c = 8 * uu + t;
