@@ -918,18 +918,23 @@ def reference_arm(args, world, rank):
     thr = oracle.default_threads()
     units = batch.B * batch.H
     sizes = np.diff(batch.offsets)
+    prep = oracle.Prepared(batch, nthreads=thr)  # converted once, outside the timed steps
 
     def run(u0, u1):
-        oracle.verify(batch, nthreads=thr, unit_begin=u0, unit_end=u1)
-        oracle.commit(batch, nthreads=thr, unit_begin=u0, unit_end=u1)
+        prep.verify(u0, u1)
+        prep.commit(u0, u1)
         return int(sum(sizes[u // batch.H] for u in range(u0, u1)))
 
-    probe_units = min(units, max(1, 2 * thr))
+    probe_units = min(units, max(1, 4 * thr))
+    run(0, probe_units)  # first touch of the converted arrays
     t0 = time.perf_counter()
     run(0, probe_units)
     t_unit = (time.perf_counter() - t0) / probe_units
     budget_s = 60.0
-    per_step = int(max(1, min(units, budget_s / max(1, args.steps) / max(t_unit, 1e-9))))
+    # at least one unit per host thread per step (else the cores idle), at most
+    # the whole batch, else what keeps the timed steps near the budget
+    per_step = int(max(min(units, thr),
+                       min(units, budget_s / max(1, args.steps) / max(t_unit, 1e-9))))
     for w in range(max(0, min(args.warmup, 2))):
         run(0, per_step)
     node_heads, u0 = 0, 0

@@ -131,6 +131,46 @@ def verify(batch, nthreads: Optional[int] = None, unit_begin: int = 0, unit_end:
     return O, U, logP
 
 
+class Prepared:
+    """A batch converted once (float64 copies, output arrays allocated once)
+    for repeated calls over ranges of (request, head) units: the same C
+    routines and arguments as verify() and commit(), without re-marshalling
+    the whole batch on every call.  The benchmark's reference arm times the
+    oracle this way; outputs are overwritten by each call."""
+
+    def __init__(self, batch, nthreads: Optional[int] = None, lib=None):
+        self.lib = lib or load()
+        b = self.b = batch
+        self.nthreads = int(nthreads or default_threads())
+        self.offsets, self.parent = _i32(b.offsets), _i32(b.parent)
+        self.acc = _i32(b.accepted)
+        self.S, self.q, self.k, self.v = _f64(b.S_pre), _f64(b.q), _f64(b.k), _f64(b.v)
+        self.g, self.bt = _f64(b.gamma), _f64(b.beta)
+        self.O = np.zeros((b.N, b.H, b.dv))
+        self.U = np.zeros((b.N, b.H, b.dv))
+        self.logP = np.zeros((b.N, b.H))
+        self.S_new = np.zeros((b.B, b.H, b.dk, b.dv))
+
+    def verify(self, unit_begin: int, unit_end: int) -> None:
+        b = self.b
+        st = self.lib.oracle_verify(b.B, b.H, b.dk, b.dv, _ptr(self.offsets), _ptr(self.parent),
+                                    _ptr(self.S), _ptr(self.q), _ptr(self.k), _ptr(self.v),
+                                    _ptr(self.g), _ptr(self.bt), _ptr(self.O), _ptr(self.U),
+                                    _ptr(self.logP), int(unit_begin), int(unit_end),
+                                    self.nthreads)
+        if st != OK:
+            raise ValueError(f"oracle_verify status {st}")
+
+    def commit(self, unit_begin: int, unit_end: int) -> None:
+        b = self.b
+        st = self.lib.oracle_commit(b.B, b.H, b.dk, b.dv, _ptr(self.offsets), _ptr(self.parent),
+                                    _ptr(self.acc), _ptr(self.S), _ptr(self.k), _ptr(self.v),
+                                    _ptr(self.g), _ptr(self.bt), _ptr(self.S_new),
+                                    int(unit_begin), int(unit_end), self.nthreads)
+        if st != OK:
+            raise ValueError(f"oracle_commit status {st}")
+
+
 def commit(batch, accepted=None, nthreads: Optional[int] = None, unit_begin: int = 0,
            unit_end: int = -1, lib=None):
     """Committed state [B,H,dk,dv] float64 after replaying each accepted path
