@@ -94,7 +94,8 @@ def test_fp32_inputs_parity(cfg):
     """Same workloads with full-precision float32 q/k/v (the tensor-core
     value-tiled kernel, three-way bf16 operand split): float32 tolerance."""
     b = I.config_batch(cfg, dtype="f32")
-    _check(b, _run(b, dtype=torch.float32), TOL["f32"])
+    errs = _check(b, _run(b, dtype=torch.float32), TOL["f32"])
+    print(b.name, "f32", {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 @pytest.mark.parametrize("sizes,H,max_depth,shape,sigma", [
