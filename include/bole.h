@@ -123,7 +123,10 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
  * one wave of the one-CTA kernel (two CTAs per SM), where the extra CTAs
  * add parallelism; larger batches run one CTA per head, which moves more
  * state bytes per resident CTA.  These flags force either kernel (same
- * results up to rounding order); they are ignored elsewhere. */
+ * results up to rounding order); they are ignored elsewhere.  fp32 trees in
+ * the same envelope run the value-tiled kernel's fp32 form by default (no
+ * one-CTA fp32 kernel exists: with BOLE_FLAG_ONE_TILE_PER_HEAD they run the
+ * FP32 CUDA-core kernels). */
 #define BOLE_FLAG_ONE_TILE_PER_HEAD 0x8u
 #define BOLE_FLAG_VALUE_TILES 0x10u
 /* bole_tree_verify only: the round's topology step runs inside the
