@@ -236,18 +236,20 @@ def test_overlapped_round_matches_serial_launches():
     _check(b, got, 1e-2)
 
 
-@pytest.mark.parametrize("seed,sizes,depth", [(31, [100, 70], 40), (32, [128], 127), (33, [48], 20)])
+@pytest.mark.parametrize("seed,sizes,depth", [(31, [100, 70], 40), (32, [128], 127), (33, [48], 20),
+                                              (34, [80, 128], 0)])
 def test_large_tree_factors_match_dense_inverse(seed, sizes, depth):
     """The large-tree kernel keeps [M; W] = [C (I+G)^{-1}; (I+G)^{-1}] in tensor
     memory and needs no workspace; given one of B H 256 128 floats it also
-    writes [M; W] there.  Compare with a library dense inverse of the same G
+    writes [M; W] there (depth 0, the stars: M = diag(q_i . k_i), W = I,
+    formed on the CUDA cores).  Compare with a library dense inverse of the same G
     and C (Lemma 3: the log-depth product of (I + G^(2^k)) equals the finite
     Neumann sum), and O, U with the oracle."""
     from gated_deltanet_verification_gb300 import bole, device
     import pins_lib
+    shape = "chain" if depth >= 100 else "star" if depth == 0 else "random"
     b = I.random_batch(seed=seed, B=len(sizes), H=2, dk=128, dv=128, sizes=sizes,
-                       max_depth=depth, dtype="bf16", sigma=0.05, shape="chain" if depth >= 100
-                       else "random")
+                       max_depth=max(depth, 1), dtype="bf16", sigma=0.05, shape=shape)
     db = device.to_device(b)
     rb = device.alloc_round(db)
     assert bole.workspace_size(b.B, b.H, 128, 128, b.max_T, b.max_depth, db.q.dtype, 0) == 0
