@@ -278,8 +278,15 @@ conv_gates_kernel(const __grid_constant__ CUtensorMap tmXqk, const __grid_consta
                 if (d >= W) break;
                 float xv[8];
                 Vec8<T>::unpack(Vec8<T>::load(rows + (size_t)window[i][d] * n + c0), xv);
+                // channel pairs as packed fp32 FMAs (each lane rounded as fmaf)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = fmaf(wr[d][e], xv[e], y[e]);
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 acc = __ffma2_rn(make_float2(wr[d][e], wr[d][e + 1]),
+                                                  make_float2(xv[e], xv[e + 1]),
+                                                  make_float2(y[e], y[e + 1]));
+                    y[e] = acc.x;
+                    y[e + 1] = acc.y;
+                }
             }
             // bf16 outputs: the one-op form; float32 outputs: the accurate one
 #pragma unroll
@@ -293,7 +300,11 @@ conv_gates_kernel(const __grid_constant__ CUtensorMap tmXqk, const __grid_consta
             for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float r = rsqrtf(ss);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] *= r;
+            for (int e = 0; e < 8; e += 2) {
+                const float2 yr = __fmul2_rn(make_float2(y[e], y[e + 1]), make_float2(r, r));
+                y[e] = yr.x;
+                y[e + 1] = yr.y;
+            }
         }
         if (live) Vec8<T>::store(out + ((size_t)(o + i) * H + h) * n + c0, y);
     }
