@@ -946,6 +946,15 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
         prefetch_tensormap(&tmS);
         tma_prefetch_l2_3d(&tmS, kTile * hv, unit * kD, layer);
     }
+    // Tensor memory at entry: the SM starts the next CTA of the kernel once
+    // this one has given up its allocation permit, so all seven CTAs of an SM
+    // start together and, in a launch overlapping the verification, begin
+    // their state prefetch during its last wave (config 2 step 35.2 -> 33.5 us;
+    // allocating after the first round trip staggered them by one each).
+    if (warp == 0) {
+        tmem_alloc(tslot, 64);
+        tmem_relinquish();
+    }
     // Everything the verification (or the sampler) wrote -- U, log P, the
     // accepted node, the status -- is read after the wait.  The status word,
     // the accepted node and the request's extent come in one round trip;
@@ -957,14 +966,6 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
     const int o = offsets[b], T = offsets[b + 1] - o;
     const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
     const bool work = a >= 0 && !bad;
-    // Tensor memory after this first round trip: the SM starts the next CTA
-    // once this one has given up its allocation permit, and staggering the
-    // seven CTAs of an SM by a round trip measured faster than starting them
-    // together.
-    if (warp == 0) {
-        tmem_alloc(tslot, 64);
-        tmem_relinquish();
-    }
     // stage the request's parent links (coalesced), then walk the accepted path
     if (work)
         for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
