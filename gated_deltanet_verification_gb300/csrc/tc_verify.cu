@@ -955,20 +955,24 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
         tmem_alloc(tslot, 64);
         tmem_relinquish();
     }
-    // Everything the verification (or the sampler) wrote -- U, log P, the
-    // accepted node, the status -- is read after the wait.  The status word,
-    // the accepted node and the request's extent come in one round trip;
-    // uniform early exit (the status is read by one thread).
+    // The request's extent and its parent links are caller inputs that no
+    // call of the round writes: read before the wait, so that a launch
+    // overlapping the verification has them during its last wave.  What the
+    // verification (or the sampler) wrote -- U, log P, the accepted node, the
+    // status -- is read after it; the status word and the accepted node come
+    // in one round trip (uniform early exit: the status is read by one thread).
+    static_assert(kCommitThreads >= kMaxTree, "one parent link per thread");
+    const int o = offsets[b], T = offsets[b + 1] - o;
+    const bool ext_ok = T > 0 && T <= kMaxTree && o >= 0 && o + T <= N;
+    const int my_par = (ext_ok && tid < T) ? parent[o + tid] : -1;
     pdl_wait();
     int *sfault = plen + 2;
     if (tid == 0) *sfault = *(const volatile int32_t *)st;
     const int a = accepted[b];
-    const int o = offsets[b], T = offsets[b + 1] - o;
-    const bool bad = a >= 0 && (a >= T || o < 0 || o + T > N || T > kMaxTree);
+    const bool bad = a >= 0 && (a >= T || !ext_ok);
     const bool work = a >= 0 && !bad;
-    // stage the request's parent links (coalesced), then walk the accepted path
-    if (work)
-        for (int i = tid; i < T; i += kCommitThreads) spar[i] = parent[o + i];
+    // stage the parent links, then walk the accepted path
+    if (work && tid < T) spar[tid] = my_par;
     if (tid == 32) *flag = 0;
     tc_fence_before();
     __syncthreads();

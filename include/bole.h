@@ -104,7 +104,7 @@ typedef enum bole_dtype { BOLE_F32 = 0, BOLE_BF16 = 1 } bole_dtype;
  * kernel that does not let its dependents start early.  The kernel may then
  * begin while that one drains: before waiting for it, it reads only
  * caller-owned inputs that none of these calls writes (S_pre / S, q, k, v,
- * gamma, beta, offsets); the status word and everything the previous call
+ * gamma, beta, offsets, parent); the status word and everything the previous call
  * produced are read after the wait.  Without the flag every launch starts
  * only after the previous kernel has ended. */
 #define BOLE_FLAG_OVERLAP_LAUNCH 0x2u
