@@ -77,6 +77,9 @@ def parse_args(argv=None):
                    help="the workload's q/k/v (and O) dtype: f32 draws the same values at full "
                         "float32 precision (tensor-core value tiles for trees of up to 32 "
                         "nodes; commit on the CUDA cores)")
+    p.add_argument("--no-fuse", action="store_true",
+                   help="run each round as verify -> commit even where the previous round's "
+                        "commit can be fused into the verification (bole_commit_verify)")
     p.add_argument("--pack-round", action="store_true",
                    help="run the round as pack -> verify -> commit even where the "
                         "verification can form the topology itself")
@@ -145,6 +148,7 @@ def algorithmic(batch, inline_topology=False):
 # source file of each tensor-core kernel (a recorded DRAM figure is only
 # reported while that file is unchanged)
 KERNEL_SOURCES = {"tc_verify_kernel": "tc_verify.cu", "tc_commit_kernel": "tc_verify.cu",
+                  "tc_commit_verify": "tc_verify.cu",
                   "tc_big_fused_kernel": "tc_big.cu", "tc_vtile_kernel": "tc_vtile.cu"}
 
 
@@ -373,11 +377,19 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     probe_db = device.to_device(batch, device=dev)
     # the topology step inside the verification where the kernels allow it
     inline = (not args.pack_round) and device.inline_topology_supported(probe_db, flags)
+    # the previous round's commit fused into each verification (one state read
+    # per round instead of two), where bole_commit_verify applies
+    fz = (inline and not args.no_fuse and not args.value_tiles
+          and device.commit_verify_supported(probe_db, flags))
     del probe_db
     if inline:
         flags |= bole.FLAG_INLINE_TOPOLOGY
     alg = algorithmic(batch, inline)
-    step_bytes = alg["pack"] + alg["verify"] + alg["commit"]
+    # fused: the verification's and the commit's bytes less one read of the state
+    alg["commit_verify"] = (alg["verify"] + alg["commit"]
+                            - batch.B * batch.H * batch.dk * batch.dv * 4)
+    step_bytes = (alg["commit_verify"] if fz
+                  else alg["pack"] + alg["verify"] + alg["commit"])
     # L2 hygiene: rotate over enough input copies that > 3x L2 is touched
     # between reuses; a workload too small for that (more than MAX_SETS
     # copies) keeps two copies and writes a buffer of twice the L2 before
@@ -407,13 +419,26 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     tc_used = fused or big or vtile
     # pack (unless the verification forms the topology), verify (one tensor-core
     # kernel, or the CUDA-core producer + solve), commit
-    launches_per_step = (0 if inline else 1) + (1 if tc_used else 2) + 1
+    launches_per_step = 1 if fz else (0 if inline else 1) + (1 if tc_used else 2) + 1
+    # Step j of a period: input copy j % n_sets; with the fused round the copies
+    # alternate their U / logP pair, parity (j // n_sets) % 2, so a period is
+    # two passes over the copies and every copy is back at parity 0 after it.
+    period = 2 * n_sets if fz else n_sets
 
-    def step(i):
-        device.run_round(*sets[i % n_sets], flags, stream)
+    def one_round(j, cs):
+        db, rb = sets[j % n_sets]
+        if fz:
+            device.commit_verify_round(db, rb, (j // n_sets) % 2, cs)
+        else:
+            device.run_round(db, rb, flags, cs)
 
-    for i in range(args.warmup):
-        step(i)
+    if fz:  # the first round of each copy: a plain verification (its factors
+        for db, rb in sets:  # are what the first fused round commits)
+            device.alloc_alt(db, rb)
+            device.verify(db, rb, flags, stream)
+    warm = -(-args.warmup // period) * period if fz else args.warmup
+    for i in range(warm):
+        one_round(i, stream)
     torch.cuda.synchronize()
     for _, rb in sets:
         bole.check_status(rb.status, "warm-up")
@@ -424,17 +449,17 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     # on every input copy in turn (replayed while whole passes remain), one
     # graph per copy serves the rest and the flushed steps.
     graphs = []
-    for i in range(n_sets):
+    for j in range(period):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            device.run_round(*sets[i], flags, torch.cuda.current_stream())
+            one_round(j, torch.cuda.current_stream())
         graphs.append(g)
     g_all = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_all):
-        for i in range(n_sets):
-            device.run_round(*sets[i], flags, torch.cuda.current_stream())
-    for i in range(n_sets):
-        graphs[i].replay()
+        for j in range(period):
+            one_round(j, torch.cuda.current_stream())
+    for j in range(period):
+        graphs[j].replay()
     g_all.replay()
     torch.cuda.synchronize()
     for _, rb in sets:
@@ -454,15 +479,17 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         for i in range(steps):
             flush_buf.fill_(float(i & 1))
             evs[i][0].record(stream)
-            graphs[i % n_sets].replay()
+            graphs[i % period].replay()
             evs[i][1].record(stream)
     else:
         start.record(stream)
-        for _ in range(steps // n_sets):
+        for _ in range(steps // period):
             g_all.replay()
-        for i in range(steps % n_sets):
-            graphs[i].replay()
+        for j in range(steps % period):
+            graphs[j].replay()
         end.record(stream)
+    for j in range(steps % period, period if steps % period else 0):
+        graphs[j].replay()  # untimed: every copy back at parity 0
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -478,6 +505,28 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     #      each replay ----
     ks = max(1, min(args.kernel_steps, steps))
     per_kernel = {"pack": [], "verify": [], "commit": []}
+    if fz:  # the fused kernel: whole periods (both parities on every copy)
+        per_kernel["commit_verify"] = []
+        if flush_mode:
+            reps = -(-max(1, ks) // period) * period
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(reps)]
+            for r, (a, b) in enumerate(pairs):
+                flush_buf.fill_(0.0)
+                a.record(stream)
+                graphs[r % period].replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_kernel["commit_verify"].append(sum(a.elapsed_time(b) for a, b in pairs) / reps)
+        else:
+            reps = max(1, ks // period)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g_all.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            per_kernel["commit_verify"].append(e0.elapsed_time(e1) / (reps * period))
     cflags = flags & ~bole.FLAG_INLINE_TOPOLOGY
     calls = {"pack": lambda db, rb, cs: device.pack(db, rb, cs),
              "verify": lambda db, rb, cs: device.verify(db, rb, flags, cs),
@@ -517,7 +566,7 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
         bole.check_status(rb.status, "per-kernel pass")
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
-    e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world)
+    e2e = None if args.no_e2e else run_e2e(args, batch, sets, flags, stream, world, fz)
     res = {"_batch": batch, "_flags": flags & ~bole.FLAG_INLINE_TOPOLOGY,
            "_launches": launches_per_step * steps}
     if rank != 0:
@@ -528,19 +577,20 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
     value = job_throughput(batch.N, steps, world, elapsed_ms)
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     kern_rf = {}
-    for k in ("pack", "verify", "commit"):
+    for k in ("pack", "verify", "commit") + (("commit_verify",) if fz else ()):
         if k == "pack" and inline:
             kern_rf[k] = {"ms": 0.0, "alg_bytes": 0, "note": "formed inside the verification"}
             continue
         gbs = alg[k] / (avg[k] * 1e-3) / 1e9 if avg[k] > 0 else 0.0
         kern_rf[k] = {"ms": round(avg[k], 5), "alg_bytes": int(alg[k]),
                       "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
-    dominant = max(("verify", "commit"), key=lambda k: avg[k])
+    dominant = "commit_verify" if fz else max(("verify", "commit"), key=lambda k: avg[k])
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
     verify_kernels = (["tc_vtile_kernel"] if vtile else ["tc_verify_kernel"] if fused
                       else ["tc_big_fused_kernel"] if big else [])
     commit_kernels = ["tc_commit_kernel"] if tc_dims else []
-    traffic = (recorded_traffic(verify_kernels if dominant == "verify" else commit_kernels,
+    traffic = (recorded_traffic(["tc_commit_verify"] if fz else
+                                verify_kernels if dominant == "verify" else commit_kernels,
                                 workload_key(cfg, args.shape, batch.dtype)) if tc_used else None)
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": kern_rf[dominant]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
@@ -570,10 +620,15 @@ def measure_config(args, cfg, world, rank, local_rank, dev, steps):
                    "config_index": cfg, "B": batch.B, "H": batch.H, "dk": batch.dk,
                    "dv": batch.dv, "nodes": batch.N, "max_depth": batch.max_depth,
                    "seed": seed,
-                   "kernels": ("tcgen05 value-tiled (two CTAs per head)" if vtile
+                   "kernels": ("tcgen05 (one CTA per head), the previous round's commit "
+                               "inside" if fz
+                               else "tcgen05 value-tiled (two CTAs per head)" if vtile
                                else "tcgen05 (one CTA per head)" if fused
                                else "tcgen05 fused large-tree kernel" if big else "cuda-core"),
-                   "round": ("verify (topology inside) -> commit" if inline
+                   "round": ("one launch: the previous round's commit, then this round's "
+                             "verify (topology inside) from the committed state "
+                             "(bole_commit_verify)" if fz
+                             else "verify (topology inside) -> commit" if inline
                              else "pack -> verify -> commit"),
                    "l2": (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB "
                           f"write outside the events; the inputs would need {need} copies)"
@@ -799,7 +854,7 @@ def run_layers(args, batch, flags, stream):
     return out
 
 
-def run_e2e(args, batch, sets, flags, stream, world):
+def run_e2e(args, batch, sets, flags, stream, world, fz=False):
     """Same metric through the public API with host buffers: per step the
     round's inputs (tree, q/k/v, gates, accepted) are copied from pinned host
     memory, the round runs, and O and the status word are copied back to
@@ -837,6 +892,15 @@ def run_e2e(args, batch, sets, flags, stream, world):
             view.copy_(getattr(db, n))
             setattr(db, n, view)
         packs.append(buf)
+    par = [0] * len(sets)  # fused rounds: each copy's U / logP parity
+
+    def round_(k, db, rb, cs):
+        if fz:
+            device.commit_verify_round(db, rb, par[k], cs)
+            par[k] ^= 1
+        else:
+            device.run_round(db, rb, flags, cs)
+
     O_host = torch.empty_like(rb0.O, device="cpu").pin_memory()
     st_host = torch.empty_like(rb0.status, device="cpu").pin_memory()
     h2d = total
@@ -859,7 +923,7 @@ def run_e2e(args, batch, sets, flags, stream, world):
     def plain(i):
         db, rb = sets[i % n_sets]
         packs[i % n_sets].copy_(host, non_blocking=True)
-        device.run_round(db, rb, flags, torch.cuda.current_stream())
+        round_(i % n_sets, db, rb, torch.cuda.current_stream())
         O_host.copy_(rb.O, non_blocking=True)
         st_host.copy_(rb.status, non_blocking=True)
 
@@ -883,7 +947,7 @@ def run_e2e(args, batch, sets, flags, stream, world):
             packs[k].copy_(host, non_blocking=True)
             ready[k].record(copy_stream)
         stream.wait_event(ready[k])
-        device.run_round(db, rb, flags, stream)
+        round_(k, db, rb, stream)
         O_host.copy_(rb.O, non_blocking=True)
         st_host.copy_(rb.status, non_blocking=True)
         free[k].record(stream)
@@ -899,7 +963,9 @@ def run_e2e(args, batch, sets, flags, stream, world):
             "ms_per_step": round(ms / args.steps, 5),
             "mode": "per step: one pinned-host -> device copy of the round's packed inputs on a "
                     "copy stream (overlapping the previous round), the round (" +
-                    ("verify with the topology step inside, commit" if flags & bole.FLAG_INLINE_TOPOLOGY
+                    ("the previous round's commit and this round's verify in one launch" if fz
+                     else "verify with the topology step inside, commit"
+                     if flags & bole.FLAG_INLINE_TOPOLOGY
                      else "pack, verify, commit") + "), O and status back to pinned host memory",
             "plain": {"value": round(job_throughput(batch.N, plain_steps, world, ms_plain), 1),
                       "ms_per_step": round(ms_plain / plain_steps, 5),

@@ -91,6 +91,9 @@ def lib() -> ctypes.CDLL:
             L.bole_commit_layers.argtypes = [P, I64, P, I64, I, P, I64, P, I64, P, P, P, I, I, I,
                                              I, I, I, P, U, P]
             L.bole_commit_layers.restype = I
+            L.bole_commit_verify.argtypes = [P, P, P, P, P, P, P, I, P, P, P, I, P, P, P, P, I, I,
+                                             I, I, I, I, I, P, P, P, P, U, P]
+            L.bole_commit_verify.restype = I
             L.bole_conv_gates.argtypes = [P, P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                           P, P, P, P, P, P, U, P]
             L.bole_conv_gates.restype = I
@@ -269,6 +272,35 @@ def commit(S, k, U, logP, offsets, parent, accepted, *, status=None, flags: int 
                              _ptr(offsets), _ptr(parent), _ptr(accepted), B, H, dk, dv, N,
                              _ptr(status), int(flags), _stream(stream)), "bole_commit")
     return S
+
+
+def commit_verify(S, k_prev, U_prev, logP_prev, offsets_prev, parent_prev, accepted_prev, q, k,
+                  v, gamma, beta, offsets, parent, max_T: int, max_depth: int, *, O=None, U=None,
+                  logP=None, status=None, flags: int = 0, stream=None):
+    """bole_commit_verify: the previous round's commit applied to S in place,
+    then this round's verification from the committed state (its topology
+    formed in the kernel).  Returns (O, U, logP); U and logP must be other
+    buffers than U_prev and logP_prev."""
+    B = offsets.numel() - 1
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    N_prev = k_prev.shape[0]
+    dev = q.device
+    code = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or k_prev.dtype != q.dtype:
+        raise TypeError("q, k, v and k_prev must share one dtype")
+    O = torch.empty((N, H, dv), dtype=q.dtype, device=dev) if O is None else O
+    U = torch.empty((N, H, dv), dtype=torch.float32, device=dev) if U is None else U
+    logP = torch.empty((N, H), dtype=torch.float32, device=dev) if logP is None else logP
+    if status is None:
+        status = new_status(dev)
+    _check(lib().bole_commit_verify(
+        _ptr(S), _ptr(k_prev), _ptr(U_prev), _ptr(logP_prev), _ptr(offsets_prev),
+        _ptr(parent_prev), _ptr(accepted_prev), N_prev, _ptr(q), _ptr(k), _ptr(v), code,
+        _ptr(gamma), _ptr(beta), _ptr(offsets), _ptr(parent), B, H, dk, dv, N, int(max_T),
+        int(max_depth), _ptr(O), _ptr(U), _ptr(logP), _ptr(status), int(flags), _stream(stream)),
+        "bole_commit_verify")
+    return O, U, logP
 
 
 MAX_CONV_WIDTH = 8

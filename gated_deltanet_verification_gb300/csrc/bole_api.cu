@@ -268,6 +268,57 @@ bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float
                               H, dk, dv, N, dev_status, flags, stream);
 }
 
+bole_status bole_commit_verify(float *S, const void *k_prev, const float *U_prev,
+                               const float *logP_prev, const int32_t *offsets_prev,
+                               const int32_t *parent_prev, const int32_t *accepted_prev,
+                               int N_prev, const void *q, const void *k, const void *v,
+                               bole_dtype qkv_dtype, const float *gamma, const float *beta,
+                               const int32_t *offsets, const int32_t *parent, int B, int H,
+                               int dk, int dv, int N, int max_T, int max_depth, void *O, float *U,
+                               float *logP, int32_t *dev_status, unsigned flags,
+                               bole_stream_t stream)
+{
+    if (B < 0 || N < 0 || N_prev < 0 || H < 1 || !valid_dim(dk) || !valid_dim(dv) ||
+        !valid_dtype(qkv_dtype))
+        return BOLE_ERR_INVALID_ARG;
+    if (max_T < 1 || max_T > BOLE_MAX_TREE_NODES || max_depth < 0 ||
+        max_depth > BOLE_MAX_TREE_NODES - 1)
+        return BOLE_ERR_INVALID_ARG;
+    if ((size_t)N > (size_t)B * max_T || (size_t)N_prev > (size_t)B * BOLE_MAX_TREE_NODES)
+        return BOLE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)BOLE_FLAG_OVERLAP_LAUNCH) return BOLE_ERR_INVALID_ARG;
+    if (!offsets || !offsets_prev || !accepted_prev || !dev_status || (B > 0 && !S))
+        return BOLE_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !gamma || !beta || !parent || !O || !U || !logP))
+        return BOLE_ERR_INVALID_ARG;
+    if (N_prev > 0 && (!k_prev || !U_prev || !logP_prev || !parent_prev))
+        return BOLE_ERR_INVALID_ARG;
+    // this round's outputs must not overwrite the previous round's factors
+    if (N > 0 && N_prev > 0 && (U == U_prev || logP == logP_prev)) return BOLE_ERR_INVALID_ARG;
+    const void *p16[] = {S, q, k, v, O, U, k_prev, U_prev, dev_status};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return BOLE_ERR_INVALID_ARG;
+    const void *p4[] = {gamma, beta, offsets, parent, logP, logP_prev, offsets_prev, parent_prev,
+                        accepted_prev};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return BOLE_ERR_INVALID_ARG;
+
+    VerifyArgs a = {};
+    a.S_pre = S; a.q = q; a.k = k; a.v = v; a.dtype = qkv_dtype;
+    a.gamma = gamma; a.beta = beta; a.offsets = offsets; a.parent = parent;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.N = N; a.max_T = max_T; a.max_depth = max_depth;
+    a.O = O; a.U = U; a.logP = logP; a.st = dev_status;
+    a.vk = false;
+    a.inline_topo = true;
+    if (!tc_commit_verify_supported(a)) return BOLE_ERR_UNSUPPORTED;
+    if (B == 0 || (N == 0 && N_prev == 0)) return BOLE_OK;
+    PrevArgs pr;
+    pr.k = k_prev; pr.U = U_prev; pr.logP = logP_prev;
+    pr.offsets = offsets_prev; pr.parent = parent_prev; pr.accepted = accepted_prev;
+    pr.N = N_prev;
+    return from_cuda(launch_tc_commit_verify(a, pr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t bole_select_workspace_size(int B)
 {
     if (B < 0 || B > BOLE_SELECT_MAX_REQUESTS) return 0;

@@ -126,6 +126,15 @@ cudaError_t launch_tc_vtile_verify(const VerifyArgs &a, cudaStream_t s, bool ove
 bool tc_verify_supported(const VerifyArgs &a);
 size_t tc_workspace_bytes(int B, int H, int max_T);
 cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap);
+// The previous round's commit inputs for the deferred commit (bole_commit_verify).
+struct PrevArgs {
+    const void *k;
+    const float *U, *logP;
+    const int32_t *offsets, *parent, *accepted;
+    int N;
+};
+bool tc_commit_verify_supported(const VerifyArgs &a);
+cudaError_t launch_tc_commit_verify(const VerifyArgs &a, const PrevArgs &p, cudaStream_t s);
 bool tc_big_supported(const VerifyArgs &a);
 size_t tc_big_workspace_bytes(int B, int H);
 cudaError_t launch_tc_big_verify(const VerifyArgs &a, cudaStream_t s);

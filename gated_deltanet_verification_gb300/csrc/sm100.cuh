@@ -111,6 +111,12 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 
 // Prefetch `bytes` (a multiple of 16; address 16-byte aligned) of global
 // memory into L2; nothing to wait for.
@@ -221,6 +227,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The 32-byte-swizzled form (layout 6): K-major rows of 32 B (8 tf32), 8-row
+// groups `sbo` apart; the 16-byte chunk index is XORed with (row / 4) % 2.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (0 or 1) of row `row` in a
+// 32B-swizzled K-major tile with 32-byte rows.
+__device__ __forceinline__ uint32_t sw32_chunk(int row, int chunk)
+{
+    return (uint32_t)row * 32u + ((((uint32_t)chunk) ^ (((uint32_t)row >> 2) & 1u)) << 4);
+}
+
 // Byte offset of element (row, col) of a 128B-swizzled tile whose rows are
 // 128 bytes (32 fp32): the 16-byte chunk index is XORed with row % 8.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int col_f32)
@@ -256,6 +277,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
                  : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive columns per thread (the same lane mapping), waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // The same load without its wait: several loads may be in flight, and

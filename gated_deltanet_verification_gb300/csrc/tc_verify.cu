@@ -115,12 +115,27 @@ static_assert(X_JUMP + kT * 4 <= OFF_X + X_BYTES, "factor scratch fits its regio
 static_assert(X_JMASK % 8 == 0, "aligned masks");
 constexpr int OFF_TOPO = OFF_BAR + 13 * 8;    // int [2]: first bad node, request depth
 static_assert(X_ANCAT % 16 == 0, "vector-aligned ancestor rows");
+// Deferred commit of the previous round (the FUSE kernels): its tree's parent
+// links, the accepted path (node first) and two words (path length, failure)
+// follow the mbarriers; the two operands of its product, (D_a K_a)^T and
+// U_a^T as 128 x 8 tf32 K-major tiles (32B-swizzled), use the compact-factor
+// scratch, which the gather writes only after that product has ended.
+constexpr int kFzMaxPath = 16;                // two K chunks of eight path nodes
+constexpr int OFF_FZ = VERIFY_END;            // int [128]
+constexpr int FZ_PATH = OFF_FZ + kMaxTree * 4; // int [16]
+constexpr int FZ_MISC = FZ_PATH + kFzMaxPath * 4; // int [2], then the mbarrier below
+constexpr int FZ_DONE = FZ_MISC + 8;          // one phase: the whole commit product has ended
+constexpr int FZ_DRAIN = FZ_MISC + 16;        // after a timeout: the product's issuer drains
+constexpr int VERIFY_END_FZ = FZ_MISC + 24;
+static_assert(FZ_DONE % 8 == 0, "aligned mbarrier");
+constexpr int FZ_A = X_G, FZ_B = X_G + 4096;
+static_assert(FZ_B + 4096 <= X_ANCAT && FZ_A % 256 == 0, "commit operands in the compact factors");
 // Two CTAs per SM leave 113 KB each (228 KB less 1 KB reserved per CTA); the
 // plan fills 112 KB and keeps 256 B of slack for the 1024 B alignment of the
 // dynamic base, which is aligned when the kernel has no static shared memory
 // (checked in the kernel).  A request at the 113 KB edge would drop to one CTA
 // per SM as soon as anything else claimed shared memory.
-constexpr int VERIFY_SMEM = VERIFY_END + 256;
+constexpr int VERIFY_SMEM = VERIFY_END_FZ + 256;
 static_assert(2 * (VERIFY_SMEM + 1024) <= 228 * 1024, "two verification CTAs per SM");
 static_assert(3 * VERIFY_SMEM > 228 * 1024,
               "at most two verification CTAs (2 x 256 TMEM columns) per SM");
@@ -141,6 +156,17 @@ constexpr uint32_t TM_GRAM = 128, TM_PROP = 128;                  // tensor-memo
 constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, BAR_STATE = 5,
               BAR_MMA2 = 6, BAR_TOPO = 7, BAR_STAGED = 8, BAR_CG = 9, BAR_CONV = 10, BAR_OPS = 11,
               BAR_DRAIN = 12;
+constexpr int BAR_FZ = 15; // deferred commit: a chunk's product done (slot 13 holds the
+                           // topology words)
+
+// The previous round's commit inputs for the deferred commit (FUSE): what
+// bole_commit would read, for the same B requests and H heads.
+struct PrevRound {
+    const __nv_bfloat16 *k;              // [N][H][128], the keys its verification read
+    const float *U, *logP;               // its outputs, [N][H][128] and [N][H]
+    const int32_t *offsets, *parent, *accepted;
+    int N;
+};
 
 // Verification kernel: one CTA per (request, head).  Warp 8 streams operands
 // and issues the tensor-core products.  Warps 0..7 share the rest:
@@ -162,7 +188,15 @@ constexpr int BAR_S = 0, BAR_A1 = 1, BAR_GRAM = 2, BAR_V = 3, BAR_STATE_A = 4, B
 // [Q;K] padding; warps 0 and 2 stage the Gram, warp 0 gathers and forms the
 // rows of W, warp 1 those of M (both before the state products end); warps
 // 2 and 6 form R^T; only the lanes of rows 0..31 and 64..95 carry outputs.
-template <bool VK, bool SMALL>
+// FUSE (deferred commit): before verifying, the CTA applies the previous
+// round's commit (Eq. (10)) to the state tile it has just loaded and stores
+// the committed state in place, so one state read serves both.  Warps 4..7
+// walk the previous accepted path during the prologue and stage the path
+// operands; the issuing thread runs the product (D_a K_a)^T U_a into tensor
+// memory columns 0..127 (free until the state products); the split warps add
+// P_a S_r to it row by row, store each 64-column half by TMA and split the
+// committed values.
+template <bool VK, bool SMALL, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -171,8 +205,10 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                  const int32_t *__restrict__ req_depth, int H, int N,
                  __nv_bfloat16 *__restrict__ O, float *__restrict__ Uout,
                  float *__restrict__ logP, int32_t *st, int pf_stride, int early_alloc,
-                 const int32_t *__restrict__ parent, int max_depth, int inline_topo)
+                 const int32_t *__restrict__ parent, int max_depth, int inline_topo,
+                 const PrevRound prev)
 {
+    static_assert(!(FUSE && VK), "the deferred commit supports the default state layout");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sbuf = sm + OFF_SBUF;
@@ -191,7 +227,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const int unit = blockIdx.x;
     const int b = unit / H, h = unit % H;
 
-    if (sm + VERIFY_END > smem_raw + VERIFY_SMEM) { // dynamic base too far from 1024 B
+    if (sm + VERIFY_END_FZ > smem_raw + VERIFY_SMEM) { // dynamic base too far from 1024 B
         if (tid == 0) report(st, BOLE_ERR_CUDA, b, -1, -1);
         return;
     }
@@ -222,6 +258,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
         mbar_init(&bar[BAR_DRAIN], 1);
+        if (FUSE) {
+            mbar_init(&bar[BAR_FZ], 1);
+            mbar_init(reinterpret_cast<uint64_t *>(sm + FZ_DONE), 1);
+            mbar_init(reinterpret_cast<uint64_t *>(sm + FZ_DRAIN), 1);
+        }
         fence_mbar_init();
         if (in_range) {
             // q rows 0.., k rows 64.. of each K-atom (boxes of kTmax rows)
@@ -336,6 +377,23 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             atomicMax(&stopo[1], my_depth);
         }
     }
+    // FUSE, warps 4..7 (row r): the previous round's accepted node, tree
+    // extent and parent link r, requested in the prologue (the walk along them
+    // runs after the prologue, so it never holds up the CTA's topology step).
+    int fz_o = 0, fz_ap = -1, fz_Tp = 0, fz_par = -1;
+    bool fz_go = false;
+    if (FUSE && warp >= 4 && warp < 8) {
+        const int r = tid - 128;
+        fz_ap = prev.accepted[b];
+        fz_o = prev.offsets[b];
+        fz_Tp = prev.offsets[b + 1] - fz_o;
+        const bool ext_ok = fz_Tp > 0 && fz_Tp <= kMaxTree && fz_o >= 0 && fz_o + fz_Tp <= prev.N;
+        fz_go = fz_ap >= 0 && fz_ap < fz_Tp && ext_ok;
+        if (fz_go && r < fz_Tp) fz_par = prev.parent[fz_o + r];
+    }
+    // FUSE, warps 4..7 (row r): log P of the accepted node and, for the first
+    // eight path nodes, log P_t, k_t[r] and u_t[r].
+    float fz_La = 0.f, fz_lp[8], fz_kv[8], fz_uv[8];
     if (my_depth >= kSlots) my_depth = -1; // no work for this row (the request is refused)
     if (!early_alloc && warp == 0) {
         tmem_alloc(tslot, 256);
@@ -350,6 +408,189 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const int bad_node = inline_topo && in_range ? stopo[0] : kT;
     const bool bad = !in_range || d < 0 || d >= kSlots || d >= T || bad_node < kT ||
                      (inline_topo && d > max_depth);
+    const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
+    // Bounded wait on phase 0 of barrier `i`; a timeout is recorded CTA-wide.
+    auto waitb = [&](int i) -> bool {
+        const bool r = mbar_wait(&bar[i], 0, kWaitNs);
+        if (!r) *sfail = 1;
+        return r;
+    };
+    // ---- deferred commit (FUSE) ----
+    // Issuing thread: one kind::tf32 product per chunk, (D_a K_a)^T U_a into
+    // tensor-memory columns 0..127 (lane = row of the state).
+    uint64_t *fz_done = reinterpret_cast<uint64_t *>(sm + FZ_DONE);
+    uint64_t *fz_drain = reinterpret_cast<uint64_t *>(sm + FZ_DRAIN);
+    // Split warps (row r): the previous tree's parent links staged, the
+    // accepted path walked by one thread with bole_commit's checks (a fault is
+    // reported and nothing is committed), then the first chunk's path rows
+    // read.  Returns the path length (0: nothing to commit, and fz_done is
+    // completed at once for the gather that waits on it).
+    auto fz_walk = [&](int r) -> int {
+        int *fpar = reinterpret_cast<int *>(sm + OFF_FZ);
+        int *fpath = reinterpret_cast<int *>(sm + FZ_PATH);
+        int *fmisc = reinterpret_cast<int *>(sm + FZ_MISC);
+        if (fz_go && r < fz_Tp) fpar[r] = fz_par;
+        asm volatile("bar.sync 4, 128;" ::: "memory");
+        if (r == 0) {
+            int L = 0, fail = 0, at = fz_ap, aux = fz_Tp;
+            if (fz_go) {
+                int j = fz_ap;
+                while (j >= 0) {
+                    if (L >= kFzMaxPath) { // a longer path than this kernel commits
+                        fail = BOLE_ERR_DEPTH;
+                        aux = kFzMaxPath;
+                        break;
+                    }
+                    fpath[L++] = j;
+                    const int p = fpar[j];
+                    if (p < -1 || p >= j) {
+                        fail = BOLE_ERR_BAD_TOPOLOGY;
+                        at = j;
+                        aux = -1;
+                        break;
+                    }
+                    j = p;
+                }
+            } else if (fz_ap >= 0) {
+                fail = BOLE_ERR_BAD_TOPOLOGY;
+            }
+            if (fail != 0) {
+                if (h == 0) report(st, fail, b, at, aux);
+                L = 0;
+            }
+            fmisc[0] = L;
+            if (L == 0) mbar_arrive(fz_done);
+        }
+        asm volatile("bar.sync 4, 128;" ::: "memory");
+        const int L = fmisc[0];
+        if (L > 0) {
+            fz_La = prev.logP[(size_t)(fz_o + fpath[0]) * H + h];
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt) {
+                const bool on = tt < L;
+                const size_t nh = (size_t)(fz_o + (on ? fpath[tt] : 0)) * H + h;
+                fz_lp[tt] = on ? prev.logP[nh] : 0.f;
+                fz_kv[tt] = on ? __bfloat162float(prev.k[nh * kD + r]) : 0.f;
+                fz_uv[tt] = on ? prev.U[nh * kD + r] : 0.f;
+            }
+        }
+        return L;
+    };
+    // Split warps (row r): the operands of each chunk of eight path nodes,
+    // A[r][t] = (P_a / P_t) k_t[r] and B^T[r][t] = u_t[r] (node first, as
+    // bole_commit forms them), and one kind::tf32 product per chunk,
+    // (D_a K_a)^T U_a into tensor-memory columns 0..127 (lane = row of the
+    // state), issued by thread r = 0 -- not the issuing warp, whose next
+    // product (the Gram) waits for [Q;K]; then the wait for the whole
+    // product.  Returns P_a.
+    auto fz_stage = [&](int r, int fz_len) -> float {
+        const int fz_nch = (fz_len + 7) >> 3;
+        const int *fpath = reinterpret_cast<const int *>(sm + FZ_PATH);
+        const float La = fz_La;
+        uint8_t *fa = sm + FZ_A, *fb = sm + FZ_B;
+        const uint32_t fa_s = smem_addr(fa), fb_s = smem_addr(fb);
+#pragma unroll 1
+        for (int ch = 0; ch < fz_nch; ++ch) {
+            float lp[8], kv[8], uv[8];
+            if (ch == 0) { // read in the prologue
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    lp[tt] = fz_lp[tt];
+                    kv[tt] = fz_kv[tt];
+                    uv[tt] = fz_uv[tt];
+                }
+            } else {
+                // the previous chunk's product has read the operand buffers
+                if (!mbar_wait(&bar[BAR_FZ], (uint32_t)(ch - 1) & 1u, kWaitNs)) {
+                    *sfail = 1;
+                    break;
+                }
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const int t = 8 * ch + tt;
+                    const bool on = t < fz_len;
+                    const size_t nh = (size_t)(fz_o + (on ? fpath[t] : 0)) * H + h;
+                    lp[tt] = on ? prev.logP[nh] : 0.f;
+                    kv[tt] = on ? __bfloat162float(prev.k[nh * kD + r]) : 0.f;
+                    uv[tt] = on ? prev.U[nh * kD + r] : 0.f;
+                }
+            }
+            float av[8];
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt)
+                av[tt] = 8 * ch + tt < fz_len ? expf(La - lp[tt]) * kv[tt] : 0.f;
+            *reinterpret_cast<float4 *>(fa + sw32_chunk(r, 0)) = make_float4(av[0], av[1], av[2], av[3]);
+            *reinterpret_cast<float4 *>(fa + sw32_chunk(r, 1)) = make_float4(av[4], av[5], av[6], av[7]);
+            *reinterpret_cast<float4 *>(fb + sw32_chunk(r, 0)) = make_float4(uv[0], uv[1], uv[2], uv[3]);
+            *reinterpret_cast<float4 *>(fb + sw32_chunk(r, 1)) = make_float4(uv[4], uv[5], uv[6], uv[7]);
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 4, 128;" ::: "memory");
+            if (r == 0 && !*sfail) {
+                tc_fence_after();
+                mma_tf32_ss(tmem, sdesc_sw32(fa_s, 256), sdesc_sw32(fb_s, 256), IDESC_TF32,
+                            ch > 0 ? 1u : 0u);
+                mma_commit(&bar[BAR_FZ]);
+                // a barrier with a single phase for the end of the whole product
+                // (waiters may come before or after any chunk)
+                if (ch == fz_nch - 1) mma_commit(fz_done);
+            }
+        }
+        if (!mbar_wait(fz_done, 0, kWaitNs)) *sfail = 1;
+        tc_fence_after();
+        return expf(La);
+    };
+    // After a timeout, the products thread r = 0 issued end (bounded) before
+    // the CTA frees its tensor memory.
+    auto fz_drain_products = [&](int fz_len) {
+        if (FUSE && tid == 128 && fz_len > 0) {
+            mma_commit(fz_drain);
+            mbar_wait(fz_drain, 0, kWaitNs);
+        }
+    };
+    // Split warps: every row r of the state tile becomes P_a S + D (D in
+    // tensor memory), in place in shared memory, one 64-column half at a time;
+    // one thread stores each half by TMA (in place in global memory) as soon
+    // as it is written, one bulk group per half.
+    auto fz_commit_tile = [&](int r, float Pa) {
+#pragma unroll 1
+        for (int pc = 0; pc < 2; ++pc) {
+            float d0[32], d1[32]; // both tensor-memory loads in flight at once
+            tmem_ld32_async(tmem + lane_base + 64 * pc, d0);
+            tmem_ld32_async(tmem + lane_base + 64 * pc + 32, d1);
+            tmem_wait_ld32(d0);
+            tmem_wait_ld32(d1);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                uint8_t *box = sbuf + (2 * pc + hb) * 16384;
+                const float *dv = hb ? d1 : d0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float4 *p4 = reinterpret_cast<float4 *>(box + sw128_chunk(r, c));
+                    float4 v = *p4;
+                    v.x = fmaf(Pa, v.x, dv[4 * c + 0]);
+                    v.y = fmaf(Pa, v.y, dv[4 * c + 1]);
+                    v.z = fmaf(Pa, v.z, dv[4 * c + 2]);
+                    v.w = fmaf(Pa, v.w, dv[4 * c + 3]);
+                    *p4 = v;
+                }
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 4, 128;" ::: "memory");
+            if (r == 0 && !*sfail) { // no store of a product that timed out
+                tma_store_2d(&tmS, sbuf + (2 * pc) * 16384, 64 * pc, unit * kD);
+                tma_store_2d(&tmS, sbuf + (2 * pc + 1) * 16384, 64 * pc + 32, unit * kD);
+                bulk_commit_group();
+            }
+        }
+    };
+    // Split warps: before half pc is overwritten, its store has read it.
+    auto fz_wait_half = [&](int r, int pc) {
+        if (r == 0) {
+            if (pc == 0) bulk_wait_group_read1();
+            else bulk_wait_group_read0();
+        }
+        asm volatile("bar.sync 4, 128;" ::: "memory");
+    };
     if (fault != 0 || T <= 0 || bad) {
         if (fault == 0 && h == 0 && (T > 0 || (inline_topo && T < 0))) {
             if (bad_node < kT) { // the first node whose link does not point backwards
@@ -360,22 +601,37 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                        b, -1, T > kTmax || T < 0 ? T : d);
             }
         }
+        // FUSE: the previous round's commit still applies when this round's
+        // tree is empty or refused (the commit's own inputs being valid).
+        int fzL = 0;
+        if (FUSE && fault == 0 && warp >= 4 && warp < 8) {
+            const int r = tid - 128;
+            fzL = fz_walk(r);
+            if (fzL > 0) {
+                const float Pa = fz_stage(r, fzL);
+                waitb(BAR_S); // every thread goes on (the update holds named barriers);
+                              // after a timeout nothing is stored
+                fz_commit_tile(r, Pa);
+                fz_wait_half(r, 1);
+            }
+        }
         if (issuer) { // drain the copies in flight before the CTA retires
             if (in_range) mbar_wait(&bar[BAR_A1], 0, kWaitNs);
             if (SMALL && in_range) mbar_wait(&bar[BAR_V], 0, kWaitNs);
             mbar_wait(&bar[BAR_S], 0, kWaitNs);
         }
-        if (warp == 0) tmem_dealloc(tmem, 256); // unused
+        if (FUSE) { // a product in flight after a timeout ends before the tensor memory goes
+            tc_fence_before();
+            __syncthreads();
+            if (*sfail) fz_drain_products(fzL);
+            __syncthreads();
+            tc_fence_after();
+        }
+        if (warp == 0) tmem_dealloc(tmem, 256);
         return;
     }
-    const uint32_t lane_base = (uint32_t)(rowgrp * 32) << 16;
-    // Bounded wait on phase 0 of barrier `i`; a timeout is recorded CTA-wide.
-    auto waitb = [&](int i) -> bool {
-        const bool r = mbar_wait(&bar[i], 0, kWaitNs);
-        if (!r) *sfail = 1;
-        return r;
-    };
     bool v_issued = SMALL; // the value rows' copy (issued at entry for small trees)
+    int fzL = 0;           // FUSE, split warps: the previous accepted path's length
 
     if (warp == kComputeThreads / 32) {
         // =========================== issue warp ===========================
@@ -526,6 +782,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // Compact C and G of row i, gathered in depth order (small trees:
             // warp 0 only, the rows of warp 1 are past the tree).
             ok &= waitb(BAR_STAGED);
+            if (FUSE && // the commit operands live where C and G go
+                !mbar_wait(fz_done, 0, kWaitNs)) {
+                *sfail = 1;
+                ok = false;
+            }
             const float *qk = staged_row(i), *kk = staged_row(64 + i);
             float *crow = Cc + i * kLd, *grow = Gc + i * kLd;
             float qv[kSlots], kv[kSlots]; // every load first, then the products
@@ -549,10 +810,19 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             // bf16, N-contiguous, 64-column atoms: boxes (0,1) <- columns 0..63,
             // boxes (2,3) <- columns 64..127.
             const int r = tid - 128;
+            // FUSE: first the previous round's commit of the tile (P_a S + D, each
+            // half stored by TMA as soon as it is written), then the split of the
+            // committed values, each half once its store has read it.
+            fzL = FUSE ? fz_walk(r) : 0;
+            const bool fzc = fzL > 0;
+            float Pa = 1.f; // P_a of the previous accepted node
+            if (fzc) Pa = fz_stage(r, fzL);
             ok &= waitb(BAR_S);
+            if (fzc) fz_commit_tile(r, Pa); // the previous round's commit, stored
 #pragma unroll 1
             for (int pc = 0; pc < 2; ++pc) {
                 uint8_t *box0 = sbuf + (2 * pc) * 16384, *box1 = box0 + 16384;
+                if (fzc) fz_wait_half(r, pc); // the committed half's store has read it
                 float x[64];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -581,6 +851,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 }
             }
             fence_proxy_async_smem();
+            if (FUSE) tc_fence_before(); // the commit product's tensor-memory reads
             mbar_arrive(&bar[BAR_CONV]);
         }
         ok &= waitb(BAR_TOPO);
@@ -840,6 +1111,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             mbar_wait(&bar[BAR_S], 0, kWaitNs);
             if (v_issued) mbar_wait(&bar[BAR_V], 0, kWaitNs);
         }
+        fz_drain_products(fzL); // FUSE: the commit products of the split warps
         __syncthreads();
     }
     tc_fence_after();
@@ -1269,8 +1541,10 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
     if (e == cudaSuccess) e = make_node_map(&mK, a.k, a.N, a.H, rows);
     if (e == cudaSuccess) e = make_node_map(&mV, a.v, a.N, a.H, rows);
     if (e != cudaSuccess) return e;
-    auto kernel = small ? (a.vk ? tc_verify_kernel<true, true> : tc_verify_kernel<false, true>)
-                        : (a.vk ? tc_verify_kernel<true, false> : tc_verify_kernel<false, false>);
+    auto kernel = small ? (a.vk ? tc_verify_kernel<true, true, false>
+                                : tc_verify_kernel<false, true, false>)
+                        : (a.vk ? tc_verify_kernel<true, false, false>
+                                : tc_verify_kernel<false, false, false>);
     e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -1279,7 +1553,41 @@ cudaError_t launch_tc_verify(const VerifyArgs &a, cudaStream_t s, bool overlap)
     return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
                               a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
                               a.logP, a.st, resident_ctas(2), overlap ? 0 : 1, a.parent,
-                              a.max_depth, a.inline_topo ? 1 : 0);
+                              a.max_depth, a.inline_topo ? 1 : 0, PrevRound{});
+}
+
+bool tc_commit_verify_supported(const VerifyArgs &a)
+{
+    return tc_verify_supported(a) && !a.vk;
+}
+
+cudaError_t launch_tc_commit_verify(const VerifyArgs &a, const PrevArgs &p, cudaStream_t s)
+{
+    const int units = a.B * a.H;
+    if (units == 0) return cudaSuccess;
+    const bool small = a.max_T <= kTSmall;
+    const int rows = small ? kTSmall : kT;
+    CUtensorMap mS, mQ, mK, mV;
+    // N may be 0 (every tree of this round empty: only the commit runs); the
+    // node maps then describe an extent over the previous keys that no copy
+    // reads (no tree, no q / k / v load).
+    const int n_map = a.N > 0 ? a.N : rows;
+    cudaError_t e = make_state_map(&mS, a.S_pre, units);
+    if (e == cudaSuccess) e = make_node_map(&mQ, a.N > 0 ? a.q : p.k, n_map, a.H, rows);
+    if (e == cudaSuccess) e = make_node_map(&mK, a.N > 0 ? a.k : p.k, n_map, a.H, rows);
+    if (e == cudaSuccess) e = make_node_map(&mV, a.N > 0 ? a.v : p.k, n_map, a.H, rows);
+    if (e != cudaSuccess) return e;
+    auto kernel = small ? tc_verify_kernel<false, true, true> : tc_verify_kernel<false, false, true>;
+    e = configure_once(reinterpret_cast<const void *>(kernel), VERIFY_SMEM, true);
+    if (e != cudaSuccess) return e;
+    const PrevRound prev{static_cast<const __nv_bfloat16 *>(p.k), p.U, p.logP, p.offsets,
+                         p.parent, p.accepted, p.N};
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(dim3(units), dim3(kThreads), VERIFY_SMEM, s,
+                                                 false, attr);
+    return cudaLaunchKernelEx(&cfg, kernel, mS, mQ, mK, mV, a.gamma, a.beta, a.offsets, a.anc,
+                              a.req_depth, a.H, a.N, static_cast<__nv_bfloat16 *>(a.O), a.U,
+                              a.logP, a.st, resident_ctas(2), 1, a.parent, a.max_depth, 1, prev);
 }
 
 bool tc_commit_supported(const CommitArgs &a)

@@ -57,6 +57,9 @@ class RoundBuffers:
     U: torch.Tensor
     logP: torch.Tensor
     workspace: torch.Tensor
+    # the other round's U and logP for bole_commit_verify (alloc_alt)
+    U_alt: Optional[torch.Tensor] = None
+    logP_alt: Optional[torch.Tensor] = None
 
 
 def alloc_round(db: DeviceBatch, flags: int = 0) -> RoundBuffers:
@@ -103,6 +106,37 @@ def inline_topology_supported(db: DeviceBatch, flags: int = 0) -> bool:
         return db.max_T <= 64
     return (db.q.dtype == torch.float32 and db.max_T <= 32
             and not flags & bole.FLAG_ONE_TILE_PER_HEAD)
+
+
+def commit_verify_supported(db: DeviceBatch, flags: int = 0) -> bool:
+    """Whether bole_commit_verify applies: bf16 q/k/v, dk = dv = 128, trees of
+    up to 64 nodes of depth <= 15, the default state layout."""
+    return (db.dk == 128 and db.dv == 128 and db.max_T <= 64 and db.max_depth <= 15
+            and db.q.dtype == torch.bfloat16
+            and not flags & (bole.FLAG_FORCE_SIMT | bole.FLAG_STATE_VK))
+
+
+def alloc_alt(db: DeviceBatch, rb: RoundBuffers) -> RoundBuffers:
+    """A second U / logP pair, so that consecutive bole_commit_verify rounds
+    alternate between them (a round's outputs may not overwrite the factors
+    it commits)."""
+    rb.U_alt = torch.empty_like(rb.U)
+    rb.logP_alt = torch.empty_like(rb.logP)
+    return rb
+
+
+def commit_verify_round(db: DeviceBatch, rb: RoundBuffers, parity: int, stream=None) -> None:
+    """One round of a repeated workload with the previous round's commit
+    fused into this round's verification (bole_commit_verify): the same
+    forest and inputs every round, parity 0 committing the factors in
+    (U, logP) and writing this round's into (U_alt, logP_alt), parity 1 the
+    other way round.  The first round of a sequence is a plain verification
+    (verify with FLAG_INLINE_TOPOLOGY into U, logP)."""
+    Up, Lp, Uo, Lo = ((rb.U, rb.logP, rb.U_alt, rb.logP_alt) if parity == 0
+                      else (rb.U_alt, rb.logP_alt, rb.U, rb.logP))
+    bole.commit_verify(db.S, db.k, Up, Lp, db.offsets, db.parent, db.accepted, db.q, db.k, db.v,
+                       db.gamma, db.beta, db.offsets, db.parent, db.max_T, db.max_depth, O=rb.O,
+                       U=Uo, logP=Lo, status=rb.status, stream=stream)
 
 
 def run_round(db: DeviceBatch, rb: RoundBuffers, flags: int = 0, stream=None) -> None:

@@ -313,6 +313,49 @@ bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
                                const int32_t *accepted, int n_layers, int B, int H, int dk, int dv,
                                int N, int32_t *dev_status, unsigned flags, bole_stream_t stream);
 
+/* Deferred commit fused with the next verification (Eq. (10), then the
+ * closed form of Section III on the committed state, in one launch).  In a
+ * serving loop the commit of round r and the verification of round r + 1 both
+ * stream each head's state; this call reads it once:
+ *     S <- P_a S + sum over j on the path root..a of (P_a / P_j) k_j u_j^T
+ * with the previous round's factors (exactly bole_commit with k_prev, U_prev,
+ * logP_prev, offsets_prev, parent_prev, accepted_prev, N_prev), then this
+ * round's verification from the committed S (exactly bole_tree_verify with
+ * BOLE_FLAG_INLINE_TOPOLOGY: O, U, logP of this round's forest).  Both
+ * rounds have the same B requests and H heads; their forests may differ.
+ *   - S: [B,H,dk,dv] float32 in/out (default state layout), 16-byte aligned.
+ *   - Previous round: k_prev [N_prev,H,dk] in qkv_dtype, U_prev [N_prev,H,dv],
+ *     logP_prev [N_prev,H] float32, offsets_prev [B+1], parent_prev [N_prev],
+ *     accepted_prev [B] (-1: that request's state is not committed).  U and
+ *     logP of this call must be other buffers than U_prev and logP_prev (the
+ *     same pointer returns BOLE_ERR_INVALID_ARG; partial overlaps are the
+ *     caller's to avoid): keep two and alternate them between rounds.
+ *   - This round: as bole_tree_verify (q, k, v, gamma, beta, offsets,
+ *     parent; O, U, logP written), the topology formed in the kernel.
+ *   - Supported: bf16 q/k/v (and k_prev), dk = dv = 128, max_T <= 64,
+ *     max_depth <= 15; elsewhere BOLE_ERR_UNSUPPORTED with nothing launched
+ *     (call bole_commit, then bole_tree_verify).  An accepted path of more than
+ *     16 nodes is reported as BOLE_ERR_DEPTH {code, request, accepted node,
+ *     16}; a bad accepted node, extent or parent link of the previous round
+ *     as bole_commit reports it; that request's state is left uncommitted
+ *     (its outputs of this round, computed from that state, are not to be
+ *     used).  A request whose new tree is empty or refused is still committed.
+ *   - flags: 0 or BOLE_FLAG_OVERLAP_LAUNCH (accepted and ignored: the launch
+ *     always waits for the previous kernel, whose commit or verification may
+ *     have written S).
+ *   - Device faults and the status block as for bole_tree_verify with
+ *     BOLE_FLAG_INLINE_TOPOLOGY (nothing clears dev_status).
+ * The last round of a sequence is committed with bole_commit. */
+bole_status bole_commit_verify(float *S, const void *k_prev, const float *U_prev,
+                               const float *logP_prev, const int32_t *offsets_prev,
+                               const int32_t *parent_prev, const int32_t *accepted_prev,
+                               int N_prev, const void *q, const void *k, const void *v,
+                               bole_dtype qkv_dtype, const float *gamma, const float *beta,
+                               const int32_t *offsets, const int32_t *parent, int B, int H,
+                               int dk, int dv, int N, int max_T, int max_depth, void *O, float *U,
+                               float *logP, int32_t *dev_status, unsigned flags,
+                               bole_stream_t stream);
+
 /* ---- Device-side proposal selection and forest build ----
  * (Section IV, hardware-aware budget: at run time each drafted candidate v
  * scores rho(v) = product over its path of the drafter's edge probabilities

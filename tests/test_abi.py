@@ -133,6 +133,36 @@ def test_commit_layers_host_validation_without_gpu(lib):
     assert call(0) == bole.OK
 
 
+def test_commit_verify_host_validation_without_gpu(lib):
+    """bole_commit_verify rejects bad arguments and unsupported shapes before
+    any launch: the previous round's factors may not be this round's output
+    buffers; fp32, other head sizes and trees beyond 64 nodes or depth 15
+    are the two-call sequence's (BOLE_ERR_UNSUPPORTED)."""
+    from gated_deltanet_verification_gb300 import bole
+    c = ctypes.c_void_p
+    fake, fake2, fake3 = c(1 << 20), c(2 << 20), c(3 << 20)
+    B, H, N, N_prev = 2, 3, 40, 30
+
+    def call(S=fake, U_prev=fake2, U=fake3, logP_prev=fake2, logP=fake3, dtype=1, dk=128,
+             dv=128, max_T=32, max_depth=8, flags=0, N=N, N_prev=N_prev, acc=fake):
+        return lib.bole_commit_verify(S, fake, U_prev, logP_prev, fake, fake, acc, N_prev,
+                                      fake, fake, fake, dtype, fake, fake, fake, fake, B, H, dk,
+                                      dv, N, max_T, max_depth, fake, U, logP, fake, flags, None)
+
+    assert call(S=None) == bole.ERR_INVALID_ARG
+    assert call(acc=None) == bole.ERR_INVALID_ARG
+    assert call(U=fake2) == bole.ERR_INVALID_ARG          # U aliases U_prev
+    assert call(logP=fake2) == bole.ERR_INVALID_ARG       # logP aliases logP_prev
+    assert call(flags=bole.FLAG_STATE_VK) == bole.ERR_INVALID_ARG
+    assert call(N=B * 32 + 1) == bole.ERR_INVALID_ARG     # more nodes than B * max_T
+    assert call(S=c((1 << 20) + 8)) == bole.ERR_INVALID_ARG  # 16-byte alignment
+    assert call(dtype=0) == bole.ERR_UNSUPPORTED          # fp32 q/k/v
+    assert call(dk=64) == bole.ERR_UNSUPPORTED
+    assert call(max_T=65) == bole.ERR_UNSUPPORTED
+    assert call(max_depth=16) == bole.ERR_UNSUPPORTED
+    assert call(N=0, N_prev=0) == bole.OK                 # nothing to commit or verify
+
+
 def test_state_layout_flag_keeps_the_workspace(lib):
     f = lib.bole_workspace_size
     f.restype = ctypes.c_size_t
