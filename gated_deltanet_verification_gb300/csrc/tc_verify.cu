@@ -241,7 +241,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    pdl_launch_dependents(); // an overlapped commit may start its state reads
+    // An overlapped commit may start its state reads; the deferred-commit form
+    // writes the state, so nothing after it starts before it has ended.
+    if (!FUSE) pdl_launch_dependents();
     // Caller inputs first (a launch that overlaps pack reads only these before
     // it waits): the request's extent, then the small, latency-critical reads
     // -- [Q;K] and the per-thread gamma, beta -- before the 64 KB state tile,

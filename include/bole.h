@@ -342,7 +342,7 @@ bole_status bole_commit_layers(float *S, int64_t s_layer_stride, const void *k,
  *     used).  A request whose new tree is empty or refused is still committed.
  *   - flags: 0 or BOLE_FLAG_OVERLAP_LAUNCH (accepted and ignored: the launch
  *     always waits for the previous kernel, whose commit or verification may
- *     have written S).
+ *     have written S; and no kernel after it starts before it has ended).
  *   - Device faults and the status block as for bole_tree_verify with
  *     BOLE_FLAG_INLINE_TOPOLOGY (nothing clears dev_status).
  * The last round of a sequence is committed with bole_commit. */
