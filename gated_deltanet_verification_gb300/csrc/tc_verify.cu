@@ -209,6 +209,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                  const PrevRound prev)
 {
     static_assert(!(FUSE && VK), "the deferred commit supports the default state layout");
+    constexpr bool kColGather = FUSE && !SMALL; // C and G gathered from tensor memory
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *sbuf = sm + OFF_SBUF;
@@ -256,7 +257,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         for (int i = BAR_S; i <= BAR_MMA2; ++i) mbar_init(&bar[i], 1);
         mbar_init(&bar[BAR_TOPO], kT);
         mbar_init(&bar[BAR_STAGED], SMALL ? 64 : 128);
-        mbar_init(&bar[BAR_CG], kT);
+        mbar_init(&bar[BAR_CG], kColGather ? 128 : kT); // C and G gathered apart
         mbar_init(&bar[BAR_CONV], 128);
         mbar_init(&bar[BAR_OPS], kComputeThreads);
         mbar_init(&bar[BAR_DRAIN], 1);
@@ -757,10 +758,56 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             *reinterpret_cast<uint4 *>(ancat + i * kSlots) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
             Ls[i] = L;
             Ds[i] = my_depth;
+            if (kColGather) reinterpret_cast<uint64_t *>(sm + X_JMASK)[i] = mi; // for the G gather
             if (i < T) logP[(size_t)(o + i) * H + h] = L;
             mbar_arrive(&bar[BAR_TOPO]);
         }
-        if (SMALL ? (warp == 0 || warp == 2) : warp < 4) {
+        if (kColGather && warp < 4) {
+            // Deferred commit, 64-node layout: the compact C (warps 0-1, Gram rows
+            // q_i . k_j) and G (warps 2-3, rows k_i . k_j) of node i straight from
+            // the Gram in tensor memory, with no staging -- which would wait for
+            // the state rows the first d_k half of the products frees, and in this
+            // form the state side (the commit first) is the long one.  Each thread
+            // holds its row and, column by column, writes exp(L_i - L_j) times the
+            // entry of every ancestor(-or-self) j into slot depth(j).  (Slower than
+            // the staging where the state side is short: the plain kernel stages.)
+            ok &= waitb(BAR_GRAM);
+            ok &= waitb(BAR_TOPO);
+            if (FUSE && // the commit operands live where C and G go
+                !mbar_wait(fz_done, 0, kWaitNs)) {
+                *sfail = 1;
+                ok = false;
+            }
+            tc_fence_after();
+            __syncwarp();
+            const int node = m & 63;
+            const bool gsel = m >= 64; // G: strict ancestors, times beta_i
+            const uint64_t mask =
+                node < T ? reinterpret_cast<const uint64_t *>(sm + X_JMASK)[node] : 0ull;
+            const float Li = Ls[node];
+            const float sc = gsel ? bt : 1.f;
+            float *row = (gsel ? Gc : Cc) + node * kLd;
+#pragma unroll 1
+            for (int hc = 0; hc < 2; ++hc) {
+                const uint32_t mw = (uint32_t)(mask >> (32 * hc));
+                // columns that are an ancestor of some row of the warp (warp-uniform:
+                // the others are skipped, and a half no row needs is not loaded)
+                const uint32_t any = __reduce_or_sync(0xffffffffu, mw);
+                if (any == 0u) continue;
+                float x[32];
+                tmem_ld32(tmem + TM_GRAM + 32 * hc + lane_base, x);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if ((any >> c) & 1u) {
+                        const int j = 32 * hc + c;
+                        const bool anc = ((mw >> c) & 1u) && !(gsel && j == node);
+                        if (anc) row[Ds[j]] = sc * __expf(Li - Ls[j]) * x[c];
+                    }
+                }
+            }
+            mbar_arrive(&bar[BAR_CG]);
+        }
+        if (SMALL ? (warp == 0 || warp == 2) : (!kColGather && warp < 4)) {
             // Stage the Gram rows (q.k for rows 0..63, k.k for 64..127; small
             // trees: rows 0..31 and 64..95, columns 0..31, with no wait for
             // the state products).
@@ -780,7 +827,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             }
             mbar_arrive(&bar[BAR_STAGED]);
         }
-        if (topo) {
+        if (!kColGather && topo) {
             // Compact C and G of row i, gathered in depth order (small trees:
             // warp 0 only, the rows of warp 1 are past the tree).
             ok &= waitb(BAR_STAGED);

@@ -97,3 +97,72 @@ def test_random_forest_sweep(seed):
     assert_local_parity(name, "U", U, Ue, b.offsets, tol)
     assert np.max(np.abs(logP - Le)) < 2e-4 * max(1.0, np.max(np.abs(Le))), name
     assert max(state_unit_errors(S_new, Se).values()) <= tol, name
+
+
+N_FUSED = 24
+
+
+def _fused_case(seed):
+    """Two rounds of one random workload for the deferred commit: shapes,
+    request and head counts, tree sizes from empty to 64 nodes, depths up to
+    15 (accepted paths of up to 16 nodes: one or two product chunks)."""
+    rng = np.random.default_rng(50_000 + seed)
+    B = int(rng.integers(1, 6))
+    H = int(rng.integers(1, 5))
+    rounds = []
+    for _ in range(2):
+        shape = ["random", "random", "chain", "star", "4ary"][int(rng.integers(5))]
+        cap = [32, 64][int(rng.integers(2))]
+        sizes = [int(rng.integers(0, cap + 1)) for _ in range(B)]
+        if max(sizes) == 0:
+            sizes[0] = 1
+        if shape == "chain":
+            sizes = [min(s, 16) for s in sizes]
+            max_depth = max(max(sizes) - 1, 1)
+        elif shape == "random":
+            max_depth = int(rng.integers(1, 16))
+        else:
+            max_depth = 3
+        accept = ["uniform", "deepest", "leaf"][int(rng.integers(3))]
+        rounds.append((shape, sizes, max_depth, accept))
+    return B, H, rounds
+
+
+@pytest.mark.parametrize("seed", range(N_FUSED))
+def test_commit_verify_sweep(seed):
+    """bole_commit_verify on random pairs of rounds against the oracle's commit
+    of the first round followed by its verification of the second."""
+    import copy
+    from gated_deltanet_verification_gb300 import bole, device
+    B, H, rounds = _fused_case(seed)
+    batches = [I.random_batch(seed=60_000 + 2 * seed + i, B=B, H=H, dk=128, dv=128, sizes=sz,
+                              max_depth=md, dtype="bf16", sigma=0.05, accept=acc, shape=sh)
+               for i, (sh, sz, md, acc) in enumerate(rounds)]
+    prev, cur = batches
+    dp, dc = device.to_device(prev), device.to_device(cur)
+    st = bole.new_status()
+    _, U0, L0 = bole.tree_verify(dp.S, dp.q, dp.k, dp.v, dp.gamma, dp.beta, dp.offsets, dp.parent,
+                                 None, None, None, dp.max_T, dp.max_depth, status=st,
+                                 flags=bole.FLAG_INLINE_TOPOLOGY)
+    S = dp.S.clone()
+    O, U, logP = bole.commit_verify(S, dp.k, U0, L0, dp.offsets, dp.parent, dp.accepted, dc.q,
+                                    dc.k, dc.v, dc.gamma, dc.beta, dc.offsets, dc.parent,
+                                    dc.max_T, dc.max_depth, status=st)
+    torch.cuda.synchronize()
+    bole.check_status(st, f"fused sweep case {seed}")
+    S1 = oracle.commit(prev)
+    cb = copy.copy(cur)
+    cb.S_pre = S1
+    O_ref, U_ref, lp_ref = oracle.verify(cb)
+    tol = TOL["bf16"]
+    name = f"fused sweep {seed} (B={B}, H={H}, rounds {rounds})"
+    su = state_unit_errors(S.cpu().numpy(), S1)
+    assert max(su.values()) <= tol, f"{name}: committed state worst head {max(su.values()):.3e}"
+    O = O.float().cpu().numpy().astype(np.float64)
+    U = U.cpu().numpy().astype(np.float64)
+    assert rel_fro(O, O_ref) <= tol and rel_fro(U, U_ref) <= tol, name
+    assert_local_parity(name, "O", O, O_ref, cur.offsets, tol)
+    assert_local_parity(name, "U", U, U_ref, cur.offsets, tol)
+    lp = logP.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lp - lp_ref), initial=0.0) < \
+        2e-4 * max(1.0, np.max(np.abs(lp_ref), initial=0.0)), name
