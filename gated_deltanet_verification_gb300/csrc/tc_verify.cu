@@ -191,11 +191,13 @@ struct PrevRound {
 // FUSE (deferred commit): before verifying, the CTA applies the previous
 // round's commit (Eq. (10)) to the state tile it has just loaded and stores
 // the committed state in place, so one state read serves both.  Warps 4..7
-// walk the previous accepted path during the prologue and stage the path
-// operands; the issuing thread runs the product (D_a K_a)^T U_a into tensor
-// memory columns 0..127 (free until the state products); the split warps add
-// P_a S_r to it row by row, store each 64-column half by TMA and split the
-// committed values.
+// request the previous accepted node and parent links in the prologue, walk
+// the path after it and stage the path operands; one of their threads runs
+// the product (D_a K_a)^T U_a into tensor-memory columns 0..127 (free until
+// the state products); they add P_a S_r to it row by row, store each
+// 64-column half by TMA and split the committed values.  In the 64-node
+// layout C and G are then gathered from the Gram in tensor memory (the
+// staging would wait for the state side).
 template <bool VK, bool SMALL, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQ,
