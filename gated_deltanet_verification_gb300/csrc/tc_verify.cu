@@ -292,10 +292,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (topo && inline_topo) my_par = parent[o + i];
     }
     if (issuer) {
-        mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+        if (!FUSE) { // (the deferred-commit form requests it after the prologue)
+            mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+            for (int c = 0; c < 4; ++c)
+                tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+        }
         if (SMALL && in_range) { // value rows into the padding of the q boxes
             mbar_arrive_expect_tx(&bar[BAR_V], 8192);
             tma_load_3d(sA1 + SM_V, &tmV, &bar[BAR_V], 0, h, o);
@@ -408,6 +410,18 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (FUSE && issuer) {
+        // The deferred-commit form requests the state tile only now, once the
+        // small prologue reads (this round's and the previous round's) have
+        // returned: the tile waits for the commit product anyway, and requested
+        // at entry it queued those reads behind every CTA's state burst.  Every
+        // CTA requests it (the commit of an empty or refused tree needs it, and
+        // the exit path waits for it).
+        mbar_arrive_expect_tx(&bar[BAR_S], SBUF_BYTES);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_2d(sbuf + c * 16384, &tmS, &bar[BAR_S], 32 * c, unit * kD);
+    }
     const int fault = *sfault;
     const int d = inline_topo ? stopo[1] : d_read;
     const int bad_node = inline_topo && in_range ? stopo[0] : kT;
