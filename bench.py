@@ -1,9 +1,15 @@
 """Benchmark: verified tree nodes/s for one GDN layer's verify + commit round.
 
-One step = one pass of the whole hot path over one batch: forest packing
-(bole_pack_forest), closed-form verification (bole_tree_verify) and the
-factorised commit of the accepted paths (bole_commit), all through the C ABI
-on one CUDA stream.  Inputs are seeded synthetic workloads (see
+One step = one round of the whole hot path over one batch, through the C ABI on
+one CUDA stream: the round's topology, the closed-form verification and the
+factorised commit of the accepted paths.  Where it applies (bf16 trees of up to
+64 nodes) a round is one bole_commit_verify launch -- the previous round's
+commit applied to each head's state as the verification loads it, then this
+round's verification from the committed state (one state read per round; each
+input copy's first round, in the warm-up, is a plain verification); elsewhere
+bole_tree_verify (forming the topology itself where it can, else after
+bole_pack_forest) then bole_commit.  --no-fuse times verify + commit as two
+launches.  Inputs are seeded synthetic workloads (see
 gated_deltanet_verification_gb300/inputs.py); the headline workload is the
 ragged budgeted batch (64 requests x 32 heads, trees of 8..64 nodes selected
 greedily under a 2048-node budget, depth <= 12, dk = dv = 128, bf16 q/k/v,
@@ -19,8 +25,9 @@ cost, is measured).  Inputs rotate over enough independent copies that the
 bytes touched between two uses of the same copy exceed 3x the L2 cache, so
 every step streams from HBM.  The committed state of a copy becomes that
 copy's next S_pre, as in a serving loop.  Per-kernel durations come from a
-separate pass: per call kind, a graph of that call on every input copy,
-replayed between events.  The JSON line also carries the roofline of the
+separate pass: per call kind (the fused round, and bole_tree_verify and
+bole_commit on their own), a graph of that call on every input copy, replayed
+between events.  The JSON line also carries the roofline of the
 dominant kernel, the end-to-end throughput from pinned host buffers (e2e),
 the oracle on the host cores (cpu_baseline), the clocks seen, and the rows
 beyond the round (cross-layer commit, stage 1, device-side selection).
