@@ -292,3 +292,46 @@ def test_commit_layers_is_each_layers_own_path(layout):
                 np.testing.assert_allclose(got[li, b, h], exp, rtol=1e-12, atol=1e-13)
     # layers differ (each used its own operands)
     assert not np.allclose(got[0], got[1])
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_commit_then_verify_is_the_grafted_tree(seed):
+    """The deferred commit's semantics (bole_commit_verify), pinned on the
+    oracle: committing the previous round's accepted path and then verifying
+    the new tree from the committed state is the same as verifying one tree in
+    which the new tree hangs below the accepted node's path -- the path as a
+    chain from the old state, the new roots as children of the accepted node.
+    The new nodes' outputs agree, their log P differ by log P of the accepted
+    node, and committing a new node of either gives the same state."""
+    rng = np.random.default_rng(100 + seed)
+    H = 2
+    prev = I.random_batch(seed=200 + seed, B=1, H=H, dk=4, dv=3, sizes=[9], max_depth=5,
+                          dtype="f32", sigma=0.3, accept="deepest")
+    cur = I.random_batch(seed=300 + seed, B=1, H=H, dk=4, dv=3, sizes=[7], max_depth=4,
+                         dtype="f32", sigma=0.3, accept="uniform")
+    # the accepted path, root first
+    path, j = [], int(prev.accepted[0])
+    while j >= 0:
+        path.append(j)
+        j = int(prev.parent[j])
+    path = path[::-1]
+    L, T = len(path), cur.N
+    parent = [-1] + list(range(L - 1)) + [(L - 1 if p < 0 else L + p) for p in cur.parent]
+    cat = lambda a, b: np.concatenate([a[path], b], axis=0)
+    graft = make_tree_batch([parent], prev.S_pre, cat(prev.q, cur.q), cat(prev.k, cur.k),
+                            cat(prev.v, cur.v), cat(prev.gamma, cur.gamma),
+                            cat(prev.beta, cur.beta))
+    O_g, U_g, lp_g = oracle.verify(graft, nthreads=1)
+    S1 = oracle.commit(prev, nthreads=1)
+    c1 = make_tree_batch([cur.parent], S1, cur.q, cur.k, cur.v, cur.gamma, cur.beta)
+    c1.S_pre = S1  # the committed state in fp64, as the grafted tree carries it
+    O_c, U_c, lp_c = oracle.verify(c1, nthreads=1)
+    np.testing.assert_allclose(O_g[L:], O_c, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(U_g[L:], U_c, rtol=1e-12, atol=1e-14)
+    _, _, lp_p = oracle.verify(prev, nthreads=1)
+    np.testing.assert_allclose(lp_g[L:], lp_c + lp_p[int(prev.accepted[0])], rtol=1e-12,
+                               atol=1e-13)
+    x = int(rng.integers(0, T))
+    S_g = oracle.commit(graft, accepted=np.array([L + x], np.int32), nthreads=1)
+    S_c = oracle.commit(c1, accepted=np.array([x], np.int32), nthreads=1)
+    np.testing.assert_allclose(S_g, S_c, rtol=1e-12, atol=1e-14)
