@@ -1212,11 +1212,12 @@ template <bool F32> struct CoPlan {
     static constexpr int AL = B + 4096;       // fp32: the tf32 low parts of A and B
     static constexpr int BL = AL + 8192;
     static constexpr int PATH = F32 ? BL + 4096 : AL; // int[128]
-    static constexpr int BAR = PATH + 512;    // 3 mbarriers
-    static constexpr int TSLOT = BAR + 24;
+    static constexpr int BAR = PATH + 512;    // 5 mbarriers: box, product, drain, 2 row buffers
+    static constexpr int TSLOT = BAR + 40;
     static constexpr int MISC = TSLOT + 4;    // path length, flag, status copy
     static constexpr int PAR = MISC + 16;     // int[128]: the request's parent links
-    static constexpr int SMEM = PAR + 512 + 1024;
+    static constexpr int COEF = PAR + 512;    // float[128]: exp(L_a - L_j) along a long path
+    static constexpr int SMEM = COEF + 512 + 1024;
     static constexpr int CTAS = F32 ? 5 : 7;  // per SM (x 64 tensor memory columns)
     static_assert(CTAS * (SMEM + 1024) <= 228 * 1024, "commit CTAs per SM");
     static_assert((CTAS + 1) * (SMEM + 1024) > 228 * 1024,
@@ -1238,6 +1239,28 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo)
 {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
+
+// A long accepted path (default layout, bf16 keys), by warp 0: chunk cc's
+// rows into half cc % 2 of the state buffer -- 16 key rows (256 B), then 16
+// U half-rows of this CTA's columns (256 B) -- one bulk copy per lane,
+// completing on bar[3 + cc % 2].
+template <typename KT>
+__device__ __forceinline__ void stage_path_rows(uint8_t *sS, uint64_t *bar, const int *path,
+                                                const KT *k, const float *U, int cc, int L, int o,
+                                                int H, int h, int hv)
+{
+    const int lane = threadIdx.x & 31, buf = cc & 1;
+    const int tn = min(kChunk, L - cc * kChunk);
+    uint8_t *dst = sS + buf * 8192;
+    if (lane == 0) mbar_arrive_expect_tx(&bar[3 + buf], (uint32_t)tn * 512u);
+    __syncwarp();
+    const int t = lane & 15;
+    if (t < tn) {
+        const size_t nh = (size_t)(o + path[cc * kChunk + t]) * H + h;
+        if (lane < 16) bulk_load(dst + t * 256, k + nh * kD, 256, &bar[3 + buf]);
+        else bulk_load(dst + 4096 + t * 256, U + nh * kD + kTile * hv, 256, &bar[3 + buf]);
+    }
 }
 
 template <bool VK, bool F32>
@@ -1276,9 +1299,7 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
     // dependent reads behind every CTA's state traffic); the first box is
     // requested into shared memory beside the first batch of path reads.
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        mbar_init(&bar[2], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmS);
         tma_prefetch_l2_3d(&tmS, kTile * hv, unit * kD, layer);
@@ -1310,7 +1331,9 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
     const bool work = a >= 0 && !bad;
     // stage the parent links, then walk the accepted path
     if (work && tid < T) spar[tid] = my_par;
+    int *staged = plen + 3; // last chunk whose path rows were requested (long path)
     if (tid == 32) *flag = 0;
+    if (tid == 33) *staged = -1;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1322,11 +1345,19 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
         if (warp == 0) tmem_dealloc(tmem, 64); // unused
         return;
     }
+    // The accepted path, node first: one thread walks the parent links (and
+    // reports a bad one).  In a tree of more than 32 nodes the walk stops
+    // after one chunk of nodes; a longer path is then read off a's
+    // ancestor-or-self mask, formed for every node at once by pointer jumping
+    // (log2 of the depth rounds, in the operand buffer, unused yet) --
+    // ancestors have smaller indices, so by index the mask lists the path
+    // root first.
     if (tid == 0) {
         int L = 0, j = a;
         bool ok = true;
         while (j >= 0) {
             if (L >= kMaxTree) { ok = false; break; }
+            if (L == kChunk && T > 32) { L = -1; break; } // the long walk below
             path[L++] = j;
             const int p = spar[j];
             if (p < -1 || p >= j) { ok = false; break; }
@@ -1339,8 +1370,66 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
         *plen = L;
     }
     __syncthreads();
+    if (*plen < 0) {
+        uint32_t *smk = reinterpret_cast<uint32_t *>(sA);         // [128][4]
+        int *sjp = reinterpret_cast<int *>(sA + 16 * kMaxTree);    // [128]
+        uint4 mk = make_uint4(0u, 0u, 0u, 0u);
+        int jp = -1;
+        if (tid < T) {
+            const uint32_t bit = 1u << (tid & 31);
+            mk = make_uint4(tid < 32 ? bit : 0u, (tid >> 5) == 1 ? bit : 0u,
+                            (tid >> 5) == 2 ? bit : 0u, (tid >> 5) == 3 ? bit : 0u);
+            jp = spar[tid];
+            if (jp >= tid) jp = -1; // a link that is not backwards ends the walk (checked below)
+            *reinterpret_cast<uint4 *>(smk + 4 * tid) = mk;
+            sjp[tid] = jp;
+        }
+#pragma unroll 1
+        for (int r = 0; r < 7; ++r) { // 2^7 >= 128 nodes
+            if (!__syncthreads_or(jp >= 0)) break;
+            uint4 nm = make_uint4(0u, 0u, 0u, 0u);
+            int j2 = -1;
+            if (jp >= 0) {
+                nm = *reinterpret_cast<const uint4 *>(smk + 4 * jp);
+                j2 = sjp[jp];
+            }
+            __syncthreads();
+            if (jp >= 0) {
+                mk.x |= nm.x; mk.y |= nm.y; mk.z |= nm.z; mk.w |= nm.w;
+                jp = j2;
+            }
+            if (tid < T) {
+                *reinterpret_cast<uint4 *>(smk + 4 * tid) = mk;
+                sjp[tid] = jp;
+            }
+        }
+        __syncthreads();
+        const uint4 ma = *reinterpret_cast<const uint4 *>(smk + 4 * a);
+        const int La_len = __popc(ma.x) + __popc(ma.y) + __popc(ma.z) + __popc(ma.w);
+        if (tid < T) {
+            const int wd = tid >> 5;
+            const uint32_t w = wd == 0 ? ma.x : wd == 1 ? ma.y : wd == 2 ? ma.z : ma.w;
+            if ((w >> (tid & 31)) & 1u) { // on the path: position by the path nodes below it
+                const int rank = __popc(w & ((1u << (tid & 31)) - 1u)) +
+                                 (wd > 0 ? __popc(ma.x) : 0) + (wd > 1 ? __popc(ma.y) : 0) +
+                                 (wd > 2 ? __popc(ma.z) : 0);
+                path[La_len - 1 - rank] = tid;
+                if (rank == 0 && spar[tid] != -1) { // the path ends in a bad link
+                    if (hv == 0 && layer == 0) report(st, BOLE_ERR_BAD_TOPOLOGY, b, tid, -1);
+                    *flag = 1;
+                }
+            }
+        }
+        if (tid == 0) *plen = La_len;
+    }
+    __syncthreads();
     const int L = *plen;
-    if (L > kBatch && *(volatile int *)flag == 0) {
+    // A path of more than one chunk (default layout, bf16 keys): its rows are
+    // staged by bulk copies two chunks ahead instead of read per thread in
+    // dependent batches.
+    const bool longp = !VK && !F32 && L > kChunk &&
+                       ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(U)) & 15) == 0;
+    if (!longp && L > kBatch && *(volatile int *)flag == 0) {
         // A path longer than one batch: every node's key and delta rows go
         // to L2 now, so that the batches below, each a dependent round trip,
         // meet L2 instead of DRAM.  A side: the row of 128 (key, or VK: U),
@@ -1362,10 +1451,60 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
     const uint32_t sa = smem_addr(sA), sb = smem_addr(sB);
     int nload = 0; // state boxes requested on bar[0] (thread 0)
     const int nchunks = (*(volatile int *)flag != 0) ? 0 : (L + kChunk - 1) / kChunk;
+    // Long path: the rows of chunks 0 and 1 are requested into the state
+    // buffer (free until the epilogue), each later chunk's once the buffer
+    // half it reuses has been read.
+    float *scoef = reinterpret_cast<float *>(sm + P::COEF);
+    if (longp && nchunks > 0) {
+        if (warp == 0) {
+            stage_path_rows(sS, bar, path, k, U, 0, L, o, H, h, hv);
+            stage_path_rows(sS, bar, path, k, U, 1, L, o, H, h, hv); // L > 16: two chunks
+            if (tid == 0) *staged = 1;
+            if (tid == 0) tma_prefetch_l2_3d(&tmS, kTile * hv + 32, unit * kD, layer); // second box
+        }
+        // the key-side coefficients exp(L_a - L_j) of every path node at once
+        if (tid < L) scoef[tid] = expf(La - logP[(size_t)(o + path[tid]) * H + h]);
+        __syncthreads();
+    }
     for (int ch = 0; ch < nchunks; ++ch) {
         const int tn = min(kChunk, L - ch * kChunk); // path nodes in this chunk
+        if constexpr (!VK && !F32) {
+            if (longp) {
+                const int buf = ch & 1;
+                if (!mbar_wait(&bar[3 + buf], (uint32_t)(ch >> 1) & 1u, kWaitNs)) {
+                    report(st, BOLE_ERR_TIMEOUT, b, -1, 9);
+                    *flag = 1;
+                }
+                const __nv_bfloat16 *krow = reinterpret_cast<const __nv_bfloat16 *>(sS + buf * 8192);
+                const float *urow = reinterpret_cast<const float *>(sS + buf * 8192 + 4096);
+                // A[r][t] = coef_t k_t[r] (row r = tid), B^T[c][t] = U_t[64 hv + c]
+                // (row c = tid < 64); columns past the path are zeros
+#pragma unroll
+                for (int c4 = 0; c4 < kChunk / 4; ++c4) {
+                    float av[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = 4 * c4 + e;
+                        av[e] = t < tn ? scoef[ch * kChunk + t] * __bfloat162float(krow[t * kD + tid])
+                                       : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(sA + sw64_offset(tid, 4 * c4)) =
+                        make_float4(av[0], av[1], av[2], av[3]);
+                    if (tid < kTile) {
+                        float bv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int t = 4 * c4 + e;
+                            bv[e] = t < tn ? urow[t * kTile + tid] : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(sB + sw64_offset(tid, 4 * c4)) =
+                            make_float4(bv[0], bv[1], bv[2], bv[3]);
+                    }
+                }
+            }
+        }
 #pragma unroll 1
-        for (int t0 = 0; t0 < kChunk; t0 += kBatch) {
+        for (int t0 = 0; t0 < (longp ? 0 : kChunk); t0 += kBatch) {
             // Every path-dependent read of the batch at once: the decay of
             // each path node (each thread forms its own coefficients), entry
             // r = tid of the A-side row (key, or VK: U) and, for c = tid < 64,
@@ -1490,6 +1629,20 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
             }
             mma_commit(&bar[1]);
         }
+        // Long path: every thread has read this chunk's staged rows, so its
+        // buffer takes the rows of chunk ch + 2, or, after the last chunk, the
+        // first state box (the whole buffer is free then).
+        if (longp && warp == 0 &&
+            __shfl_sync(0xffffffffu, (int)(*(volatile int *)flag == 0), 0) != 0) {
+            if (ch + 2 < nchunks) {
+                stage_path_rows(sS, bar, path, k, U, ch + 2, L, o, H, h, hv);
+                if (tid == 0) *staged = ch + 2;
+            } else if (ch == nchunks - 1 && tid == 0) {
+                ++nload;
+                mbar_arrive_expect_tx(&bar[0], 16384);
+                tma_load_3d(sS, &tmS, &bar[0], kTile * hv, unit * kD, layer);
+            }
+        }
         if (!mbar_wait(&bar[1], ch & 1, kWaitNs)) {
             report(st, BOLE_ERR_TIMEOUT, b, -1, 7);
             *flag = 1;
@@ -1521,25 +1674,29 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
                 __syncthreads();
                 if (!ok) break;
             }
-            if (!mbar_wait(&bar[0], (uint32_t)cb, kWaitNs)) {
+            if (ok && !mbar_wait(&bar[0], (uint32_t)cb, kWaitNs)) {
                 report(st, BOLE_ERR_TIMEOUT, b, -1, 8);
                 *flag = 1;
             }
             if (*(volatile int *)flag == 0) {
                 float x[32];
                 tmem_ld32(tmem + lane_base + cb * 32, x);
-                float4 s4[8]; // the row read whole before any of it is written back
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    s4[c4] = *reinterpret_cast<const float4 *>(sS + sw128_offset(r, 4 * c4));
+                for (int q = 0; q < 2; ++q) { // the row in two halves (fewer live registers)
+                    float4 s4[4];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    float4 v = s4[c4];
-                    v.x = fmaf(Pa, v.x, x[4 * c4 + 0]);
-                    v.y = fmaf(Pa, v.y, x[4 * c4 + 1]);
-                    v.z = fmaf(Pa, v.z, x[4 * c4 + 2]);
-                    v.w = fmaf(Pa, v.w, x[4 * c4 + 3]);
-                    *reinterpret_cast<float4 *>(sS + sw128_offset(r, 4 * c4)) = v;
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        s4[c4] = *reinterpret_cast<const float4 *>(sS + sw128_offset(r, 16 * q + 4 * c4));
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float4 v = s4[c4];
+                        const float *xq = x + 16 * q + 4 * c4;
+                        v.x = fmaf(Pa, v.x, xq[0]);
+                        v.y = fmaf(Pa, v.y, xq[1]);
+                        v.z = fmaf(Pa, v.z, xq[2]);
+                        v.w = fmaf(Pa, v.w, xq[3]);
+                        *reinterpret_cast<float4 *>(sS + sw128_offset(r, 16 * q + 4 * c4)) = v;
+                    }
                 }
                 fence_proxy_async_smem();
             }
@@ -1561,6 +1718,10 @@ tc_commit_kernel(const __grid_constant__ CUtensorMap tmS, const void *__restrict
             mma_commit(&bar[2]);
             mbar_wait(&bar[2], 0, kWaitNs);
             if (nload > 0) mbar_wait(&bar[0], (uint32_t)(nload - 1) & 1u, kWaitNs);
+            // the last requested chunk of each staging buffer
+            const int last = *staged;
+            for (int cc = last; cc >= 0 && cc >= last - 1; --cc)
+                mbar_wait(&bar[3 + (cc & 1)], (uint32_t)(cc >> 1) & 1u, kWaitNs);
         }
         __syncthreads();
     }
