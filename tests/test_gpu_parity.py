@@ -167,6 +167,72 @@ def test_commit_edge_paths(which):
         assert np.array_equal(got["S_new"], b.S_pre.astype(np.float64))
 
 
+def _node_depths(parent):
+    """Depth of every node of one parent-before-child tree (root depth 0)."""
+    d = []
+    for p in parent:
+        d.append(0 if p < 0 else d[p] + 1)
+    return d
+
+
+@pytest.mark.parametrize("shape", ["chain", "spine"])
+def test_commit_long_accepted_paths(shape):
+    """Accepted paths of more than one 16-node product chunk: 17, 33, 64 and
+    128 nodes in trees of more than 32 nodes (the walker's first chunk, then
+    pointer jumping over the ancestor masks; the rows staged two chunks
+    ahead) and 20 nodes in a 30-node tree (walked serially, rows staged); on
+    spines with side branches the deepest node of each."""
+    if shape == "chain":
+        b = I.random_batch(seed=71, B=5, H=2, dk=128, dv=128, sizes=[128, 40, 64, 100, 30],
+                           max_depth=127, dtype="bf16", sigma=0.05, shape="chain")
+        b.accepted[:] = [127, 16, 32, 63, 19]
+    else:  # a spine with side branches: path nodes are not consecutive indices
+        rng = np.random.default_rng(72)
+        trees = []
+        for T in (128, 96, 70, 128):
+            par, tip = [-1], 0
+            for i in range(1, T):
+                if rng.random() < 0.6:
+                    par.append(tip)
+                    tip = i
+                else:
+                    par.append(int(rng.integers(0, i)))
+            trees.append(np.asarray(par, np.int32))
+        depth = max(max(_node_depths(t)) for t in trees)
+        b = I.make_batch("spine72", rng, trees, 2, 128, 128, "bf16", depth, 0.05, "deepest")
+        assert min(_node_depths(t)[b.accepted[i]] for i, t in enumerate(trees)) >= 16
+    _check(b, _run(b), TOL["bf16"])
+
+
+@pytest.mark.parametrize("bad_parent", [45, -7])
+def test_commit_reports_a_bad_link_deep_on_the_path(bad_parent):
+    """A parent link that is not backwards 24 nodes up a 64-node accepted
+    path (found by pointer jumping, not by the walker's first chunk): the
+    commit reports {BOLE_ERR_BAD_TOPOLOGY, request, node, -1} and leaves that
+    request's state as it was; the other request is committed."""
+    from gated_deltanet_verification_gb300 import bole, device
+    b = I.random_batch(seed=73, B=2, H=2, dk=128, dv=128, sizes=[64, 40], max_depth=63,
+                       dtype="bf16", sigma=0.05, shape="chain")
+    b.accepted[:] = [63, 30]
+    db = device.to_device(b)
+    rb = device.alloc_round(db)
+    device.pack(db, rb)
+    device.verify(db, rb, 0)
+    torch.cuda.synchronize()
+    bole.check_status(rb.status)
+    S0 = db.S.clone()
+    bad = torch.as_tensor(b.parent.copy(), device="cuda")
+    bad[40] = bad_parent  # node 40 of request 0
+    st = bole.new_status()
+    bole.commit(db.S, db.k, rb.U, rb.logP, db.offsets, bad, db.accepted, status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [bole.ERR_BAD_TOPOLOGY, 0, 40, -1]
+    assert torch.equal(db.S[0], S0[0])
+    S_new = oracle.commit(b)
+    su = state_unit_errors(db.S.cpu().numpy().astype(np.float64), S_new)
+    assert max(su[(1, h)] for h in range(b.H)) <= TOL["bf16"]
+
+
 def test_device_topology_faults():
     """Bad parents and over-deep trees are reported in the status block; the
     verification and commit kernels then leave their outputs untouched."""
