@@ -277,7 +277,10 @@ bole_status bole_tree_verify_noalloc(const float *S_pre, const void *q, const vo
  * operands; fp32 k writes both operands as tf32 hi + lo and keeps three
  * products, for the float32 bound); otherwise, or with BOLE_FLAG_FORCE_SIMT,
  * the FP32 CUDA-core kernel.  Must be stream-ordered after
- * the verification.  Device faults (accepted[b] >= tree size) go to dev_status. */
+ * the verification.  Device faults go to dev_status and leave that request's
+ * state as it was: accepted[b] >= tree size, {BOLE_ERR_BAD_TOPOLOGY, b,
+ * accepted[b], tree size}; a parent link on the accepted path that does not
+ * point to an earlier node of the tree, {BOLE_ERR_BAD_TOPOLOGY, b, node, -1}. */
 bole_status bole_commit(float *S, const void *k, bole_dtype k_dtype, const float *U,
                         const float *logP, const int32_t *offsets, const int32_t *parent,
                         const int32_t *accepted, int B, int H, int dk, int dv, int N,
