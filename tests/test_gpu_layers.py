@@ -76,6 +76,11 @@ CASES = [
                                         max_depth=9, dtype="f32", sigma=0.1), 0),
     ("f32-tc", lambda: I.random_batch(seed=83, B=4, H=3, dk=128, dv=128, sizes=[32, 9, 1, 30],
                                       max_depth=12, dtype="f32", sigma=0.1), 0),
+    # fp32 keys on accepted paths of 100 and 40 nodes (the path by pointer jumping, the
+    # rows in batches of eight)
+    ("f32-chain", lambda: I.random_batch(seed=85, B=2, H=2, dk=128, dv=128, sizes=[100, 40],
+                                         max_depth=99, dtype="f32", sigma=0.1, accept="deepest",
+                                         shape="chain"), 0),
 ]
 
 
